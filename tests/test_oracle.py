@@ -1,0 +1,366 @@
+"""Pins for the fp64 oracle: each test ties the oracle to something other
+than itself -- numbers printed on the pages (tests/golden), closed forms,
+invariants of the mathematics, special cases that reduce to a library routine,
+and brute force on tiny inputs written independently here with math.fsum.
+CPU only."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from invariant_bi_rmsnorm_02_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def bf(x):
+    """python/numpy values -> bf16 tensor (exact when the values are bf16)."""
+    return torch.tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+
+
+def f64(t):
+    return t.to(torch.float64).numpy()
+
+
+# --------------------------------------------------------------------------
+# RMSNorm
+# --------------------------------------------------------------------------
+def test_rmsnorm_hand_worked():
+    # x = [3, 4]: mean of squares 12.5, root 3.5355339..., eps 0, w = 1
+    y = oracle.rmsnorm(bf([[3.0, 4.0]]), bf([1.0, 1.0]), 0.0)
+    assert y[0, 0] == pytest.approx(0.8485281374238571, abs=1e-15)
+    assert y[0, 1] == pytest.approx(1.1313708498984762, abs=1e-15)
+    # the weight multiplies element-wise: w = [2, -0.5]
+    y = oracle.rmsnorm(bf([[3.0, 4.0]]), bf([2.0, -0.5]), 0.0)
+    assert y[0, 0] == pytest.approx(1.6970562748477142, abs=1e-15)
+    assert y[0, 1] == pytest.approx(-0.5656854249492381, abs=1e-15)
+
+
+@pytest.mark.parametrize("c", [0.5, -3.0, 1e-3, 100.0])
+def test_rmsnorm_constant_row_closed_form(c):
+    # a constant row has mean square c^2: y = c / sqrt(c^2 + eps) * w
+    H, eps = 4096, 1e-6
+    w = synth.normal_bf16((H,), 7, std=0.1, mean=1.0)
+    cb = float(bf([c])[0])
+    y = oracle.rmsnorm(bf(np.full((1, H), c)), w, eps)
+    expect = cb / math.sqrt(cb * cb + eps) * f64(w)
+    np.testing.assert_allclose(y[0], expect, rtol=1e-14, atol=0)
+
+
+def test_rmsnorm_unit_rms_and_scale_invariance():
+    # with w = 1 and eps = 0 every output row has mean square exactly 1, and
+    # scaling a row by a power of two leaves it unchanged
+    x = synth.normal_bf16((5, 256), 11)
+    one = torch.ones(256, dtype=torch.bfloat16)
+    y = oracle.rmsnorm(x, one, 0.0)
+    np.testing.assert_allclose((y ** 2).mean(axis=1), 1.0, rtol=1e-13)
+    y2 = oracle.rmsnorm((x.float() * 8).to(torch.bfloat16), one, 0.0)
+    np.testing.assert_allclose(y2, y, rtol=1e-14)
+
+
+def test_rmsnorm_brute_force_fsum():
+    rng = np.random.default_rng(3)
+    for H in (1, 2, 3, 7, 16):
+        x = bf(rng.standard_normal((4, H)))
+        w = bf(rng.standard_normal(H))
+        eps = 1e-6
+        y = oracle.rmsnorm(x, w, eps)
+        xs, ws = f64(x), f64(w)
+        for i in range(4):
+            inv = 1.0 / math.sqrt(math.fsum(v * v for v in xs[i]) / H + eps)
+            for j in range(H):
+                assert y[i, j] == pytest.approx(xs[i, j] * inv * ws[j], rel=1e-14, abs=1e-300)
+
+
+def test_rmsnorm_worked_example_exact_total():
+    # one coordinate with square 1.0, 4095 with square ~3e-8: the exact total
+    # printed on the page is 1.00012285.  Our bf16 row can only approximate
+    # sqrt(3e-8) to bf16's relative half-spacing (<= 2^-8), so the total may
+    # move by at most 4095 * 3e-8 * 2 * 2^-8 ~ 9.6e-7.
+    g = golden("rmsnorm_worked_example.json")
+    H = g["H"]
+    row = np.full((1, H), math.sqrt(g["small_square"]), dtype=np.float32)
+    row[0, 0] = math.sqrt(g["large_square"])
+    _, ms = oracle.rmsnorm(bf(row), bf(np.ones(H)), 1e-6, return_mean_sq=True)
+    assert abs(ms[0] * H - g["exact_total"]) <= 1e-6
+
+
+def test_rmsnorm_dropped_eps_or_mean_is_detected():
+    # eps matters where the mean square is tiny: x = 1e-3 constant, eps 1e-6
+    # gives 1e-3 / sqrt(1e-6 + 1e-6) = 0.70710678...
+    H = 64
+    xb = bf(np.full((1, H), 2.0 ** -10))
+    v = 2.0 ** -10
+    y = oracle.rmsnorm(xb, bf(np.ones(H)), v * v)
+    np.testing.assert_allclose(y[0], 1 / math.sqrt(2.0), rtol=1e-15)
+
+
+# --------------------------------------------------------------------------
+# fp32 worked examples on the pages (pins the fp32 emulation the GPU tests
+# use to explain order effects)
+# --------------------------------------------------------------------------
+def test_absorption_example():
+    g = golden("absorption.json")
+    one = np.float32(g["large"])
+    small = np.float32(g["small"])
+    acc = one
+    for _ in range(g["count"]):
+        acc = np.float32(acc + small)
+    assert float(acc) == g["sequential_fp32"]
+    s = np.float32(0)
+    for _ in range(g["count"]):
+        s = np.float32(s + small)
+    first = np.float32(s + one)
+    assert abs(float(first) - g["small_first_fp32"]) <= g["printed_digits_abs"]
+    ulps = (float(first) - 1.0) / 2.0 ** -23
+    assert abs(ulps - g["ulp_distance_approx"]) <= 1.0
+    assert float(np.spacing(np.float32(1.0))) / 2 == pytest.approx(g["half_ulp_at_one"], rel=1e-2)
+
+
+def _tree_f32(vals):
+    vals = [np.float32(v) for v in vals]
+    while len(vals) > 1:
+        vals = [np.float32(vals[i] + vals[i + 1]) for i in range(0, len(vals), 2)]
+    return vals[0]
+
+
+def test_rmsnorm_worked_example_fp32_orders():
+    g = golden("rmsnorm_worked_example.json")
+    sq = [np.float32(g["large_square"])] + [np.float32(g["small_square"])] * (g["H"] - 1)
+    acc = np.float32(0)
+    for v in sq:                       # one block per row, sequential from index 1
+        acc = np.float32(acc + v)
+    assert abs(float(acc) - g["sequential_fp32_total"]) <= g["printed_digits_abs"]
+    L = g["split_block_len"]
+    blocks = []
+    for b in range(g["split_blocks"]):
+        chunk = sq[b * L:(b + 1) * L]
+        if b == 0:                      # the 127 small values meet first
+            blocks.append(np.float32(chunk[0] + _tree_f32(chunk[1:] + [np.float32(0)])))
+        else:
+            blocks.append(_tree_f32(chunk))
+    assert abs(float(blocks[0]) - g["split_block0_fp32"]) <= g["printed_digits_abs"]
+    assert float(blocks[1]) == pytest.approx(g["split_other_block_fp32"], rel=2e-3)
+    total = _tree_f32(blocks)
+    assert abs(float(total) - g["split_fp32_total"]) <= g["printed_digits_abs"]
+    assert float(total) - float(acc) == pytest.approx(g["difference"], rel=1e-3)
+
+
+# --------------------------------------------------------------------------
+# GEMM
+# --------------------------------------------------------------------------
+def test_gemm_identity_weight():
+    A = synth.normal_bf16((9, 64), 21)
+    W = torch.eye(64, dtype=torch.bfloat16)
+    np.testing.assert_array_equal(oracle.gemm(A, W), f64(A))
+
+
+def test_gemm_small_integers_match_integer_matmul():
+    rng = np.random.default_rng(5)
+    A = rng.integers(-2, 3, size=(13, 40))
+    W = rng.integers(-2, 3, size=(24, 40))
+    C = oracle.gemm(bf(A), bf(W))
+    np.testing.assert_array_equal(C, (A.astype(np.int64) @ W.T.astype(np.int64)).astype(np.float64))
+
+
+def test_gemm_brute_force_nonsquare():
+    # W is [N, K]: a transposed operand would read the wrong elements
+    rng = np.random.default_rng(6)
+    A = bf(rng.standard_normal((3, 7)))
+    W = bf(rng.standard_normal((5, 7)))
+    C = oracle.gemm(A, W)
+    a, w = f64(A), f64(W)
+    for i in range(3):
+        for n in range(5):
+            assert C[i, n] == pytest.approx(math.fsum(a[i, k] * w[n, k] for k in range(7)), rel=1e-14, abs=1e-14)
+
+
+def test_gemm_rank_one_closed_form():
+    a = bf(np.linspace(-2, 2, 6))
+    b = bf(np.linspace(0.5, 3, 4))
+    K = 96
+    A = a[:, None].expand(6, K).contiguous()
+    W = b[:, None].expand(4, K).contiguous()
+    C = oracle.gemm(A, W)
+    np.testing.assert_allclose(C, K * np.outer(f64(a), f64(b)), rtol=1e-15)
+
+
+def test_gemm_row_sample_matches_full():
+    A = synth.normal_bf16((17, 48), 31)
+    W = synth.normal_bf16((20, 48), 32, std=0.02)
+    full = oracle.gemm(A, W)
+    rows = np.array([16, 0, 5])
+    np.testing.assert_array_equal(oracle.gemm(A, W, rows=rows), full[rows])
+
+
+# --------------------------------------------------------------------------
+# attention
+# --------------------------------------------------------------------------
+def _dense_cache(K, V, page=4):
+    """K, V [L, Hkv, D] bf16 -> a paged cache with a reversed page order."""
+    L, Hkv, D = K.shape
+    npg = -(-L // page)
+    kc = torch.zeros(npg, Hkv, page, D, dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    bt = torch.zeros(1, npg, dtype=torch.int32)
+    for blk in range(npg):
+        phys = npg - 1 - blk
+        bt[0, blk] = phys
+        n = min(page, L - blk * page)
+        kc[phys, :, :n] = K[blk * page: blk * page + n].transpose(0, 1)
+        vc[phys, :, :n] = V[blk * page: blk * page + n].transpose(0, 1)
+    return kc, vc, bt
+
+
+def _brute_attention(q, K, V, n, scale, G):
+    """independent statement with math.exp / math.fsum, tiny inputs only"""
+    qf, kf, vf = f64(q), f64(K), f64(V)
+    Hq, D = qf.shape
+    out = np.zeros((Hq, D))
+    for h in range(Hq):
+        s = [scale * math.fsum(qf[h, d] * kf[t, h // G, d] for d in range(D)) for t in range(n)]
+        mx = max(s)
+        e = [math.exp(v - mx) for v in s]
+        den = math.fsum(e)
+        for d in range(D):
+            out[h, d] = math.fsum(e[t] * vf[t, h // G, d] for t in range(n)) / den
+    return out
+
+
+def test_attention_brute_force_decode_and_causal():
+    Hq, Hkv, D, L = 4, 2, 8, 11
+    q = synth.normal_bf16((L, Hq, D), 41)
+    K = synth.normal_bf16((L, Hkv, D), 42)
+    V = synth.normal_bf16((L, Hkv, D), 43)
+    kc, vc, bt = _dense_cache(K, V)
+    scale = 1 / math.sqrt(D)
+    dec = oracle.decode_attention(q[-1:], kc, vc, bt, [L], scale)
+    np.testing.assert_allclose(dec[0], _brute_attention(q[-1], K, V, L, scale, 2), rtol=1e-12, atol=1e-14)
+    pre = oracle.prefill_attention(q, 0, np.arange(L), kc, vc, bt, scale)
+    for p in range(L):
+        np.testing.assert_allclose(pre[p], _brute_attention(q[p], K, V, p + 1, scale, 2),
+                                   rtol=1e-12, atol=1e-14)
+
+
+def test_attention_single_key_returns_v():
+    q = synth.normal_bf16((1, 4, 64), 51)
+    K = synth.normal_bf16((1, 2, 64), 52)
+    V = synth.normal_bf16((1, 2, 64), 53)
+    kc, vc, bt = _dense_cache(K, V, page=16)
+    out = oracle.decode_attention(q, kc, vc, bt, [1], 0.125)
+    for h in range(4):
+        np.testing.assert_array_equal(out[0, h], f64(V[0, h // 2]))
+
+
+def test_attention_identical_keys_gives_mean_of_v():
+    L, D = 37, 64
+    k = synth.normal_bf16((1, 1, D), 61)
+    K = k.expand(L, 1, D).contiguous()
+    V = synth.normal_bf16((L, 1, D), 62)
+    q = synth.normal_bf16((1, 1, D), 63)
+    kc, vc, bt = _dense_cache(K, V, page=16)
+    out = oracle.decode_attention(q, kc, vc, bt, [L], 1 / 8)
+    np.testing.assert_allclose(out[0, 0], f64(V[:, 0]).mean(axis=0), rtol=0, atol=1e-14)
+
+
+def test_attention_dominant_key_selects_its_value():
+    L, D = 20, 64
+    K = torch.zeros(L, 1, D, dtype=torch.bfloat16)
+    for t in range(L):
+        K[t, 0, t] = 1.0
+    V = synth.normal_bf16((L, 1, D), 71)
+    q = torch.zeros(1, 1, D, dtype=torch.bfloat16)
+    q[0, 0, 13] = 1024.0          # score gap 1024/8 = 128 -> weight e^-128 elsewhere
+    kc, vc, bt = _dense_cache(K, V, page=16)
+    out = oracle.decode_attention(q, kc, vc, bt, [L], 1 / 8)
+    np.testing.assert_allclose(out[0, 0], f64(V[13, 0]), rtol=0, atol=1e-40)
+
+
+def test_attention_gqa_head_mapping():
+    Hq, Hkv, D, L = 8, 2, 16, 9
+    K = synth.normal_bf16((L, Hkv, D), 81)
+    V = torch.empty(L, Hkv, D, dtype=torch.bfloat16)
+    for g in range(Hkv):
+        V[:, g] = float(g + 1)
+    q = synth.normal_bf16((1, Hq, D), 82)
+    kc, vc, bt = _dense_cache(K, V)
+    out = oracle.decode_attention(q, kc, vc, bt, [L], 0.25)
+    for h in range(Hq):
+        np.testing.assert_allclose(out[0, h], h // (Hq // Hkv) + 1.0, rtol=1e-15)
+
+
+def test_attention_independent_of_physical_page_order():
+    kv = synth.paged_kv([37, 5, 64], 2, 32, 16, seed=91)
+    q = synth.normal_bf16((3, 4, 32), 92)
+    out = oracle.decode_attention(q, kv.k_cache, kv.v_cache, kv.block_table, kv.kv_lens, 0.2)
+    perm = torch.randperm(kv.num_pages, generator=torch.Generator().manual_seed(5))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(kv.num_pages)
+    kc2, vc2 = kv.k_cache[perm], kv.v_cache[perm]
+    bt2 = inv[kv.block_table.long()].to(torch.int32)
+    out2 = oracle.decode_attention(q, kc2, vc2, bt2, kv.kv_lens, 0.2)
+    np.testing.assert_array_equal(out, out2)
+
+
+@pytest.mark.parametrize("plan", [("size", 1), ("size", 3), ("size", 16), ("size", 64),
+                                  ("size", 256), ("count", 1), ("count", 4), ("count", 7)])
+def test_split_merge_equals_full_softmax(plan):
+    # the log-sum-exp merge of any split plan is an exact rearrangement
+    kv = synth.paged_kv([300, 1, 17, 64, 129], 2, 16, 16, seed=101)
+    q = synth.normal_bf16((5, 4, 16), 102)
+    full = oracle.decode_attention(q, kv.k_cache, kv.v_cache, kv.block_table, kv.kv_lens, 0.25)
+    kind, val = plan
+    split = oracle.attention(q, np.arange(5), kv.kv_lens, kv.k_cache, kv.v_cache, kv.block_table,
+                             0.25, split_size=val if kind == "size" else 0,
+                             split_count=val if kind == "count" else 0)
+    np.testing.assert_allclose(split, full, rtol=1e-12, atol=1e-13)
+
+
+def test_split_plans_match_pages():
+    g = golden("split_plan.json")
+    for c in g["fixed_size"]:
+        st = oracle.split_starts_fixed_size(c["L"], c["S"])
+        assert list(np.diff(st)) == c["sizes"]
+    for c in g["fixed_count"]:
+        st = oracle.split_starts_fixed_count(c["L"], c["count"])
+        assert list(np.diff(st)) == c["sizes"]
+
+    def chunk_start(st, k):
+        return max(s for s in st[:-1] if s <= k)
+
+    for L, start in g["key_index_300"]["fixed_size_chunk_start"].items():
+        assert chunk_start(oracle.split_starts_fixed_size(int(L), 256), 300) == start
+    for L, start in g["key_index_300"]["fixed_count_chunk_start"].items():
+        assert chunk_start(oracle.split_starts_fixed_count(int(L), 4), 300) == start
+
+
+def test_block_count_example():
+    g = golden("block_count.json")
+    nblk = lambda n: len(oracle.split_starts_fixed_size(n, g["block"])) - 1
+    assert nblk(g["cached"]) == g["cached_blocks"]
+    assert nblk(g["new"]) == g["new_blocks"]
+    assert nblk(g["cached"]) + nblk(g["new"]) == g["separate_total_blocks"]
+    assert nblk(g["cached"] + g["new"]) == g["together_blocks"]
+
+
+def test_split_plan_boundaries_depend_only_on_absolute_index():
+    # fixed size: the chunk holding key k is the same at every length > k
+    for k in (0, 255, 256, 300, 1000):
+        starts = {max(s for s in oracle.split_starts_fixed_size(L, 256)[:-1] if s <= k)
+                  for L in range(k + 1, k + 600, 37)}
+        assert starts == {k // 256 * 256}
+
+
+def test_oracle_thread_count_does_not_change_results():
+    A = synth.normal_bf16((33, 64), 111)
+    W = synth.normal_bf16((40, 64), 112)
+    np.testing.assert_array_equal(oracle.gemm(A, W, nthreads=1), oracle.gemm(A, W, nthreads=7))
