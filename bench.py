@@ -1,0 +1,513 @@
+#!/usr/bin/env python
+"""Benchmark of the batch-invariant hot path on one GB300 (or N replicas).
+
+One step is one pass of the whole path over one batch of synthetic input,
+shaped like a Llama-3-8B layer in a serving iteration:
+
+  1. KV write   : the 64 decode requests' newest K/V rows into the paged cache
+  2. RMSNorm    : x [8192, 4096]
+  3. QKV GEMM   : [8192, 4096] x [6144, 4096]^T
+  4. MLP-up GEMM: [8192, 4096] x [14336, 4096]^T
+  5. decode     : 64 requests, 32 q / 8 kv heads, D=128, KV lengths
+                  log-uniform in 1..32768 (growing one token per step), split
+                  size 256 (split kernel + merge kernel)
+  6. prefill    : one 2048-token chunk (positions 6144..8191) of an 8192-token
+                  prompt, same heads, split size 256
+
+The headline is the GEMMs' TFLOP/s (flops of both GEMMs / their device time,
+CUDA events on the launching stream); every other kernel is reported beside
+it against its own roofline, and the whole step is also run in the
+batch-variant mode to report the cost of invariance (t_invariant / t_variant
+- 1 per kernel).  L2 is flushed (a 256 MB write) before every step; inputs are
+resident in HBM when the timed region starts.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+this path) on a bounded sample of the same workload, on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+M, H, N_QKV, N_UP = 8192, 4096, 6144, 14336
+EPS = 1e-6
+DEC = dict(B=64, Hq=32, Hkv=8, D=128, page=16, S=256, max_len=32768)
+PRE = dict(T=8192, chunk=2048, start=6144)
+METRIC = "bi_gemm TFLOP/s, RMSNorm/decode-attn HBM GB/s (% peak); invariant slowdown"
+WORKLOAD = ("Llama-3-8B-shaped layer slice: RMSNorm 8192x4096 -> QKV GEMM 4096->6144 and "
+            "MLP-up GEMM 4096->14336 at M=8192; GQA decode 64 requests (32/8 heads, D=128, "
+            "KV log-uniform 1..32768, page 16, split 256); causal prefill chunk of 2048 at "
+            "position 6144 of an 8192-token prompt; KV write of the decode tokens")
+
+
+# ---------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"],
+                    bf16_sust=d.get("bf16_tflops_sustained", d["bf16_tflops"]), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="fallback")
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "invariant_bi_rmsnorm_02_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "gemm_tc_kernel": ("gemm.cu", "device_common.cuh"),
+    "rmsnorm_row_kernel": ("rmsnorm.cu",),
+    "attn_decode_split_kernel": ("attention.cu", "device_common.cuh"),
+    "attn_prefill_kernel": ("attention.cu", "device_common.cuh"),
+}
+
+
+def profiled_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of that kernel; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_sha") != source_hash(*KERNEL_SOURCES[kernel]):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons with nvidia-smi while running."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc, self.lines = index, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workload
+class Workload:
+    """Device-resident inputs of one step, seeded."""
+
+    def __init__(self, dev, rank, reserve):
+        import invariant_bi_rmsnorm_02_gb300 as bi
+        from invariant_bi_rmsnorm_02_gb300 import synth
+        self.bi, self.dev = bi, dev
+        s = 100000 * rank
+        self.x = synth.normal_bf16((M, H), s + 1, device=dev)
+        self.w = synth.normal_bf16((H,), s + 2, std=0.1, mean=1.0, device=dev)
+        self.Wqkv = synth.normal_bf16((N_QKV, H), s + 3, std=0.02, device=dev)
+        self.Wup = synth.normal_bf16((N_UP, H), s + 4, std=0.02, device=dev)
+        self.y = torch.empty_like(self.x)
+        self.qkv = torch.empty(M, N_QKV, dtype=torch.bfloat16, device=dev)
+        self.up = torch.empty(M, N_UP, dtype=torch.bfloat16, device=dev)
+        d = DEC
+        lens = synth.loguniform_int(d["B"], 1, d["max_len"] - reserve, s + 5).tolist()
+        self.kv = synth.paged_kv(lens, d["Hkv"], d["D"], d["page"], s + 6,
+                                 reserve_tokens=reserve, device=dev)
+        self.lens0 = self.kv.kv_lens.clone()
+        self.lens = self.kv.kv_lens.clone()
+        self.seq = torch.arange(d["B"], dtype=torch.int32, device=dev)
+        self.q = synth.normal_bf16((d["B"], d["Hq"], d["D"]), s + 7, device=dev)
+        self.k_new = synth.normal_bf16((d["B"], d["Hkv"], d["D"]), s + 8, device=dev)
+        self.v_new = synth.normal_bf16((d["B"], d["Hkv"], d["D"]), s + 9, device=dev)
+        self.dec_out = torch.empty_like(self.q)
+        self.dec_ws = {}
+        for mode in (bi.INVARIANT, bi.VARIANT):
+            nb = bi.bi_attn_decode_workspace_size(d["B"], d["Hq"], d["Hkv"], d["D"],
+                                                  d["max_len"], d["S"], mode)
+            self.dec_ws[mode] = torch.empty(nb // 4 + 4, dtype=torch.float32, device=dev)
+        self.pkv = synth.paged_kv([PRE["T"]], d["Hkv"], d["D"], d["page"], s + 10, device=dev)
+        self.pq = synth.normal_bf16((PRE["chunk"], d["Hq"], d["D"]), s + 11, device=dev)
+        self.pout = torch.empty_like(self.pq)
+        self.cu = torch.tensor([0, PRE["chunk"]], dtype=torch.int32, device=dev)
+        self.pstart = torch.tensor([PRE["start"]], dtype=torch.int32, device=dev)
+        self.pkl = torch.tensor([PRE["start"] + PRE["chunk"]], dtype=torch.int32, device=dev)
+        self.rms_ws = torch.empty(bi.bi_rmsnorm_workspace_size(M, H, bi.VARIANT) // 4 + 4,
+                                  dtype=torch.float32, device=dev)
+        gws = max(bi.bi_gemm_workspace_size(M, n, H, bi.VARIANT) for n in (N_QKV, N_UP))
+        self.gemm_ws = torch.empty(gws // 4 + 4, dtype=torch.float32, device=dev)
+
+    def reset_lengths(self):
+        self.lens.copy_(self.lens0)
+
+    # each entry: (name, callable); launches counted per call
+    def ops(self, mode):
+        bi, d = self.bi, DEC
+        def kv_write():
+            bi.bi_kv_write(self.k_new, self.v_new, self.seq, self.lens, self.kv.k_cache,
+                           self.kv.v_cache, self.kv.block_table)
+            self.lens.add_(1)
+        return [
+            ("kv_write", kv_write, 1),
+            ("rmsnorm", lambda: bi.bi_rmsnorm(self.x, self.w, self.y, EPS, mode, self.rms_ws), 1),
+            ("gemm_qkv", lambda: bi.bi_gemm(self.y, self.Wqkv, self.qkv, mode, 0, self.gemm_ws), 1),
+            ("gemm_up", lambda: bi.bi_gemm(self.y, self.Wup, self.up, mode, 0, self.gemm_ws), 1),
+            ("decode", lambda: bi.bi_attn_decode(
+                self.q, self.kv.k_cache, self.kv.v_cache, self.kv.block_table, self.lens,
+                self.dec_out, None, max_kv_len=d["max_len"], split_size=d["S"],
+                sm_scale=d["D"] ** -0.5, mode=mode, workspace=self.dec_ws[mode]), 2),
+            ("prefill", lambda: bi.bi_attn_prefill_chunk(
+                self.pq, self.cu, self.pstart, self.pkv.k_cache, self.pkv.v_cache,
+                self.pkv.block_table, self.pkl, self.pout, None, max_q_len=PRE["chunk"],
+                max_kv_len=PRE["T"], split_size=d["S"], sm_scale=d["D"] ** -0.5, mode=mode),
+             1),
+        ]
+
+    def launches(self):
+        """Our kernel launches per invariant step: KV write, RMSNorm, two GEMMs,
+        decode split + merge, prefill."""
+        return sum(n for _, _, n in self.ops(self.bi.INVARIANT))
+
+    # algorithmic work per launch
+    def work(self):
+        d = DEC
+        lens = self.lens.double()
+        kv_bytes = float(lens.sum()) * d["Hkv"] * d["D"] * 2 * 2  # at the step's mean length
+        qo = d["B"] * d["Hq"] * d["D"] * 2 * 2
+        T0, C = PRE["start"], PRE["chunk"]
+        causal_keys = sum(p + 1 for p in range(T0, T0 + C))
+        return {
+            "kv_write": {"bytes": d["B"] * d["Hkv"] * d["D"] * 2 * 2 * 2},
+            "rmsnorm": {"bytes": 2 * M * H * 2 + H * 2},
+            "gemm_qkv": {"flops": 2.0 * M * N_QKV * H, "bytes": 2.0 * (M * H + N_QKV * H + M * N_QKV)},
+            "gemm_up": {"flops": 2.0 * M * N_UP * H, "bytes": 2.0 * (M * H + N_UP * H + M * N_UP)},
+            "decode": {"bytes": kv_bytes + qo, "flops": 4.0 * d["Hq"] * d["D"] * float(lens.sum())},
+            "prefill": {"flops": 4.0 * d["Hq"] * d["D"] * causal_keys,
+                        "bytes": (T0 + C) * d["Hkv"] * d["D"] * 2 * 2 + 2 * C * d["Hq"] * d["D"] * 2},
+        }
+
+
+def timed_steps(wl, mode, steps, warmup, flush, stream, dist_barrier):
+    ops = wl.ops(mode)
+    names = [n for n, _, _ in ops]
+    per = {n: 0.0 for n in names}
+    wl.reset_lengths()
+    for _ in range(warmup):
+        flush.zero_()
+        for _, fn, _ in ops:
+            fn()
+    torch.cuda.synchronize()
+    wl.reset_lengths()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(steps)]
+    mean_lens = []
+    dist_barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for s in range(steps):
+            flush.zero_()
+            ev[s][0].record(stream)
+            for i, (_, fn, _) in enumerate(ops):
+                fn()
+                ev[s][i + 1].record(stream)
+    torch.cuda.synchronize()
+    dist_barrier()
+    step_ms = []
+    for s in range(steps):
+        for i, n in enumerate(names):
+            per[n] += ev[s][i].elapsed_time(ev[s][i + 1])
+        step_ms.append(ev[s][0].elapsed_time(ev[s][-1]))
+    return {n: v / steps for n, v in per.items()}, sum(step_ms) / steps
+
+
+def e2e_steps(wl, steps, warmup, stream):
+    """The GEMM metric end to end through the public API with host buffers:
+    pinned host inputs copied in, the path run, the results copied out."""
+    bi = wl.bi
+    hx = wl.x.cpu().pin_memory()
+    hq = wl.q.cpu().pin_memory()
+    hk, hv = wl.k_new.cpu().pin_memory(), wl.v_new.cpu().pin_memory()
+    hpq = wl.pq.cpu().pin_memory()
+    hqkv = torch.empty(wl.qkv.shape, dtype=torch.bfloat16).pin_memory()
+    hup = torch.empty(wl.up.shape, dtype=torch.bfloat16).pin_memory()
+    hdec = torch.empty(wl.dec_out.shape, dtype=torch.bfloat16).pin_memory()
+    hpre = torch.empty(wl.pout.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hq, hk, hv, hpq))
+    d2h = sum(t.numel() * t.element_size() for t in (hqkv, hup, hdec, hpre))
+    ops = wl.ops(bi.INVARIANT)
+
+    def one():
+        wl.x.copy_(hx, non_blocking=True)
+        wl.q.copy_(hq, non_blocking=True)
+        wl.k_new.copy_(hk, non_blocking=True)
+        wl.v_new.copy_(hv, non_blocking=True)
+        wl.pq.copy_(hpq, non_blocking=True)
+        for _, fn, _ in ops:
+            fn()
+        hqkv.copy_(wl.qkv, non_blocking=True)
+        hup.copy_(wl.up, non_blocking=True)
+        hdec.copy_(wl.dec_out, non_blocking=True)
+        hpre.copy_(wl.pout, non_blocking=True)
+
+    wl.reset_lengths()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            one()
+        stream.synchronize()
+        wl.reset_lengths()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            one()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps, h2d, d2h
+
+
+# ------------------------------------------------------------- CPU oracle leg
+def oracle_gemm_sample(rows, seed=0):
+    """The oracle's GEMM rows of both projections on a row sample; returns
+    (flops, seconds, threads)."""
+    import numpy as np
+    import oracle
+    from invariant_bi_rmsnorm_02_gb300 import synth
+    x = synth.normal_bf16((rows, H), seed + 1)
+    w = synth.normal_bf16((H,), seed + 2, std=0.1, mean=1.0)
+    Wq = synth.normal_bf16((N_QKV, H), seed + 3, std=0.02)
+    Wu = synth.normal_bf16((N_UP, H), seed + 4, std=0.02)
+    y = oracle.rmsnorm(x, w, EPS)
+    yb = torch.from_numpy(y).to(torch.bfloat16)
+    t = time.perf_counter()
+    oracle.gemm(yb, Wq)
+    oracle.gemm(yb, Wu)
+    dt = time.perf_counter() - t
+    flops = 2.0 * rows * H * (N_QKV + N_UP)
+    return flops, dt, oracle.default_threads()
+
+
+def cpu_baseline(min_seconds=10.0):
+    import oracle
+    oracle.build()
+    rows = max(1, oracle.default_threads())
+    f, dt, th = oracle_gemm_sample(rows)
+    reps, tot_f, tot_t = 1, f, dt
+    while tot_t < min_seconds and reps < 8:
+        f, dt, _ = oracle_gemm_sample(rows, seed=reps)
+        tot_f += f
+        tot_t += dt
+        reps += 1
+    return {"value": tot_f / tot_t / 1e12, "unit": "TFLOP/s", "cores": th, "kind": "oracle",
+            "sample": "%d x %d rows (one per oracle thread) of the QKV and MLP-up GEMMs "
+                      "(K=4096, N=6144+14336), fp64, %.1f s" % (reps, rows, tot_t)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    rows = max(1, oracle.default_threads())
+    for i in range(args.warmup):
+        oracle_gemm_sample(rows, seed=i)
+    tot_f = tot_t = 0.0
+    for i in range(args.steps):
+        f, dt, th = oracle_gemm_sample(rows, seed=100 + i)
+        tot_f += f
+        tot_t += dt
+    val = tot_f / tot_t / 1e12
+    cb = {"value": val, "unit": "TFLOP/s", "cores": th, "kind": "oracle",
+          "sample": "per step %d rows (one per oracle thread) of the QKV and MLP-up GEMMs at "
+                    "K=4096, fp64" % rows}
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * tot_t / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample_rows_per_step": rows},
+            "cpu_baseline": cb,
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------- main arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    import invariant_bi_rmsnorm_02_gb300 as bi
+    bi.load()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peaks = load_peaks()
+    reserve = 2 * (args.warmup + args.steps) + 8
+    wl = Workload(dev, rank, reserve)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    with ClockSampler(local) as clk:
+        inv, inv_step = timed_steps(wl, bi.INVARIANT, args.steps, args.warmup, flush, stream,
+                                    barrier)
+    var, var_step = timed_steps(wl, bi.VARIANT, args.steps, args.warmup, flush, stream, barrier)
+    status = bi.bi_check_device_errors()
+    if status != bi.OK:
+        raise RuntimeError("device error during the bench: %s" % bi.bi_status_string(status))
+    work = wl.work()
+    gemm_flops = work["gemm_qkv"]["flops"] + work["gemm_up"]["flops"]
+    gemm_ms = inv["gemm_qkv"] + inv["gemm_up"]
+    # max over ranks of the timed quantities
+    t = torch.tensor([gemm_ms, inv_step], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    gemm_ms_max, step_ms_max = float(t[0]), float(t[1])
+    value = world * gemm_flops / (gemm_ms_max * 1e-3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = e2e_steps(wl, max(3, args.steps // 2), args.warmup, stream)
+        te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        if dist is not None:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        e2e = {"value": world * gemm_flops / (float(te[0]) * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": float(te[0])}
+
+    comps = {}
+    for n in inv:
+        wk = work[n]
+        c = {"ms": inv[n], "ms_variant": var[n], "slowdown": inv[n] / var[n] - 1.0}
+        if "flops" in wk and n in ("gemm_qkv", "gemm_up", "prefill"):
+            c["tflops"] = wk["flops"] / (inv[n] * 1e-3) / 1e12
+            c["frac_of_bf16_peak"] = c["tflops"] / peaks["bf16_sust"]
+        if "bytes" in wk:
+            c["gbs"] = wk["bytes"] / (inv[n] * 1e-3) / 1e9
+            c["frac_of_hbm_peak"] = c["gbs"] / peaks["hbm"]
+        comps[n] = c
+    dom = max(inv, key=lambda n: inv[n])
+    if dom in ("gemm_qkv", "gemm_up"):
+        kname, bound, unit = "gemm_tc_kernel", "tensor", "TFLOP/s"
+        achieved, peak = comps[dom]["tflops"], peaks["bf16_sust"]
+    elif dom == "prefill":
+        kname, bound, unit = "attn_prefill_kernel", "tensor", "TFLOP/s"
+        achieved, peak = comps[dom]["tflops"], peaks["bf16_sust"]
+    else:
+        kname = {"rmsnorm": "rmsnorm_row_kernel", "decode": "attn_decode_split_kernel"}.get(dom, dom)
+        bound, unit, achieved, peak = "hbm", "GB/s", comps[dom]["gbs"], peaks["hbm"]
+    traffic = profiled_traffic(kname) if kname in KERNEL_SOURCES else None
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": traffic, "kernel": kname, "op": dom,
+                "peak_source": peaks["src"] + (" sustained bf16" if unit == "TFLOP/s" else " HBM copy")}
+
+    launches = wl.launches() * args.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, N(0,1) K/V/Q)",
+        "config": {"workload": WORKLOAD, "M": M, "hidden": H, "n_qkv": N_QKV, "n_up": N_UP,
+                   "decode_requests": DEC["B"], "split_size": DEC["S"],
+                   "prefill_chunk": PRE["chunk"], "mode": "invariant",
+                   "l2": "flushed (256 MB write) before every step",
+                   "parallelism": "replicas (dp%d, no collective on the data path)" % world},
+        "roofline": roofline,
+        "components": comps,
+        "invariant_slowdown": {"step": inv_step / var_step - 1.0,
+                               "gemm": gemm_ms / (var["gemm_qkv"] + var["gemm_up"]) - 1.0,
+                               "ms_per_step_variant": var_step},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

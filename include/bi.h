@@ -1,0 +1,228 @@
+/*
+ * bi.h -- C ABI of libbi: batch-invariant reduction kernels for GB300 (sm_103a).
+ *
+ * The three reductions of an LLM forward pass -- RMSNorm, the linear-layer
+ * GEMM and attention over a paged KV cache -- written so that every output
+ * row is a function of its own inputs only: the same bytes whatever the batch
+ * size, the row's position in the batch, the neighbouring rows, the KV-cache
+ * length of other requests or the way a prompt is cut into prefill chunks.
+ *
+ * Pages this interface follows:
+ *   [P1] "Reproducible LLM Inference - Batch Invariance, the Cost of
+ *        Determinism, and Where Bitwise Identity Is Actually Required"
+ *        (hidekazu-konishi.com)
+ *   [P3] "Your Answer Depends on Who Else Is in the Batch" (praveentn.live)
+ * Batch invariance is defined in P1 §5.1: the result for one element of a
+ * batch does not change when the batch changes.  P1 §5.3-5.5 name the three
+ * operations and the freedom each kernel must give up.
+ *
+ * Conventions (all entry points):
+ *   - Tensor pointers are DEVICE pointers owned by the caller; bf16 means IEEE
+ *     bfloat16 (passed as void*), row-major, densely packed unless a stride is
+ *     given.  Every tensor pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Calls are asynchronous on that stream; they never synchronise
+ *     and never allocate device memory.  Scratch space ("workspace") is
+ *     provided by the caller; its size comes from the matching *_workspace_size
+ *     query, which is pure host arithmetic except where noted.
+ *   - Return: BI_OK, or an error code; on an argument error nothing is
+ *     launched.  Errors found on the device (a page id outside the pool, a
+ *     kv length beyond the page table, a bounded wait that ran out) do not
+ *     fault the GPU: the kernel skips the access, records the code in a
+ *     per-device error word and returns; bi_check_device_errors reads it.
+ *   - Modes: BI_MODE_INVARIANT is the batch-invariant kernel.  BI_MODE_VARIANT
+ *     is the same arithmetic with the reduction split chosen from the batch
+ *     shape (split-K for the GEMM, a split row for RMSNorm, a fixed split
+ *     COUNT for attention), i.e. what a shape-tuned kernel does; it is
+ *     deterministic run to run but not batch-invariant, and exists to measure
+ *     the cost of invariance (P1 §8).
+ *   - Only the current CUDA device is used.
+ */
+#ifndef BI_H
+#define BI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum bi_status {
+  BI_OK = 0,
+  BI_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misaligned pointer */
+  BI_ERR_UNSUPPORTED = 2,   /* shape outside what the kernels implement */
+  BI_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+  BI_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+  BI_ERR_DEVICE_BOUNDS = 5, /* device-side check: index outside a buffer */
+  BI_ERR_TIMEOUT = 6        /* device-side bounded wait ran out */
+} bi_status;
+
+typedef enum bi_mode {
+  BI_MODE_INVARIANT = 0,
+  BI_MODE_VARIANT = 1
+} bi_mode;
+
+/* ------------------------------------------------------------------------ */
+/* RMSNorm  (P1 §5.3-5.4; P3 "Where the reductions are", "A Concrete Example") */
+/* ------------------------------------------------------------------------ */
+/* y[i,:] = x[i,:] * (mean_j x[i,j]^2 + eps)^(-1/2) * w
+ *   x [M,H] bf16, w [H] bf16, y [M,H] bf16 (y may not alias x).
+ *   Sum of squares in fp32; one rounding to bf16 at the end.
+ * INVARIANT: one row per thread block; the block shape and the order of the
+ *   in-row reduction depend on H only (P1 §5.3: more rows only means more
+ *   rows per core).  Needs no workspace.
+ * VARIANT: when M is small the row is cut into s chunks reduced by separate
+ *   blocks and combined in a second pass (P1 §5.3; P3's 32-block example);
+ *   s is chosen from M and the SM count.  Workspace: see below.
+ * Requirements: H % 8 == 0, 8 <= H <= 65536, M >= 0 (M == 0 is a no-op).
+ * Errors: BI_ERR_INVALID_ARG (null/misaligned), BI_ERR_UNSUPPORTED (H),
+ *   BI_ERR_WORKSPACE, BI_ERR_CUDA. */
+bi_status bi_rmsnorm(const void* x, const void* w, void* y, int64_t M, int64_t H,
+                     float eps, bi_mode mode, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/* Bytes of workspace bi_rmsnorm needs: 0 for BI_MODE_INVARIANT; for
+ * BI_MODE_VARIANT an upper bound (M * 64 * 4).  Host arithmetic only. */
+size_t bi_rmsnorm_workspace_size(int64_t M, int64_t H, bi_mode mode);
+
+/* ------------------------------------------------------------------------ */
+/* GEMM  (P1 §3.3, §5.4; P3 "Where the reductions are")                     */
+/* ------------------------------------------------------------------------ */
+/* C[i,n] = sum_k A[i,k] * W[n,k]
+ *   A [M,K] bf16 (activations, K contiguous), W [N,K] bf16 (a Linear weight,
+ *   K contiguous), C [M,N] bf16.  fp32 accumulation in tensor memory, one
+ *   rounding to bf16 at the end.
+ * INVARIANT: one tile shape (128 x 256 outputs), one tensor-core instruction
+ *   (tcgen05.mma kind::f16, 128x256x16) and one K order (k-blocks of 64 in
+ *   increasing k) for every M; no split-K, no stream-K (P1 §5.4: the
+ *   instruction and the split are the two freedoms to give up).  Needs no
+ *   workspace.
+ * VARIANT: same tile and instruction, but K is split into s slices chosen
+ *   from M, N and the SM count (split-K, P1 §5.4); fp32 slice results are
+ *   summed in slice order by a second kernel.  s = variant_splits if > 0.
+ * Requirements: M >= 0, N >= 1, K >= 1, N % 8 == 0, K % 8 == 0 (16-byte rows
+ *   for the tensor-memory-access engine), all dims < 2^31.
+ * Errors: as bi_rmsnorm. */
+bi_status bi_gemm(const void* A, const void* W, void* C, int64_t M, int64_t N, int64_t K,
+                  bi_mode mode, int variant_splits, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace bi_gemm needs: 0 for BI_MODE_INVARIANT.  For
+ * BI_MODE_VARIANT it queries the current device's SM count (so it needs a
+ * GPU) and returns splits * M * N * 4 for the split count bi_gemm will use;
+ * (size_t)-1 if the device cannot be queried. */
+size_t bi_gemm_workspace_size(int64_t M, int64_t N, int64_t K, bi_mode mode,
+                              int variant_splits);
+
+/* Split count bi_gemm uses in BI_MODE_VARIANT for this shape on a device
+ * with num_sms SMs (1 = no split).  Host arithmetic only. */
+int bi_gemm_variant_splits(int64_t M, int64_t N, int64_t K, int num_sms);
+
+/* ------------------------------------------------------------------------ */
+/* Attention over a paged KV cache  (P1 §5.5; P3 "The attention detail that */
+/* gets missed")                                                            */
+/* ------------------------------------------------------------------------ */
+/* Common layout:
+ *   k_cache, v_cache [num_pages][Hkv][page_size][D] bf16.  Token t of
+ *     sequence b lives in page block_table[b*max_blocks_per_seq + t/page_size]
+ *     at slot t % page_size.  The caller writes the K/V of new tokens into
+ *     the cache and extends block_table / kv_lens BEFORE calling attention,
+ *     so cached and new tokens are read from one layout and reduced alike
+ *     (P1 §5.5).
+ *   block_table [B][max_blocks_per_seq] int32, kv_lens [B] int32: device.
+ *   Grouped-query attention: q-head h reads kv-head h / (Hq/Hkv).
+ *   scores = sm_scale * q.k (pass 1/sqrt(D) for the usual scale); softmax
+ *   over the visible keys; out = sum softmax * v.
+ *   out is bf16; out_f32 (may be NULL) receives the same values before the
+ *   final rounding, in fp32, same layout.
+ * Split plan (BI_MODE_INVARIANT, P1 §5.5 fixed split SIZE): the keys
+ *   0..L-1 of a query are cut at multiples of split_size; each chunk is
+ *   reduced with an online softmax over key tiles of 64 in increasing order
+ *   (partial max m, sum l, unnormalised o), and the chunks are merged by a
+ *   left fold in chunk order with the log-sum-exp rule, then o/l is rounded.
+ *   Boundaries depend on absolute key indices only, never on L, B, the grid
+ *   or the chunking of a prompt.
+ * BI_MODE_VARIANT (fixed split COUNT, the plan the pages reject): the keys
+ *   are cut into c chunks at floor(j*L/c), c = variant_splits if > 0, else
+ *   chosen from B, Hkv and the SM count.
+ * A sequence with L == 0 produces zeros.
+ * Requirements: D in {64, 128}; Hq % Hkv == 0 and Hq/Hkv <= 16;
+ *   page_size == 16; split_size a positive multiple of 64; num_pages >= 1;
+ *   max_blocks_per_seq >= 1.
+ * Device checks: a page id outside [0, num_pages) or a kv length above
+ *   max_blocks_per_seq*page_size (or above max_kv_len) is recorded as
+ *   BI_ERR_DEVICE_BOUNDS and the offending sequence is skipped. */
+
+/* Decode: one new query token per sequence.
+ *   q [B][Hq][D] bf16, out [B][Hq][D] bf16.
+ *   max_kv_len: host-side upper bound on kv_lens (sizes the grid only).
+ *   Workspace: bi_attn_decode_workspace_size(...) bytes. */
+bi_status bi_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_table, const int32_t* kv_lens, void* out,
+                         float* out_f32, int B, int Hq, int Hkv, int D, int page_size,
+                         int64_t num_pages, int max_blocks_per_seq, int max_kv_len,
+                         int split_size, float sm_scale, bi_mode mode,
+                         int variant_splits, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/* Bytes of workspace bi_attn_decode needs (split partials m, l, o in fp32).
+ * Host arithmetic, except that BI_MODE_VARIANT with variant_splits <= 0
+ * queries the current device's SM count ((size_t)-1 if that fails). */
+size_t bi_attn_decode_workspace_size(int B, int Hq, int Hkv, int D, int max_kv_len,
+                                     int split_size, bi_mode mode, int variant_splits);
+
+/* Causal prefill of one chunk per sequence (P1 §5.5, §6.4: a prompt may
+ * arrive in chunks; every token's reduction must not depend on the chunking).
+ *   q [total_q][Hq][D] bf16: the chunk tokens of all sequences, sequence b
+ *     owning rows cu_q[b] .. cu_q[b+1]-1 (cu_q [B+1] int32, device).
+ *   q_start_pos [B] int32 (device): absolute position of sequence b's first
+ *     chunk token; token i of the chunk sits at position q_start_pos[b]+i and
+ *     attends to keys 0..q_start_pos[b]+i.  kv_lens[b] must be at least
+ *     q_start_pos[b] + chunk length (the cache already holds the chunk).
+ *   out [total_q][Hq][D] bf16 (+ optional out_f32).
+ *   max_q_len: host bound on the chunk lengths; max_kv_len: host bound on
+ *     kv_lens.  Both size the grid only.
+ * In BI_MODE_INVARIANT the result at every position is bit-identical to
+ * bi_attn_decode in BI_MODE_INVARIANT with L = position + 1 and the same
+ * split_size.  BI_MODE_VARIANT sizes the chunks from max_kv_len and c
+ * (split size = 64 * ceil(max_kv_len / (64 c))), so results move with the
+ * chunking.  Needs no workspace (pass NULL, 0). */
+bi_status bi_attn_prefill_chunk(const void* q, const int32_t* cu_q,
+                                const int32_t* q_start_pos, const void* k_cache,
+                                const void* v_cache, const int32_t* block_table,
+                                const int32_t* kv_lens, void* out, float* out_f32, int B,
+                                int Hq, int Hkv, int D, int page_size, int64_t num_pages,
+                                int max_blocks_per_seq, int64_t total_q, int max_q_len,
+                                int max_kv_len, int split_size, float sm_scale,
+                                bi_mode mode, int variant_splits, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/* Write K/V rows of new tokens into the paged cache (the precondition of
+ * both attention calls, P1 §5.5).  k_new, v_new [n_tokens][Hkv][D] bf16;
+ * token i goes to sequence seq[i] at absolute position pos[i] (int32 device
+ * arrays), i.e. page block_table[seq*max_blocks + pos/page_size], slot
+ * pos % page_size.  Pure data movement, no arithmetic.  Bounds are checked
+ * on the device as for attention. */
+bi_status bi_kv_write(const void* k_new, const void* v_new, const int32_t* seq,
+                      const int32_t* pos, int64_t n_tokens, void* k_cache, void* v_cache,
+                      const int32_t* block_table, int Hkv, int D, int page_size,
+                      int64_t num_pages, int max_blocks_per_seq, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Errors and introspection                                                 */
+/* ------------------------------------------------------------------------ */
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns BI_OK, the first recorded device error, or BI_ERR_CUDA. */
+bi_status bi_check_device_errors(void* stream);
+
+/* Static English description of a status code (never NULL). */
+const char* bi_status_string(bi_status status);
+
+/* Library version, "major.minor.patch". */
+const char* bi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BI_H */

@@ -1,3 +1,287 @@
-"""placeholder until the C ABI exists"""
-def load():
-    raise RuntimeError("libbi.so not built")
+"""Thin ctypes binding over libbi.so (the C ABI in include/bi.h).
+
+The functions named ``bi_*`` mirror the C entry points one to one: they take
+torch tensors that already live on the GPU, pass their device pointers and the
+current CUDA stream, and raise ``BiError`` on a non-OK status.  The short
+names (``rmsnorm``, ``gemm``, ``attn_decode``, ``attn_prefill_chunk``,
+``kv_write``) additionally allocate the outputs and the workspace with torch.
+No arithmetic of the method happens here; every step runs in the CUDA
+kernels, and a missing library is an error, never a fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbi.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_BOUNDS, ERR_TIMEOUT = range(7)
+INVARIANT, VARIANT = 0, 1
+
+__all__ = [
+    "BiError", "INVARIANT", "VARIANT", "LIB_PATH", "load", "library_path", "OK",
+    "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_WORKSPACE", "ERR_CUDA", "ERR_DEVICE_BOUNDS",
+    "ERR_TIMEOUT",
+    "bi_rmsnorm", "bi_rmsnorm_workspace_size", "bi_gemm", "bi_gemm_workspace_size",
+    "bi_gemm_variant_splits", "bi_attn_decode", "bi_attn_decode_workspace_size",
+    "bi_attn_prefill_chunk", "bi_kv_write", "bi_check_device_errors", "bi_status_string",
+    "bi_version", "rmsnorm", "gemm", "attn_decode", "attn_prefill_chunk", "kv_write",
+    "EXPORTED_SYMBOLS",
+]
+
+# every function include/bi.h declares
+EXPORTED_SYMBOLS = (
+    "bi_rmsnorm", "bi_rmsnorm_workspace_size", "bi_gemm", "bi_gemm_workspace_size",
+    "bi_gemm_variant_splits", "bi_attn_decode", "bi_attn_decode_workspace_size",
+    "bi_attn_prefill_chunk", "bi_kv_write", "bi_check_device_errors", "bi_status_string",
+    "bi_version",
+)
+
+
+class BiError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what, _status_text(status), status))
+
+
+_lock = threading.Lock()
+_lib = None
+
+_vp, _i64, _i32, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
+                             ctypes.c_size_t)
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load(build_if_missing: bool = True):
+    """Load libbi.so (building it with nvcc first if it is absent)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            if not build_if_missing:
+                raise RuntimeError("libbi.so is not built (run the package's build step)")
+            from . import build as _build
+            _build.build()
+        import torch.cuda  # noqa: F401  (loads the CUDA runtime torch ships)
+        lib = ctypes.CDLL(LIB_PATH)
+        sig = {
+            "bi_rmsnorm": (_i32, [_vp, _vp, _vp, _i64, _i64, _f32, _i32, _vp, _sz, _vp]),
+            "bi_rmsnorm_workspace_size": (_sz, [_i64, _i64, _i32]),
+            "bi_gemm": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp, _sz, _vp]),
+            "bi_gemm_workspace_size": (_sz, [_i64, _i64, _i64, _i32, _i32]),
+            "bi_gemm_variant_splits": (_i32, [_i64, _i64, _i64, _i32]),
+            "bi_attn_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                      _i32, _i64, _i32, _i32, _i32, _f32, _i32, _i32, _vp, _sz,
+                                      _vp]),
+            "bi_attn_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                                    _i32]),
+            "bi_attn_prefill_chunk": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                             _i32, _i32, _i32, _i32, _i64, _i32, _i64, _i32,
+                                             _i32, _i32, _f32, _i32, _i32, _vp, _sz, _vp]),
+            "bi_kv_write": (_i32, [_vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i32,
+                                   _i64, _i32, _vp]),
+            "bi_check_device_errors": (_i32, [_vp]),
+            "bi_status_string": (ctypes.c_char_p, [_i32]),
+            "bi_version": (ctypes.c_char_p, []),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _status_text(status: int) -> str:
+    try:
+        return load().bi_status_string(status).decode()
+    except Exception:  # pragma: no cover - library not loadable
+        return "status"
+
+
+def _check(status: int, what: str) -> None:
+    if status != OK:
+        raise BiError(status, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+# ---------------------------------------------------------------- raw entry points
+def bi_rmsnorm(x, w, y, eps, mode=INVARIANT, workspace=None, stream=None):
+    M, H = x.shape
+    wp, wb = _ws(workspace)
+    _check(load().bi_rmsnorm(_ptr(x, torch.bfloat16, "x"), _ptr(w, torch.bfloat16, "w"),
+                             _ptr(y, torch.bfloat16, "y"), M, H, float(eps), int(mode), wp, wb,
+                             _stream(stream)), "bi_rmsnorm")
+
+
+def bi_rmsnorm_workspace_size(M, H, mode=INVARIANT) -> int:
+    return int(load().bi_rmsnorm_workspace_size(M, H, int(mode)))
+
+
+def bi_gemm(A, W, C, mode=INVARIANT, variant_splits=0, workspace=None, stream=None):
+    M, K = A.shape
+    N = W.shape[0]
+    wp, wb = _ws(workspace)
+    _check(load().bi_gemm(_ptr(A, torch.bfloat16, "A"), _ptr(W, torch.bfloat16, "W"),
+                          _ptr(C, torch.bfloat16, "C"), M, N, K, int(mode), int(variant_splits),
+                          wp, wb, _stream(stream)), "bi_gemm")
+
+
+def bi_gemm_workspace_size(M, N, K, mode=INVARIANT, variant_splits=0) -> int:
+    return int(load().bi_gemm_workspace_size(M, N, K, int(mode), int(variant_splits)))
+
+
+def bi_gemm_variant_splits(M, N, K, num_sms) -> int:
+    return int(load().bi_gemm_variant_splits(M, N, K, int(num_sms)))
+
+
+def bi_attn_decode(q, k_cache, v_cache, block_table, kv_lens, out, out_f32=None, *,
+                   max_kv_len, split_size, sm_scale, mode=INVARIANT, variant_splits=0,
+                   workspace=None, stream=None):
+    B, Hq, D = q.shape
+    num_pages, Hkv, page, D2 = k_cache.shape
+    wp, wb = _ws(workspace)
+    _check(load().bi_attn_decode(
+        _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, torch.bfloat16, "k_cache"),
+        _ptr(v_cache, torch.bfloat16, "v_cache"), _ptr(block_table, torch.int32, "block_table"),
+        _ptr(kv_lens, torch.int32, "kv_lens"), _ptr(out, torch.bfloat16, "out"),
+        _ptr(out_f32, torch.float32, "out_f32"), B, Hq, Hkv, D, page, num_pages,
+        block_table.shape[1], int(max_kv_len), int(split_size), float(sm_scale), int(mode),
+        int(variant_splits), wp, wb, _stream(stream)), "bi_attn_decode")
+
+
+def bi_attn_decode_workspace_size(B, Hq, Hkv, D, max_kv_len, split_size, mode=INVARIANT,
+                                  variant_splits=0) -> int:
+    return int(load().bi_attn_decode_workspace_size(B, Hq, Hkv, D, max_kv_len, split_size,
+                                                    int(mode), int(variant_splits)))
+
+
+def bi_attn_prefill_chunk(q, cu_q, q_start_pos, k_cache, v_cache, block_table, kv_lens, out,
+                          out_f32=None, *, max_q_len, max_kv_len, split_size, sm_scale,
+                          mode=INVARIANT, variant_splits=0, workspace=None, stream=None):
+    total_q, Hq, D = q.shape
+    num_pages, Hkv, page, _ = k_cache.shape
+    B = kv_lens.shape[0]
+    wp, wb = _ws(workspace)
+    _check(load().bi_attn_prefill_chunk(
+        _ptr(q, torch.bfloat16, "q"), _ptr(cu_q, torch.int32, "cu_q"),
+        _ptr(q_start_pos, torch.int32, "q_start_pos"), _ptr(k_cache, torch.bfloat16, "k_cache"),
+        _ptr(v_cache, torch.bfloat16, "v_cache"), _ptr(block_table, torch.int32, "block_table"),
+        _ptr(kv_lens, torch.int32, "kv_lens"), _ptr(out, torch.bfloat16, "out"),
+        _ptr(out_f32, torch.float32, "out_f32"), B, Hq, Hkv, D, page, num_pages,
+        block_table.shape[1], total_q, int(max_q_len), int(max_kv_len), int(split_size),
+        float(sm_scale), int(mode), int(variant_splits), wp, wb, _stream(stream)),
+        "bi_attn_prefill_chunk")
+
+
+def bi_kv_write(k_new, v_new, seq, pos, k_cache, v_cache, block_table, stream=None):
+    n, Hkv, D = k_new.shape
+    num_pages, _, page, _ = k_cache.shape
+    _check(load().bi_kv_write(
+        _ptr(k_new, torch.bfloat16, "k_new"), _ptr(v_new, torch.bfloat16, "v_new"),
+        _ptr(seq, torch.int32, "seq"), _ptr(pos, torch.int32, "pos"), n,
+        _ptr(k_cache, torch.bfloat16, "k_cache"), _ptr(v_cache, torch.bfloat16, "v_cache"),
+        _ptr(block_table, torch.int32, "block_table"), Hkv, D, page, num_pages,
+        block_table.shape[1], _stream(stream)), "bi_kv_write")
+
+
+def bi_check_device_errors(stream=None) -> int:
+    return int(load().bi_check_device_errors(_stream(stream)))
+
+
+def bi_status_string(status: int) -> str:
+    return load().bi_status_string(int(status)).decode()
+
+
+def bi_version() -> str:
+    return load().bi_version().decode()
+
+
+# ---------------------------------------------------------- allocating helpers
+def _workspace(nbytes: int, device) -> torch.Tensor | None:
+    if nbytes == 0:
+        return None
+    if nbytes == 2 ** 64 - 1:
+        raise BiError(ERR_CUDA, "workspace size query")
+    return torch.empty((nbytes + 15) // 16 * 4, dtype=torch.float32, device=device)
+
+
+def rmsnorm(x, w, eps=1e-6, mode=INVARIANT, stream=None):
+    y = torch.empty_like(x)
+    ws = _workspace(bi_rmsnorm_workspace_size(x.shape[0], x.shape[1], mode), x.device)
+    bi_rmsnorm(x, w, y, eps, mode, ws, stream)
+    return y
+
+
+def gemm(A, W, mode=INVARIANT, variant_splits=0, stream=None):
+    C = torch.empty(A.shape[0], W.shape[0], dtype=torch.bfloat16, device=A.device)
+    ws = _workspace(bi_gemm_workspace_size(A.shape[0], W.shape[0], A.shape[1], mode,
+                                           variant_splits), A.device)
+    bi_gemm(A, W, C, mode, variant_splits, ws, stream)
+    return C
+
+
+def attn_decode(q, k_cache, v_cache, block_table, kv_lens, *, max_kv_len, split_size,
+                sm_scale=None, mode=INVARIANT, variant_splits=0, want_f32=False, stream=None):
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    sm_scale = D ** -0.5 if sm_scale is None else sm_scale
+    out = torch.empty_like(q)
+    out32 = torch.empty(q.shape, dtype=torch.float32, device=q.device) if want_f32 else None
+    ws = _workspace(bi_attn_decode_workspace_size(B, Hq, Hkv, D, max_kv_len, split_size, mode,
+                                                  variant_splits), q.device)
+    bi_attn_decode(q, k_cache, v_cache, block_table, kv_lens, out, out32,
+                   max_kv_len=max_kv_len, split_size=split_size, sm_scale=sm_scale, mode=mode,
+                   variant_splits=variant_splits, workspace=ws, stream=stream)
+    return (out, out32) if want_f32 else out
+
+
+def attn_prefill_chunk(q, cu_q, q_start_pos, k_cache, v_cache, block_table, kv_lens, *,
+                       max_q_len, max_kv_len, split_size, sm_scale=None, mode=INVARIANT,
+                       variant_splits=0, want_f32=False, stream=None):
+    D = q.shape[2]
+    sm_scale = D ** -0.5 if sm_scale is None else sm_scale
+    out = torch.empty_like(q)
+    out32 = torch.empty(q.shape, dtype=torch.float32, device=q.device) if want_f32 else None
+    bi_attn_prefill_chunk(q, cu_q, q_start_pos, k_cache, v_cache, block_table, kv_lens, out,
+                          out32, max_q_len=max_q_len, max_kv_len=max_kv_len,
+                          split_size=split_size, sm_scale=sm_scale, mode=mode,
+                          variant_splits=variant_splits, stream=stream)
+    return (out, out32) if want_f32 else out
+
+
+def kv_write(k_new, v_new, seq, pos, k_cache, v_cache, block_table, stream=None):
+    bi_kv_write(k_new, v_new, seq, pos, k_cache, v_cache, block_table, stream)

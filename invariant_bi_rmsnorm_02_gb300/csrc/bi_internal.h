@@ -1,0 +1,75 @@
+// bi_internal.h -- host-side interface between the C ABI layer (abi.cu) and
+// the translation units that hold the kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "bi.h"
+
+namespace bi {
+
+// ---- per-device state kept by abi.cu --------------------------------------
+// Device address of the current device's error word (nullptr on failure).
+int* device_error_word();
+// SM count of the current device (0 on failure); cached per device.
+int device_sm_count();
+// Encode a 2-D bf16 tensor map (rows x cols, row stride = cols elements) with
+// a box of box_rows x box_cols and 128-byte swizzling.  Returns false if the
+// driver entry point is unavailable or the encoding is rejected.
+bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                       uint32_t box_rows, uint32_t box_cols);
+
+inline bi_status cuda_status(cudaError_t e) { return e == cudaSuccess ? BI_OK : BI_ERR_CUDA; }
+
+// ---- RMSNorm (rmsnorm.cu) ---------------------------------------------------
+bi_status launch_rmsnorm_invariant(const void* x, const void* w, void* y, int64_t M, int64_t H,
+                                   float eps, int* err, cudaStream_t s);
+int rmsnorm_variant_splits(int64_t M, int64_t H, int num_sms);
+bi_status launch_rmsnorm_variant(const void* x, const void* w, void* y, int64_t M, int64_t H,
+                                 float eps, int splits, float* ws, int* err, cudaStream_t s);
+
+// ---- GEMM (gemm.cu) ---------------------------------------------------------
+constexpr int kGemmBM = 128;
+constexpr int kGemmBN = 256;
+constexpr int kGemmBK = 64;
+bi_status launch_gemm(const void* A, const void* W, void* C, int64_t M, int64_t N, int64_t K,
+                      int splits, float* ws, int* err, cudaStream_t s);
+
+// ---- attention (attention.cu) -------------------------------------------------
+struct AttnArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;
+  const int32_t* kv_lens;
+  const int32_t* cu_q;        // prefill only
+  const int32_t* q_start;     // prefill only
+  void* out;
+  float* out_f32;
+  int B, Hq, Hkv, D, page_size;
+  int64_t num_pages;
+  int max_blocks;
+  int max_kv_len;
+  int64_t total_q;            // prefill only
+  int max_q_len;              // prefill only
+  int split_size;             // invariant: fixed split size
+  int split_count;            // variant: fixed split count (decode)
+  bool variant;
+  float sm_scale;
+  float* ws;                  // decode partials
+  int max_splits;             // decode: partial slots per (b, q-head)
+  int* err;
+};
+int attn_decode_max_splits(int max_kv_len, int split_size, bool variant, int split_count);
+int attn_variant_split_count(int B, int Hkv, int num_sms);
+bi_status launch_attn_decode(const AttnArgs& a, cudaStream_t s);
+bi_status launch_attn_prefill(const AttnArgs& a, cudaStream_t s);
+bi_status launch_kv_write(const void* k_new, const void* v_new, const int32_t* seq,
+                          const int32_t* pos, int64_t n_tokens, void* k_cache, void* v_cache,
+                          const int32_t* block_table, int Hkv, int D, int page_size,
+                          int64_t num_pages, int max_blocks, int* err, cudaStream_t s);
+
+}  // namespace bi

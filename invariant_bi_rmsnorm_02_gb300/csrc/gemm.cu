@@ -1,0 +1,383 @@
+// gemm.cu -- C = A * W^T in bf16 with fp32 accumulation, on the 5th-generation
+// tensor cores (tcgen05.mma, accumulators in tensor memory), operands staged
+// by TMA.
+//
+// Batch invariance ("Reproducible LLM Inference", §5.4): a matmul loses it in
+// two ways -- splitting K when M and N are small, and switching to a
+// different tensor-core instruction or tile at small batch, since each
+// instruction has its own internal order.  This kernel has one configuration
+// for every shape: a 128 x 256 output tile, the instruction
+// tcgen05.mma.cta_group::1.kind::f16 with M=128 N=256 K=16, and the k-blocks
+// of 64 accumulated in increasing k into one fp32 accumulator, rounded to
+// bf16 once.  A row of C therefore depends only on its row of A, W and K:
+// rows beyond M in a partial tile are zero-filled by TMA and never mix with
+// real rows.  The work distribution (which block takes which tile) may vary
+// with M; the arithmetic of a tile does not.
+//
+// The batch-variant mode (split-K, §5.4) runs the same tile over s slices of
+// the k-blocks, writes fp32 partial tiles, and sums them in slice order in a
+// second kernel.
+//
+// Structure: persistent blocks (one per SM), 6 warps:
+//   warp 0    : TMA producer, fills a 4-stage ring of (A 128x64, W 256x64)
+//               tiles, 128-byte swizzled, completion on mbarriers;
+//   warp 1    : allocates 512 tensor-memory columns; one thread issues the
+//               MMAs into one of two 256-column accumulators and commits
+//               them to the ring's "empty" barriers;
+//   warps 2-5 : epilogue; each reads its 32 accumulator lanes (rows) with
+//               tcgen05.ld, converts and stores, then frees the accumulator,
+//               so the epilogue of one tile overlaps the MMAs of the next.
+// Every wait is bounded; a wait that runs out records BI_ERR_TIMEOUT, tells
+// the other roles to stop, waits (bounded) for its copies and MMAs in flight,
+// frees tensor memory and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "bi_internal.h"
+#include "device_common.cuh"
+
+namespace bi {
+namespace {
+
+constexpr int BM = kGemmBM, BN = kGemmBN, BK = kGemmBK;
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 2;
+constexpr int kBBytes = BN * BK * 2;
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;  // two BN-column fp32 accumulators
+constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                            (static_cast<uint32_t>(BN >> 3) << 17) |
+                            (static_cast<uint32_t>(BM >> 4) << 24);
+
+// Shared-memory matrix descriptor for a K-major tile written by TMA with
+// 128-byte swizzling: rows of 64 bf16 (128 B), 8-row groups 1024 B apart
+// (stride byte offset), descriptor version 1, layout SWIZZLE_128B (2).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;            // leading byte offset (unused here)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;    // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;            // version
+  d |= static_cast<uint64_t>(2) << 61;            // 128-byte swizzle
+  return d;
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns of the accumulator.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+        "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+        "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+        "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct GemmParams {
+  __nv_bfloat16* C;
+  float* ws;      // split-K partials [splits][M][N] (variant only)
+  int* err;
+  int M, N, K;
+  int m_tiles, n_tiles, splits, kb_total, kb_per_split;
+};
+
+struct Unit {
+  int m_tile, n_tile, split, kb0, kb1;
+};
+
+__device__ __forceinline__ Unit unit_of(int u, const GemmParams& p) {
+  const int tiles = p.m_tiles * p.n_tiles;
+  Unit w;
+  w.split = u / tiles;
+  const int r = u - w.split * tiles;
+  w.n_tile = r % p.n_tiles;  // n fastest: concurrent blocks share A rows, W stays in L2
+  w.m_tile = r / p.n_tiles;
+  w.kb0 = w.split * p.kb_per_split;
+  w.kb1 = min(w.kb0 + p.kb_per_split, p.kb_total);
+  return w;
+}
+
+template <bool kF32Out>
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(
+    const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
+    const GemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int units = p.m_tiles * p.n_tiles * p.splits;
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&ta);
+    prefetch_tmap(&tb);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit w = unit_of(u, p);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          tma_load_2d(sA + stage * kABytes, &ta, kb * BK, w.m_tile * BM, &full[stage]);
+          tma_load_2d(sB + stage * kBBytes, &tb, kb * BK, w.n_tile * BN, &full[stage]);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // let the copies already issued land before the block goes away
+        const int first = issued > kStages ? issued - kStages : 0;
+        for (int i = first; i < issued; ++i)
+          mbar_wait(&full[i % kStages], (i / kStages) & 1, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ----------------------------------------------------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit w = unit_of(u, p);
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase, p.err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = smem_desc(smem_u32(sA + stage * kABytes));
+          const uint64_t bd = smem_desc(smem_u32(sB + stage * kBBytes));
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)  // +32 bytes along K per step
+            tc_mma(d_tmem, ad + 2u * k, bd + 2u * k, (kb > w.kb0 || k > 0) ? 1u : 0u);
+          tc_commit(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        tc_commit(drain);  // all issued MMAs done before tensor memory is freed
+        mbar_wait(drain, 0, nullptr);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int wq = warp & 3;  // this warp may access accumulator lanes 32*wq ..
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const Unit w = unit_of(u, p);
+      if (!mbar_wait(&tfull[acc], acc_phase, p.err, abort_flag)) break;
+      __syncwarp();
+      tc_fence_after();
+      const int row = w.m_tile * BM + wq * 32 + lane;
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(wq * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tbase + c * 32, v);
+        const int col0 = w.n_tile * BN + c * 32;
+        if (row < p.M) {
+          if constexpr (kF32Out) {
+            float* dst = p.ws + (static_cast<int64_t>(w.split) * p.M + row) * p.N + col0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (col0 + 4 * q < p.N)
+                *reinterpret_cast<uint4*>(dst + 4 * q) =
+                    make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          } else {
+            __nv_bfloat16* dst = p.C + static_cast<int64_t>(row) * p.N + col0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (col0 + 8 * q < p.N) {
+                uint4 o;
+                o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+                o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+                o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+                o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+                *reinterpret_cast<uint4*>(dst + 8 * q) = o;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// C = bf16(sum_s ws[s]) in slice order, 4 columns per thread.
+__global__ void splitk_reduce_kernel(const float4* __restrict__ ws, uint2* __restrict__ C,
+                                     int64_t mn4, int splits) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < mn4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 a = ws[i];
+    for (int s = 1; s < splits; ++s) {
+      const float4 b = ws[s * mn4 + i];
+      a.x = __fadd_rn(a.x, b.x);
+      a.y = __fadd_rn(a.y, b.y);
+      a.z = __fadd_rn(a.z, b.z);
+      a.w = __fadd_rn(a.w, b.w);
+    }
+    C[i] = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+  }
+}
+
+}  // namespace
+
+bi_status launch_gemm(const void* A, const void* W, void* C, int64_t M, int64_t N, int64_t K,
+                      int splits, float* ws, int* err, cudaStream_t s) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return BI_ERR_CUDA;
+  CUtensorMap ta, tb;
+  if (!make_tmap_2d_bf16(&ta, A, static_cast<uint64_t>(M), static_cast<uint64_t>(K), BM, BK) ||
+      !make_tmap_2d_bf16(&tb, W, static_cast<uint64_t>(N), static_cast<uint64_t>(K), BN, BK))
+    return BI_ERR_CUDA;
+  GemmParams p{};
+  p.C = static_cast<__nv_bfloat16*>(C);
+  p.ws = ws;
+  p.err = err;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.m_tiles = static_cast<int>((M + BM - 1) / BM);
+  p.n_tiles = static_cast<int>((N + BN - 1) / BN);
+  p.kb_total = static_cast<int>((K + BK - 1) / BK);
+  if (splits < 1) splits = 1;
+  if (splits > p.kb_total) splits = p.kb_total;
+  p.kb_per_split = (p.kb_total + splits - 1) / splits;
+  p.splits = (p.kb_total + p.kb_per_split - 1) / p.kb_per_split;  // no empty slice
+  const int64_t units = static_cast<int64_t>(p.m_tiles) * p.n_tiles * p.splits;
+  if (units > 0x7fffffff) return BI_ERR_UNSUPPORTED;
+  const int grid = static_cast<int>(units < sms ? units : sms);
+  if (p.splits == 1) {
+    if (cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess)
+      return BI_ERR_CUDA;
+    gemm_tc_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, p);
+    return cuda_status(cudaGetLastError());
+  }
+  if (cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemBytes)) != cudaSuccess)
+    return BI_ERR_CUDA;
+  gemm_tc_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, p);
+  const int64_t mn4 = M * N / 4;
+  const int rb = static_cast<int>((mn4 + 255) / 256 < 4 * sms ? (mn4 + 255) / 256 : 4 * sms);
+  splitk_reduce_kernel<<<rb, 256, 0, s>>>(reinterpret_cast<const float4*>(ws),
+                                          static_cast<uint2*>(C), mn4, p.splits);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace bi

@@ -1,0 +1,134 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every function include/bi.h declares, sizes workspaces by host
+arithmetic, and rejects bad arguments before it touches the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import invariant_bi_rmsnorm_02_gb300 as bi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bi.h")
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(bi_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return bi.load()
+
+
+def test_header_lists_the_entry_points():
+    names = header_functions()
+    for n in ("bi_rmsnorm", "bi_gemm", "bi_attn_decode", "bi_attn_prefill_chunk"):
+        assert n in names
+    assert sorted(bi.EXPORTED_SYMBOLS) == names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings_and_version(lib):
+    assert bi.bi_status_string(0) == "ok"
+    for s in range(1, 7):
+        assert bi.bi_status_string(s) not in ("ok", "unknown status")
+    assert bi.bi_status_string(99) == "unknown status"
+    assert re.fullmatch(r"\d+\.\d+\.\d+", bi.bi_version())
+
+
+def test_workspace_sizes_are_host_arithmetic(lib):
+    assert bi.bi_rmsnorm_workspace_size(8192, 4096, bi.INVARIANT) == 0
+    assert bi.bi_rmsnorm_workspace_size(3, 4096, bi.VARIANT) == 3 * 64 * 4
+    assert bi.bi_gemm_workspace_size(8192, 6144, 4096, bi.INVARIANT) == 0
+    assert bi.bi_gemm_workspace_size(1, 6144, 4096, bi.VARIANT, 4) == 4 * 6144 * 4
+    # decode partials: B * Hq * ceil(max_kv_len / S) * (D + 2) floats
+    assert bi.bi_attn_decode_workspace_size(64, 32, 8, 128, 32768, 256, bi.INVARIANT) == \
+        64 * 32 * 128 * 130 * 4
+    assert bi.bi_attn_decode_workspace_size(8, 4, 2, 64, 512, 64, bi.VARIANT, 5) == \
+        8 * 4 * 5 * 66 * 4
+
+
+def test_gemm_variant_split_count(lib):
+    # split-K only when the tiles do not cover the SMs, at least 4 k-blocks per slice
+    assert bi.bi_gemm_variant_splits(8192, 6144, 4096, 152) == 1
+    assert bi.bi_gemm_variant_splits(1, 6144, 4096, 152) == 8     # 24 tiles -> 8 slices
+    assert bi.bi_gemm_variant_splits(1, 14336, 4096, 152) == 4    # 56 tiles
+    assert bi.bi_gemm_variant_splits(1, 512, 256, 152) == 1       # K = 4 k-blocks
+    assert bi.bi_gemm_variant_splits(256, 6144, 4096, 152) == 4   # 48 tiles
+
+
+def _call_rms(lib, x, w, y, M, H, eps=1e-6, mode=0, ws=None, wsb=0):
+    return lib.bi_rmsnorm(x, w, y, M, H, eps, mode, ws, wsb, None)
+
+
+def test_rmsnorm_argument_checks(lib):
+    p = 1 << 20  # a 16-byte aligned fake address: never dereferenced on these paths
+    assert _call_rms(lib, p, p, p, 4, 7) == bi.ERR_UNSUPPORTED
+    assert _call_rms(lib, p, p, p, 4, 4 * 65536) == bi.ERR_UNSUPPORTED
+    assert _call_rms(lib, p, p, p, -1, 4096) == bi.ERR_INVALID_ARG
+    assert _call_rms(lib, None, p, p, 4, 4096) == bi.ERR_INVALID_ARG
+    assert _call_rms(lib, p + 2, p, p, 4, 4096) == bi.ERR_INVALID_ARG
+    assert _call_rms(lib, p, p, p, 4, 4096, mode=7) == bi.ERR_INVALID_ARG
+    assert _call_rms(lib, p, p, p, 4, 4096, eps=-1.0) == bi.ERR_INVALID_ARG
+    assert _call_rms(lib, None, None, None, 0, 4096) == bi.OK  # empty batch: no-op
+
+
+def test_gemm_argument_checks(lib):
+    p = 1 << 20
+    g = lambda *a: lib.bi_gemm(*a)
+    assert g(p, p, p, 4, 100, 64, 0, 0, None, 0, None) == bi.ERR_UNSUPPORTED   # N % 8
+    assert g(p, p, p, 4, 128, 60, 0, 0, None, 0, None) == bi.ERR_UNSUPPORTED   # K % 8
+    assert g(p, p, p, 4, 0, 64, 0, 0, None, 0, None) == bi.ERR_INVALID_ARG
+    assert g(p, None, p, 4, 128, 64, 0, 0, None, 0, None) == bi.ERR_INVALID_ARG
+    assert g(p, p, p + 8, 4, 128, 64, 0, 0, None, 0, None) == bi.ERR_INVALID_ARG
+    assert g(None, None, None, 0, 128, 64, 0, 0, None, 0, None) == bi.OK
+
+
+def _decode(lib, **kw):
+    p = 1 << 20
+    a = dict(q=p, k=p, v=p, bt=p, kl=p, out=p, o32=None, B=2, Hq=4, Hkv=2, D=64, page=16,
+             npages=8, maxblk=4, maxkv=64, S=64, scale=0.125, mode=0, vs=0, ws=p, wsb=1 << 20)
+    a.update(kw)
+    return lib.bi_attn_decode(a["q"], a["k"], a["v"], a["bt"], a["kl"], a["out"], a["o32"],
+                              a["B"], a["Hq"], a["Hkv"], a["D"], a["page"], a["npages"],
+                              a["maxblk"], a["maxkv"], a["S"], a["scale"], a["mode"], a["vs"],
+                              a["ws"], a["wsb"], None)
+
+
+def test_attention_argument_checks(lib):
+    assert _decode(lib, D=96) == bi.ERR_UNSUPPORTED
+    assert _decode(lib, Hq=6, Hkv=4) == bi.ERR_UNSUPPORTED
+    assert _decode(lib, Hq=34, Hkv=2) == bi.ERR_UNSUPPORTED       # group of 17 > 16
+    assert _decode(lib, page=32) == bi.ERR_UNSUPPORTED
+    assert _decode(lib, S=100) == bi.ERR_UNSUPPORTED
+    assert _decode(lib, q=None) == bi.ERR_INVALID_ARG
+    assert _decode(lib, out=(1 << 20) + 4) == bi.ERR_INVALID_ARG
+    assert _decode(lib, npages=0) == bi.ERR_INVALID_ARG
+    assert _decode(lib, B=0) == bi.OK
+
+
+def test_binding_rejects_host_tensors():
+    import torch
+    x = torch.zeros(2, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        bi.bi_rmsnorm(x, x[0], x, 1e-6)
+
+
+def test_product_package_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "invariant_bi_rmsnorm_02_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "liboracle" not in text, f
