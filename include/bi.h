@@ -68,6 +68,8 @@ typedef enum bi_mode {
 /* ------------------------------------------------------------------------ */
 /* y[i,:] = x[i,:] * (mean_j x[i,j]^2 + eps)^(-1/2) * w
  *   x [M,H] bf16, w [H] bf16, y [M,H] bf16 (y may not alias x).
+ *   y_f32 (may be NULL): [M,H] fp32, the same values before the final
+ *   rounding to bf16.
  *   Sum of squares in fp32; one rounding to bf16 at the end.
  * INVARIANT: one row per thread block; the block shape and the order of the
  *   in-row reduction depend on H only (P1 §5.3: more rows only means more
@@ -78,9 +80,9 @@ typedef enum bi_mode {
  * Requirements: H % 8 == 0, 8 <= H <= 65536, M >= 0 (M == 0 is a no-op).
  * Errors: BI_ERR_INVALID_ARG (null/misaligned), BI_ERR_UNSUPPORTED (H),
  *   BI_ERR_WORKSPACE, BI_ERR_CUDA. */
-bi_status bi_rmsnorm(const void* x, const void* w, void* y, int64_t M, int64_t H,
-                     float eps, bi_mode mode, void* workspace, size_t workspace_bytes,
-                     void* stream);
+bi_status bi_rmsnorm(const void* x, const void* w, void* y, float* y_f32, int64_t M,
+                     int64_t H, float eps, bi_mode mode, void* workspace,
+                     size_t workspace_bytes, void* stream);
 
 /* Bytes of workspace bi_rmsnorm needs: 0 for BI_MODE_INVARIANT; for
  * BI_MODE_VARIANT an upper bound (M * 64 * 4).  Host arithmetic only. */

@@ -73,7 +73,7 @@ def load(build_if_missing: bool = True):
         import torch.cuda  # noqa: F401  (loads the CUDA runtime torch ships)
         lib = ctypes.CDLL(LIB_PATH)
         sig = {
-            "bi_rmsnorm": (_i32, [_vp, _vp, _vp, _i64, _i64, _f32, _i32, _vp, _sz, _vp]),
+            "bi_rmsnorm": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _f32, _i32, _vp, _sz, _vp]),
             "bi_rmsnorm_workspace_size": (_sz, [_i64, _i64, _i32]),
             "bi_gemm": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp, _sz, _vp]),
             "bi_gemm_workspace_size": (_sz, [_i64, _i64, _i64, _i32, _i32]),
@@ -139,12 +139,13 @@ def _ws(workspace):
 
 
 # ---------------------------------------------------------------- raw entry points
-def bi_rmsnorm(x, w, y, eps, mode=INVARIANT, workspace=None, stream=None):
+def bi_rmsnorm(x, w, y, eps, mode=INVARIANT, workspace=None, stream=None, y_f32=None):
     M, H = x.shape
     wp, wb = _ws(workspace)
     _check(load().bi_rmsnorm(_ptr(x, torch.bfloat16, "x"), _ptr(w, torch.bfloat16, "w"),
-                             _ptr(y, torch.bfloat16, "y"), M, H, float(eps), int(mode), wp, wb,
-                             _stream(stream)), "bi_rmsnorm")
+                             _ptr(y, torch.bfloat16, "y"), _ptr(y_f32, torch.float32, "y_f32"),
+                             M, H, float(eps), int(mode), wp, wb, _stream(stream)),
+           "bi_rmsnorm")
 
 
 def bi_rmsnorm_workspace_size(M, H, mode=INVARIANT) -> int:
@@ -239,11 +240,12 @@ def _workspace(nbytes: int, device) -> torch.Tensor | None:
     return torch.empty((nbytes + 15) // 16 * 4, dtype=torch.float32, device=device)
 
 
-def rmsnorm(x, w, eps=1e-6, mode=INVARIANT, stream=None):
+def rmsnorm(x, w, eps=1e-6, mode=INVARIANT, want_f32=False, stream=None):
     y = torch.empty_like(x)
+    y32 = torch.empty(x.shape, dtype=torch.float32, device=x.device) if want_f32 else None
     ws = _workspace(bi_rmsnorm_workspace_size(x.shape[0], x.shape[1], mode), x.device)
-    bi_rmsnorm(x, w, y, eps, mode, ws, stream)
-    return y
+    bi_rmsnorm(x, w, y, eps, mode, ws, stream, y_f32=y32)
+    return (y, y32) if want_f32 else y
 
 
 def gemm(A, W, mode=INVARIANT, variant_splits=0, stream=None):

@@ -128,8 +128,9 @@ size_t bi_rmsnorm_workspace_size(int64_t M, int64_t H, bi_mode mode) {
   return static_cast<size_t>(M) * 64u * sizeof(float);
 }
 
-bi_status bi_rmsnorm(const void* x, const void* w, void* y, int64_t M, int64_t H, float eps,
-                     bi_mode mode, void* workspace, size_t workspace_bytes, void* stream) {
+bi_status bi_rmsnorm(const void* x, const void* w, void* y, float* y_f32, int64_t M, int64_t H,
+                     float eps, bi_mode mode, void* workspace, size_t workspace_bytes,
+                     void* stream) {
   if (M < 0 || H <= 0) return BI_ERR_INVALID_ARG;
   if (mode != BI_MODE_INVARIANT && mode != BI_MODE_VARIANT) return BI_ERR_INVALID_ARG;
   if (H % 8 != 0 || H < 8 || H > 65536) return BI_ERR_UNSUPPORTED;
@@ -137,10 +138,12 @@ bi_status bi_rmsnorm(const void* x, const void* w, void* y, int64_t M, int64_t H
   if (M == 0) return BI_OK;
   if (!x || !w || !y) return BI_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return BI_ERR_INVALID_ARG;
+  if (y_f32 && !aligned16(y_f32)) return BI_ERR_INVALID_ARG;
   if (!(eps >= 0.0f)) return BI_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* err = device_error_word();
-  if (mode == BI_MODE_INVARIANT) return launch_rmsnorm_invariant(x, w, y, M, H, eps, err, s);
+  if (mode == BI_MODE_INVARIANT)
+    return launch_rmsnorm_invariant(x, w, y, y_f32, M, H, eps, err, s);
   const int sms = device_sm_count();
   if (sms <= 0) return BI_ERR_CUDA;
   const int splits = rmsnorm_variant_splits(M, H, sms);
@@ -148,8 +151,8 @@ bi_status bi_rmsnorm(const void* x, const void* w, void* y, int64_t M, int64_t H
     const size_t need = static_cast<size_t>(M) * splits * sizeof(float);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return BI_ERR_WORKSPACE;
   }
-  return launch_rmsnorm_variant(x, w, y, M, H, eps, splits, static_cast<float*>(workspace), err,
-                                s);
+  return launch_rmsnorm_variant(x, w, y, y_f32, M, H, eps, splits,
+                                static_cast<float*>(workspace), err, s);
 }
 
 // --------------------------------------------------------------------- GEMM

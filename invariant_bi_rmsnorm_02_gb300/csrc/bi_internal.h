@@ -25,11 +25,12 @@ bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64
 inline bi_status cuda_status(cudaError_t e) { return e == cudaSuccess ? BI_OK : BI_ERR_CUDA; }
 
 // ---- RMSNorm (rmsnorm.cu) ---------------------------------------------------
-bi_status launch_rmsnorm_invariant(const void* x, const void* w, void* y, int64_t M, int64_t H,
-                                   float eps, int* err, cudaStream_t s);
+bi_status launch_rmsnorm_invariant(const void* x, const void* w, void* y, float* y_f32,
+                                   int64_t M, int64_t H, float eps, int* err, cudaStream_t s);
 int rmsnorm_variant_splits(int64_t M, int64_t H, int num_sms);
-bi_status launch_rmsnorm_variant(const void* x, const void* w, void* y, int64_t M, int64_t H,
-                                 float eps, int splits, float* ws, int* err, cudaStream_t s);
+bi_status launch_rmsnorm_variant(const void* x, const void* w, void* y, float* y_f32, int64_t M,
+                                 int64_t H, float eps, int splits, float* ws, int* err,
+                                 cudaStream_t s);
 
 // ---- GEMM (gemm.cu) ---------------------------------------------------------
 constexpr int kGemmBM = 128;

@@ -58,15 +58,23 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return warp_sum(t);
 }
 
-__device__ __forceinline__ uint4 scale_row8(const uint4& xv, const uint4& wv, float r) {
+// y = (x * r) * w for 8 elements; the bf16 result is returned, the fp32
+// values are also stored to yf (8 floats) when it is not null.
+__device__ __forceinline__ uint4 scale_row8(const uint4& xv, const uint4& wv, float r,
+                                            float* yf) {
   const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
   const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
   uint32_t o[4];
+  float f[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    float a = __fmul_rn(__fmul_rn(bf16_lo(xs[i]), r), bf16_lo(ws[i]));
-    float b = __fmul_rn(__fmul_rn(bf16_hi(xs[i]), r), bf16_hi(ws[i]));
-    o[i] = pack_bf16x2(a, b);
+    f[2 * i] = __fmul_rn(__fmul_rn(bf16_lo(xs[i]), r), bf16_lo(ws[i]));
+    f[2 * i + 1] = __fmul_rn(__fmul_rn(bf16_hi(xs[i]), r), bf16_hi(ws[i]));
+    o[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+  }
+  if (yf) {
+    reinterpret_cast<float4*>(yf)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4*>(yf)[1] = make_float4(f[4], f[5], f[6], f[7]);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
@@ -79,7 +87,8 @@ __device__ __forceinline__ float inv_rms(float sum_sq, float inv_h, float eps) {
 template <int VPT>
 __global__ void __launch_bounds__(1024) rmsnorm_row_kernel(const uint4* __restrict__ x,
                                                            const uint4* __restrict__ w,
-                                                           uint4* __restrict__ y, int nvec,
+                                                           uint4* __restrict__ y,
+                                                           float* __restrict__ yf, int nvec,
                                                            float inv_h, float eps) {
   __shared__ float red[32];
   const int64_t row = blockIdx.x;
@@ -98,7 +107,8 @@ __global__ void __launch_bounds__(1024) rmsnorm_row_kernel(const uint4* __restri
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     const int v = threadIdx.x + k * blockDim.x;
-    if (v < nvec) __stcs(yr + v, scale_row8(xv[k], __ldg(w + v), r));
+    if (v < nvec)
+      __stcs(yr + v, scale_row8(xv[k], __ldg(w + v), r, yf ? yf + (row * nvec + v) * 8 : nullptr));
   }
 }
 
@@ -136,7 +146,8 @@ __global__ void __launch_bounds__(256) rmsnorm_split_partial(const uint4* __rest
 __global__ void __launch_bounds__(256) rmsnorm_split_finish(const uint4* __restrict__ x,
                                                             const uint4* __restrict__ w,
                                                             const float* __restrict__ part,
-                                                            uint4* __restrict__ y, int nvec,
+                                                            uint4* __restrict__ y,
+                                                            float* __restrict__ yf, int nvec,
                                                             int chunk_vec, float inv_h,
                                                             float eps) {
   const int c = blockIdx.x, s = gridDim.x;
@@ -151,13 +162,14 @@ __global__ void __launch_bounds__(256) rmsnorm_split_finish(const uint4* __restr
   const float r = inv_rms(p[0], inv_h, eps);
   const int64_t base = row * nvec + (int64_t)c * chunk_vec;
   for (int v = threadIdx.x; v < chunk_vec; v += blockDim.x)
-    y[base + v] = scale_row8(__ldg(x + base + v), __ldg(w + c * chunk_vec + v), r);
+    y[base + v] = scale_row8(__ldg(x + base + v), __ldg(w + c * chunk_vec + v), r,
+                             yf ? yf + (base + v) * 8 : nullptr);
 }
 
 }  // namespace
 
-bi_status launch_rmsnorm_invariant(const void* x, const void* w, void* y, int64_t M, int64_t H,
-                                   float eps, int* err, cudaStream_t s) {
+bi_status launch_rmsnorm_invariant(const void* x, const void* w, void* y, float* y_f32,
+                                   int64_t M, int64_t H, float eps, int* err, cudaStream_t s) {
   (void)err;
   if (M == 0) return BI_OK;
   const RowShape sh = row_shape(H);
@@ -168,10 +180,10 @@ bi_status launch_rmsnorm_invariant(const void* x, const void* w, void* y, int64_
   const auto* wp = static_cast<const uint4*>(w);
   auto* yp = static_cast<uint4*>(y);
   switch (sh.vpt) {
-    case 1: rmsnorm_row_kernel<1><<<grid, sh.threads, 0, s>>>(xp, wp, yp, nvec, inv_h, eps); break;
-    case 2: rmsnorm_row_kernel<2><<<grid, sh.threads, 0, s>>>(xp, wp, yp, nvec, inv_h, eps); break;
-    case 4: rmsnorm_row_kernel<4><<<grid, sh.threads, 0, s>>>(xp, wp, yp, nvec, inv_h, eps); break;
-    case 8: rmsnorm_row_kernel<8><<<grid, sh.threads, 0, s>>>(xp, wp, yp, nvec, inv_h, eps); break;
+    case 1: rmsnorm_row_kernel<1><<<grid, sh.threads, 0, s>>>(xp, wp, yp, y_f32, nvec, inv_h, eps); break;
+    case 2: rmsnorm_row_kernel<2><<<grid, sh.threads, 0, s>>>(xp, wp, yp, y_f32, nvec, inv_h, eps); break;
+    case 4: rmsnorm_row_kernel<4><<<grid, sh.threads, 0, s>>>(xp, wp, yp, y_f32, nvec, inv_h, eps); break;
+    case 8: rmsnorm_row_kernel<8><<<grid, sh.threads, 0, s>>>(xp, wp, yp, y_f32, nvec, inv_h, eps); break;
     default: return BI_ERR_UNSUPPORTED;
   }
   return cuda_status(cudaGetLastError());
@@ -186,10 +198,11 @@ int rmsnorm_variant_splits(int64_t M, int64_t H, int num_sms) {
   return s;
 }
 
-bi_status launch_rmsnorm_variant(const void* x, const void* w, void* y, int64_t M, int64_t H,
-                                 float eps, int splits, float* ws, int* err, cudaStream_t s) {
+bi_status launch_rmsnorm_variant(const void* x, const void* w, void* y, float* y_f32, int64_t M,
+                                 int64_t H, float eps, int splits, float* ws, int* err,
+                                 cudaStream_t s) {
   if (M == 0) return BI_OK;
-  if (splits <= 1) return launch_rmsnorm_invariant(x, w, y, M, H, eps, err, s);
+  if (splits <= 1) return launch_rmsnorm_invariant(x, w, y, y_f32, M, H, eps, err, s);
   if (M > 65535) return BI_ERR_UNSUPPORTED;
   const int nvec = static_cast<int>(H / 8);
   const int chunk_vec = nvec / splits;
@@ -199,7 +212,7 @@ bi_status launch_rmsnorm_variant(const void* x, const void* w, void* y, int64_t 
                                                  chunk_vec);
   rmsnorm_split_finish<<<grid, threads, 0, s>>>(
       static_cast<const uint4*>(x), static_cast<const uint4*>(w), ws, static_cast<uint4*>(y),
-      nvec, chunk_vec, 1.0f / static_cast<float>(H), eps);
+      y_f32, nvec, chunk_vec, 1.0f / static_cast<float>(H), eps);
   return cuda_status(cudaGetLastError());
 }
 

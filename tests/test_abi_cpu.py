@@ -68,7 +68,7 @@ def test_gemm_variant_split_count(lib):
 
 
 def _call_rms(lib, x, w, y, M, H, eps=1e-6, mode=0, ws=None, wsb=0):
-    return lib.bi_rmsnorm(x, w, y, M, H, eps, mode, ws, wsb, None)
+    return lib.bi_rmsnorm(x, w, y, None, M, H, eps, mode, ws, wsb, None)
 
 
 def test_rmsnorm_argument_checks(lib):

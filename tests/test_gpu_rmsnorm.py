@@ -104,21 +104,24 @@ def worked_example_rows(n, H=4096):
 
 def test_rmsnorm_variant_is_not_batch_invariant(cuda):
     # negative control: the split-row variant reduces a row in 32 chunks at
-    # M = 1 and in one block at M = 1024, so some rows' bytes change with the
-    # batch size; the invariant kernel's bytes do not.  An order change moves
-    # the fp32 sum by a few units in the last place, which flips the bf16
-    # rounding of a handful of elements in a fraction of the rows.
-    H, R = 4096, 1024
+    # M = 1 and in one block at M = 1024.  The two orders round the fp32 sum
+    # of squares differently in a good share of rows; that shows in the fp32
+    # output (y_f32) and only rarely survives the bf16 rounding, since a
+    # bf16 square has at most 16 significant bits.  The invariant kernel's
+    # bytes never move, in either output.
+    H, R = 4096, 256
     x = synth.normal_bf16((R, H), 2400, device=cuda)
     w = torch.ones(H, dtype=torch.bfloat16, device=cuda)
-    inv_ref = bi.rmsnorm(x, w, EPS, bi.INVARIANT)
-    var_ref = bi.rmsnorm(x, w, EPS, bi.VARIANT)      # M = 1024: no split
+    big = torch.cat([x, synth.normal_bf16((1024 - R, H), 2401, device=cuda)])
+    inv_ref, inv_ref32 = bi.rmsnorm(big, w, EPS, bi.INVARIANT, want_f32=True)
+    var_ref, var_ref32 = bi.rmsnorm(big, w, EPS, bi.VARIANT, want_f32=True)  # no split
     differing = 0
     for i in range(R):
         row = x[i:i + 1].contiguous()
-        assert same_bytes(bi.rmsnorm(row, w, EPS, bi.INVARIANT), inv_ref[i:i + 1]), i
-        yv = bi.rmsnorm(row, w, EPS, bi.VARIANT)
-        differing += int(not same_bytes(yv, var_ref[i:i + 1]))
+        yi, yi32 = bi.rmsnorm(row, w, EPS, bi.INVARIANT, want_f32=True)
+        assert same_bytes(yi, inv_ref[i:i + 1]) and same_bytes(yi32, inv_ref32[i:i + 1]), i
+        yv, yv32 = bi.rmsnorm(row, w, EPS, bi.VARIANT, want_f32=True)
+        differing += int(not same_bytes(yv32, var_ref32[i:i + 1]))
     assert differing > 0, "variant mode unexpectedly batch-invariant"
     # the worked example's crafted rows stay within tolerance in both modes
     xc = worked_example_rows(8).to(cuda)
@@ -126,6 +129,15 @@ def test_rmsnorm_variant_is_not_batch_invariant(cuda):
     for mode in (bi.INVARIANT, bi.VARIANT):
         g = f64(bi.rmsnorm(xc, w, EPS, mode))
         check_close(g, r, rms_bound(g, r, H), "worked example mode=%d" % mode)
+
+
+def test_rmsnorm_f32_output_is_the_unrounded_result(cuda):
+    x = synth.normal_bf16((64, 4096), 2500, device=cuda)
+    w = synth.normal_bf16((4096,), 2501, std=0.1, mean=1.0, device=cuda)
+    for M, mode in ((64, bi.INVARIANT), (1, bi.VARIANT), (64, bi.VARIANT)):
+        y, y32 = bi.rmsnorm(x[:M].contiguous(), w, EPS, mode, want_f32=True)
+        assert same_bytes(y, y32.to(torch.bfloat16))
+        assert same_bytes(bi.rmsnorm(x[:M].contiguous(), w, EPS, mode), y)
 
 
 def test_rmsnorm_empty_batch(cuda):
