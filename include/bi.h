@@ -174,6 +174,32 @@ bi_status bi_attn_decode(const void* q, const void* k_cache, const void* v_cache
 size_t bi_attn_decode_workspace_size(int B, int Hq, int Hkv, int D, int max_kv_len,
                                      int split_size, bi_mode mode, int variant_splits);
 
+/* Decode without a caller workspace, for callers that cannot allocate device
+ * memory (an engine that has given all of HBM to its KV-cache pool and
+ * forbids further allocations, a plugin whose host framework owns the
+ * allocator).  The pages describe no such entry point; it is a convenience of
+ * this library.
+ * Same arguments, layout and result as bi_attn_decode in BI_MODE_INVARIANT
+ * (bit-identical output), minus mode and workspace.  The scratch comes from a
+ * fixed array of BI_NOALLOC_SCRATCH_BYTES inside the library, reserved on
+ * every GPU that loads this code until the process exits; the call itself
+ * allocates nothing.
+ * Limit: bi_attn_decode_workspace_size(B, Hq, Hkv, D, max_kv_len, split_size,
+ *   BI_MODE_INVARIANT, 0) must not exceed BI_NOALLOC_SCRATCH_BYTES, else the
+ *   call returns BI_ERR_WORKSPACE and launches nothing.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture begins.
+ * All calls share the array: calls whose kernels overlap on the GPU race with
+ * each other, so order them (e.g. issue them on one stream).
+ * Errors: as bi_attn_decode, plus BI_ERR_WORKSPACE for the size limit. */
+#define BI_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+bi_status bi_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* block_table, const int32_t* kv_lens, void* out,
+                                 float* out_f32, int B, int Hq, int Hkv, int D, int page_size,
+                                 int64_t num_pages, int max_blocks_per_seq, int max_kv_len,
+                                 int split_size, float sm_scale, void* stream);
+
 /* Causal prefill of one chunk per sequence (P1 §5.5, §6.4: a prompt may
  * arrive in chunks; every token's reduction must not depend on the chunking).
  *   q [total_q][Hq][D] bf16: the chunk tokens of all sequences, sequence b

@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libbi.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_BOUNDS, ERR_TIMEOUT = range(7)
 INVARIANT, VARIANT = 0, 1
+NOALLOC_SCRATCH_BYTES = 32 << 20   # BI_NOALLOC_SCRATCH_BYTES in include/bi.h
 
 __all__ = [
     "BiError", "INVARIANT", "VARIANT", "LIB_PATH", "load", "library_path", "OK",
@@ -29,7 +30,7 @@ __all__ = [
     "bi_rmsnorm", "bi_rmsnorm_workspace_size", "bi_gemm", "bi_gemm_workspace_size",
     "bi_gemm_variant_splits", "bi_attn_decode", "bi_attn_decode_workspace_size",
     "bi_attn_prefill_chunk", "bi_kv_write", "bi_check_device_errors", "bi_status_string",
-    "bi_version", "rmsnorm", "gemm", "attn_decode", "attn_prefill_chunk", "kv_write",
+    "bi_version", "bi_attn_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "rmsnorm", "gemm", "attn_decode", "attn_prefill_chunk", "kv_write",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -38,7 +39,7 @@ EXPORTED_SYMBOLS = (
     "bi_rmsnorm", "bi_rmsnorm_workspace_size", "bi_gemm", "bi_gemm_workspace_size",
     "bi_gemm_variant_splits", "bi_attn_decode", "bi_attn_decode_workspace_size",
     "bi_attn_prefill_chunk", "bi_kv_write", "bi_check_device_errors", "bi_status_string",
-    "bi_version",
+    "bi_version", "bi_attn_decode_noalloc",
 )
 
 
@@ -88,6 +89,9 @@ def load(build_if_missing: bool = True):
                                              _i32, _i32, _f32, _i32, _i32, _vp, _sz, _vp]),
             "bi_kv_write": (_i32, [_vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i32,
                                    _i64, _i32, _vp]),
+            "bi_attn_decode_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32,
+                                              _i32, _i32, _i32, _i64, _i32, _i32, _i32, _f32,
+                                              _vp]),
             "bi_check_device_errors": (_i32, [_vp]),
             "bi_status_string": (ctypes.c_char_p, [_i32]),
             "bi_version": (ctypes.c_char_p, []),
@@ -182,6 +186,21 @@ def bi_attn_decode(q, k_cache, v_cache, block_table, kv_lens, out, out_f32=None,
         _ptr(out_f32, torch.float32, "out_f32"), B, Hq, Hkv, D, page, num_pages,
         block_table.shape[1], int(max_kv_len), int(split_size), float(sm_scale), int(mode),
         int(variant_splits), wp, wb, _stream(stream)), "bi_attn_decode")
+
+
+def bi_attn_decode_noalloc(q, k_cache, v_cache, block_table, kv_lens, out, out_f32=None, *,
+                           max_kv_len, split_size, sm_scale, stream=None):
+    """Decode without a workspace argument (scratch from the library's fixed
+    array); for callers that cannot allocate device memory."""
+    B, Hq, D = q.shape
+    num_pages, Hkv, page, _ = k_cache.shape
+    _check(load().bi_attn_decode_noalloc(
+        _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, torch.bfloat16, "k_cache"),
+        _ptr(v_cache, torch.bfloat16, "v_cache"), _ptr(block_table, torch.int32, "block_table"),
+        _ptr(kv_lens, torch.int32, "kv_lens"), _ptr(out, torch.bfloat16, "out"),
+        _ptr(out_f32, torch.float32, "out_f32"), B, Hq, Hkv, D, page, num_pages,
+        block_table.shape[1], int(max_kv_len), int(split_size), float(sm_scale),
+        _stream(stream)), "bi_attn_decode_noalloc")
 
 
 def bi_attn_decode_workspace_size(B, Hq, Hkv, D, max_kv_len, split_size, mode=INVARIANT,
