@@ -147,7 +147,7 @@ int bi_gemm_variant_splits(int64_t M, int64_t N, int64_t K, int num_sms);
  *   or the chunking of a prompt.
  * BI_MODE_VARIANT (fixed split COUNT, the plan the pages reject): the keys
  *   are cut into c chunks at floor(j*L/c), c = variant_splits if > 0, else
- *   chosen from B, Hkv and the SM count.
+ *   c = min(64, max(ceil(2*#SM / (B*Hkv)), ceil(max_kv_len / 1024))).
  * A sequence with L == 0 produces zeros.
  * Requirements: D in {64, 128}; Hq % Hkv == 0 and Hq/Hkv <= 16;
  *   page_size == 16; split_size a positive multiple of 64; num_pages >= 1;
@@ -168,7 +168,11 @@ bi_status bi_attn_decode(const void* q, const void* k_cache, const void* v_cache
                          int variant_splits, void* workspace, size_t workspace_bytes,
                          void* stream);
 
-/* Bytes of workspace bi_attn_decode needs (split partials m, l, o in fp32).
+/* Bytes of workspace bi_attn_decode needs: the unit list of the split plan
+ * (16 bytes per (sequence, split)) and the split partials m, l, o in fp32,
+ * i.e. 256 + up256(16*B*S_max) + up256(8*B*Hq*S_max) + 4*B*Hq*S_max*D with
+ * S_max = ceil(max_kv_len / split_size) (the variant's count in
+ * BI_MODE_VARIANT) and up256 rounding up to a multiple of 256.
  * Host arithmetic, except that BI_MODE_VARIANT with variant_splits <= 0
  * queries the current device's SM count ((size_t)-1 if that fails). */
 size_t bi_attn_decode_workspace_size(int B, int Hq, int Hkv, int D, int max_kv_len,

@@ -240,10 +240,10 @@ size_t bi_attn_decode_workspace_size(int B, int Hq, int Hkv, int D, int max_kv_l
   if (mode == BI_MODE_VARIANT && count <= 0) {
     const int sms = device_sm_count();
     if (sms <= 0) return static_cast<size_t>(-1);
-    count = attn_variant_split_count(B, Hkv, sms);
+    count = attn_variant_split_count(B, Hkv, max_kv_len, sms);
   }
   const int ms = attn_decode_max_splits(max_kv_len, split_size, mode == BI_MODE_VARIANT, count);
-  return static_cast<size_t>(B) * Hq * ms * (static_cast<size_t>(D) + 2) * sizeof(float);
+  return attn_decode_workspace_bytes(B, Hq, D, ms);
 }
 
 bi_status bi_attn_decode(const void* q, const void* k_cache, const void* v_cache,
@@ -268,14 +268,13 @@ bi_status bi_attn_decode(const void* q, const void* k_cache, const void* v_cache
     if (c <= 0) {
       const int sms = device_sm_count();
       if (sms <= 0) return BI_ERR_CUDA;
-      c = attn_variant_split_count(B, Hkv, sms);
+      c = attn_variant_split_count(B, Hkv, max_kv_len, sms);
     }
     a.split_count = c;
   }
   a.max_splits = attn_decode_max_splits(max_kv_len, split_size, a.variant, a.split_count);
   if (a.max_splits > 0) {
-    const size_t need = static_cast<size_t>(B) * Hq * a.max_splits * (static_cast<size_t>(D) + 2) *
-                        sizeof(float);
+    const size_t need = attn_decode_workspace_bytes(B, Hq, D, a.max_splits);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return BI_ERR_WORKSPACE;
   }
   a.ws = static_cast<float*>(workspace);
@@ -313,7 +312,7 @@ bi_status bi_attn_prefill_chunk(const void* q, const int32_t* cu_q, const int32_
     if (c <= 0) {
       const int sms = device_sm_count();
       if (sms <= 0) return BI_ERR_CUDA;
-      c = attn_variant_split_count(B, Hkv, sms);
+      c = attn_variant_split_count(B, Hkv, max_kv_len, sms);
     }
     // chunk-derived split size: the boundaries move with the chunk's length
     const int per = (max_kv_len + c - 1) / c;

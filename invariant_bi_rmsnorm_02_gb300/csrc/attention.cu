@@ -14,22 +14,27 @@
 //     fixed, non-parallel clean-up step).
 //   * New tokens are written into the paged cache before attention runs, so
 //     cached and fresh keys are read from one layout (§5.5).
-// Decode runs one thread block per (sequence, kv head, split) and a separate
-// merge kernel; prefill runs one block per (query block, kv head, sequence)
-// and folds its splits in registers as it goes.  Both call the same tile step
-// and the same fold, so a prefill row at position p is bit-identical to a
-// decode with L = p + 1, whatever the chunking.
+// Decode runs a small plan kernel (the list of (sequence, split) units), a
+// persistent split kernel whose blocks walk that list, and a merge kernel;
+// prefill runs one block per (query block, kv head, sequence) and folds its
+// splits as it goes.  Both call the same tile step and the same fold, so a
+// prefill row at position p is bit-identical to a decode with L = p + 1,
+// whatever the chunking.
 //
-// Arithmetic of the tile step (identical in both kernels): scores by
-// mma.sync m16n8k16 bf16 -> fp32 over D in increasing k; scaling by
-// sm_scale*log2(e) and exp2f; P is split into a bf16 high part and a bf16
-// low part (P - hi) and both are multiplied with V, so the probabilities keep
-// ~16 significant bits; row max / row sum by a fixed shuffle tree.  Explicit
-// __fmul_rn/__fadd_rn keep the compiler from contracting differently in the
-// two kernels.
+// The tile step works on transposed scores: S^T = K Q^T (keys are the MMA's
+// M dimension, query rows its N dimension, 8 per n-tile) and O^T = V^T P^T,
+// with mma.sync m16n8k16 bf16 -> fp32, every sum over k in increasing order.
+// P^T comes from the S^T accumulators by an in-register 8x8 transpose
+// (movmatrix).  A decode row group (the G query heads of one kv head) fills
+// one 8-wide n-tile, so padding costs at most half of an n-tile.  Scores are
+// scaled by sm_scale*log2(e) and exponentiated with exp2f; P is split into a
+// bf16 high part and a bf16 low part (P - hi), both multiplied with V, so the
+// probabilities keep ~16 significant bits.  Column max / sum use a fixed
+// shuffle tree.  Explicit __fmul_rn/__fadd_rn keep the compiler from
+// contracting differently in the two kernels.
 //
-// K/V staging: each 16-token page of one kv head is a contiguous
-// [16][D] bf16 block; a 2-D TMA tensor map over the cache viewed as
+// K/V staging: each 16-token page of one kv head is a contiguous [16][D]
+// bf16 block; a 2-D TMA tensor map over the cache viewed as
 // [num_pages*Hkv*16][D] copies it into shared memory with 128-byte swizzling
 // (one 16x64 box per 64 columns), completion counted on an mbarrier.
 #include <cuda.h>
@@ -48,6 +53,7 @@ constexpr int kTile = 64;              // keys per tile (4 pages)
 constexpr int kPagesPerTile = kTile / kPage;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
+constexpr int kPgRegs = 4;             // page ids held in registers per unit: 32 * 4
 
 template <int D>
 struct TileGeom {
@@ -66,19 +72,22 @@ __device__ __forceinline__ uint32_t tile_off(int n, int d) {
 }
 
 // ----------------------------------------------------------- warp MMA helpers
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr));
 }
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
-                                          uint32_t& r2, uint32_t& r3) {
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr));
 }
-// D(16x8,f32) += A(16x16,bf16,row) * B(16x8,bf16,col)
+__device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+// C(16x8,f32) += A(16x16,bf16,row) * B(16x8,bf16,col)
 __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
   asm volatile(
@@ -89,143 +98,160 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
 }
 
 // ------------------------------------------------------------- split state
-// Per thread: rows g = lane/4 (index 0) and g + 8 (index 1) of the warp's 16
-// rows; o[nd] holds columns 8*nd + 2*(lane%4) + {0,1} of both rows.
-template <int D>
+// NQ n-tiles of 8 query columns.  Per thread, column index cc in {0,1} is
+// query 8*nq + 2*(lane%4) + cc; o[md][nq] holds O^T rows d = 16*md + lane/4
+// (c = 0,1) and d + 8 (c = 2,3), columns 2*(lane%4) + (c & 1).
+template <int D, int NQ>
 struct SplitState {
-  float m[2], l[2];
-  float o[D / 8][4];
+  float m[NQ][2], l[NQ][2];
+  float o[D / 16][NQ][4];
   __device__ __forceinline__ void reset() {
-    m[0] = m[1] = -CUDART_INF_F;
-    l[0] = l[1] = 0.0f;
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+    for (int nq = 0; nq < NQ; ++nq) {
+      m[nq][0] = m[nq][1] = -CUDART_INF_F;
+      l[nq][0] = l[nq][1] = 0.0f;
+#pragma unroll
+      for (int md = 0; md < D / 16; ++md)
+        o[md][nq][0] = o[md][nq][1] = o[md][nq][2] = o[md][nq][3] = 0.0f;
+    }
   }
 };
 
-// Shared address this lane hands to ldmatrix for the Q (A operand, row-major
-// 16 x D, padded rows) fragment of k-step 0; k-step ks adds 32*ks bytes.
-template <int D>
-__device__ __forceinline__ uint32_t q_lane_addr(const __nv_bfloat16* qs) {
+// Q^T fragments (B operand: k = d, n = query) for every k-step from a
+// row-major [8*NQ][stride] bf16 shared tile.
+template <int D, int NQ>
+__device__ __forceinline__ void load_q_frags(uint32_t (&qf)[NQ][D / 16][2],
+                                             const __nv_bfloat16* qs, int stride) {
   const int lane = threadIdx.x & 31;
-  const int row = (lane & 7) + (((lane >> 3) & 1) << 3);
-  const int col = (lane >> 4) << 3;
-  return smem_u32(qs + row * TileGeom<D>::kQStride + col);
+#pragma unroll
+  for (int nq = 0; nq < NQ; ++nq)
+#pragma unroll
+    for (int kp = 0; kp < D / 32; ++kp) {
+      uint32_t r[4];
+      ldsm_x4(smem_u32(qs + (8 * nq + (lane & 7)) * stride + 32 * kp + 8 * (lane >> 3)), r);
+      qf[nq][2 * kp][0] = r[0];
+      qf[nq][2 * kp][1] = r[1];
+      qf[nq][2 * kp + 1][0] = r[2];
+      qf[nq][2 * kp + 1][1] = r[3];
+    }
 }
 
-// One tile of 64 keys (absolute indices key0 .. key0+63) for the warp's 16
-// rows.  Row i sees key k iff lo <= k < hi[i].  A row that sees no key of the
-// tile is left exactly as it was.
-template <int D>
-__device__ __forceinline__ void tile_step(SplitState<D>& st, uint32_t qaddr, uint32_t kbase,
-                                          uint32_t vbase, int key0, int lo, const int (&hi)[2],
-                                          float scale_log2) {
+// One tile of 64 keys (absolute indices key0 .. key0+63).  Query column
+// (nq, cc) sees key k iff lo <= k < hi[nq][cc].  A column that sees no key
+// of the tile is left exactly as it was.
+template <int D, int NQ>
+__device__ __forceinline__ void tile_step(SplitState<D, NQ>& st,
+                                          const uint32_t (&qf)[NQ][D / 16][2], uint32_t kbase,
+                                          uint32_t vbase, int key0, int lo,
+                                          const int (&hi)[NQ][2], float scale_log2) {
   const int lane = threadIdx.x & 31;
-  const int t = lane & 3;
-  // ---- scores S = Q K^T, 8 n-tiles of 8 keys; every score accumulates the
-  // k-steps 0, 1, ..., D/16-1 in that order
-  float s[8][4];
+  const int g = lane >> 2, mi = lane >> 3, r8 = lane & 7;
+  // ---- S^T = K Q^T: 4 m-tiles of 16 keys; each score sums k-steps in order
+  float s[4][NQ][4];
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.0f;
+  for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-  for (int kp = 0; kp < D / 32; ++kp) {
-    uint32_t qa[4], qb[4];
-    ldsm_x4(qaddr + kp * 64, qa[0], qa[1], qa[2], qa[3]);
-    ldsm_x4(qaddr + kp * 64 + 32, qb[0], qb[1], qb[2], qb[3]);
+    for (int nq = 0; nq < NQ; ++nq) s[mt][nq][0] = s[mt][nq][1] = s[mt][nq][2] = s[mt][nq][3] = 0.0f;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      uint32_t b0, b1, b2, b3;
-      const int key = nt * 8 + (lane & 7);
-      const int col = kp * 32 + ((lane >> 3) << 3);
-      ldsm_x4(kbase + tile_off<D>(key, col), b0, b1, b2, b3);
-      mma_bf16(s[nt], qa, b0, b1);
-      mma_bf16(s[nt], qb, b2, b3);
+  for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t a[4];
+      ldsm_x4(kbase + tile_off<D>(16 * mt + r8 + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1)), a);
+#pragma unroll
+      for (int nq = 0; nq < NQ; ++nq) mma_bf16(s[mt][nq], a, qf[nq][ks][0], qf[nq][ks][1]);
+    }
+  // ---- scale, mask, column max
+  float mx[NQ][2];
+#pragma unroll
+  for (int nq = 0; nq < NQ; ++nq) {
+    mx[nq][0] = mx[nq][1] = -CUDART_INF_F;
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int cc = c & 1;
+        const int k = key0 + 16 * mt + g + 8 * (c >> 1);
+        const bool ok = k >= lo && k < hi[nq][cc];
+        const float x = ok ? __fmul_rn(s[mt][nq][c], scale_log2) : -CUDART_INF_F;
+        s[mt][nq][c] = x;
+        mx[nq][cc] = fmaxf(mx[nq][cc], x);
+      }
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      mx[nq][cc] = fmaxf(mx[nq][cc], __shfl_xor_sync(kFull, mx[nq][cc], 4));
+      mx[nq][cc] = fmaxf(mx[nq][cc], __shfl_xor_sync(kFull, mx[nq][cc], 8));
+      mx[nq][cc] = fmaxf(mx[nq][cc], __shfl_xor_sync(kFull, mx[nq][cc], 16));
     }
   }
-  // ---- scale, mask, row max
-  float mx[2] = {-CUDART_INF_F, -CUDART_INF_F};
+  // ---- probabilities, rescale factors, column sums
+  float alpha[NQ][2];
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
+  for (int nq = 0; nq < NQ; ++nq) {
+    float mnew[2];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int ri = c >> 1;
-      const int k = key0 + nt * 8 + 2 * t + (c & 1);
-      const bool ok = k >= lo && k < hi[ri];
-      const float x = ok ? __fmul_rn(s[nt][c], scale_log2) : -CUDART_INF_F;
-      s[nt][c] = x;
-      mx[ri] = fmaxf(mx[ri], x);
+    for (int cc = 0; cc < 2; ++cc) {
+      if (mx[nq][cc] == -CUDART_INF_F) {  // no visible key: exact no-op for this column
+        alpha[nq][cc] = 1.0f;
+        mnew[cc] = st.m[nq][cc];
+      } else {
+        mnew[cc] = fmaxf(st.m[nq][cc], mx[nq][cc]);
+        alpha[nq][cc] =
+            st.m[nq][cc] == -CUDART_INF_F ? 0.0f : exp2f(__fsub_rn(st.m[nq][cc], mnew[cc]));
+      }
+    }
+    float cs[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int cc = c & 1;
+        const float x = s[mt][nq][c];
+        const float pv = x == -CUDART_INF_F ? 0.0f : exp2f(__fsub_rn(x, mnew[cc]));
+        s[mt][nq][c] = pv;
+        cs[cc] = __fadd_rn(cs[cc], pv);
+      }
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      cs[cc] = __fadd_rn(cs[cc], __shfl_xor_sync(kFull, cs[cc], 4));
+      cs[cc] = __fadd_rn(cs[cc], __shfl_xor_sync(kFull, cs[cc], 8));
+      cs[cc] = __fadd_rn(cs[cc], __shfl_xor_sync(kFull, cs[cc], 16));
+      st.l[nq][cc] = __fadd_rn(__fmul_rn(st.l[nq][cc], alpha[nq][cc]), cs[cc]);
+      st.m[nq][cc] = mnew[cc];
     }
 #pragma unroll
-  for (int ri = 0; ri < 2; ++ri) {
-    mx[ri] = fmaxf(mx[ri], __shfl_xor_sync(kFull, mx[ri], 1));
-    mx[ri] = fmaxf(mx[ri], __shfl_xor_sync(kFull, mx[ri], 2));
+    for (int md = 0; md < D / 16; ++md)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) st.o[md][nq][c] = __fmul_rn(st.o[md][nq][c], alpha[nq][c & 1]);
   }
-  // ---- probabilities, rescale factors
-  float alpha[2], mnew[2];
-#pragma unroll
-  for (int ri = 0; ri < 2; ++ri) {
-    if (mx[ri] == -CUDART_INF_F) {  // no visible key: exact no-op for this row
-      alpha[ri] = 1.0f;
-      mnew[ri] = st.m[ri];
-    } else {
-      mnew[ri] = fmaxf(st.m[ri], mx[ri]);
-      alpha[ri] = st.m[ri] == -CUDART_INF_F ? 0.0f : exp2f(__fsub_rn(st.m[ri], mnew[ri]));
-    }
-  }
-  float rs[2] = {0.0f, 0.0f};
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int ri = c >> 1;
-      const float x = s[nt][c];
-      const float p = x == -CUDART_INF_F ? 0.0f : exp2f(__fsub_rn(x, mnew[ri]));
-      s[nt][c] = p;
-      rs[ri] = __fadd_rn(rs[ri], p);
-    }
-#pragma unroll
-  for (int ri = 0; ri < 2; ++ri) {
-    rs[ri] = __fadd_rn(rs[ri], __shfl_xor_sync(kFull, rs[ri], 1));
-    rs[ri] = __fadd_rn(rs[ri], __shfl_xor_sync(kFull, rs[ri], 2));
-    st.l[ri] = __fadd_rn(__fmul_rn(st.l[ri], alpha[ri]), rs[ri]);
-    st.m[ri] = mnew[ri];
-  }
-#pragma unroll
-  for (int nd = 0; nd < D / 8; ++nd) {
-    st.o[nd][0] = __fmul_rn(st.o[nd][0], alpha[0]);
-    st.o[nd][1] = __fmul_rn(st.o[nd][1], alpha[0]);
-    st.o[nd][2] = __fmul_rn(st.o[nd][2], alpha[1]);
-    st.o[nd][3] = __fmul_rn(st.o[nd][3], alpha[1]);
-  }
-  // ---- O += P V with P = hi + lo (two bf16 parts), keys in order
+  // ---- O^T += V^T P^T with P = hi + lo (two bf16 parts), keys in order
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk) {
-    uint32_t ph[4], pl[4];
+    uint32_t bh[NQ][2], bl[NQ][2];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int nt = 2 * kk + (q >> 1);
-      const int c = (q & 1) * 2;
-      const float p0 = s[nt][c], p1 = s[nt][c + 1];
-      const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
-      const float l0 = __fsub_rn(p0, __bfloat162float(h0));
-      const float l1 = __fsub_rn(p1, __bfloat162float(h1));
-      __nv_bfloat162 hh;
-      hh.x = h0;
-      hh.y = h1;
-      ph[q] = *reinterpret_cast<uint32_t*>(&hh);
-      pl[q] = pack_bf16x2(l0, l1);
-    }
+    for (int nq = 0; nq < NQ; ++nq)
 #pragma unroll
-    for (int np = 0; np < D / 16; ++np) {
-      uint32_t b0, b1, b2, b3;
-      const int mi = lane >> 3;
-      const int key = kk * 16 + (lane & 7) + ((mi & 1) << 3);
-      const int col = np * 16 + ((mi >> 1) << 3);
-      ldsm_x4_t(vbase + tile_off<D>(key, col), b0, b1, b2, b3);
-      mma_bf16(st.o[2 * np], ph, b0, b1);
-      mma_bf16(st.o[2 * np], pl, b0, b1);
-      mma_bf16(st.o[2 * np + 1], ph, b2, b3);
-      mma_bf16(st.o[2 * np + 1], pl, b2, b3);
+      for (int half = 0; half < 2; ++half) {
+        const float p0 = s[kk][nq][2 * half], p1 = s[kk][nq][2 * half + 1];
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
+        __nv_bfloat162 hh;
+        hh.x = h0;
+        hh.y = h1;
+        const uint32_t hp = *reinterpret_cast<uint32_t*>(&hh);
+        const uint32_t lp = pack_bf16x2(__fsub_rn(p0, __bfloat162float(h0)),
+                                        __fsub_rn(p1, __bfloat162float(h1)));
+        bh[nq][half] = transpose8x8(hp);
+        bl[nq][half] = transpose8x8(lp);
+      }
+#pragma unroll
+    for (int md = 0; md < D / 16; ++md) {
+      uint32_t a[4];
+      ldsm_x4_t(vbase + tile_off<D>(16 * kk + r8 + 8 * (mi >> 1), 16 * md + 8 * (mi & 1)), a);
+#pragma unroll
+      for (int nq = 0; nq < NQ; ++nq) {
+        mma_bf16(st.o[md][nq], a, bh[nq][0], bh[nq][1]);
+        mma_bf16(st.o[md][nq], a, bl[nq][0], bl[nq][1]);
+      }
     }
   }
 }
@@ -240,25 +266,14 @@ __device__ __forceinline__ float lse_mix(float a, float ca, float b, float cb) {
   return __fadd_rn(__fmul_rn(a, ca), __fmul_rn(b, cb));
 }
 
-__device__ __forceinline__ void store_out(void* out, float* out_f32, int64_t idx, float v0,
-                                          float v1) {
-  *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(out) + idx) = pack_bf16x2(v0, v1);
-  if (out_f32) *reinterpret_cast<float2*>(out_f32 + idx) = make_float2(v0, v1);
-}
-
 // ---------------------------------------------------------------- staging
-// Issue the TMA copies of tile `key0` (pages below `limit` only) into buf.
+// Issue the TMA copies of the first np pages of a tile; page ids in pid.
 template <int D>
-__device__ __forceinline__ void issue_tile(uint8_t* buf, uint64_t* bar, const CUtensorMap* km,
-                                           const CUtensorMap* vm, const int32_t* bt_row,
-                                           int key0, int limit, int Hkv, int h) {
-  int np = 0;
-  for (int p = 0; p < kPagesPerTile; ++p)
-    if (key0 + p * kPage < limit) ++np;
-  mbar_arrive_expect_tx(bar, np * 2 * TileGeom<D>::kPageBytes);
+__device__ __forceinline__ void issue_pages(uint8_t* buf, uint64_t* bar, const CUtensorMap* km,
+                                            const CUtensorMap* vm, const int (&pid)[4], int np,
+                                            int Hkv, int h) {
   for (int p = 0; p < np; ++p) {
-    const int page = bt_row[(key0 >> 4) + p];
-    const int y = (page * Hkv + h) * kPage;
+    const int y = (pid[p] * Hkv + h) * kPage;
 #pragma unroll
     for (int hf = 0; hf < TileGeom<D>::kHalves; ++hf) {
       const int off = (p * TileGeom<D>::kHalves + hf) * 2048;
@@ -266,6 +281,13 @@ __device__ __forceinline__ void issue_tile(uint8_t* buf, uint64_t* bar, const CU
       tma_load_2d(buf + TileGeom<D>::kKBytes + off, vm, hf * 64, y, bar);
     }
   }
+}
+
+__device__ __forceinline__ int pages_below(int key0, int limit) {
+  int np = 0;
+#pragma unroll
+  for (int p = 0; p < kPagesPerTile; ++p) np += (key0 + p * kPage < limit) ? 1 : 0;
+  return np;
 }
 
 // Zero the V rows of keys >= limit in a landed tile (unwritten cache slots may
@@ -304,7 +326,10 @@ struct KernelParams {
   const int32_t* q_start;
   void* out;
   float* out_f32;
-  float* ws;
+  int* unit_count;   // decode plan: number of (sequence, split) units
+  int4* units;       // decode plan: {b, j, lo, hi} per unit
+  float* ml;         // decode partials: {m, l} per (b, q-head, split)
+  float* o;          // decode partials: o[D] per (b, q-head, split)
   int* err;
   int B, Hq, Hkv, G, max_blocks, max_kv_len, split_size, split_count, max_splits;
   int64_t num_pages;
@@ -316,56 +341,91 @@ __device__ __forceinline__ bool len_ok(int L, const KernelParams& p) {
   return L >= 0 && L <= p.max_kv_len && L <= p.max_blocks * kPage;
 }
 
+// --------------------------------------------------------------- decode plan
+// One block: the list of (sequence, split) units, in sequence order.  The
+// fixed split size gives ceil(L/S) units with boundaries at multiples of S;
+// the variant gives `split_count` units at floor(j*L/c) (some may be empty).
+constexpr int kPlanThreads = 1024;
+
+__global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const KernelParams p) {
+  __shared__ int warp_tot[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int chunk = (p.B + kPlanThreads - 1) / kPlanThreads;
+  const int b0 = min(p.B, tid * chunk), b1 = min(p.B, b0 + chunk);
+  int n = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int L = p.kv_lens[b];
+    if (!len_ok(L, p)) {
+      record_error(p.err, BI_ERR_DEVICE_BOUNDS);
+      continue;
+    }
+    if (L > 0) n += p.variant ? p.split_count : (L + p.split_size - 1) / p.split_size;
+  }
+  // block exclusive scan of n
+  int incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = warp_tot[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFull, wi, o);
+      if (lane >= o) wi += v;
+    }
+    warp_tot[lane] = wi - w;  // exclusive
+    if (lane == 31) *p.unit_count = wi;
+  }
+  __syncthreads();
+  int base = warp_tot[warp] + incl - n;
+  for (int b = b0; b < b1; ++b) {
+    const int L = p.kv_lens[b];
+    if (!len_ok(L, p) || L == 0) continue;
+    const int ns = p.variant ? p.split_count : (L + p.split_size - 1) / p.split_size;
+    for (int j = 0; j < ns; ++j) {
+      int lo, hi;
+      if (p.variant) {
+        lo = (int)(((int64_t)j * L) / ns);
+        hi = (int)(((int64_t)(j + 1) * L) / ns);
+      } else {
+        lo = j * p.split_size;
+        hi = min(lo + p.split_size, L);
+      }
+      p.units[base++] = make_int4(b, j, lo, hi);
+    }
+  }
+}
+
 // ------------------------------------------------------------ decode split
-// Block (j, h, b): split j of sequence b, kv head h, all G query heads of the
-// group as rows 0..G-1 of one m16 tile.  One warp.
-template <int D>
+// Persistent: block x takes units u = x, x + gridDim.x, ... of the plan (unit
+// u = split u / Hkv, kv head u % Hkv).  One warp per block; the G query heads
+// of the kv head are the columns of NQ 8-wide n-tiles.  The TMA ring of two
+// tiles runs across unit boundaries; the page ids of the unit being loaded
+// are fetched once into registers.  A unit whose pages are not all in the
+// pool is recorded as BI_ERR_DEVICE_BOUNDS and marked with l = -1.
+constexpr int kQueue = 4;
+
+template <int D, int NQ>
 __global__ void __launch_bounds__(32) attn_decode_split_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const KernelParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* bufs = smem;                                           // 2 tile buffers
-  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(smem + 2 * TileGeom<D>::kBufBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(qs + 16 * TileGeom<D>::kQStride);
+  uint8_t* bufs = smem;  // 2 tile buffers
+  __nv_bfloat16* qbuf = reinterpret_cast<__nv_bfloat16*>(smem + 2 * TileGeom<D>::kBufBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qbuf + 2 * 8 * NQ * D);
+  __shared__ int4 q_unit[kQueue];   // b, j, lo, hi of opened units
+  __shared__ int q_head[kQueue];    // kv head h, or -(h+1) if the unit's pages are bad
 
-  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x;
-  const int L = p.kv_lens[b];
-  if (!len_ok(L, p)) {
-    if (j == 0 && h == 0 && lane == 0) record_error(p.err, BI_ERR_DEVICE_BOUNDS);
-    return;
-  }
-  int lo, hi;
-  if (p.variant) {
-    if (j >= p.split_count) return;
-    lo = (int)(((int64_t)j * L) / p.split_count);
-    hi = (int)(((int64_t)(j + 1) * L) / p.split_count);
-  } else {
-    lo = j * p.split_size;
-    if (lo >= L) return;
-    hi = min(lo + p.split_size, L);
-  }
-  const int G = p.G;
-  const int64_t slot0 = ((int64_t)b * p.Hq + (int64_t)h * G) * p.max_splits + j;
-  float* ws_ml = p.ws;
-  float* ws_o = p.ws + (int64_t)p.B * p.Hq * p.max_splits * 2;
-  const int32_t* bt_row = p.block_table + (int64_t)b * p.max_blocks;
-  const int first_tile = lo & ~(kTile - 1);
-  bool ok = lo < hi && pages_ok(bt_row, first_tile, hi, p.num_pages, lane, 32);
-  ok = __all_sync(kFull, ok);
-  if (!ok) {
-    if (lo < hi && lane == 0) record_error(p.err, BI_ERR_DEVICE_BOUNDS);
-    if (lane < G) {
-      const int64_t slot = slot0 + (int64_t)lane * p.max_splits;
-      ws_ml[2 * slot] = -CUDART_INF_F;
-      ws_ml[2 * slot + 1] = 0.0f;
-    }
-    return;
-  }
-  const int ntiles = (hi - first_tile + kTile - 1) / kTile;
-
+  const int G = p.G, Hkv = p.Hkv;
+  const int U = *p.unit_count * Hkv;
   if (lane == 0) {
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
@@ -373,146 +433,263 @@ __global__ void __launch_bounds__(32) attn_decode_split_kernel(
     mbar_init(&bars[1], 1);
     fence_mbar_init();
   }
-  __syncwarp();
-  if (lane == 0) {
-    issue_tile<D>(bufs, &bars[0], &kmap, &vmap, bt_row, first_tile, hi, p.Hkv, h);
-    if (ntiles > 1)
-      issue_tile<D>(bufs + TileGeom<D>::kBufBytes, &bars[1], &kmap, &vmap, bt_row,
-                    first_tile + kTile, hi, p.Hkv, h);
-  }
-  // Q rows of the group -> padded shared tile (rows >= G are zero)
-  for (int i = lane; i < 16 * (D / 8); i += 32) {
-    const int r = i / (D / 8), c = (i % (D / 8)) * 8;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < G)
-      v = *reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.Hq + h * G + r) * D + c);
-    *reinterpret_cast<uint4*>(qs + r * TileGeom<D>::kQStride + c) = v;
+  // padding query rows G .. 8*NQ-1 stay zero in both buffers
+  {
+    const int pad = (8 * NQ - G) * (D / 8);  // 16-byte chunks per buffer
+    for (int i = lane; i < 2 * pad; i += 32) {
+      const int bsel = i / pad, rem = i % pad;
+      const int r = G + rem / (D / 8), c = (rem % (D / 8)) * 8;
+      *reinterpret_cast<uint4*>(qbuf + (bsel * 8 * NQ + r) * D + c) = make_uint4(0, 0, 0, 0);
+    }
   }
   __syncwarp();
-  const uint32_t qaddr = q_lane_addr<D>(qs);
 
-  SplitState<D> st;
-  st.reset();
-  const int g = lane >> 2;
-  const int hi_r[2] = {g < G ? hi : lo, g + 8 < G ? hi : lo};
-  bool alive = true;
-  int stuck = 0;
-  for (int i = 0; i < ntiles; ++i) {
-    const int bi_ = i & 1;
-    uint8_t* buf = bufs + bi_ * TileGeom<D>::kBufBytes;
-    const bool landed = mbar_wait(&bars[bi_], (i >> 1) & 1, p.err);
-    if (!__all_sync(kFull, landed)) {
-      alive = false;
-      stuck = i;
-      break;
+  // ---- load cursor
+  int lu = blockIdx.x;      // next unit to open
+  bool l_open = false;      // a valid unit is being loaded
+  int l_tile = 0, l_ntiles = 0, l_first = 0, l_hi = 0, l_h = 0, l_b = 0;
+  int pg[kPgRegs];
+  int n_pushed = 0, n_popped = 0, n_issued = 0, n_done = 0, q_issued = 0, q_used = 0;
+
+  auto open_unit = [&]() -> bool {
+    if (n_pushed - n_popped >= kQueue || lu >= U) return false;
+    const int h = lu % Hkv;
+    const int4 d = p.units[lu / Hkv];
+    lu += gridDim.x;
+    const int first = d.z & ~(kTile - 1);
+    const int npg = d.z < d.w ? (d.w - first + kPage - 1) / kPage : 0;
+    const int32_t* bt_row = p.block_table + (int64_t)d.x * p.max_blocks;
+    bool ok = true;
+#pragma unroll
+    for (int k = 0; k < kPgRegs; ++k) {
+      const int idx = lane + 32 * k;
+      pg[k] = idx < npg ? bt_row[(first >> 4) + idx] : 0;
+      if (idx < npg && (pg[k] < 0 || pg[k] >= p.num_pages)) ok = false;
     }
-    const int key0 = first_tile + i * kTile;
-    if (key0 + kTile > hi) {
-      clear_v_tail<D>(buf, key0, hi, lane, 32);
-      __syncwarp();
-    }
-    tile_step<D>(st, qaddr, smem_u32(buf), smem_u32(buf + TileGeom<D>::kKBytes), key0, lo, hi_r,
-                 p.scale_log2);
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (i + 2 < ntiles && lane == 0) {
-      issue_tile<D>(buf, &bars[bi_], &kmap, &vmap, bt_row, key0 + 2 * kTile, hi, p.Hkv, h);
-    }
-  }
-  if (!alive) {
-    // a copy never landed: give the copies still in flight a bounded wait,
-    // mark this split empty and leave
+    if (npg > 32 * kPgRegs &&
+        !pages_ok(bt_row, first + 32 * kPgRegs * kPage, d.w, p.num_pages, lane, 32))
+      ok = false;
+    ok = __all_sync(kFull, ok);
     if (lane == 0) {
-      mbar_wait(&bars[stuck & 1], (stuck >> 1) & 1, nullptr);
-      if (stuck + 1 < ntiles) mbar_wait(&bars[(stuck + 1) & 1], ((stuck + 1) >> 1) & 1, nullptr);
+      q_unit[n_pushed % kQueue] = d;
+      q_head[n_pushed % kQueue] = ok ? h : -(h + 1);
+      if (!ok) record_error(p.err, BI_ERR_DEVICE_BOUNDS);
     }
     __syncwarp();
-    if (lane < G) {
-      const int64_t slot = slot0 + (int64_t)lane * p.max_splits;
-      ws_ml[2 * slot] = -CUDART_INF_F;
-      ws_ml[2 * slot + 1] = 0.0f;
+    ++n_pushed;
+    if (ok && npg > 0) {
+      l_open = true;
+      l_tile = 0;
+      l_first = first;
+      l_ntiles = (d.w - first + kTile - 1) / kTile;
+      l_hi = d.w;
+      l_h = h;
+      l_b = d.x;
     }
-    return;
+    return true;
+  };
+
+  // issue the next tile of the load cursor into the free ring slot, if any
+  auto issue = [&]() {
+    if (n_issued - n_done >= 2) return;
+    while (!l_open) {
+      if (!open_unit()) return;
+    }
+    const int key0 = l_first + l_tile * kTile;
+    const int np = pages_below(key0, l_hi);
+    int pid[4];
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) {
+      const int idx = 4 * l_tile + pp;  // page index within the unit
+      int v = 0;
+#pragma unroll
+      for (int k = 0; k < kPgRegs; ++k) {
+        const int sv = __shfl_sync(kFull, pg[k], idx & 31);
+        if ((idx >> 5) == k) v = sv;
+      }
+      pid[pp] = v;
+    }
+    if (4 * l_tile + 4 > 32 * kPgRegs) {  // long split: page ids past the registers
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp)
+        if (4 * l_tile + pp >= 32 * kPgRegs && pp < np)
+          pid[pp] =
+              p.block_table[(int64_t)l_b * p.max_blocks + (l_first >> 4) + 4 * l_tile + pp];
+    }
+    const int slot = n_issued & 1;
+    if (lane == 0) {
+      uint8_t* buf = bufs + slot * TileGeom<D>::kBufBytes;
+      const uint32_t qbytes = l_tile == 0 ? (uint32_t)(G * D * 2) : 0u;
+      mbar_arrive_expect_tx(&bars[slot], np * 2 * TileGeom<D>::kPageBytes + qbytes);
+      if (l_tile == 0)
+        bulk_load(qbuf + (q_issued & 1) * 8 * NQ * D,
+                  p.q + ((int64_t)l_b * p.Hq + (int64_t)l_h * G) * D, qbytes, &bars[slot]);
+      issue_pages<D>(buf, &bars[slot], &kmap, &vmap, pid, np, Hkv, l_h);
+    }
+    if (l_tile == 0) ++q_issued;
+    ++n_issued;
+    if (++l_tile == l_ntiles) l_open = false;
+  };
+
+  issue();
+  issue();
+  SplitState<D, NQ> st;
+  uint32_t qf[NQ][D / 16][2];
+  const int g = lane >> 2, t = lane & 3;
+  bool alive = true;
+  while (alive) {
+    if (n_popped == n_pushed) {
+      issue();  // opens the next units (and loads their first tile) if any are left
+      if (n_popped == n_pushed) break;
+    }
+    const int4 d = q_unit[n_popped % kQueue];
+    const int hv = q_head[n_popped % kQueue];
+    const bool pages_good = hv >= 0;
+    const int h = pages_good ? hv : -hv - 1;
+    const int b = d.x, j = d.y, lo = d.z, hi = d.w;
+    if (!pages_good || lo >= hi) {
+      // bad pages (l = -1 makes the merge emit zeros) or an empty split
+      if (lane < G) {
+        const int64_t s = ((int64_t)b * p.Hq + (int64_t)h * G + lane) * p.max_splits + j;
+        p.ml[2 * s] = -CUDART_INF_F;
+        p.ml[2 * s + 1] = pages_good ? 0.0f : -1.0f;
+      }
+      ++n_popped;
+      issue();
+      continue;
+    }
+    const int64_t slot0 = ((int64_t)b * p.Hq + (int64_t)h * G) * p.max_splits + j;
+    const int first = lo & ~(kTile - 1);
+    const int ntiles = (hi - first + kTile - 1) / kTile;
+    int hcol[NQ][2];
+#pragma unroll
+    for (int nq = 0; nq < NQ; ++nq)
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) hcol[nq][cc] = (8 * nq + 2 * t + cc) < G ? hi : lo;
+    for (int ti = 0; ti < ntiles; ++ti) {
+      const int slot = n_done & 1;
+      const bool landed = mbar_wait(&bars[slot], (n_done >> 1) & 1, p.err);
+      if (!__all_sync(kFull, landed)) {
+        alive = false;
+        break;
+      }
+      uint8_t* buf = bufs + slot * TileGeom<D>::kBufBytes;
+      if (ti == 0) {
+        load_q_frags<D, NQ>(qf, qbuf + (q_used & 1) * 8 * NQ * D, D);
+        ++q_used;
+        st.reset();
+      }
+      const int key0 = first + ti * kTile;
+      if (key0 + kTile > hi) {
+        clear_v_tail<D>(buf, key0, hi, lane, 32);
+        __syncwarp();
+      }
+      tile_step<D, NQ>(st, qf, smem_u32(buf), smem_u32(buf + TileGeom<D>::kKBytes), key0, lo,
+                       hcol, p.scale_log2);
+      ++n_done;
+      fence_proxy_async_smem();
+      __syncwarp();
+      issue();
+    }
+    if (!alive) break;
+    // ---- partial state of the valid columns
+#pragma unroll
+    for (int nq = 0; nq < NQ; ++nq)
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int col = 8 * nq + 2 * t + cc;
+        if (col >= G) continue;
+        const int64_t s = slot0 + (int64_t)col * p.max_splits;
+        if (g == 0) {
+          p.ml[2 * s] = st.m[nq][cc];
+          p.ml[2 * s + 1] = st.l[nq][cc];
+        }
+        float* orow = p.o + s * D;
+#pragma unroll
+        for (int md = 0; md < D / 16; ++md) {
+          orow[16 * md + g] = st.o[md][nq][cc];
+          orow[16 * md + g + 8] = st.o[md][nq][2 + cc];
+        }
+      }
+    ++n_popped;
   }
-  // ---- write the partial state of rows < G
-  const int t = lane & 3;
-#pragma unroll
-  for (int ri = 0; ri < 2; ++ri) {
-    const int r = g + 8 * ri;
-    if (r >= G) continue;
-    const int64_t slot = slot0 + (int64_t)r * p.max_splits;
-    if (t == 0) {
-      ws_ml[2 * slot] = st.m[ri];
-      ws_ml[2 * slot + 1] = st.l[ri];
-    }
-    float* orow = ws_o + slot * D;
-#pragma unroll
-    for (int nd = 0; nd < D / 8; ++nd)
-      *reinterpret_cast<float2*>(orow + nd * 8 + 2 * t) =
-          make_float2(st.o[nd][2 * ri], st.o[nd][2 * ri + 1]);
+  if (!alive && lane == 0) {
+    // a copy never landed: give the copies still in flight a bounded wait
+    for (int i = n_done; i < n_issued; ++i) mbar_wait(&bars[i & 1], (i >> 1) & 1, nullptr);
   }
 }
 
 // ------------------------------------------------------------ decode merge
 // Block (qh, b), D/2 threads: left fold over the splits in index order, then
-// o / l.  Empty splits (variant plan at L < count) are skipped.
+// o / l.  Empty splits are skipped; a split marked l = -1 (bad pages) makes
+// the whole row zero.
 template <int D>
 __global__ void __launch_bounds__(64) attn_decode_merge_kernel(const KernelParams p) {
   const int qh = blockIdx.x, b = blockIdx.y;
   const int d = threadIdx.x * 2;
   const int64_t row = (int64_t)b * p.Hq + qh;
+  const int64_t oidx = row * D + d;
   const int L = p.kv_lens[b];
-  if (!len_ok(L, p) || L == 0) {
-    store_out(p.out, p.out_f32, row * D + d, 0.0f, 0.0f);
-    return;
-  }
-  const int ns = p.variant ? p.split_count : (L + p.split_size - 1) / p.split_size;
-  const float* ml = p.ws + row * p.max_splits * 2;
-  const float* ob = p.ws + (int64_t)p.B * p.Hq * p.max_splits * 2 + row * p.max_splits * D;
-  float m = -CUDART_INF_F, l = 0.0f, o0 = 0.0f, o1 = 0.0f;
-  bool have = false;
-  for (int j = 0; j < ns; ++j) {
-    const float mj = ml[2 * j], lj = ml[2 * j + 1];
-    if (mj == -CUDART_INF_F) continue;  // empty split
-    const float2 oj = *reinterpret_cast<const float2*>(ob + (int64_t)j * D + d);
-    if (!have) {
-      m = mj; l = lj; o0 = oj.x; o1 = oj.y;
-      have = true;
-    } else {
-      float mn, ca, cb;
-      lse_coeffs(m, mj, mn, ca, cb);
-      l = lse_mix(l, ca, lj, cb);
-      o0 = lse_mix(o0, ca, oj.x, cb);
-      o1 = lse_mix(o1, ca, oj.y, cb);
-      m = mn;
+  float r0 = 0.0f, r1 = 0.0f;
+  if (len_ok(L, p) && L > 0) {
+    const int ns = p.variant ? p.split_count : (L + p.split_size - 1) / p.split_size;
+    const float* ml = p.ml + row * p.max_splits * 2;
+    const float* ob = p.o + row * p.max_splits * D;
+    float m = -CUDART_INF_F, l = 0.0f, o0 = 0.0f, o1 = 0.0f;
+    bool have = false, bad = false;
+    for (int j = 0; j < ns; ++j) {
+      const float mj = ml[2 * j], lj = ml[2 * j + 1];
+      if (lj < 0.0f) bad = true;
+      if (mj == -CUDART_INF_F) continue;  // empty split
+      const float2 oj = *reinterpret_cast<const float2*>(ob + (int64_t)j * D + d);
+      if (!have) {
+        m = mj;
+        l = lj;
+        o0 = oj.x;
+        o1 = oj.y;
+        have = true;
+      } else {
+        float mn, ca, cb;
+        lse_coeffs(m, mj, mn, ca, cb);
+        l = lse_mix(l, ca, lj, cb);
+        o0 = lse_mix(o0, ca, oj.x, cb);
+        o1 = lse_mix(o1, ca, oj.y, cb);
+        m = mn;
+      }
+    }
+    if (have && !bad) {
+      r0 = __fdiv_rn(o0, l);
+      r1 = __fdiv_rn(o1, l);
     }
   }
-  if (!have) {
-    store_out(p.out, p.out_f32, row * D + d, 0.0f, 0.0f);
-    return;
-  }
-  store_out(p.out, p.out_f32, row * D + d, __fdiv_rn(o0, l), __fdiv_rn(o1, l));
+  *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.out) + oidx) = pack_bf16x2(r0, r1);
+  if (p.out_f32) *reinterpret_cast<float2*>(p.out_f32 + oidx) = make_float2(r0, r1);
 }
 
 // ------------------------------------------------------------- prefill
-// Block (qb, h, b): kNW warps; each warp owns 16 rows = TPW tokens x G heads
-// of query block qb of sequence b, kv head h.  Tiles of 64 keys are staged
-// once per block and shared by the warps; splits are folded in registers.
+// Block (qb, h, b): kPrefillWarps warps; each warp owns 16 query columns =
+// TPW tokens x G heads of query block qb of sequence b, kv head h (two 8-wide
+// n-tiles).  Tiles of 64 keys are staged once per block and shared by the
+// warps; splits are folded as they complete, with the merged state of each
+// warp's columns kept in shared memory.
 constexpr int kPrefillWarps = 8;
+constexpr int kPrefillNQ = 2;
 
 template <int D>
 __global__ void __launch_bounds__(kPrefillWarps * 32, 1) attn_prefill_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const KernelParams p) {
+  constexpr int NQ = kPrefillNQ;
+  constexpr int NV = (D / 16) * NQ * 4;  // o values per thread
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* bufs = smem;
   __nv_bfloat16* qs_all = reinterpret_cast<__nv_bfloat16*>(smem + 2 * TileGeom<D>::kBufBytes);
-  // merged state of each warp's rows, thread-private: value i of lane l at
-  // [i * 32 + l] (i = 4 * nd + c, as in SplitState::o)
+  // merged state of each warp's columns, thread-private: value i of lane l at
+  // [i * 32 + l]; reused at the end to stage the output rows
   float* mg_all = reinterpret_cast<float*>(qs_all + kPrefillWarps * 16 * TileGeom<D>::kQStride);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(mg_all + kPrefillWarps * (D / 2) * 32);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(mg_all + kPrefillWarps * NV * 32);
   __shared__ int s_abort;
 
   const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -542,6 +719,16 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 1) attn_prefill_kernel(
       return;
     }
   }
+  auto issue_tile = [&](int i) {  // thread 0 only
+    uint8_t* buf = bufs + (i & 1) * TileGeom<D>::kBufBytes;
+    const int key0 = i * kTile;
+    const int np = pages_below(key0, kvl);
+    int pid[4];
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) pid[pp] = pp < np ? bt_row[(key0 >> 4) + pp] : 0;
+    mbar_arrive_expect_tx(&bars[i & 1], np * 2 * TileGeom<D>::kPageBytes);
+    issue_pages<D>(buf, &bars[i & 1], &kmap, &vmap, pid, np, p.Hkv, h);
+  };
   if (tid == 0) {
     s_abort = 0;
     prefetch_tmap(&kmap);
@@ -552,12 +739,10 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 1) attn_prefill_kernel(
   }
   __syncthreads();
   if (tid == 0) {
-    issue_tile<D>(bufs, &bars[0], &kmap, &vmap, bt_row, 0, kvl, p.Hkv, h);
-    if (ntiles > 1)
-      issue_tile<D>(bufs + TileGeom<D>::kBufBytes, &bars[1], &kmap, &vmap, bt_row, kTile, kvl,
-                    p.Hkv, h);
+    issue_tile(0);
+    if (ntiles > 1) issue_tile(1);
   }
-  // this warp's rows: row r -> token r / G, head r % G of the group
+  // this warp's columns: column r -> token r / G, head r % G of the group
   __nv_bfloat16* qs = qs_all + warp * 16 * TileGeom<D>::kQStride;
   for (int i = lane; i < 16 * (D / 8); i += 32) {
     const int r = i / (D / 8), c = (i % (D / 8)) * 8;
@@ -569,20 +754,31 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 1) attn_prefill_kernel(
     *reinterpret_cast<uint4*>(qs + r * TileGeom<D>::kQStride + c) = v;
   }
   __syncwarp();
-  const uint32_t qaddr = q_lane_addr<D>(qs);
+  uint32_t qf[NQ][D / 16][2];
+  load_q_frags<D, NQ>(qf, qs, TileGeom<D>::kQStride);
 
-  const int g = lane >> 2, t = lane & 3;
-  int pos[2];  // absolute position of the two rows, -1 for padding rows
+  const int t = lane & 3;
+  int pos[NQ][2];  // absolute position of each column, -1 for padding
 #pragma unroll
-  for (int ri = 0; ri < 2; ++ri) {
-    const int r = g + 8 * ri;
-    const int tk = warp * TPW + r / G;
-    pos[ri] = (r < TPW * G && tk < ntok) ? start + tok0 + tk : -1;
-  }
-  float* mgo = mg_all + warp * (D / 2) * 32 + lane;
-  SplitState<D> st;  // current split
-  float mg_m[2] = {-CUDART_INF_F, -CUDART_INF_F}, mg_l[2] = {0.0f, 0.0f};
-  bool have[2] = {false, false};
+  for (int nq = 0; nq < NQ; ++nq)
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      const int r = 8 * nq + 2 * t + cc;
+      const int tk = warp * TPW + r / G;
+      pos[nq][cc] = (r < TPW * G && tk < ntok) ? start + tok0 + tk : -1;
+    }
+  float* mgo = mg_all + warp * NV * 32 + lane;
+  SplitState<D, NQ> st;
+  float mg_m[NQ][2], mg_l[NQ][2];
+  bool have[NQ][2];
+#pragma unroll
+  for (int nq = 0; nq < NQ; ++nq)
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      mg_m[nq][cc] = -CUDART_INF_F;
+      mg_l[nq][cc] = 0.0f;
+      have[nq][cc] = false;
+    }
   const int S = p.split_size;
   for (int i = 0; i < ntiles; ++i) {
     const int bi_ = i & 1;
@@ -590,7 +786,7 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 1) attn_prefill_kernel(
     const int key0 = i * kTile;
     const int lo = (key0 / S) * S;  // split start
     if (key0 == lo) st.reset();
-    bool landed = mbar_wait(&bars[bi_], (i >> 1) & 1, p.err, &s_abort);
+    const bool landed = mbar_wait(&bars[bi_], (i >> 1) & 1, p.err, &s_abort);
     if (__syncthreads_or(!landed)) {
       if (tid == 0) {
         s_abort = 1;
@@ -604,59 +800,89 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 1) attn_prefill_kernel(
       clear_v_tail<D>(buf, key0, kvl, tid, blockDim.x);
       __syncthreads();
     }
-    int hi_r[2];
+    int hcol[NQ][2];
 #pragma unroll
-    for (int ri = 0; ri < 2; ++ri) hi_r[ri] = pos[ri] >= lo ? min(lo + S, pos[ri] + 1) : lo;
-    tile_step<D>(st, qaddr, smem_u32(buf), smem_u32(buf + TileGeom<D>::kKBytes), key0, lo, hi_r,
-                 p.scale_log2);
+    for (int nq = 0; nq < NQ; ++nq)
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc)
+        hcol[nq][cc] = pos[nq][cc] >= lo ? min(lo + S, pos[nq][cc] + 1) : lo;
+    tile_step<D, NQ>(st, qf, smem_u32(buf), smem_u32(buf + TileGeom<D>::kKBytes), key0, lo, hcol,
+                     p.scale_log2);
     fence_proxy_async_smem();
     __syncthreads();
-    if (i + 2 < ntiles && tid == 0) {
-      issue_tile<D>(buf, &bars[bi_], &kmap, &vmap, bt_row, key0 + 2 * kTile, kvl, p.Hkv, h);
-    }
-    // end of split: fold it into the merged state (rows that reach it)
+    if (i + 2 < ntiles && tid == 0) issue_tile(i + 2);
+    // end of split: fold it into the merged state (columns that reach it)
     if (key0 + kTile == lo + S || i + 1 == ntiles) {
 #pragma unroll
-      for (int ri = 0; ri < 2; ++ri) {
-        if (pos[ri] < lo) continue;
-        if (!have[ri]) {
-          mg_m[ri] = st.m[ri];
-          mg_l[ri] = st.l[ri];
+      for (int nq = 0; nq < NQ; ++nq)
 #pragma unroll
-          for (int nd = 0; nd < D / 8; ++nd) {
-            mgo[(4 * nd + 2 * ri) * 32] = st.o[nd][2 * ri];
-            mgo[(4 * nd + 2 * ri + 1) * 32] = st.o[nd][2 * ri + 1];
-          }
-          have[ri] = true;
-        } else {
-          float mn, ca, cb;
-          lse_coeffs(mg_m[ri], st.m[ri], mn, ca, cb);
-          mg_l[ri] = lse_mix(mg_l[ri], ca, st.l[ri], cb);
+        for (int cc = 0; cc < 2; ++cc) {
+          if (pos[nq][cc] < lo) continue;
+          if (!have[nq][cc]) {
+            mg_m[nq][cc] = st.m[nq][cc];
+            mg_l[nq][cc] = st.l[nq][cc];
 #pragma unroll
-          for (int nd = 0; nd < D / 8; ++nd) {
-            float* a0 = &mgo[(4 * nd + 2 * ri) * 32];
-            float* a1 = &mgo[(4 * nd + 2 * ri + 1) * 32];
-            *a0 = lse_mix(*a0, ca, st.o[nd][2 * ri], cb);
-            *a1 = lse_mix(*a1, ca, st.o[nd][2 * ri + 1], cb);
+            for (int md = 0; md < D / 16; ++md)
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf)
+                mgo[((md * NQ + nq) * 4 + 2 * hf + cc) * 32] = st.o[md][nq][2 * hf + cc];
+            have[nq][cc] = true;
+          } else {
+            float mn, ca, cb;
+            lse_coeffs(mg_m[nq][cc], st.m[nq][cc], mn, ca, cb);
+            mg_l[nq][cc] = lse_mix(mg_l[nq][cc], ca, st.l[nq][cc], cb);
+#pragma unroll
+            for (int md = 0; md < D / 16; ++md)
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                float* a = &mgo[((md * NQ + nq) * 4 + 2 * hf + cc) * 32];
+                *a = lse_mix(*a, ca, st.o[md][nq][2 * hf + cc], cb);
+              }
+            mg_m[nq][cc] = mn;
           }
-          mg_m[ri] = mn;
         }
-      }
     }
   }
   if (s_abort) return;
-  // ---- out = o / l for the real rows
+  // ---- out = o / l; stage the warp's rows as [column][d] fp32, then store
+  float res[NV];
 #pragma unroll
-  for (int ri = 0; ri < 2; ++ri) {
-    if (pos[ri] < 0) continue;
-    const int r = g + 8 * ri;
+  for (int md = 0; md < D / 16; ++md)
+#pragma unroll
+    for (int nq = 0; nq < NQ; ++nq)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int i = (md * NQ + nq) * 4 + c;
+        res[i] = pos[nq][c & 1] < 0 ? 0.0f : __fdiv_rn(mgo[i * 32], mg_l[nq][c & 1]);
+      }
+  __syncwarp();
+  float* stage = mg_all + warp * NV * 32;  // [16 columns][D]
+  const int g = lane >> 2;
+#pragma unroll
+  for (int md = 0; md < D / 16; ++md)
+#pragma unroll
+    for (int nq = 0; nq < NQ; ++nq)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int col = 8 * nq + 2 * t + (c & 1);
+        const int d = 16 * md + g + 8 * (c >> 1);
+        stage[col * D + d] = res[(md * NQ + nq) * 4 + c];
+      }
+  __syncwarp();
+  for (int i = lane; i < 16 * (D / 8); i += 32) {
+    const int r = i / (D / 8), c8 = (i % (D / 8)) * 8;
     const int tk = warp * TPW + r / G;
-    const int64_t orow = ((int64_t)(q_begin + tok0 + tk) * p.Hq + h * G + r % G) * D;
-#pragma unroll
-    for (int nd = 0; nd < D / 8; ++nd)
-      store_out(p.out, p.out_f32, orow + nd * 8 + 2 * t,
-                __fdiv_rn(mgo[(4 * nd + 2 * ri) * 32], mg_l[ri]),
-                __fdiv_rn(mgo[(4 * nd + 2 * ri + 1) * 32], mg_l[ri]));
+    if (r >= TPW * G || tk >= ntok) continue;
+    const int64_t orow = ((int64_t)(q_begin + tok0 + tk) * p.Hq + h * G + r % G) * D + c8;
+    const float4 v0 = *reinterpret_cast<const float4*>(stage + r * D + c8);
+    const float4 v1 = *reinterpret_cast<const float4*>(stage + r * D + c8 + 4);
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow) =
+        make_uint4(pack_bf16x2(v0.x, v0.y), pack_bf16x2(v0.z, v0.w), pack_bf16x2(v1.x, v1.y),
+                   pack_bf16x2(v1.z, v1.w));
+    if (p.out_f32) {
+      *reinterpret_cast<float4*>(p.out_f32 + orow) = v0;
+      *reinterpret_cast<float4*>(p.out_f32 + orow + 4) = v1;
+    }
   }
 }
 
@@ -687,14 +913,14 @@ __global__ void kv_write_kernel(const uint4* __restrict__ k_new, const uint4* __
   }
 }
 
-template <int D>
+template <int D, int NQ>
 size_t decode_smem() {
-  return 1024 + 2 * TileGeom<D>::kBufBytes + 16 * TileGeom<D>::kQStride * 2 + 64;
+  return 1024 + 2 * TileGeom<D>::kBufBytes + 2 * 8 * NQ * D * 2 + 64;
 }
 template <int D>
 size_t prefill_smem() {
   return 1024 + 2 * TileGeom<D>::kBufBytes + kPrefillWarps * 16 * TileGeom<D>::kQStride * 2 +
-         kPrefillWarps * (D / 2) * 32 * 4 + 64;
+         kPrefillWarps * (D / 16) * kPrefillNQ * 4 * 32 * 4 + 64;
 }
 
 KernelParams make_params(const AttnArgs& a) {
@@ -706,7 +932,6 @@ KernelParams make_params(const AttnArgs& a) {
   p.q_start = a.q_start;
   p.out = a.out;
   p.out_f32 = a.out_f32;
-  p.ws = a.ws;
   p.err = a.err;
   p.B = a.B;
   p.Hq = a.Hq;
@@ -735,16 +960,47 @@ cudaError_t set_smem(K kernel, size_t bytes) {
                               static_cast<int>(bytes));
 }
 
-template <int D>
+// Workspace carve-up for decode: [unit count | units | {m,l} | o].
+struct DecodeWs {
+  size_t units_off, ml_off, o_off, total;
+};
+DecodeWs decode_ws_layout(int B, int Hq, int D, int max_splits) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  DecodeWs w;
+  const size_t slots = static_cast<size_t>(B) * Hq * max_splits;
+  w.units_off = 256;
+  w.ml_off = w.units_off + up(static_cast<size_t>(B) * max_splits * sizeof(int4));
+  w.o_off = w.ml_off + up(slots * 2 * sizeof(float));
+  w.total = w.o_off + slots * D * sizeof(float);
+  return w;
+}
+
+template <int D, int NQ>
 bi_status decode_impl(const AttnArgs& a, cudaStream_t s) {
-  CUtensorMap km, vm;
-  if (!make_kv_maps(a, &km, &vm)) return BI_ERR_CUDA;
-  const KernelParams p = make_params(a);
+  KernelParams p = make_params(a);
   if (a.max_splits > 0) {
-    const size_t sm = decode_smem<D>();
-    if (set_smem(attn_decode_split_kernel<D>, sm) != cudaSuccess) return BI_ERR_CUDA;
-    const dim3 grid(a.max_splits, a.Hkv, a.B);
-    attn_decode_split_kernel<D><<<grid, 32, sm, s>>>(km, vm, p);
+    CUtensorMap km, vm;
+    if (!make_kv_maps(a, &km, &vm)) return BI_ERR_CUDA;
+    const DecodeWs w = decode_ws_layout(a.B, a.Hq, a.D, a.max_splits);
+    char* base = reinterpret_cast<char*>(a.ws);
+    p.unit_count = reinterpret_cast<int*>(base);
+    p.units = reinterpret_cast<int4*>(base + w.units_off);
+    p.ml = reinterpret_cast<float*>(base + w.ml_off);
+    p.o = reinterpret_cast<float*>(base + w.o_off);
+    attn_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+    const size_t sm = decode_smem<D, NQ>();
+    if (set_smem(attn_decode_split_kernel<D, NQ>, sm) != cudaSuccess) return BI_ERR_CUDA;
+    static int per_sm[2][3] = {};
+    int& occ = per_sm[D == 128][NQ];
+    if (occ == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                        &occ, attn_decode_split_kernel<D, NQ>, 32, sm) != cudaSuccess)
+      return BI_ERR_CUDA;
+    const int sms = device_sm_count();
+    if (sms <= 0 || occ <= 0) return BI_ERR_CUDA;
+    const int64_t max_units = static_cast<int64_t>(a.B) * a.Hkv * a.max_splits;
+    const int64_t cap = static_cast<int64_t>(occ) * sms;
+    const int grid = static_cast<int>(max_units < cap ? max_units : cap);
+    attn_decode_split_kernel<D, NQ><<<grid, 32, sm, s>>>(km, vm, p);
   }
   attn_decode_merge_kernel<D><<<dim3(a.Hq, a.B), D / 2, 0, s>>>(p);
   return cuda_status(cudaGetLastError());
@@ -766,10 +1022,13 @@ bi_status prefill_impl(const AttnArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-int attn_variant_split_count(int B, int Hkv, int num_sms) {
-  // FlashDecoding-style: enough splits that B * Hkv * c blocks cover the SMs twice
+int attn_variant_split_count(int B, int Hkv, int max_kv_len, int num_sms) {
+  // one count for the whole batch: enough units to cover the SMs twice, and
+  // at least one per 1024 keys of the longest sequence
   const int64_t units = static_cast<int64_t>(B) * Hkv;
   int64_t c = (2 * static_cast<int64_t>(num_sms) + units - 1) / (units > 0 ? units : 1);
+  const int64_t by_len = (static_cast<int64_t>(max_kv_len) + 1023) / 1024;
+  if (by_len > c) c = by_len;
   if (c < 1) c = 1;
   if (c > 64) c = 64;
   return static_cast<int>(c);
@@ -781,9 +1040,15 @@ int attn_decode_max_splits(int max_kv_len, int split_size, bool variant, int spl
   return (max_kv_len + split_size - 1) / split_size;
 }
 
+size_t attn_decode_workspace_bytes(int B, int Hq, int D, int max_splits) {
+  if (B <= 0 || max_splits <= 0) return 0;
+  return decode_ws_layout(B, Hq, D, max_splits).total;
+}
+
 bi_status launch_attn_decode(const AttnArgs& a, cudaStream_t s) {
-  if (a.D == 64) return decode_impl<64>(a, s);
-  if (a.D == 128) return decode_impl<128>(a, s);
+  const int G = a.Hq / a.Hkv;
+  if (a.D == 64) return G <= 8 ? decode_impl<64, 1>(a, s) : decode_impl<64, 2>(a, s);
+  if (a.D == 128) return G <= 8 ? decode_impl<128, 1>(a, s) : decode_impl<128, 2>(a, s);
   return BI_ERR_UNSUPPORTED;
 }
 

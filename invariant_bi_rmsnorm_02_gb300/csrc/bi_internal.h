@@ -65,7 +65,8 @@ struct AttnArgs {
   int* err;
 };
 int attn_decode_max_splits(int max_kv_len, int split_size, bool variant, int split_count);
-int attn_variant_split_count(int B, int Hkv, int num_sms);
+int attn_variant_split_count(int B, int Hkv, int max_kv_len, int num_sms);
+size_t attn_decode_workspace_bytes(int B, int Hq, int D, int max_splits);
 bi_status launch_attn_decode(const AttnArgs& a, cudaStream_t s);
 bi_status launch_attn_prefill(const AttnArgs& a, cudaStream_t s);
 bi_status launch_kv_write(const void* k_new, const void* v_new, const int32_t* seq,

@@ -115,19 +115,35 @@ struct GemmParams {
   int* err;
   int M, N, K;
   int m_tiles, n_tiles, splits, kb_total, kb_per_split;
+  int group;      // tiles of the L2-resident operand per raster group
+  int m_fast;     // 1: A rows stay resident, W streams; 0: the other way round
 };
 
 struct Unit {
   int m_tile, n_tile, split, kb0, kb1;
 };
 
+// Tile order (it never changes a tile's arithmetic, only which block runs
+// it and when): the smaller operand is kept resident in L2 in groups of
+// `group` tiles while the other one streams past it once per group.
 __device__ __forceinline__ Unit unit_of(int u, const GemmParams& p) {
   const int tiles = p.m_tiles * p.n_tiles;
   Unit w;
   w.split = u / tiles;
   const int r = u - w.split * tiles;
-  w.n_tile = r % p.n_tiles;  // n fastest: concurrent blocks share A rows, W stays in L2
-  w.m_tile = r / p.n_tiles;
+  if (p.m_fast) {
+    const int per = p.group * p.n_tiles;
+    const int g = r / per, rr = r - g * per;
+    const int gs = min(p.group, p.m_tiles - g * p.group);
+    w.n_tile = rr / gs;
+    w.m_tile = g * p.group + rr % gs;
+  } else {
+    const int per = p.group * p.m_tiles;
+    const int g = r / per, rr = r - g * per;
+    const int gs = min(p.group, p.n_tiles - g * p.group);
+    w.m_tile = rr / gs;
+    w.n_tile = g * p.group + rr % gs;
+  }
   w.kb0 = w.split * p.kb_per_split;
   w.kb1 = min(w.kb0 + p.kb_per_split, p.kb_total);
   return w;
@@ -359,6 +375,14 @@ bi_status launch_gemm(const void* A, const void* W, void* C, int64_t M, int64_t 
   if (splits > p.kb_total) splits = p.kb_total;
   p.kb_per_split = (p.kb_total + splits - 1) / splits;
   p.splits = (p.kb_total + p.kb_per_split - 1) / p.kb_per_split;  // no empty slice
+  // raster: keep the smaller operand in L2 (about 40 MB of it per group)
+  const int64_t resident_budget = int64_t(40) << 20;
+  p.m_fast = M <= N ? 1 : 0;
+  const int64_t tile_bytes = static_cast<int64_t>(p.m_fast ? BM : BN) * K * 2;
+  int64_t grp = resident_budget / (tile_bytes > 0 ? tile_bytes : 1);
+  if (grp < 1) grp = 1;
+  const int span = p.m_fast ? p.m_tiles : p.n_tiles;
+  p.group = static_cast<int>(grp < span ? grp : span);
   const int64_t units = static_cast<int64_t>(p.m_tiles) * p.n_tiles * p.splits;
   if (units > 0x7fffffff) return BI_ERR_UNSUPPORTED;
   const int grid = static_cast<int>(units < sms ? units : sms);

@@ -4,7 +4,8 @@
 //
 // Invariant kernel ("Reproducible LLM Inference", §5.3): one row per thread
 // block.  The block shape and every step of the in-row reduction are fixed by
-// H alone: thread t owns the 16-byte vectors t, t+T, t+2T, ... of the row and
+// H alone: thread t owns the 16-byte vectors t, t+T, t+2T, ... of the row
+// (loaded up front, so each thread has several 16-byte loads in flight) and
 // accumulates their squares in that order (fp32 fused multiply-add); the 32
 // lanes of a warp are combined by a fixed xor-butterfly of shuffles; the
 // warps' sums are combined by the same butterfly over warp indices.  A larger
@@ -119,7 +120,7 @@ struct RowShape {
 };
 RowShape row_shape(int64_t H) {
   const int nvec = static_cast<int>(H / 8);
-  int vpt = nvec >= 64 ? 2 : 1;
+  int vpt = nvec >= 256 ? 4 : (nvec >= 64 ? 2 : 1);
   while ((nvec + vpt - 1) / vpt > 1024) vpt *= 2;
   int t = (nvec + vpt - 1) / vpt;
   t = (t + 31) / 32 * 32;

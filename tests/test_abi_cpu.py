@@ -51,11 +51,16 @@ def test_workspace_sizes_are_host_arithmetic(lib):
     assert bi.bi_rmsnorm_workspace_size(3, 4096, bi.VARIANT) == 3 * 64 * 4
     assert bi.bi_gemm_workspace_size(8192, 6144, 4096, bi.INVARIANT) == 0
     assert bi.bi_gemm_workspace_size(1, 6144, 4096, bi.VARIANT, 4) == 4 * 6144 * 4
-    # decode partials: B * Hq * ceil(max_kv_len / S) * (D + 2) floats
+    # decode: unit list + split partials, each area rounded up to 256 bytes
+    up = lambda x: (x + 255) // 256 * 256
+
+    def dec(B, Hq, D, S_max):
+        return 256 + up(16 * B * S_max) + up(8 * B * Hq * S_max) + 4 * B * Hq * S_max * D
     assert bi.bi_attn_decode_workspace_size(64, 32, 8, 128, 32768, 256, bi.INVARIANT) == \
-        64 * 32 * 128 * 130 * 4
+        dec(64, 32, 128, 128)
     assert bi.bi_attn_decode_workspace_size(8, 4, 2, 64, 512, 64, bi.VARIANT, 5) == \
-        8 * 4 * 5 * 66 * 4
+        dec(8, 4, 64, 5)
+    assert bi.bi_attn_decode_workspace_size(3, 4, 2, 64, 0, 64, bi.INVARIANT) == 0
 
 
 def test_gemm_variant_split_count(lib):
