@@ -18,7 +18,8 @@ The headline is the GEMMs' TFLOP/s (flops of both GEMMs / their device time,
 CUDA events on the launching stream); every other kernel is reported beside
 it against its own roofline, and the whole step is also run in the
 batch-variant mode to report the cost of invariance (t_invariant / t_variant
-- 1 per kernel).  L2 is flushed (a 256 MB write) before every step; inputs are
+- 1 per kernel).  L2 is flushed (a 256 MB write, then a 256 MB read so the dirty
+lines drain outside the timed region) before every step; inputs are
 resident in HBM when the timed region starts.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -212,7 +213,7 @@ class Workload:
             ("decode", lambda: bi.bi_attn_decode(
                 self.q, self.kv.k_cache, self.kv.v_cache, self.kv.block_table, self.lens,
                 self.dec_out, None, max_kv_len=d["max_len"], split_size=d["S"],
-                sm_scale=d["D"] ** -0.5, mode=mode, workspace=self.dec_ws[mode]), 2),
+                sm_scale=d["D"] ** -0.5, mode=mode, workspace=self.dec_ws[mode]), 3),
             ("prefill", lambda: bi.bi_attn_prefill_chunk(
                 self.pq, self.cu, self.pstart, self.pkv.k_cache, self.pkv.v_cache,
                 self.pkv.block_table, self.pkl, self.pout, None, max_q_len=PRE["chunk"],
@@ -222,7 +223,7 @@ class Workload:
 
     def launches(self):
         """Our kernel launches per invariant step: KV write, RMSNorm, two GEMMs,
-        decode split + merge, prefill."""
+        decode plan + split + merge, prefill."""
         return sum(n for _, _, n in self.ops(self.bi.INVARIANT))
 
     # algorithmic work per launch
@@ -242,6 +243,22 @@ class Workload:
             "prefill": {"flops": 4.0 * d["Hq"] * d["D"] * causal_keys,
                         "bytes": (T0 + C) * d["Hkv"] * d["D"] * 2 * 2 + 2 * C * d["Hq"] * d["D"] * 2},
         }
+
+
+class L2Flush:
+    """Evicts the step's data from L2 before a timed step: a 256 MB write (twice
+    the L2), then a 256 MB read of a second buffer, so that the dirty lines the
+    write leaves behind drain to HBM before the timed region, not inside it."""
+
+    def __init__(self, dev):
+        n = 256 * 1024 * 1024 // 4
+        self.w = torch.empty(n, dtype=torch.float32, device=dev)
+        self.r = torch.zeros(n, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def zero_(self):
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.sink)
 
 
 def timed_steps(wl, mode, steps, warmup, flush, stream, dist_barrier):
@@ -423,7 +440,7 @@ def main():
     peaks = load_peaks()
     reserve = 2 * (args.warmup + args.steps) + 8
     wl = Workload(dev, rank, reserve)
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.Stream(dev)
 
     with ClockSampler(local) as clk:
@@ -488,7 +505,7 @@ def main():
         "config": {"workload": WORKLOAD, "M": M, "hidden": H, "n_qkv": N_QKV, "n_up": N_UP,
                    "decode_requests": DEC["B"], "split_size": DEC["S"],
                    "prefill_chunk": PRE["chunk"], "mode": "invariant",
-                   "l2": "flushed (256 MB write) before every step",
+                   "l2": "flushed before every step (256 MB write, then 256 MB read of another buffer)",
                    "parallelism": "replicas (dp%d, no collective on the data path)" % world},
         "roofline": roofline,
         "components": comps,

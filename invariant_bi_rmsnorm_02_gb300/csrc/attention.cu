@@ -42,6 +42,8 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include <utility>
+
 #include "bi_internal.h"
 #include "device_common.cuh"
 
@@ -425,7 +427,6 @@ __global__ void __launch_bounds__(32) attn_decode_split_kernel(
 
   const int lane = threadIdx.x;
   const int G = p.G, Hkv = p.Hkv;
-  const int U = *p.unit_count * Hkv;
   if (lane == 0) {
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
@@ -433,6 +434,9 @@ __global__ void __launch_bounds__(32) attn_decode_split_kernel(
     mbar_init(&bars[1], 1);
     fence_mbar_init();
   }
+  launch_dependents();     // the merge kernel may queue up behind this grid
+  grid_dependency_wait();  // the plan kernel's unit list is complete from here on
+  const int U = *p.unit_count * Hkv;
   // padding query rows G .. 8*NQ-1 stay zero in both buffers
   {
     const int pad = (8 * NQ - G) * (D / 8);  // 16-byte chunks per buffer
@@ -622,44 +626,70 @@ __global__ void __launch_bounds__(32) attn_decode_split_kernel(
 // ------------------------------------------------------------ decode merge
 // Block (qh, b), D/2 threads: left fold over the splits in index order, then
 // o / l.  Empty splits are skipped; a split marked l = -1 (bad pages) makes
-// the whole row zero.
+// the whole row zero.  The {m, l} pairs are staged in shared memory a chunk
+// at a time and the partial rows are loaded kMergeAhead at once, so the fold
+// (which stays strictly in split order) does not wait on one round trip per
+// split.
+constexpr int kMergeChunk = 128;
+constexpr int kMergeAhead = 16;
+
+struct MergeState {
+  float m, l, o0, o1;
+  bool have, bad;
+};
+
+__device__ __forceinline__ void merge_one(MergeState& st, float2 ml, float2 oj) {
+  if (ml.y < 0.0f) st.bad = true;
+  if (ml.x == -CUDART_INF_F) return;  // empty split
+  if (!st.have) {
+    st.m = ml.x;
+    st.l = ml.y;
+    st.o0 = oj.x;
+    st.o1 = oj.y;
+    st.have = true;
+  } else {
+    float mn, ca, cb;
+    lse_coeffs(st.m, ml.x, mn, ca, cb);
+    st.l = lse_mix(st.l, ca, ml.y, cb);
+    st.o0 = lse_mix(st.o0, ca, oj.x, cb);
+    st.o1 = lse_mix(st.o1, ca, oj.y, cb);
+    st.m = mn;
+  }
+}
+
 template <int D>
-__global__ void __launch_bounds__(64) attn_decode_merge_kernel(const KernelParams p) {
+__global__ void __launch_bounds__(D / 2) attn_decode_merge_kernel(const KernelParams p) {
+  __shared__ float2 sml[kMergeChunk];
   const int qh = blockIdx.x, b = blockIdx.y;
   const int d = threadIdx.x * 2;
   const int64_t row = (int64_t)b * p.Hq + qh;
   const int64_t oidx = row * D + d;
   const int L = p.kv_lens[b];
+  grid_dependency_wait();  // every split kernel block has finished
   float r0 = 0.0f, r1 = 0.0f;
   if (len_ok(L, p) && L > 0) {
     const int ns = p.variant ? p.split_count : (L + p.split_size - 1) / p.split_size;
-    const float* ml = p.ml + row * p.max_splits * 2;
-    const float* ob = p.o + row * p.max_splits * D;
-    float m = -CUDART_INF_F, l = 0.0f, o0 = 0.0f, o1 = 0.0f;
-    bool have = false, bad = false;
-    for (int j = 0; j < ns; ++j) {
-      const float mj = ml[2 * j], lj = ml[2 * j + 1];
-      if (lj < 0.0f) bad = true;
-      if (mj == -CUDART_INF_F) continue;  // empty split
-      const float2 oj = *reinterpret_cast<const float2*>(ob + (int64_t)j * D + d);
-      if (!have) {
-        m = mj;
-        l = lj;
-        o0 = oj.x;
-        o1 = oj.y;
-        have = true;
-      } else {
-        float mn, ca, cb;
-        lse_coeffs(m, mj, mn, ca, cb);
-        l = lse_mix(l, ca, lj, cb);
-        o0 = lse_mix(o0, ca, oj.x, cb);
-        o1 = lse_mix(o1, ca, oj.y, cb);
-        m = mn;
+    const float2* ml = reinterpret_cast<const float2*>(p.ml) + row * p.max_splits;
+    const float* ob = p.o + row * p.max_splits * D + d;
+    MergeState st{-CUDART_INF_F, 0.0f, 0.0f, 0.0f, false, false};
+    for (int j0 = 0; j0 < ns; j0 += kMergeChunk) {
+      const int cnt = min(kMergeChunk, ns - j0);
+      __syncthreads();
+      for (int i = threadIdx.x; i < cnt; i += blockDim.x) sml[i] = ml[j0 + i];
+      __syncthreads();
+      for (int j = 0; j < cnt; j += kMergeAhead) {
+        float2 ov[kMergeAhead];
+#pragma unroll
+        for (int u = 0; u < kMergeAhead; ++u)
+          if (j + u < cnt) ov[u] = *reinterpret_cast<const float2*>(ob + (int64_t)(j0 + j + u) * D);
+#pragma unroll
+        for (int u = 0; u < kMergeAhead; ++u)
+          if (j + u < cnt) merge_one(st, sml[j + u], ov[u]);
       }
     }
-    if (have && !bad) {
-      r0 = __fdiv_rn(o0, l);
-      r1 = __fdiv_rn(o1, l);
+    if (st.have && !st.bad) {
+      r0 = __fdiv_rn(st.o0, st.l);
+      r1 = __fdiv_rn(st.o1, st.l);
     }
   }
   *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.out) + oidx) = pack_bf16x2(r0, r1);
@@ -954,6 +984,24 @@ bool make_kv_maps(const AttnArgs& a, CUtensorMap* km, CUtensorMap* vm) {
          make_tmap_2d_bf16(vm, a.v_cache, rows, a.D, kPage, 64);
 }
 
+// Launch with programmatic stream serialisation: the kernel may begin while
+// the previous one in the stream drains, and waits for it in-kernel.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <typename K>
 cudaError_t set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1000,7 +1048,13 @@ bi_status decode_impl(const AttnArgs& a, cudaStream_t s) {
     const int64_t max_units = static_cast<int64_t>(a.B) * a.Hkv * a.max_splits;
     const int64_t cap = static_cast<int64_t>(occ) * sms;
     const int grid = static_cast<int>(max_units < cap ? max_units : cap);
-    attn_decode_split_kernel<D, NQ><<<grid, 32, sm, s>>>(km, vm, p);
+    if (launch_pdl(attn_decode_split_kernel<D, NQ>, dim3(grid), dim3(32), sm, s, km, vm, p) !=
+        cudaSuccess)
+      return BI_ERR_CUDA;
+    if (launch_pdl(attn_decode_merge_kernel<D>, dim3(a.Hq, a.B), dim3(D / 2), 0, s, p) !=
+        cudaSuccess)
+      return BI_ERR_CUDA;
+    return BI_OK;
   }
   attn_decode_merge_kernel<D><<<dim3(a.Hq, a.B), D / 2, 0, s>>>(p);
   return cuda_status(cudaGetLastError());

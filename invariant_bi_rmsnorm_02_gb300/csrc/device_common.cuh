@@ -105,6 +105,19 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ------------------------------------------------------------------ PDL
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialisation attribute may start while the previous kernel on the
+// stream is still running; it must call grid_dependency_wait() before it
+// reads anything that kernel writes.  launch_dependents() lets the next
+// kernel in the stream start its own prologue early.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ bf16
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
