@@ -213,7 +213,8 @@ class Workload:
             ("decode", lambda: bi.bi_attn_decode(
                 self.q, self.kv.k_cache, self.kv.v_cache, self.kv.block_table, self.lens,
                 self.dec_out, None, max_kv_len=d["max_len"], split_size=d["S"],
-                sm_scale=d["D"] ** -0.5, mode=mode, workspace=self.dec_ws[mode]), 3),
+                sm_scale=d["D"] ** -0.5, mode=mode, workspace=self.dec_ws[mode]),
+             2 if d["B"] <= 128 else 3),
             ("prefill", lambda: bi.bi_attn_prefill_chunk(
                 self.pq, self.cu, self.pstart, self.pkv.k_cache, self.pkv.v_cache,
                 self.pkv.block_table, self.pkl, self.pout, None, max_q_len=PRE["chunk"],
@@ -223,7 +224,7 @@ class Workload:
 
     def launches(self):
         """Our kernel launches per invariant step: KV write, RMSNorm, two GEMMs,
-        decode plan + split + merge, prefill."""
+        decode split + merge (plus a plan kernel above 128 sequences), prefill."""
         return sum(n for _, _, n in self.ops(self.bi.INVARIANT))
 
     # algorithmic work per launch

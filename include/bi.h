@@ -170,9 +170,10 @@ bi_status bi_attn_decode(const void* q, const void* k_cache, const void* v_cache
 
 /* Bytes of workspace bi_attn_decode needs: the unit list of the split plan
  * (16 bytes per (sequence, split)) and the split partials m, l, o in fp32,
- * i.e. 256 + up256(16*B*S_max) + up256(8*B*Hq*S_max) + 4*B*Hq*S_max*D with
+ * i.e. 256 + up256(16*B*S_max) + up256(8*B*Hq*E) + 4*B*Hq*S_max*D with
  * S_max = ceil(max_kv_len / split_size) (the variant's count in
- * BI_MODE_VARIANT) and up256 rounding up to a multiple of 256.
+ * BI_MODE_VARIANT), E = S_max rounded up to an even number and up256
+ * rounding up to a multiple of 256.
  * Host arithmetic, except that BI_MODE_VARIANT with variant_splits <= 0
  * queries the current device's SM count ((size_t)-1 if that fails). */
 size_t bi_attn_decode_workspace_size(int B, int Hq, int Hkv, int D, int max_kv_len,

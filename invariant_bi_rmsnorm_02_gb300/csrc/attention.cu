@@ -55,7 +55,6 @@ constexpr int kTile = 64;              // keys per tile (4 pages)
 constexpr int kPagesPerTile = kTile / kPage;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kPgRegs = 4;             // page ids held in registers per unit: 32 * 4
 
 template <int D>
 struct TileGeom {
@@ -334,6 +333,10 @@ struct KernelParams {
   float* o;          // decode partials: o[D] per (b, q-head, split)
   int* err;
   int B, Hq, Hkv, G, max_blocks, max_kv_len, split_size, split_count, max_splits;
+  int ml_stride;     // decode partials: {m, l} pairs per (b, q-head) row, even
+  int local_plan;    // decode: the split kernel works out its units itself
+  int merge_slots;   // decode merge: staged chunks in flight
+  int* order;        // decode, in-kernel plan: sequences by decreasing split count
   int64_t num_pages;
   float scale_log2;
   bool variant;
@@ -404,16 +407,32 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const KernelPar
 }
 
 // ------------------------------------------------------------ decode split
-// Persistent: block x takes units u = x, x + gridDim.x, ... of the plan (unit
-// u = split u / Hkv, kv head u % Hkv).  One warp per block; the G query heads
-// of the kv head are the columns of NQ 8-wide n-tiles.  The TMA ring of two
-// tiles runs across unit boundaries; the page ids of the unit being loaded
-// are fetched once into registers.  A unit whose pages are not all in the
-// pool is recorded as BI_ERR_DEVICE_BOUNDS and marked with l = -1.
+// Persistent: block x takes units u = x, x + gridDim.x, ... (unit u = split
+// u / Hkv of the plan, kv head u % Hkv).  One warp per block; the G query
+// heads of the kv head are the columns of NQ 8-wide n-tiles.  The TMA ring
+// of two tiles runs across unit boundaries.
+// Units are opened (descriptor, page ids checked and staged in shared
+// memory) only at unit boundaries, kQueue ahead of the compute; the page ids
+// of the next unit are fetched into registers one unit before they are
+// checked, so their latency hides behind a unit's worth of tiles, and the
+// tile loop itself reads nothing but shared memory.  A unit whose pages are
+// not all in the pool is recorded as BI_ERR_DEVICE_BOUNDS and marked with
+// l = -1.
 constexpr int kQueue = 4;
+constexpr int kUnitPages = 64;                     // page ids staged per unit
+constexpr int kLocalSlabs = 4;                     // 32 sequences per slab
+constexpr int kLocalPlanMax = 32 * kLocalSlabs;    // largest batch planned in-kernel
 
+__device__ __forceinline__ int unit_tiles(int4 d) {  // {b, j, lo, hi}
+  return d.z < d.w ? (d.w - (d.z & ~(kTile - 1)) + kTile - 1) / kTile : 0;
+}
+
+// One warp per block and at most three blocks per SM (shared memory), so
+// registers are not what limits residency: the bound lets ptxas keep the
+// whole tile step in registers instead of its default of 128 for this
+// block size, which measurably starved the G <= 8 instantiation.
 template <int D, int NQ>
-__global__ void __launch_bounds__(32) attn_decode_split_kernel(
+__global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const KernelParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -422,8 +441,9 @@ __global__ void __launch_bounds__(32) attn_decode_split_kernel(
   uint8_t* bufs = smem;  // 2 tile buffers
   __nv_bfloat16* qbuf = reinterpret_cast<__nv_bfloat16*>(smem + 2 * TileGeom<D>::kBufBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(qbuf + 2 * 8 * NQ * D);
-  __shared__ int4 q_unit[kQueue];   // b, j, lo, hi of opened units
-  __shared__ int q_head[kQueue];    // kv head h, or -(h+1) if the unit's pages are bad
+  __shared__ int4 q_unit[kQueue];              // b, j, lo, hi of opened units
+  __shared__ int q_head[kQueue];               // kv head h, or -(h+1) if its pages are bad
+  __shared__ int q_pid[kQueue][kUnitPages];    // page ids of the unit's first pages
 
   const int lane = threadIdx.x;
   const int G = p.G, Hkv = p.Hkv;
@@ -434,9 +454,6 @@ __global__ void __launch_bounds__(32) attn_decode_split_kernel(
     mbar_init(&bars[1], 1);
     fence_mbar_init();
   }
-  launch_dependents();     // the merge kernel may queue up behind this grid
-  grid_dependency_wait();  // the plan kernel's unit list is complete from here on
-  const int U = *p.unit_count * Hkv;
   // padding query rows G .. 8*NQ-1 stay zero in both buffers
   {
     const int pad = (8 * NQ - G) * (D / 8);  // 16-byte chunks per buffer
@@ -446,79 +463,161 @@ __global__ void __launch_bounds__(32) attn_decode_split_kernel(
       *reinterpret_cast<uint4*>(qbuf + (bsel * 8 * NQ + r) * D + c) = make_uint4(0, 0, 0, 0);
     }
   }
-  __syncwarp();
+  launch_dependents();     // the merge kernel may queue up behind this grid
+  grid_dependency_wait();  // inputs and the plan kernel's unit list are complete from here
+  // Units in sequence order.  For small batches the running split count
+  // (inclusive) and the length of every sequence are kept in shared memory;
+  // the sequence of split s is the number of sequences whose running count
+  // is <= s, found with one ballot per 32 sequences.
+  __shared__ int s_incl[kLocalPlanMax], s_len[kLocalPlanMax];
+  int total = 0;
+  if (p.local_plan) {
+#pragma unroll
+    for (int k = 0; k < kLocalSlabs; ++k) {
+      const int b = lane + 32 * k;
+      int L = 0, n = 0;
+      if (b < p.B) {
+        L = p.kv_lens[b];
+        if (!len_ok(L, p)) {
+          record_error(p.err, BI_ERR_DEVICE_BOUNDS);
+          L = 0;
+        }
+        if (L > 0) n = p.variant ? p.split_count : (L + p.split_size - 1) / p.split_size;
+      }
+      int v = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v += t;
+      }
+      s_incl[b] = total + v;
+      s_len[b] = L;
+      total += __shfl_sync(kFull, v, 31);
+    }
+    __syncwarp();
+    // the merge takes sequences longest first: rank of sequence x among all
+    // (more splits first, then lower index)
+    for (int x = blockIdx.x; x < p.B; x += gridDim.x) {
+      auto splits = [&](int b) { return s_incl[b] - (b > 0 ? s_incl[b - 1] : 0); };
+      const int nx = splits(x);
+      int ahead = 0;
+#pragma unroll
+      for (int k = 0; k < kLocalSlabs; ++k) {
+        const int b = lane + 32 * k;
+        if (b < p.B) {
+          const int nb = splits(b);
+          ahead += (nb > nx || (nb == nx && b < x)) ? 1 : 0;
+        }
+      }
+      ahead = __reduce_add_sync(kFull, ahead);
+      if (lane == 0) p.order[ahead] = x;
+    }
+  } else {
+    total = *p.unit_count;
+  }
+  const int U = total * Hkv;
+  auto unit_at = [&](int s) -> int4 {  // {b, j, lo, hi} of split s; warp-uniform s
+    if (!p.local_plan) return p.units[s];
+    int b = 0;
+#pragma unroll
+    for (int k = 0; k < kLocalSlabs; ++k)
+      b += __popc(__ballot_sync(kFull, s_incl[lane + 32 * k] <= s));
+    const int L = s_len[b];
+    const int j = s - (b > 0 ? s_incl[b - 1] : 0);
+    int lo, hi;
+    if (p.variant) {
+      lo = (int)(((int64_t)j * L) / p.split_count);
+      hi = (int)(((int64_t)(j + 1) * L) / p.split_count);
+    } else {
+      lo = j * p.split_size;
+      hi = min(lo + p.split_size, L);
+    }
+    return make_int4(b, j, lo, hi);
+  };
 
-  // ---- load cursor
-  int lu = blockIdx.x;      // next unit to open
-  bool l_open = false;      // a valid unit is being loaded
-  int l_tile = 0, l_ntiles = 0, l_first = 0, l_hi = 0, l_h = 0, l_b = 0;
-  int pg[kPgRegs];
-  int n_pushed = 0, n_popped = 0, n_issued = 0, n_done = 0, q_issued = 0, q_used = 0;
-
-  auto open_unit = [&]() -> bool {
-    if (n_pushed - n_popped >= kQueue || lu >= U) return false;
-    const int h = lu % Hkv;
-    const int4 d = p.units[lu / Hkv];
+  // ---- opening units: one pending (page ids in flight), kQueue opened
+  int lu = blockIdx.x;  // next unit to fetch
+  bool pend = false;
+  int4 pd = make_int4(0, 0, 0, 0);
+  int ph = 0;
+  int ppg[kUnitPages / 32];
+  int n_pushed = 0, n_popped = 0;
+  int l_q = 0, l_tile = 0;
+  int n_issued = 0, n_done = 0, q_issued = 0, q_used = 0;
+  auto fetch = [&]() {
+    pend = lu < U;
+    if (!pend) return;
+    ph = lu % Hkv;
+    pd = unit_at(lu / Hkv);
     lu += gridDim.x;
-    const int first = d.z & ~(kTile - 1);
-    const int npg = d.z < d.w ? (d.w - first + kPage - 1) / kPage : 0;
-    const int32_t* bt_row = p.block_table + (int64_t)d.x * p.max_blocks;
+    const int first = pd.z & ~(kTile - 1);
+    const int npg = pd.z < pd.w ? (pd.w - first + kPage - 1) / kPage : 0;
+    const int32_t* bt = p.block_table + (int64_t)pd.x * p.max_blocks + (first >> 4);
+#pragma unroll
+    for (int k = 0; k < kUnitPages / 32; ++k) {
+      const int idx = lane + 32 * k;
+      ppg[k] = idx < npg ? bt[idx] : 0;
+    }
+  };
+  auto push = [&]() {  // check the pending unit's pages and queue it
+    const int slot = n_pushed % kQueue;
+    const int first = pd.z & ~(kTile - 1);
+    const int npg = pd.z < pd.w ? (pd.w - first + kPage - 1) / kPage : 0;
     bool ok = true;
 #pragma unroll
-    for (int k = 0; k < kPgRegs; ++k) {
+    for (int k = 0; k < kUnitPages / 32; ++k) {
       const int idx = lane + 32 * k;
-      pg[k] = idx < npg ? bt_row[(first >> 4) + idx] : 0;
-      if (idx < npg && (pg[k] < 0 || pg[k] >= p.num_pages)) ok = false;
+      if (idx < npg) {
+        if (ppg[k] < 0 || ppg[k] >= p.num_pages) ok = false;
+        q_pid[slot][idx] = ppg[k];
+      }
     }
-    if (npg > 32 * kPgRegs &&
-        !pages_ok(bt_row, first + 32 * kPgRegs * kPage, d.w, p.num_pages, lane, 32))
-      ok = false;
+    if (npg > kUnitPages) {
+      const int32_t* bt_row = p.block_table + (int64_t)pd.x * p.max_blocks;
+      if (!pages_ok(bt_row, first + kUnitPages * kPage, pd.w, p.num_pages, lane, 32)) ok = false;
+    }
     ok = __all_sync(kFull, ok);
     if (lane == 0) {
-      q_unit[n_pushed % kQueue] = d;
-      q_head[n_pushed % kQueue] = ok ? h : -(h + 1);
+      q_unit[slot] = pd;
+      q_head[slot] = ok ? ph : -(ph + 1);
       if (!ok) record_error(p.err, BI_ERR_DEVICE_BOUNDS);
     }
     __syncwarp();
     ++n_pushed;
-    if (ok && npg > 0) {
-      l_open = true;
-      l_tile = 0;
-      l_first = first;
-      l_ntiles = (d.w - first + kTile - 1) / kTile;
-      l_hi = d.w;
-      l_h = h;
-      l_b = d.x;
+  };
+  auto top_up = [&]() {
+    // a slot is reused only once both the compute and the load cursor are past it
+    while (pend && n_pushed - n_popped < kQueue && n_pushed - l_q < kQueue) {
+      push();
+      fetch();
     }
-    return true;
   };
 
-  // issue the next tile of the load cursor into the free ring slot, if any
-  auto issue = [&]() {
+  // ---- load cursor: queue position l_q, tile l_tile of that unit
+  auto issue = [&]() {  // the next tile into the free ring slot, if any
     if (n_issued - n_done >= 2) return;
-    while (!l_open) {
-      if (!open_unit()) return;
+    int4 d;
+    int h;
+    for (;;) {  // skip opened units with nothing to load
+      if (l_q >= n_pushed) return;
+      d = q_unit[l_q % kQueue];
+      h = q_head[l_q % kQueue];
+      if (h >= 0 && l_tile < unit_tiles(d)) break;
+      ++l_q;
+      l_tile = 0;
     }
-    const int key0 = l_first + l_tile * kTile;
-    const int np = pages_below(key0, l_hi);
+    const int qs = l_q % kQueue;
+    const int first = d.z & ~(kTile - 1);
+    const int key0 = first + l_tile * kTile;
+    const int np = pages_below(key0, d.w);
     int pid[4];
 #pragma unroll
     for (int pp = 0; pp < 4; ++pp) {
       const int idx = 4 * l_tile + pp;  // page index within the unit
-      int v = 0;
-#pragma unroll
-      for (int k = 0; k < kPgRegs; ++k) {
-        const int sv = __shfl_sync(kFull, pg[k], idx & 31);
-        if ((idx >> 5) == k) v = sv;
-      }
-      pid[pp] = v;
-    }
-    if (4 * l_tile + 4 > 32 * kPgRegs) {  // long split: page ids past the registers
-#pragma unroll
-      for (int pp = 0; pp < 4; ++pp)
-        if (4 * l_tile + pp >= 32 * kPgRegs && pp < np)
-          pid[pp] =
-              p.block_table[(int64_t)l_b * p.max_blocks + (l_first >> 4) + 4 * l_tile + pp];
+      pid[pp] = pp >= np                ? 0
+                : idx < kUnitPages      ? q_pid[qs][idx]
+                                        : p.block_table[(int64_t)d.x * p.max_blocks +
+                                                        (first >> 4) + idx];
     }
     const int slot = n_issued & 1;
     if (lane == 0) {
@@ -527,42 +626,44 @@ __global__ void __launch_bounds__(32) attn_decode_split_kernel(
       mbar_arrive_expect_tx(&bars[slot], np * 2 * TileGeom<D>::kPageBytes + qbytes);
       if (l_tile == 0)
         bulk_load(qbuf + (q_issued & 1) * 8 * NQ * D,
-                  p.q + ((int64_t)l_b * p.Hq + (int64_t)l_h * G) * D, qbytes, &bars[slot]);
-      issue_pages<D>(buf, &bars[slot], &kmap, &vmap, pid, np, Hkv, l_h);
+                  p.q + ((int64_t)d.x * p.Hq + (int64_t)h * G) * D, qbytes, &bars[slot]);
+      issue_pages<D>(buf, &bars[slot], &kmap, &vmap, pid, np, Hkv, h);
     }
     if (l_tile == 0) ++q_issued;
     ++n_issued;
-    if (++l_tile == l_ntiles) l_open = false;
+    if (++l_tile == unit_tiles(d)) {
+      ++l_q;
+      l_tile = 0;
+    }
   };
 
+  fetch();
+  top_up();
   issue();
   issue();
   SplitState<D, NQ> st;
   uint32_t qf[NQ][D / 16][2];
   const int g = lane >> 2, t = lane & 3;
   bool alive = true;
-  while (alive) {
-    if (n_popped == n_pushed) {
-      issue();  // opens the next units (and loads their first tile) if any are left
-      if (n_popped == n_pushed) break;
-    }
+  while (alive && n_popped < n_pushed) {
     const int4 d = q_unit[n_popped % kQueue];
     const int hv = q_head[n_popped % kQueue];
     const bool pages_good = hv >= 0;
     const int h = pages_good ? hv : -hv - 1;
     const int b = d.x, j = d.y, lo = d.z, hi = d.w;
+    const int64_t row0 = (int64_t)b * p.Hq + (int64_t)h * G;  // first q-head row
     if (!pages_good || lo >= hi) {
       // bad pages (l = -1 makes the merge emit zeros) or an empty split
       if (lane < G) {
-        const int64_t s = ((int64_t)b * p.Hq + (int64_t)h * G + lane) * p.max_splits + j;
+        const int64_t s = (row0 + lane) * p.ml_stride + j;
         p.ml[2 * s] = -CUDART_INF_F;
         p.ml[2 * s + 1] = pages_good ? 0.0f : -1.0f;
       }
       ++n_popped;
+      top_up();
       issue();
       continue;
     }
-    const int64_t slot0 = ((int64_t)b * p.Hq + (int64_t)h * G) * p.max_splits + j;
     const int first = lo & ~(kTile - 1);
     const int ntiles = (hi - first + kTile - 1) / kTile;
     int hcol[NQ][2];
@@ -603,12 +704,12 @@ __global__ void __launch_bounds__(32) attn_decode_split_kernel(
       for (int cc = 0; cc < 2; ++cc) {
         const int col = 8 * nq + 2 * t + cc;
         if (col >= G) continue;
-        const int64_t s = slot0 + (int64_t)col * p.max_splits;
+        const int64_t sm = (row0 + col) * p.ml_stride + j;
         if (g == 0) {
-          p.ml[2 * s] = st.m[nq][cc];
-          p.ml[2 * s + 1] = st.l[nq][cc];
+          p.ml[2 * sm] = st.m[nq][cc];
+          p.ml[2 * sm + 1] = st.l[nq][cc];
         }
-        float* orow = p.o + s * D;
+        float* orow = p.o + ((row0 + col) * p.max_splits + j) * D;
 #pragma unroll
         for (int md = 0; md < D / 16; ++md) {
           orow[16 * md + g] = st.o[md][nq][cc];
@@ -616,6 +717,8 @@ __global__ void __launch_bounds__(32) attn_decode_split_kernel(
         }
       }
     ++n_popped;
+    top_up();
+    issue();
   }
   if (!alive && lane == 0) {
     // a copy never landed: give the copies still in flight a bounded wait
@@ -624,74 +727,130 @@ __global__ void __launch_bounds__(32) attn_decode_split_kernel(
 }
 
 // ------------------------------------------------------------ decode merge
-// Block (qh, b), D/2 threads: left fold over the splits in index order, then
-// o / l.  Empty splits are skipped; a split marked l = -1 (bad pages) makes
-// the whole row zero.  The {m, l} pairs are staged in shared memory a chunk
-// at a time and the partial rows are loaded kMergeAhead at once, so the fold
-// (which stays strictly in split order) does not wait on one round trip per
-// split.
-constexpr int kMergeChunk = 128;
-constexpr int kMergeAhead = 16;
-
-struct MergeState {
-  float m, l, o0, o1;
-  bool have, bad;
-};
-
-__device__ __forceinline__ void merge_one(MergeState& st, float2 ml, float2 oj) {
-  if (ml.y < 0.0f) st.bad = true;
-  if (ml.x == -CUDART_INF_F) return;  // empty split
-  if (!st.have) {
-    st.m = ml.x;
-    st.l = ml.y;
-    st.o0 = oj.x;
-    st.o1 = oj.y;
-    st.have = true;
-  } else {
-    float mn, ca, cb;
-    lse_coeffs(st.m, ml.x, mn, ca, cb);
-    st.l = lse_mix(st.l, ca, ml.y, cb);
-    st.o0 = lse_mix(st.o0, ca, oj.x, cb);
-    st.o1 = lse_mix(st.o1, ca, oj.y, cb);
-    st.m = mn;
-  }
-}
+// Block (qh, b), D/2 threads (two output columns each): left fold over the
+// splits in index order, then o / l.  Empty splits are skipped; a split
+// marked l = -1 (bad pages) makes the whole row zero.  The partial rows and
+// their {m, l} pairs are staged by bulk copies in chunks of kMergeChunk
+// splits, merge_slots chunks in flight, so the fold (strictly in split order)
+// runs from shared memory while later chunks are still arriving.
+constexpr int kMergeChunk = 16;
+constexpr int kMergeSlots = 4;
 
 template <int D>
 __global__ void __launch_bounds__(D / 2) attn_decode_merge_kernel(const KernelParams p) {
-  __shared__ float2 sml[kMergeChunk];
-  const int qh = blockIdx.x, b = blockIdx.y;
-  const int d = threadIdx.x * 2;
-  const int64_t row = (int64_t)b * p.Hq + qh;
-  const int64_t oidx = row * D + d;
-  const int L = p.kv_lens[b];
+  extern __shared__ __align__(16) float mo[];  // [slot][kMergeChunk][D]
+  __shared__ __align__(16) float2 sml[kMergeSlots][kMergeChunk];
+  __shared__ float2 scoef[kMergeChunk];  // ca, cb of each split of the chunk
+  __shared__ int skind[kMergeChunk];     // 0 empty, 1 first non-empty, 2 fold in
+  __shared__ uint64_t bars[kMergeSlots];
+  __shared__ int s_abort, s_bad;
+  const int qh = blockIdx.x, tid = threadIdx.x;
+  const int d = tid * 2;
   grid_dependency_wait();  // every split kernel block has finished
-  float r0 = 0.0f, r1 = 0.0f;
-  if (len_ok(L, p) && L > 0) {
-    const int ns = p.variant ? p.split_count : (L + p.split_size - 1) / p.split_size;
-    const float2* ml = reinterpret_cast<const float2*>(p.ml) + row * p.max_splits;
-    const float* ob = p.o + row * p.max_splits * D + d;
-    MergeState st{-CUDART_INF_F, 0.0f, 0.0f, 0.0f, false, false};
-    for (int j0 = 0; j0 < ns; j0 += kMergeChunk) {
-      const int cnt = min(kMergeChunk, ns - j0);
-      __syncthreads();
-      for (int i = threadIdx.x; i < cnt; i += blockDim.x) sml[i] = ml[j0 + i];
-      __syncthreads();
-      for (int j = 0; j < cnt; j += kMergeAhead) {
-        float2 ov[kMergeAhead];
+  const int b = p.order ? p.order[blockIdx.y] : blockIdx.y;
+  const int64_t row = (int64_t)b * p.Hq + qh;
+  const int L = p.kv_lens[b];
+  const int ns = (len_ok(L, p) && L > 0)
+                     ? (p.variant ? p.split_count : (L + p.split_size - 1) / p.split_size)
+                     : 0;
+  const int nch = (ns + kMergeChunk - 1) / kMergeChunk;
+  const int slots = p.merge_slots;
+  const float2* mlrow = reinterpret_cast<const float2*>(p.ml) + row * p.ml_stride;
+  const float* orow = p.o + row * p.max_splits * D;
+  auto issue = [&](int c) {  // thread 0: chunk c into slot c % slots
+    const int j0 = c * kMergeChunk, cnt = min(kMergeChunk, ns - j0), slot = c % slots;
+    const uint32_t ob = cnt * D * 4, mb = ((cnt + 1) & ~1) * 8;  // the row stride is even
+    mbar_arrive_expect_tx(&bars[slot], ob + mb);
+    bulk_load(mo + slot * kMergeChunk * D, orow + (int64_t)j0 * D, ob, &bars[slot]);
+    bulk_load(&sml[slot][0], mlrow + j0, mb, &bars[slot]);
+  };
+  if (tid == 0) {
+    s_abort = 0;
+    s_bad = 0;
+    for (int i = 0; i < slots; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+    for (int c = 0; c < nch && c < slots; ++c) issue(c);
+  }
+  __syncthreads();
+  // The left fold in split order, with its data dependences split apart: the
+  // running max before each split is a prefix max (exact in any order), so
+  // warp 0 derives every split's coefficients of a chunk at once, and the
+  // fold proper is a chain of products and sums, bit-identical to folding
+  // one split at a time.
+  float run_m = -CUDART_INF_F;  // warp 0: max over the splits folded so far
+  bool have = false;            // warp 0: a non-empty split was folded
+  float o0 = 0.0f, o1 = 0.0f, l = 0.0f;
+  bool ok = true;
+  for (int c = 0; c < nch; ++c) {
+    const int slot = c % slots;
+    const int cnt = min(kMergeChunk, ns - c * kMergeChunk);
+    const bool landed = mbar_wait(&bars[slot], (c / slots) & 1, p.err, &s_abort);
+    if (__syncthreads_or(!landed)) {
+      // a copy never arrived: bounded waits for the ones still in flight
+      if (tid == 0)
+        for (int i = c; i < nch && i < c + slots; ++i)
+          mbar_wait(&bars[i % slots], (i / slots) & 1, nullptr);
+      ok = false;
+      break;
+    }
+    if (tid < 32) {
+      float m = -CUDART_INF_F, lj = 0.0f;
+      if (tid < cnt) {
+        const float2 v = sml[slot][tid];
+        m = v.x;
+        lj = v.y;
+      }
+      const bool nonempty = m != -CUDART_INF_F;
+      float pm = m;  // inclusive prefix max over the chunk
 #pragma unroll
-        for (int u = 0; u < kMergeAhead; ++u)
-          if (j + u < cnt) ov[u] = *reinterpret_cast<const float2*>(ob + (int64_t)(j0 + j + u) * D);
-#pragma unroll
-        for (int u = 0; u < kMergeAhead; ++u)
-          if (j + u < cnt) merge_one(st, sml[j + u], ov[u]);
+      for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(kFull, pm, o);
+        if (tid >= o) pm = fmaxf(pm, t);
+      }
+      float before = __shfl_up_sync(kFull, pm, 1);
+      before = fmaxf(run_m, tid == 0 ? -CUDART_INF_F : before);
+      const unsigned ne = __ballot_sync(kFull, nonempty);
+      const bool had = have || (ne & ((1u << tid) - 1u)) != 0;
+      if (__any_sync(kFull, lj < 0.0f) && tid == 0) s_bad = 1;
+      if (tid < cnt) {
+        float ca = 0.0f, cb = 0.0f;
+        if (nonempty && had) {
+          float mn;
+          lse_coeffs(before, m, mn, ca, cb);
+        }
+        scoef[tid] = make_float2(ca, cb);
+        skind[tid] = nonempty ? (had ? 2 : 1) : 0;
+      }
+      run_m = fmaxf(run_m, __shfl_sync(kFull, pm, 31));
+      have = have || ne != 0;
+    }
+    __syncthreads();
+    const float* ms = mo + slot * kMergeChunk * D + d;
+#pragma unroll 4
+    for (int j = 0; j < cnt; ++j) {
+      const int kind = skind[j];
+      const float2 oj = *reinterpret_cast<const float2*>(ms + j * D);
+      const float lj = sml[slot][j].y;
+      if (kind == 1) {
+        o0 = oj.x;
+        o1 = oj.y;
+        l = lj;
+      } else if (kind == 2) {
+        const float2 cf = scoef[j];
+        l = lse_mix(l, cf.x, lj, cf.y);
+        o0 = lse_mix(o0, cf.x, oj.x, cf.y);
+        o1 = lse_mix(o1, cf.x, oj.y, cf.y);
       }
     }
-    if (st.have && !st.bad) {
-      r0 = __fdiv_rn(st.o0, st.l);
-      r1 = __fdiv_rn(st.o1, st.l);
-    }
+    __syncthreads();  // slot and coefficients free again
+    if (tid == 0 && c + slots < nch) issue(c + slots);
   }
+  float r0 = 0.0f, r1 = 0.0f;
+  if (ok && ns > 0 && !s_bad && l > 0.0f) {
+    r0 = __fdiv_rn(o0, l);
+    r1 = __fdiv_rn(o1, l);
+  }
+  const int64_t oidx = row * D + d;
   *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.out) + oidx) = pack_bf16x2(r0, r1);
   if (p.out_f32) *reinterpret_cast<float2*>(p.out_f32 + oidx) = make_float2(r0, r1);
 }
@@ -1008,24 +1167,29 @@ cudaError_t set_smem(K kernel, size_t bytes) {
                               static_cast<int>(bytes));
 }
 
-// Workspace carve-up for decode: [unit count | units | {m,l} | o].
+// Workspace carve-up for decode: [unit count | units | {m,l} | o].  The
+// {m, l} rows hold an even number of pairs so that every row starts on a
+// 16-byte boundary for the merge's bulk copies.
 struct DecodeWs {
   size_t units_off, ml_off, o_off, total;
+  int ml_stride;
 };
 DecodeWs decode_ws_layout(int B, int Hq, int D, int max_splits) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   DecodeWs w;
-  const size_t slots = static_cast<size_t>(B) * Hq * max_splits;
+  w.ml_stride = (max_splits + 1) & ~1;
+  const size_t rows = static_cast<size_t>(B) * Hq;
   w.units_off = 256;
   w.ml_off = w.units_off + up(static_cast<size_t>(B) * max_splits * sizeof(int4));
-  w.o_off = w.ml_off + up(slots * 2 * sizeof(float));
-  w.total = w.o_off + slots * D * sizeof(float);
+  w.o_off = w.ml_off + up(rows * w.ml_stride * 2 * sizeof(float));
+  w.total = w.o_off + rows * max_splits * D * sizeof(float);
   return w;
 }
 
 template <int D, int NQ>
 bi_status decode_impl(const AttnArgs& a, cudaStream_t s) {
   KernelParams p = make_params(a);
+  p.merge_slots = 1;
   if (a.max_splits > 0) {
     CUtensorMap km, vm;
     if (!make_kv_maps(a, &km, &vm)) return BI_ERR_CUDA;
@@ -1035,7 +1199,12 @@ bi_status decode_impl(const AttnArgs& a, cudaStream_t s) {
     p.units = reinterpret_cast<int4*>(base + w.units_off);
     p.ml = reinterpret_cast<float*>(base + w.ml_off);
     p.o = reinterpret_cast<float*>(base + w.o_off);
-    attn_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+    p.ml_stride = w.ml_stride;
+    p.local_plan = a.B <= kLocalPlanMax;
+    if (p.local_plan) p.order = reinterpret_cast<int*>(base + w.units_off);  // units unused
+    const int chunks = (a.max_splits + kMergeChunk - 1) / kMergeChunk;
+    p.merge_slots = chunks < kMergeSlots ? chunks : kMergeSlots;
+    if (!p.local_plan) attn_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
     const size_t sm = decode_smem<D, NQ>();
     if (set_smem(attn_decode_split_kernel<D, NQ>, sm) != cudaSuccess) return BI_ERR_CUDA;
     static int per_sm[2][3] = {};
@@ -1051,13 +1220,13 @@ bi_status decode_impl(const AttnArgs& a, cudaStream_t s) {
     if (launch_pdl(attn_decode_split_kernel<D, NQ>, dim3(grid), dim3(32), sm, s, km, vm, p) !=
         cudaSuccess)
       return BI_ERR_CUDA;
-    if (launch_pdl(attn_decode_merge_kernel<D>, dim3(a.Hq, a.B), dim3(D / 2), 0, s, p) !=
-        cudaSuccess)
-      return BI_ERR_CUDA;
-    return BI_OK;
   }
-  attn_decode_merge_kernel<D><<<dim3(a.Hq, a.B), D / 2, 0, s>>>(p);
-  return cuda_status(cudaGetLastError());
+  // at most 32 KB: under the default dynamic shared memory limit
+  const size_t msm = static_cast<size_t>(p.merge_slots) * kMergeChunk * D * sizeof(float);
+  if (launch_pdl(attn_decode_merge_kernel<D>, dim3(a.Hq, a.B), dim3(D / 2), msm, s, p) !=
+      cudaSuccess)
+    return BI_ERR_CUDA;
+  return BI_OK;
 }
 
 template <int D>

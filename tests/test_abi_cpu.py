@@ -55,11 +55,14 @@ def test_workspace_sizes_are_host_arithmetic(lib):
     up = lambda x: (x + 255) // 256 * 256
 
     def dec(B, Hq, D, S_max):
-        return 256 + up(16 * B * S_max) + up(8 * B * Hq * S_max) + 4 * B * Hq * S_max * D
+        E = S_max + (S_max & 1)   # {m, l} rows padded to an even count
+        return 256 + up(16 * B * S_max) + up(8 * B * Hq * E) + 4 * B * Hq * S_max * D
     assert bi.bi_attn_decode_workspace_size(64, 32, 8, 128, 32768, 256, bi.INVARIANT) == \
         dec(64, 32, 128, 128)
     assert bi.bi_attn_decode_workspace_size(8, 4, 2, 64, 512, 64, bi.VARIANT, 5) == \
         dec(8, 4, 64, 5)
+    assert bi.bi_attn_decode_workspace_size(3, 5, 5, 64, 64 * 7, 64, bi.INVARIANT) == \
+        dec(3, 5, 64, 7)
     assert bi.bi_attn_decode_workspace_size(3, 4, 2, 64, 0, 64, bi.INVARIANT) == 0
 
 

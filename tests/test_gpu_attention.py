@@ -154,6 +154,32 @@ def test_decode_kv_growth_gqa_full_size(cuda):
     assert bi.bi_check_device_errors() == bi.OK
 
 
+def test_decode_large_batch_plan_matches_small_batches(cuda):
+    # above 128 sequences the split plan is built by its own kernel, below it
+    # inside the split kernel: both give every request the same bytes, which
+    # also match the oracle on a sample
+    B, Hq, Hkv, D, S = 300, 32, 8, 128, 256
+    lens = synth.loguniform_int(B, 1, 2048, 5150)
+    lens[7] = 0
+    kv = to_dev(synth.paged_kv(lens.tolist(), Hkv, D, 16, 5151), cuda)
+    q = synth.normal_bf16((B, Hq, D), 5152, device=cuda)
+    for mode in (bi.INVARIANT, bi.VARIANT):
+        out, out32 = decode(q, kv, 2048, S, mode, splits=3)
+        for b0 in range(0, B, 100):
+            sl = slice(b0, b0 + 100)
+            o, o32 = decode(q[sl].contiguous(), kv, 2048, S, mode, splits=3,
+                            kv_lens=kv.kv_lens[sl].contiguous(),
+                            bt=kv.block_table[sl].contiguous())
+            assert same_bytes(o32, out32[sl]) and same_bytes(o, out[sl]), (mode, b0)
+        assert (out32[7] == 0).all()
+        rows = [0, 7, 150, 299, int(torch.argmax(kv.kv_lens))]
+        ref = oracle.decode_attention(q[rows].cpu(), kv.k_cache.cpu(), kv.v_cache.cpu(),
+                                      kv.block_table[rows].cpu(), kv.kv_lens[rows].cpu(),
+                                      D ** -0.5)
+        check_attn(out[rows], out32[rows], ref, "decode B=300 mode=%d" % mode)
+    assert bi.bi_check_device_errors() == bi.OK
+
+
 # ----------------------------------------------------------------- prefill
 def prefill(q, cu, starts, kv, kv_lens, max_q, max_kv, S, mode=bi.INVARIANT, splits=0):
     return bi.attn_prefill_chunk(q, cu, starts, kv.k_cache, kv.v_cache, kv.block_table,
