@@ -19,8 +19,11 @@ CUDA events on the launching stream); every other kernel is reported beside
 it against its own roofline, and the whole step is also run in the
 batch-variant mode to report the cost of invariance (t_invariant / t_variant
 - 1 per kernel).  L2 is flushed (a 256 MB write, then a 256 MB read so the dirty
-lines drain outside the timed region) before every step; inputs are
-resident in HBM when the timed region starts.
+lines drain outside the timed region) before every kernel of the step, so
+each kernel is timed on a cold, clean L2 and none pays for the write-back of
+its predecessor's output; the step time is the sum of the kernels' times.
+Inputs are resident in HBM when the timed region starts.  The end-to-end
+line runs the same kernels back to back with host copies around them.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -273,24 +276,27 @@ def timed_steps(wl, mode, steps, warmup, flush, stream, dist_barrier):
             fn()
     torch.cuda.synchronize()
     wl.reset_lengths()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(ops))] for _ in range(steps)]
     mean_lens = []
     dist_barrier()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for s in range(steps):
-            flush.zero_()
-            ev[s][0].record(stream)
             for i, (_, fn, _) in enumerate(ops):
+                flush.zero_()
+                ev[s][2 * i].record(stream)
                 fn()
-                ev[s][i + 1].record(stream)
+                ev[s][2 * i + 1].record(stream)
     torch.cuda.synchronize()
     dist_barrier()
     step_ms = []
     for s in range(steps):
+        t = 0.0
         for i, n in enumerate(names):
-            per[n] += ev[s][i].elapsed_time(ev[s][i + 1])
-        step_ms.append(ev[s][0].elapsed_time(ev[s][-1]))
+            d = ev[s][2 * i].elapsed_time(ev[s][2 * i + 1])
+            per[n] += d
+            t += d
+        step_ms.append(t)
     return {n: v / steps for n, v in per.items()}, sum(step_ms) / steps
 
 
@@ -506,7 +512,8 @@ def main():
         "config": {"workload": WORKLOAD, "M": M, "hidden": H, "n_qkv": N_QKV, "n_up": N_UP,
                    "decode_requests": DEC["B"], "split_size": DEC["S"],
                    "prefill_chunk": PRE["chunk"], "mode": "invariant",
-                   "l2": "flushed before every step (256 MB write, then 256 MB read of another buffer)",
+                   "l2": "flushed before every kernel (256 MB write, then 256 MB read of another "
+                         "buffer); step time = sum of the kernels' times",
                    "parallelism": "replicas (dp%d, no collective on the data path)" % world},
         "roofline": roofline,
         "components": comps,
