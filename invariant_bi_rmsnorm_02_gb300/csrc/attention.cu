@@ -46,6 +46,7 @@
 
 #include "bi_internal.h"
 #include "device_common.cuh"
+#include "tcgen05.cuh"
 
 namespace bi {
 namespace {
@@ -62,7 +63,6 @@ struct TileGeom {
   static constexpr int kPageBytes = kHalves * 2048;      // one page of K (or V)
   static constexpr int kKBytes = kPagesPerTile * kPageBytes;
   static constexpr int kBufBytes = 2 * kKBytes;          // K then V
-  static constexpr int kQStride = D + 8;                 // padded Q row (elements)
 };
 
 // byte offset of (key n of the tile, column d) in a swizzled K or V tile
@@ -855,39 +855,69 @@ __global__ void __launch_bounds__(D / 2) attn_decode_merge_kernel(const KernelPa
   if (p.out_f32) *reinterpret_cast<float2*>(p.out_f32 + oidx) = make_float2(r0, r1);
 }
 
-// ------------------------------------------------------------- prefill
-// Block (qb, h, b): kPrefillWarps warps; each warp owns 16 query columns =
-// TPW tokens x G heads of query block qb of sequence b, kv head h (two 8-wide
-// n-tiles).  Tiles of 64 keys are staged once per block and shared by the
-// warps; splits are folded as they complete, with the merged state of each
-// warp's columns kept in shared memory.
-constexpr int kPrefillWarps = 8;
-constexpr int kPrefillNQ = 2;
+// ---------------------------------------------------- prefill (tcgen05)
+// Block (qb, h, b): 128 query rows -- up to 128 / G tokens times the G heads
+// of kv head h (row r is token r / G, head r % G) -- with four softmax warps
+// (thread r owns row r, which is tensor-memory lane r) and a producer warp
+// whose lane 0 issues the TMA copies and the MMAs.  Per tile of 64 keys:
+//   S = Q K^T   tcgen05.mma M=128 N=64, k = d in steps of 16, into TMEM;
+//   softmax     each thread on its own row, with the decode tile step's
+//               per-element arithmetic, key summation tree and P = hi + lo
+//               split; P is staged in shared memory (K-major, swizzled);
+//   O += P V    tcgen05.mma M=128 N=D, for each 16-key chunk the hi part then
+//               the lo part, V read as an MN-major operand.
+// tcgen05.mma and mma.sync give bit-identical fp32 results for the same
+// operands and k order, so every output row equals the decode of its
+// position bit for bit.  The split state (m, l in registers, o in TMEM) is
+// folded into the merged state (a second TMEM region) at each split end.
+// The tile loop is serial (MMA, softmax, MMA); blocks are started longest
+// first.
+constexpr int kPfRows = 128;
+constexpr int kPfThreads = 160;
 
 template <int D>
-__global__ void __launch_bounds__(kPrefillWarps * 32, 1) attn_prefill_kernel(
+struct PfGeom {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kQBytes = kHalves * kPfRows * 128;  // [half][row][128 B]
+  static constexpr int kKBytes = kHalves * kTile * 128;     // [half][key][128 B]
+  static constexpr int kStageBytes = 2 * kKBytes;           // K then V
+  static constexpr int kPBytes = kPfRows * 128;             // [row][64 keys] bf16
+  static constexpr int kStageOff = kQBytes;
+  static constexpr int kPOff = kStageOff + 2 * kStageBytes;  // P high part, then low
+  static constexpr int kBarOff = kPOff + 2 * kPBytes;
+  static constexpr int kSmem = 1024 + kBarOff + 64;
+  static constexpr uint32_t kTmemCols = D == 128 ? 512 : 256;
+  static constexpr uint32_t kColS = 0, kColO = 64, kColM = 64 + D;  // S, split o, merged o
+};
+
+template <int D>
+__global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const KernelParams p) {
-  constexpr int NQ = kPrefillNQ;
-  constexpr int NV = (D / 16) * NQ * 4;  // o values per thread
+  using Gm = PfGeom<D>;
+  constexpr uint32_t kIdescS = umma_idesc_bf16(kPfRows, kTile, false, false);
+  constexpr uint32_t kIdescPV = umma_idesc_bf16(kPfRows, D, false, true);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* bufs = smem;
-  __nv_bfloat16* qs_all = reinterpret_cast<__nv_bfloat16*>(smem + 2 * TileGeom<D>::kBufBytes);
-  // merged state of each warp's columns, thread-private: value i of lane l at
-  // [i * 32 + l]; reused at the end to stage the output rows
-  float* mg_all = reinterpret_cast<float*>(qs_all + kPrefillWarps * 16 * TileGeom<D>::kQStride);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(mg_all + kPrefillWarps * NV * 32);
+  uint8_t* qs = smem;
+  uint8_t* stages = smem + Gm::kStageOff;
+  uint8_t* ph = smem + Gm::kPOff;
+  uint8_t* pl = ph + Gm::kPBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Gm::kBarOff);  // full[2], sdone, pdone
+  uint64_t* sdone = bars + 2;
+  uint64_t* pdone = bars + 3;
+  __shared__ uint32_t tmem_slot;
   __shared__ int s_abort;
 
-  const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = p.G, TPW = 16 / G;
-  const int QB = kPrefillWarps * TPW;
+  const int qb = gridDim.x - 1 - blockIdx.x;  // the longest query blocks start first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const bool producer = tid == kPfRows;
+  const int G = p.G, TPB = kPfRows / G;
   const int q_begin = p.cu_q[b];
   const int q_len = p.cu_q[b + 1] - q_begin;
-  const int tok0 = qb * QB;
+  const int tok0 = qb * TPB;
   if (tok0 >= q_len) return;
   const int start = p.q_start[b];
   const int kvl = p.kv_lens[b];
@@ -895,7 +925,7 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 1) attn_prefill_kernel(
     if (tid == 0) record_error(p.err, BI_ERR_DEVICE_BOUNDS);
     return;
   }
-  const int ntok = min(QB, q_len - tok0);
+  const int ntok = min(TPB, q_len - tok0);
   const int p_last = start + tok0 + ntok - 1;  // last position in this block
   const int32_t* bt_row = p.block_table + (int64_t)b * p.max_blocks;
   const int ntiles = (p_last + kTile) / kTile;  // tiles 0 .. covering key p_last
@@ -908,171 +938,274 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 1) attn_prefill_kernel(
       return;
     }
   }
-  auto issue_tile = [&](int i) {  // thread 0 only
-    uint8_t* buf = bufs + (i & 1) * TileGeom<D>::kBufBytes;
+  auto issue_tile = [&](int i) {  // producer only
+    uint8_t* st = stages + (i & 1) * Gm::kStageBytes;
     const int key0 = i * kTile;
     const int np = pages_below(key0, kvl);
-    int pid[4];
+    mbar_arrive_expect_tx(&bars[i & 1], np * 2 * Gm::kHalves * 2048);
+    for (int pp = 0; pp < np; ++pp) {
+      const int y = (bt_row[(key0 >> 4) + pp] * p.Hkv + h) * kPage;
 #pragma unroll
-    for (int pp = 0; pp < 4; ++pp) pid[pp] = pp < np ? bt_row[(key0 >> 4) + pp] : 0;
-    mbar_arrive_expect_tx(&bars[i & 1], np * 2 * TileGeom<D>::kPageBytes);
-    issue_pages<D>(buf, &bars[i & 1], &kmap, &vmap, pid, np, p.Hkv, h);
+      for (int hf = 0; hf < Gm::kHalves; ++hf) {
+        const int off = hf * (kTile * 128) + pp * 2048;
+        tma_load_2d(st + off, &kmap, hf * 64, y, &bars[i & 1]);
+        tma_load_2d(st + Gm::kKBytes + off, &vmap, hf * 64, y, &bars[i & 1]);
+      }
+    }
   };
   if (tid == 0) {
     s_abort = 0;
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
   }
+  if (warp == 0) tmem_alloc(&tmem_slot, Gm::kTmemCols);
+  // Q rows, swizzled K-major [half][row][128 B]; padding rows are zero
+  for (int i = tid; i < kPfRows * (D / 8); i += kPfThreads) {
+    const int r = i / (D / 8), c = i % (D / 8);
+    const int tk = r / G;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < TPB * G && tk < ntok)
+      v = *reinterpret_cast<const uint4*>(
+          p.q + ((int64_t)(q_begin + tok0 + tk) * p.Hq + h * G + r % G) * D + c * 8);
+    *reinterpret_cast<uint4*>(qs + (c >> 3) * (kPfRows * 128) + sw128_off(r, c & 7)) = v;
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
-  if (tid == 0) {
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  if (producer) {
     issue_tile(0);
     if (ntiles > 1) issue_tile(1);
   }
-  // this warp's columns: column r -> token r / G, head r % G of the group
-  __nv_bfloat16* qs = qs_all + warp * 16 * TileGeom<D>::kQStride;
-  for (int i = lane; i < 16 * (D / 8); i += 32) {
-    const int r = i / (D / 8), c = (i % (D / 8)) * 8;
-    const int tk = warp * TPW + r / G;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < TPW * G && tk < ntok)
-      v = *reinterpret_cast<const uint4*>(
-          p.q + ((int64_t)(q_begin + tok0 + tk) * p.Hq + h * G + r % G) * D + c);
-    *reinterpret_cast<uint4*>(qs + r * TileGeom<D>::kQStride + c) = v;
-  }
-  __syncwarp();
-  uint32_t qf[NQ][D / 16][2];
-  load_q_frags<D, NQ>(qf, qs, TileGeom<D>::kQStride);
 
-  const int t = lane & 3;
-  int pos[NQ][2];  // absolute position of each column, -1 for padding
-#pragma unroll
-  for (int nq = 0; nq < NQ; ++nq)
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      const int r = 8 * nq + 2 * t + cc;
-      const int tk = warp * TPW + r / G;
-      pos[nq][cc] = (r < TPW * G && tk < ntok) ? start + tok0 + tk : -1;
-    }
-  float* mgo = mg_all + warp * NV * 32 + lane;
-  SplitState<D, NQ> st;
-  float mg_m[NQ][2], mg_l[NQ][2];
-  bool have[NQ][2];
-#pragma unroll
-  for (int nq = 0; nq < NQ; ++nq)
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      mg_m[nq][cc] = -CUDART_INF_F;
-      mg_l[nq][cc] = 0.0f;
-      have[nq][cc] = false;
-    }
+  // ---- per-row state (softmax threads)
+  const int r = tid;
+  const int tk = r / G;
+  const int pos = (tid < kPfRows && r < TPB * G && tk < ntok) ? start + tok0 + tk : -1;
+  const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's lanes
+  float m = -CUDART_INF_F, l = 0.0f, mg_m = -CUDART_INF_F, mg_l = 0.0f;
+  bool have = false;
   const int S = p.split_size;
+  int n_issued = ntiles > 1 ? 2 : 1, n_landed = 0;  // producer: tiles copied / seen landed
+  int s_iss = -1, p_iss = -1;                        // producer: last tile of each MMA commit
+  bool ok = true;
   for (int i = 0; i < ntiles; ++i) {
-    const int bi_ = i & 1;
-    uint8_t* buf = bufs + bi_ * TileGeom<D>::kBufBytes;
+    const int stg = i & 1;
+    uint8_t* st = stages + stg * Gm::kStageBytes;
     const int key0 = i * kTile;
     const int lo = (key0 / S) * S;  // split start
-    if (key0 == lo) st.reset();
-    const bool landed = mbar_wait(&bars[bi_], (i >> 1) & 1, p.err, &s_abort);
-    if (__syncthreads_or(!landed)) {
-      if (tid == 0) {
-        s_abort = 1;
-        mbar_wait(&bars[bi_], (i >> 1) & 1, nullptr);
-        if (i + 1 < ntiles) mbar_wait(&bars[(i + 1) & 1], ((i + 1) >> 1) & 1, nullptr);
+    const bool split_first = key0 == lo;
+    const bool split_last = key0 + kTile == lo + S || i + 1 == ntiles;
+    // ---- S = Q K^T
+    if (producer) {
+      ok = mbar_wait(&bars[stg], (i >> 1) & 1, p.err, &s_abort);
+      if (ok) {
+        n_landed = i + 1;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t ad = umma_desc_sw128(
+              smem_u32(qs) + (ks >> 2) * (kPfRows * 128) + (ks & 3) * 32, 16, 1024);
+          const uint64_t bd = umma_desc_sw128(
+              smem_u32(st) + (ks >> 2) * (kTile * 128) + (ks & 3) * 32, 16, 1024);
+          tc_mma(tmem + Gm::kColS, ad, bd, kIdescS, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(sdone);
+        s_iss = i;
       }
-      __syncthreads();
+    }
+    // ---- softmax of this row over the tile
+    float alpha = 1.0f;
+    if (tid < kPfRows) {
+      ok = mbar_wait(&bars[stg], (i >> 1) & 1, p.err, &s_abort) &&
+           mbar_wait(sdone, i & 1, p.err, &s_abort);
+    }
+    if (__syncthreads_or(!ok)) {
+      ok = false;  // the same for every thread from here on
       break;
     }
-    if (key0 + kTile > kvl) {
-      clear_v_tail<D>(buf, key0, kvl, tid, blockDim.x);
-      __syncthreads();
-    }
-    int hcol[NQ][2];
-#pragma unroll
-    for (int nq = 0; nq < NQ; ++nq)
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc)
-        hcol[nq][cc] = pos[nq][cc] >= lo ? min(lo + S, pos[nq][cc] + 1) : lo;
-    tile_step<D, NQ>(st, qf, smem_u32(buf), smem_u32(buf + TileGeom<D>::kKBytes), key0, lo, hcol,
-                     p.scale_log2);
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (i + 2 < ntiles && tid == 0) issue_tile(i + 2);
-    // end of split: fold it into the merged state (columns that reach it)
-    if (key0 + kTile == lo + S || i + 1 == ntiles) {
-#pragma unroll
-      for (int nq = 0; nq < NQ; ++nq)
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          if (pos[nq][cc] < lo) continue;
-          if (!have[nq][cc]) {
-            mg_m[nq][cc] = st.m[nq][cc];
-            mg_l[nq][cc] = st.l[nq][cc];
-#pragma unroll
-            for (int md = 0; md < D / 16; ++md)
-#pragma unroll
-              for (int hf = 0; hf < 2; ++hf)
-                mgo[((md * NQ + nq) * 4 + 2 * hf + cc) * 32] = st.o[md][nq][2 * hf + cc];
-            have[nq][cc] = true;
-          } else {
-            float mn, ca, cb;
-            lse_coeffs(mg_m[nq][cc], st.m[nq][cc], mn, ca, cb);
-            mg_l[nq][cc] = lse_mix(mg_l[nq][cc], ca, st.l[nq][cc], cb);
-#pragma unroll
-            for (int md = 0; md < D / 16; ++md)
-#pragma unroll
-              for (int hf = 0; hf < 2; ++hf) {
-                float* a = &mgo[((md * NQ + nq) * 4 + 2 * hf + cc) * 32];
-                *a = lse_mix(*a, ca, st.o[md][nq][2 * hf + cc], cb);
-              }
-            mg_m[nq][cc] = mn;
-          }
+    if (tid < kPfRows) {
+      tc_fence_after();
+      if (key0 + kTile > kvl) {  // keys past the end: zero their V rows
+        const int first = kvl - key0;
+        for (int idx = tid; idx < (kTile - first) * Gm::kHalves * 8; idx += kPfRows) {
+          const int n = first + idx / (Gm::kHalves * 8);
+          const int rem = idx % (Gm::kHalves * 8);
+          *reinterpret_cast<uint4*>(st + Gm::kKBytes + (rem >> 3) * (kTile * 128) + n * 128 +
+                                    (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
+      }
+      uint32_t sv[2][32];
+      tmem_ld32_nowait(trow + Gm::kColS, sv[0]);
+      tmem_ld32_nowait(trow + Gm::kColS + 32, sv[1]);
+      tmem_wait_ld();
+      const int hi = pos >= lo ? min(lo + S, pos + 1) : lo;  // visible keys [lo, hi)
+      float x[kTile];
+      float mx = -CUDART_INF_F;
+#pragma unroll
+      for (int j = 0; j < kTile; ++j) {
+        const int k = key0 + j;
+        const float sj = __uint_as_float(sv[j >> 5][j & 31]);
+        x[j] = (k >= lo && k < hi) ? __fmul_rn(sj, p.scale_log2) : -CUDART_INF_F;
+        mx = fmaxf(mx, x[j]);
+      }
+      float mnew;
+      if (mx == -CUDART_INF_F) {  // no visible key: exact no-op for this row
+        mnew = m;
+      } else {
+        mnew = fmaxf(m, mx);
+        alpha = m == -CUDART_INF_F ? 0.0f : exp2f(__fsub_rn(m, mnew));
+      }
+      // key j goes to partial sum j % 8, each summed in increasing key
+      // order, then the pairwise tree ((0+1)+(2+3))+((4+5)+(6+7))
+      float cs[8];
+#pragma unroll
+      for (int g8 = 0; g8 < 8; ++g8) cs[g8] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < kTile; ++j) {
+        const float pj = x[j] == -CUDART_INF_F ? 0.0f : exp2f(__fsub_rn(x[j], mnew));
+        x[j] = pj;
+        cs[j & 7] = __fadd_rn(cs[j & 7], pj);
+      }
+      const float csum = __fadd_rn(__fadd_rn(__fadd_rn(cs[0], cs[1]), __fadd_rn(cs[2], cs[3])),
+                                   __fadd_rn(__fadd_rn(cs[4], cs[5]), __fadd_rn(cs[6], cs[7])));
+      l = __fadd_rn(__fmul_rn(l, alpha), csum);
+      m = mnew;
+      // P = hi + lo, both bf16, into shared memory
+#pragma unroll
+      for (int c = 0; c < kTile / 8; ++c) {
+        uint32_t wh[4], wl[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = x[8 * c + 2 * e], p1 = x[8 * c + 2 * e + 1];
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
+          __nv_bfloat162 hh;
+          hh.x = h0;
+          hh.y = h1;
+          wh[e] = *reinterpret_cast<uint32_t*>(&hh);
+          wl[e] = pack_bf16x2(__fsub_rn(p0, __bfloat162float(h0)),
+                              __fsub_rn(p1, __bfloat162float(h1)));
+        }
+        *reinterpret_cast<uint4*>(ph + sw128_off(r, c)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        *reinterpret_cast<uint4*>(pl + sw128_off(r, c)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+      }
+      // o *= alpha (the split's first tile starts o afresh instead)
+      if (!split_first && __any_sync(kFull, alpha != 1.0f)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(trow + Gm::kColO + 32 * c, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            v[e] = __float_as_uint(__fmul_rn(__uint_as_float(v[e]), alpha));
+          tmem_st32(trow + Gm::kColO + 32 * c, v);
+        }
+        tmem_wait_st();
+      }
+      fence_proxy_async_smem();  // P and the zeroed V rows, for the tensor core
+      tc_fence_before();
+    }
+    __syncthreads();
+    // ---- O += P V: per 16-key chunk the hi part, then the lo part
+    if (producer) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk) {
+        const uint64_t bd =
+            umma_desc_sw128(smem_u32(st + Gm::kKBytes) + kk * 2048, kTile * 128, 1024);
+        const uint64_t adh = umma_desc_sw128(smem_u32(ph) + kk * 32, 16, 1024);
+        const uint64_t adl = umma_desc_sw128(smem_u32(pl) + kk * 32, 16, 1024);
+        tc_mma(tmem + Gm::kColO, adh, bd, kIdescPV, (split_first && kk == 0) ? 0u : 1u);
+        tc_mma(tmem + Gm::kColO, adl, bd, kIdescPV, 1u);
+      }
+      tc_commit(pdone);
+      p_iss = i;
+    }
+    ok = mbar_wait(pdone, i & 1, p.err, &s_abort);
+    if (__syncthreads_or(!ok)) {
+      ok = false;  // the same for every thread from here on
+      break;
+    }
+    tc_fence_after();
+    if (producer && i + 2 < ntiles) {
+      issue_tile(i + 2);  // both MMAs that read this stage are complete
+      n_issued = i + 3;
+    }
+    // ---- end of a split: fold it into the merged state
+    if (tid < kPfRows && split_last) {
+      const bool part = pos >= lo;
+      float mn = 0.0f, ca = 0.0f, cb = 0.0f;
+      if (part && have) lse_coeffs(mg_m, m, mn, ca, cb);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t vo[32], vm[32];
+        tmem_ld32_nowait(trow + Gm::kColO + 32 * c, vo);
+        tmem_ld32_nowait(trow + Gm::kColM + 32 * c, vm);
+        tmem_wait_ld();
+        if (part) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            vm[e] = have ? __float_as_uint(lse_mix(__uint_as_float(vm[e]), ca,
+                                                   __uint_as_float(vo[e]), cb))
+                         : vo[e];
+        }
+        tmem_st32(trow + Gm::kColM + 32 * c, vm);
+      }
+      tmem_wait_st();
+      if (part) {
+        if (have) {
+          mg_l = lse_mix(mg_l, ca, l, cb);
+          mg_m = mn;
+        } else {
+          mg_m = m;
+          mg_l = l;
+          have = true;
+        }
+      }
+      m = -CUDART_INF_F;
+      l = 0.0f;
+    }
+    tc_fence_before();
+  }
+  if (!ok) {
+    // a wait ran out: bounded waits for the copies and MMAs still in flight
+    if (producer) {
+      for (int j = n_landed; j < n_issued; ++j) mbar_wait(&bars[j & 1], (j >> 1) & 1, nullptr);
+      if (s_iss >= 0) mbar_wait(sdone, s_iss & 1, nullptr);
+      if (p_iss >= 0) mbar_wait(pdone, p_iss & 1, nullptr);
+    }
+  } else if (tid < kPfRows) {
+    // ---- out = o / l of the merged state, bf16 (and fp32)
+    const int64_t orow = ((int64_t)(q_begin + tok0 + tk) * p.Hq + h * G + r % G) * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t v[32];
+      tmem_ld32(trow + Gm::kColM + 32 * c, v);  // the whole warp loads
+      if (pos < 0) continue;
+      float o[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = __fdiv_rn(__uint_as_float(v[e]), mg_l);
+#pragma unroll
+      for (int e = 0; e < 32; e += 8) {
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + 32 * c + e) =
+            make_uint4(pack_bf16x2(o[e], o[e + 1]), pack_bf16x2(o[e + 2], o[e + 3]),
+                       pack_bf16x2(o[e + 4], o[e + 5]), pack_bf16x2(o[e + 6], o[e + 7]));
+        if (p.out_f32) {
+          *reinterpret_cast<float4*>(p.out_f32 + orow + 32 * c + e) =
+              make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+          *reinterpret_cast<float4*>(p.out_f32 + orow + 32 * c + e + 4) =
+              make_float4(o[e + 4], o[e + 5], o[e + 6], o[e + 7]);
+        }
+      }
     }
   }
-  if (s_abort) return;
-  // ---- out = o / l; stage the warp's rows as [column][d] fp32, then store
-  float res[NV];
-#pragma unroll
-  for (int md = 0; md < D / 16; ++md)
-#pragma unroll
-    for (int nq = 0; nq < NQ; ++nq)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int i = (md * NQ + nq) * 4 + c;
-        res[i] = pos[nq][c & 1] < 0 ? 0.0f : __fdiv_rn(mgo[i * 32], mg_l[nq][c & 1]);
-      }
-  __syncwarp();
-  float* stage = mg_all + warp * NV * 32;  // [16 columns][D]
-  const int g = lane >> 2;
-#pragma unroll
-  for (int md = 0; md < D / 16; ++md)
-#pragma unroll
-    for (int nq = 0; nq < NQ; ++nq)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int col = 8 * nq + 2 * t + (c & 1);
-        const int d = 16 * md + g + 8 * (c >> 1);
-        stage[col * D + d] = res[(md * NQ + nq) * 4 + c];
-      }
-  __syncwarp();
-  for (int i = lane; i < 16 * (D / 8); i += 32) {
-    const int r = i / (D / 8), c8 = (i % (D / 8)) * 8;
-    const int tk = warp * TPW + r / G;
-    if (r >= TPW * G || tk >= ntok) continue;
-    const int64_t orow = ((int64_t)(q_begin + tok0 + tk) * p.Hq + h * G + r % G) * D + c8;
-    const float4 v0 = *reinterpret_cast<const float4*>(stage + r * D + c8);
-    const float4 v1 = *reinterpret_cast<const float4*>(stage + r * D + c8 + 4);
-    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow) =
-        make_uint4(pack_bf16x2(v0.x, v0.y), pack_bf16x2(v0.z, v0.w), pack_bf16x2(v1.x, v1.y),
-                   pack_bf16x2(v1.z, v1.w));
-    if (p.out_f32) {
-      *reinterpret_cast<float4*>(p.out_f32 + orow) = v0;
-      *reinterpret_cast<float4*>(p.out_f32 + orow + 4) = v1;
-    }
-  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, Gm::kTmemCols);
 }
 
 // --------------------------------------------------------------- KV write
@@ -1106,12 +1239,6 @@ template <int D, int NQ>
 size_t decode_smem() {
   return 1024 + 2 * TileGeom<D>::kBufBytes + 2 * 8 * NQ * D * 2 + 64;
 }
-template <int D>
-size_t prefill_smem() {
-  return 1024 + 2 * TileGeom<D>::kBufBytes + kPrefillWarps * 16 * TileGeom<D>::kQStride * 2 +
-         kPrefillWarps * (D / 16) * kPrefillNQ * 4 * 32 * 4 + 64;
-}
-
 KernelParams make_params(const AttnArgs& a) {
   KernelParams p{};
   p.q = static_cast<const __nv_bfloat16*>(a.q);
@@ -1235,11 +1362,11 @@ bi_status prefill_impl(const AttnArgs& a, cudaStream_t s) {
   if (!make_kv_maps(a, &km, &vm)) return BI_ERR_CUDA;
   KernelParams p = make_params(a);
   const int G = a.Hq / a.Hkv;
-  const int QB = kPrefillWarps * (16 / G);
-  const int nqb = (a.max_q_len + QB - 1) / QB;
-  const size_t sm = prefill_smem<D>();
+  const int TPB = kPfRows / G;  // tokens per block
+  const int nqb = (a.max_q_len + TPB - 1) / TPB;
+  const size_t sm = PfGeom<D>::kSmem;
   if (set_smem(attn_prefill_kernel<D>, sm) != cudaSuccess) return BI_ERR_CUDA;
-  attn_prefill_kernel<D><<<dim3(nqb, a.Hkv, a.B), kPrefillWarps * 32, sm, s>>>(km, vm, p);
+  attn_prefill_kernel<D><<<dim3(nqb, a.Hkv, a.B), kPfThreads, sm, s>>>(km, vm, p);
   return cuda_status(cudaGetLastError());
 }
 

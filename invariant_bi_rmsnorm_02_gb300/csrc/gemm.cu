@@ -36,6 +36,7 @@
 
 #include "bi_internal.h"
 #include "device_common.cuh"
+#include "tcgen05.cuh"
 
 namespace bi {
 namespace {
@@ -49,64 +50,12 @@ constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;  // two BN-column fp32 accumulators
 constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
 
-// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
-// (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 in bits
-// 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                            (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(BM >> 4) << 24);
+constexpr uint32_t kIdesc = umma_idesc_bf16(BM, BN, false, false);
 
-// Shared-memory matrix descriptor for a K-major tile written by TMA with
-// 128-byte swizzling: rows of 64 bf16 (128 B), 8-row groups 1024 B apart
-// (stride byte offset), descriptor version 1, layout SWIZZLE_128B (2).
+// K-major tiles written by TMA with 128-byte swizzling: rows of 64 bf16
+// (128 B), 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
-  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(1) << 16;            // leading byte offset (unused here)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;    // stride byte offset
-  d |= static_cast<uint64_t>(1) << 46;            // version
-  d |= static_cast<uint64_t>(2) << 61;            // 128-byte swizzle
-  return d;
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive on `bar` once every MMA issued so far by this thread has completed.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-// 32 lanes x 32 consecutive fp32 columns of the accumulator.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
-        "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
-        "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
-        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
-        "=r"(v[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  return umma_desc_sw128(saddr, 16, 1024);
 }
 
 struct GemmParams {
@@ -185,11 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(
     fence_mbar_init();
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(tmem_slot)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tmem_alloc(tmem_slot, kTmemCols);
   }
   tc_fence_before();
   __syncthreads();
@@ -253,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(
           const uint64_t bd = smem_desc(smem_u32(sB + stage * kBBytes));
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)  // +32 bytes along K per step
-            tc_mma(d_tmem, ad + 2u * k, bd + 2u * k, (kb > w.kb0 || k > 0) ? 1u : 0u);
+            tc_mma(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
           tc_commit(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;
@@ -328,9 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(kTmemCols)
-                 : "memory");
+    tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
