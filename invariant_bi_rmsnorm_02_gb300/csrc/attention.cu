@@ -857,23 +857,30 @@ __global__ void __launch_bounds__(D / 2) attn_decode_merge_kernel(const KernelPa
 
 // ---------------------------------------------------- prefill (tcgen05)
 // Block (qb, h, b): 128 query rows -- up to 128 / G tokens times the G heads
-// of kv head h (row r is token r / G, head r % G) -- with four softmax warps
-// (thread r owns row r, which is tensor-memory lane r) and a producer warp
-// whose lane 0 issues the TMA copies and the MMAs.  Per tile of 64 keys:
-//   S = Q K^T   tcgen05.mma M=128 N=64, k = d in steps of 16, into TMEM;
-//   softmax     each thread on its own row, with the decode tile step's
-//               per-element arithmetic, key summation tree and P = hi + lo
-//               split; P is staged in shared memory (K-major, swizzled);
-//   O += P V    tcgen05.mma M=128 N=D, for each 16-key chunk the hi part then
-//               the lo part, V read as an MN-major operand.
+// of kv head h (row r is token r / G, head r % G).  Per tile of 64 keys:
+//   S = Q K^T   tcgen05.mma M=128 N=64, k = d in steps of 16, into one of two
+//               TMEM buffers;
+//   softmax     the decode tile step's per-element arithmetic, key summation
+//               tree and P = hi + lo split, row by row; P goes to one of two
+//               shared buffers (K-major, swizzled);
+//   O += P V    tcgen05.mma M=128 N=D, per 16-key chunk the hi part then the
+//               lo part, V read as an MN-major operand.
 // tcgen05.mma and mma.sync give bit-identical fp32 results for the same
 // operands and k order, so every output row equals the decode of its
-// position bit for bit.  The split state (m, l in registers, o in TMEM) is
-// folded into the merged state (a second TMEM region) at each split end.
-// The tile loop is serial (MMA, softmax, MMA); blocks are started longest
-// first.
+// position bit for bit.
+// Warps 0-7 run the softmax: warps q and q+4 share rows 32q..32q+31 (TMEM
+// lanes of quadrant q); warp q takes keys 0-31 of each tile and the first D/2
+// output columns, warp q+4 keys 32-63 and the other columns.  The pair
+// exchanges the row maximum, and the first warp's partial key sums seed the
+// second warp's, so the summation order is the decode's.  Warp 8 is the
+// producer: TMA copies into a three-stage ring, MMA issue.  The S MMA of the
+// next tile and the PV MMA of this one run while the softmax works.  The
+// split state is folded into the merged state (a second TMEM region) at each
+// split end.  Blocks are started longest first.
 constexpr int kPfRows = 128;
-constexpr int kPfThreads = 160;
+constexpr int kPfSoftmaxWarps = 8;
+constexpr int kPfThreads = (kPfSoftmaxWarps + 1) * 32;
+constexpr int kPfStages = 3;
 
 template <int D>
 struct PfGeom {
@@ -881,20 +888,29 @@ struct PfGeom {
   static constexpr int kQBytes = kHalves * kPfRows * 128;  // [half][row][128 B]
   static constexpr int kKBytes = kHalves * kTile * 128;     // [half][key][128 B]
   static constexpr int kStageBytes = 2 * kKBytes;           // K then V
-  static constexpr int kPBytes = kPfRows * 128;             // [row][64 keys] bf16
+  static constexpr int kPBytes = kPfRows * 128;             // one part of P: [row][64 keys]
   static constexpr int kStageOff = kQBytes;
-  static constexpr int kPOff = kStageOff + 2 * kStageBytes;  // P high part, then low
-  static constexpr int kBarOff = kPOff + 2 * kPBytes;
-  static constexpr int kSmem = 1024 + kBarOff + 64;
+  static constexpr int kPOff = kStageOff + kPfStages * kStageBytes;  // [buffer][hi, lo]
+  static constexpr int kXOff = kPOff + 4 * kPBytes;
+  static constexpr int kXFloats = 2 * kPfRows + 8 * kPfRows + kPfRows + 32;
+  static constexpr int kBarOff = kXOff + kXFloats * 4;
+  static constexpr int kNumBars = kPfStages + 8;  // full[], sfull[2], sfree[2], pready[2], pdone[2]
+  static constexpr int kSmem = 1024 + kBarOff + kNumBars * 8;
   static constexpr uint32_t kTmemCols = D == 128 ? 512 : 256;
-  static constexpr uint32_t kColS = 0, kColO = 64, kColM = 64 + D;  // S, split o, merged o
+  // S buffers at columns 0 and 64, the split's o at 128, the merged o after it
+  static constexpr uint32_t kColS = 0, kColO = 128, kColM = 128 + D;
 };
+
+__device__ __forceinline__ void pair_sync(int id) {
+  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
 
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const KernelParams p) {
   using Gm = PfGeom<D>;
+  constexpr int DH = D / 2;  // output columns per softmax warp
   constexpr uint32_t kIdescS = umma_idesc_bf16(kPfRows, kTile, false, false);
   constexpr uint32_t kIdescPV = umma_idesc_bf16(kPfRows, D, false, true);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -902,18 +918,22 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
                                              ~uintptr_t(1023));
   uint8_t* qs = smem;
   uint8_t* stages = smem + Gm::kStageOff;
-  uint8_t* ph = smem + Gm::kPOff;
-  uint8_t* pl = ph + Gm::kPBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Gm::kBarOff);  // full[2], sdone, pdone
-  uint64_t* sdone = bars + 2;
-  uint64_t* pdone = bars + 3;
+  uint8_t* pbuf = smem + Gm::kPOff;
+  float* xmax = reinterpret_cast<float*>(smem + Gm::kXOff);  // [2][128] row max per key half
+  float* xcs = xmax + 2 * kPfRows;                             // [8][128] partial key sums
+  float* xl = xcs + 8 * kPfRows;                               // [128] merged l
+  int* xok = reinterpret_cast<int*>(xl + kPfRows);             // [3 points][2 halves][4 pairs]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Gm::kBarOff);
+  uint64_t* sfull = full + kPfStages;
+  uint64_t* sfree = sfull + 2;
+  uint64_t* pready = sfree + 2;
+  uint64_t* pdone = pready + 2;
   __shared__ uint32_t tmem_slot;
   __shared__ int s_abort;
 
   const int qb = gridDim.x - 1 - blockIdx.x;  // the longest query blocks start first
   const int h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const bool producer = tid == kPfRows;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.G, TPB = kPfRows / G;
   const int q_begin = p.cu_q[b];
   const int q_len = p.cu_q[b + 1] - q_begin;
@@ -938,26 +958,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       return;
     }
   }
-  auto issue_tile = [&](int i) {  // producer only
-    uint8_t* st = stages + (i & 1) * Gm::kStageBytes;
-    const int key0 = i * kTile;
-    const int np = pages_below(key0, kvl);
-    mbar_arrive_expect_tx(&bars[i & 1], np * 2 * Gm::kHalves * 2048);
-    for (int pp = 0; pp < np; ++pp) {
-      const int y = (bt_row[(key0 >> 4) + pp] * p.Hkv + h) * kPage;
-#pragma unroll
-      for (int hf = 0; hf < Gm::kHalves; ++hf) {
-        const int off = hf * (kTile * 128) + pp * 2048;
-        tma_load_2d(st + off, &kmap, hf * 64, y, &bars[i & 1]);
-        tma_load_2d(st + Gm::kKBytes + off, &vmap, hf * 64, y, &bars[i & 1]);
-      }
-    }
-  };
+  const int S = p.split_size;
   if (tid == 0) {
     s_abort = 0;
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
-    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < kPfStages; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sfull[i], 1);
+      mbar_init(&sfree[i], kPfSoftmaxWarps);
+      mbar_init(&pready[i], kPfSoftmaxWarps);
+      mbar_init(&pdone[i], 1);
+    }
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&tmem_slot, Gm::kTmemCols);
@@ -976,174 +988,140 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  if (producer) {
-    issue_tile(0);
-    if (ntiles > 1) issue_tile(1);
-  }
 
-  // ---- per-row state (softmax threads)
-  const int r = tid;
-  const int tk = r / G;
-  const int pos = (tid < kPfRows && r < TPB * G && tk < ntok) ? start + tok0 + tk : -1;
-  const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's lanes
-  float m = -CUDART_INF_F, l = 0.0f, mg_m = -CUDART_INF_F, mg_l = 0.0f;
-  bool have = false;
-  const int S = p.split_size;
-  int n_issued = ntiles > 1 ? 2 : 1, n_landed = 0;  // producer: tiles copied / seen landed
-  int s_iss = -1, p_iss = -1;                        // producer: last tile of each MMA commit
-  bool ok = true;
-  for (int i = 0; i < ntiles; ++i) {
-    const int stg = i & 1;
-    uint8_t* st = stages + stg * Gm::kStageBytes;
-    const int key0 = i * kTile;
-    const int lo = (key0 / S) * S;  // split start
-    const bool split_first = key0 == lo;
-    const bool split_last = key0 + kTile == lo + S || i + 1 == ntiles;
-    // ---- S = Q K^T
-    if (producer) {
-      ok = mbar_wait(&bars[stg], (i >> 1) & 1, p.err, &s_abort);
-      if (ok) {
-        n_landed = i + 1;
-        tc_fence_after();
+  if (warp == kPfSoftmaxWarps) {
+    // ================================================================ producer
+    auto issue_tile = [&](int i) {  // lane 0
+      const int stg = i % kPfStages;
+      uint8_t* st = stages + stg * Gm::kStageBytes;
+      const int key0 = i * kTile;
+      const int np = pages_below(key0, kvl);
+      mbar_arrive_expect_tx(&full[stg], np * 2 * Gm::kHalves * 2048);
+      for (int pp = 0; pp < np; ++pp) {
+        const int y = (bt_row[(key0 >> 4) + pp] * p.Hkv + h) * kPage;
+#pragma unroll
+        for (int hf = 0; hf < Gm::kHalves; ++hf) {
+          const int off = hf * (kTile * 128) + pp * 2048;
+          tma_load_2d(st + off, &kmap, hf * 64, y, &full[stg]);
+          tma_load_2d(st + Gm::kKBytes + off, &vmap, hf * 64, y, &full[stg]);
+        }
+      }
+    };
+    int issued = min(kPfStages, ntiles), landed = 0;
+    uint64_t* last_bar = nullptr;  // the latest MMA commit
+    uint32_t last_par = 0;
+    if (lane == 0)
+      for (int i = 0; i < issued; ++i) issue_tile(i);
+    // S of tile i once its copy landed and its TMEM buffer is free; the V
+    // rows past the end of the sequence are zeroed before any PV reads them
+    auto issue_s = [&](int i) -> bool {
+      const int b2 = i & 1;
+      const int stg = i % kPfStages;
+      uint8_t* st = stages + stg * Gm::kStageBytes;
+      bool w = mbar_wait(&full[stg], (i / kPfStages) & 1, p.err, &s_abort);
+      if (i >= 2) w = w && mbar_wait(&sfree[b2], ((i - 2) >> 1) & 1, p.err, &s_abort);
+      if (!__all_sync(kFull, w)) return false;
+      landed = i + 1;
+      tc_fence_after();
+      if (lane == 0) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint64_t ad = umma_desc_sw128(
               smem_u32(qs) + (ks >> 2) * (kPfRows * 128) + (ks & 3) * 32, 16, 1024);
           const uint64_t bd = umma_desc_sw128(
               smem_u32(st) + (ks >> 2) * (kTile * 128) + (ks & 3) * 32, 16, 1024);
-          tc_mma(tmem + Gm::kColS, ad, bd, kIdescS, ks > 0 ? 1u : 0u);
+          tc_mma(tmem + Gm::kColS + 64 * b2, ad, bd, kIdescS, ks > 0 ? 1u : 0u);
         }
-        tc_commit(sdone);
-        s_iss = i;
+        tc_commit(&sfull[b2]);
       }
-    }
-    // ---- softmax of this row over the tile
-    float alpha = 1.0f;
-    if (tid < kPfRows) {
-      ok = mbar_wait(&bars[stg], (i >> 1) & 1, p.err, &s_abort) &&
-           mbar_wait(sdone, i & 1, p.err, &s_abort);
-    }
-    if (__syncthreads_or(!ok)) {
-      ok = false;  // the same for every thread from here on
-      break;
-    }
-    if (tid < kPfRows) {
-      tc_fence_after();
-      if (key0 + kTile > kvl) {  // keys past the end: zero their V rows
+      last_bar = &sfull[b2];
+      last_par = (i >> 1) & 1;
+      const int key0 = i * kTile;
+      if (key0 + kTile > kvl) {
         const int first = kvl - key0;
-        for (int idx = tid; idx < (kTile - first) * Gm::kHalves * 8; idx += kPfRows) {
+        for (int idx = lane; idx < (kTile - first) * Gm::kHalves * 8; idx += 32) {
           const int n = first + idx / (Gm::kHalves * 8);
           const int rem = idx % (Gm::kHalves * 8);
           *reinterpret_cast<uint4*>(st + Gm::kKBytes + (rem >> 3) * (kTile * 128) + n * 128 +
                                     (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();
+        __syncwarp();
       }
-      uint32_t sv[2][32];
-      tmem_ld32_nowait(trow + Gm::kColS, sv[0]);
-      tmem_ld32_nowait(trow + Gm::kColS + 32, sv[1]);
-      tmem_wait_ld();
-      const int hi = pos >= lo ? min(lo + S, pos + 1) : lo;  // visible keys [lo, hi)
-      float x[kTile];
-      float mx = -CUDART_INF_F;
-#pragma unroll
-      for (int j = 0; j < kTile; ++j) {
-        const int k = key0 + j;
-        const float sj = __uint_as_float(sv[j >> 5][j & 31]);
-        x[j] = (k >= lo && k < hi) ? __fmul_rn(sj, p.scale_log2) : -CUDART_INF_F;
-        mx = fmaxf(mx, x[j]);
+      return true;
+    };
+    bool ok = issue_s(0);
+    for (int i = 0; i < ntiles && ok; ++i) {
+      const int b2 = i & 1;
+      const uint32_t ph2 = (i >> 1) & 1;
+      uint8_t* st = stages + (i % kPfStages) * Gm::kStageBytes;
+      const bool split_first = (i * kTile) % S == 0;
+      // the next tile's S goes to the tensor core ahead of this tile's PV,
+      // so that the softmax of tile i + 1 overlaps PV(i)
+      if (i + 1 < ntiles && !issue_s(i + 1)) {
+        ok = false;
+        break;
       }
-      float mnew;
-      if (mx == -CUDART_INF_F) {  // no visible key: exact no-op for this row
-        mnew = m;
-      } else {
-        mnew = fmaxf(m, mx);
-        alpha = m == -CUDART_INF_F ? 0.0f : exp2f(__fsub_rn(m, mnew));
+      ok = mbar_wait(&pready[b2], ph2, p.err, &s_abort);
+      if (!__all_sync(kFull, ok)) {
+        ok = false;
+        break;
       }
-      // key j goes to partial sum j % 8, each summed in increasing key
-      // order, then the pairwise tree ((0+1)+(2+3))+((4+5)+(6+7))
-      float cs[8];
-#pragma unroll
-      for (int g8 = 0; g8 < 8; ++g8) cs[g8] = 0.0f;
-#pragma unroll
-      for (int j = 0; j < kTile; ++j) {
-        const float pj = x[j] == -CUDART_INF_F ? 0.0f : exp2f(__fsub_rn(x[j], mnew));
-        x[j] = pj;
-        cs[j & 7] = __fadd_rn(cs[j & 7], pj);
-      }
-      const float csum = __fadd_rn(__fadd_rn(__fadd_rn(cs[0], cs[1]), __fadd_rn(cs[2], cs[3])),
-                                   __fadd_rn(__fadd_rn(cs[4], cs[5]), __fadd_rn(cs[6], cs[7])));
-      l = __fadd_rn(__fmul_rn(l, alpha), csum);
-      m = mnew;
-      // P = hi + lo, both bf16, into shared memory
-#pragma unroll
-      for (int c = 0; c < kTile / 8; ++c) {
-        uint32_t wh[4], wl[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = x[8 * c + 2 * e], p1 = x[8 * c + 2 * e + 1];
-          const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
-          __nv_bfloat162 hh;
-          hh.x = h0;
-          hh.y = h1;
-          wh[e] = *reinterpret_cast<uint32_t*>(&hh);
-          wl[e] = pack_bf16x2(__fsub_rn(p0, __bfloat162float(h0)),
-                              __fsub_rn(p1, __bfloat162float(h1)));
-        }
-        *reinterpret_cast<uint4*>(ph + sw128_off(r, c)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-        *reinterpret_cast<uint4*>(pl + sw128_off(r, c)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-      }
-      // o *= alpha (the split's first tile starts o afresh instead)
-      if (!split_first && __any_sync(kFull, alpha != 1.0f)) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(trow + Gm::kColO + 32 * c, v);
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            v[e] = __float_as_uint(__fmul_rn(__uint_as_float(v[e]), alpha));
-          tmem_st32(trow + Gm::kColO + 32 * c, v);
-        }
-        tmem_wait_st();
-      }
-      fence_proxy_async_smem();  // P and the zeroed V rows, for the tensor core
-      tc_fence_before();
-    }
-    __syncthreads();
-    // ---- O += P V: per 16-key chunk the hi part, then the lo part
-    if (producer) {
       tc_fence_after();
+      if (lane == 0) {  // ---- O += P V, per 16-key chunk the hi part then the lo part
+        const uint32_t pa = smem_u32(pbuf + b2 * 2 * Gm::kPBytes);
 #pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk) {
-        const uint64_t bd =
-            umma_desc_sw128(smem_u32(st + Gm::kKBytes) + kk * 2048, kTile * 128, 1024);
-        const uint64_t adh = umma_desc_sw128(smem_u32(ph) + kk * 32, 16, 1024);
-        const uint64_t adl = umma_desc_sw128(smem_u32(pl) + kk * 32, 16, 1024);
-        tc_mma(tmem + Gm::kColO, adh, bd, kIdescPV, (split_first && kk == 0) ? 0u : 1u);
-        tc_mma(tmem + Gm::kColO, adl, bd, kIdescPV, 1u);
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint64_t bd =
+              umma_desc_sw128(smem_u32(st + Gm::kKBytes) + kk * 2048, kTile * 128, 1024);
+          const uint64_t adh = umma_desc_sw128(pa + kk * 32, 16, 1024);
+          const uint64_t adl = umma_desc_sw128(pa + Gm::kPBytes + kk * 32, 16, 1024);
+          tc_mma(tmem + Gm::kColO, adh, bd, kIdescPV, (split_first && kk == 0) ? 0u : 1u);
+          tc_mma(tmem + Gm::kColO, adl, bd, kIdescPV, 1u);
+        }
+        tc_commit(&pdone[b2]);
       }
-      tc_commit(pdone);
-      p_iss = i;
+      last_bar = &pdone[b2];
+      last_par = ph2;
+      if (i >= 1) {  // PV of the previous tile done: its stage takes a new copy
+        ok = mbar_wait(&pdone[(i - 1) & 1], ((i - 1) >> 1) & 1, p.err, &s_abort);
+        if (!__all_sync(kFull, ok)) {
+          ok = false;
+          break;
+        }
+        if (i - 1 + kPfStages < ntiles) {
+          if (lane == 0) issue_tile(i - 1 + kPfStages);
+          issued = i - 1 + kPfStages + 1;
+        }
+      }
     }
-    ok = mbar_wait(pdone, i & 1, p.err, &s_abort);
-    if (__syncthreads_or(!ok)) {
-      ok = false;  // the same for every thread from here on
-      break;
+    if (!ok && lane == 0) {
+      // a wait ran out: bounded waits for the copies and MMAs still in flight
+      for (int j = landed; j < issued; ++j)
+        mbar_wait(&full[j % kPfStages], (j / kPfStages) & 1, nullptr);
+      if (last_bar) mbar_wait(last_bar, last_par, nullptr);
     }
-    tc_fence_after();
-    if (producer && i + 2 < ntiles) {
-      issue_tile(i + 2);  // both MMAs that read this stage are complete
-      n_issued = i + 3;
-    }
-    // ---- end of a split: fold it into the merged state
-    if (tid < kPfRows && split_last) {
-      const bool part = pos >= lo;
+  } else {
+    // ================================================================= softmax
+    const int q4 = warp & 3, hk = warp >> 2;  // row quadrant, key / column half
+    const int r = q4 * 32 + lane;
+    const int tk = r / G;
+    const int pos = (r < TPB * G && tk < ntok) ? start + tok0 + tk : -1;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+    const int bar_id = 1 + q4;
+    float m = -CUDART_INF_F, l = 0.0f;        // split state (l kept by the second warp)
+    float mg_m = -CUDART_INF_F, mg_l = 0.0f;  // merged state
+    bool have = false;
+    // fold the finished split (m_s, l_s, o in TMEM) into the merged state
+    auto fold = [&](float m_s, float l_s, int lo_s) {
+      const bool part = pos >= lo_s;
       float mn = 0.0f, ca = 0.0f, cb = 0.0f;
-      if (part && have) lse_coeffs(mg_m, m, mn, ca, cb);
+      if (part && have) lse_coeffs(mg_m, m_s, mn, ca, cb);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < DH / 32; ++c) {
         uint32_t vo[32], vm[32];
-        tmem_ld32_nowait(trow + Gm::kColO + 32 * c, vo);
-        tmem_ld32_nowait(trow + Gm::kColM + 32 * c, vm);
+        tmem_ld32_nowait(tl + Gm::kColO + hk * DH + 32 * c, vo);
+        tmem_ld32_nowait(tl + Gm::kColM + hk * DH + 32 * c, vm);
         tmem_wait_ld();
         if (part) {
 #pragma unroll
@@ -1152,52 +1130,195 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
                                                    __uint_as_float(vo[e]), cb))
                          : vo[e];
         }
-        tmem_st32(trow + Gm::kColM + 32 * c, vm);
+        tmem_st32(tl + Gm::kColM + hk * DH + 32 * c, vm);
       }
       tmem_wait_st();
       if (part) {
         if (have) {
-          mg_l = lse_mix(mg_l, ca, l, cb);
+          mg_l = lse_mix(mg_l, ca, l_s, cb);
           mg_m = mn;
         } else {
-          mg_m = m;
-          mg_l = l;
+          mg_m = m_s;
+          mg_l = l_s;
           have = true;
         }
       }
-      m = -CUDART_INF_F;
-      l = 0.0f;
+    };
+    bool ok = true;
+    for (int i = 0; i < ntiles; ++i) {
+      const int b2 = i & 1;
+      const uint32_t ph2 = (i >> 1) & 1;
+      const int key0 = i * kTile;
+      const int lo = (key0 / S) * S;  // split start
+      const bool split_first = key0 == lo;
+      float m_s = 0.0f, l_s = 0.0f;  // the split that ended with the previous tile
+      if (split_first && i > 0) {
+        m_s = m;
+        l_s = l;
+        m = -CUDART_INF_F;
+        l = 0.0f;
+      }
+      // ---- this warp's 32 keys of the tile
+      bool okw = __all_sync(kFull, mbar_wait(&sfull[b2], ph2, p.err, &s_abort));
+      uint32_t sv[32];
+      if (okw) {
+        tc_fence_after();
+        tmem_ld32(tl + Gm::kColS + 64 * b2 + 32 * hk, sv);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sfree[b2]);
+      const bool all_vis = key0 + kTile - 1 <= start + tok0;  // every row sees the tile
+      const int nvis = pos >= lo ? min(min(lo + S, pos + 1) - key0, kTile) : 0;
+      float x[32];
+      float pm = -CUDART_INF_F;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float sj = __fmul_rn(__uint_as_float(sv[j]), p.scale_log2);
+        x[j] = (all_vis || 32 * hk + j < nvis) ? sj : -CUDART_INF_F;
+        pm = fmaxf(pm, x[j]);
+      }
+      xmax[hk * kPfRows + r] = pm;
+      if (lane == 0) xok[(0 * 2 + hk) * 4 + q4] = okw;
+      pair_sync(bar_id);
+      if (!(xok[(0 * 2 + 0) * 4 + q4] && xok[(0 * 2 + 1) * 4 + q4])) {
+        ok = false;
+        break;
+      }
+      const float mx = fmaxf(xmax[r], xmax[kPfRows + r]);
+      float mnew, alpha = 1.0f;
+      if (mx == -CUDART_INF_F) {  // no visible key: exact no-op for this row
+        mnew = m;
+      } else {
+        mnew = fmaxf(m, mx);
+        alpha = m == -CUDART_INF_F ? 0.0f : exp2f(__fsub_rn(m, mnew));
+      }
+      // probabilities; key j of the tile adds to partial sum j % 8, each in
+      // increasing key order, the first warp's four keys before the second's
+      float cs[8];
+#pragma unroll
+      for (int g8 = 0; g8 < 8; ++g8) cs[g8] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float pj =
+            (all_vis || x[j] != -CUDART_INF_F) ? exp2f(__fsub_rn(x[j], mnew)) : 0.0f;
+        x[j] = pj;
+        if (hk == 0) cs[j & 7] = __fadd_rn(cs[j & 7], pj);
+      }
+      if (hk == 0) {
+#pragma unroll
+        for (int g8 = 0; g8 < 8; ++g8) xcs[g8 * kPfRows + r] = cs[g8];
+      }
+      // P = hi + lo into buffer b2, once the PV of two tiles ago has read it
+      if (i >= 2) okw = __all_sync(kFull, mbar_wait(&pdone[b2], ((i - 2) >> 1) & 1, p.err,
+                                                    &s_abort));
+      if (okw) {
+        uint8_t* ph = pbuf + b2 * 2 * Gm::kPBytes;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t wh[4], wl[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float p0 = x[8 * cc + 2 * e], p1 = x[8 * cc + 2 * e + 1];
+            const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
+            __nv_bfloat162 hh;
+            hh.x = h0;
+            hh.y = h1;
+            wh[e] = *reinterpret_cast<uint32_t*>(&hh);
+            wl[e] = pack_bf16x2(__fsub_rn(p0, __bfloat162float(h0)),
+                                __fsub_rn(p1, __bfloat162float(h1)));
+          }
+          const uint32_t off = sw128_off(r, 4 * hk + cc);
+          *reinterpret_cast<uint4*>(ph + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+          *reinterpret_cast<uint4*>(ph + Gm::kPBytes + off) =
+              make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        }
+        fence_proxy_async_smem();
+      }
+      if (lane == 0) xok[(1 * 2 + hk) * 4 + q4] = okw;
+      pair_sync(bar_id);
+      if (!(xok[(1 * 2 + 0) * 4 + q4] && xok[(1 * 2 + 1) * 4 + q4])) {
+        ok = false;
+        break;
+      }
+      if (hk == 1) {
+#pragma unroll
+        for (int g8 = 0; g8 < 8; ++g8) {
+          float c8 = xcs[g8 * kPfRows + r];
+#pragma unroll
+          for (int t4 = 0; t4 < 4; ++t4) c8 = __fadd_rn(c8, x[g8 + 8 * t4]);
+          cs[g8] = c8;
+        }
+        const float csum =
+            __fadd_rn(__fadd_rn(__fadd_rn(cs[0], cs[1]), __fadd_rn(cs[2], cs[3])),
+                      __fadd_rn(__fadd_rn(cs[4], cs[5]), __fadd_rn(cs[6], cs[7])));
+        l = __fadd_rn(__fmul_rn(l, alpha), csum);
+      }
+      m = mnew;
+      // ---- the previous tile's PV is done: fold a finished split, or o *= alpha
+      if (i >= 1)
+        okw = __all_sync(kFull, mbar_wait(&pdone[(i - 1) & 1], ((i - 1) >> 1) & 1, p.err,
+                                          &s_abort));
+      if (okw) {
+        tc_fence_after();
+        if (split_first && i > 0) {
+          fold(m_s, l_s, lo - S);
+        } else if (!split_first && __any_sync(kFull, alpha != 1.0f)) {
+#pragma unroll
+          for (int c = 0; c < DH / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tl + Gm::kColO + hk * DH + 32 * c, v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              v[e] = __float_as_uint(__fmul_rn(__uint_as_float(v[e]), alpha));
+            tmem_st32(tl + Gm::kColO + hk * DH + 32 * c, v);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pready[b2]);
+      } else {
+        ok = false;  // the next pair check stops both warps
+      }
     }
-    tc_fence_before();
-  }
-  if (!ok) {
-    // a wait ran out: bounded waits for the copies and MMAs still in flight
-    if (producer) {
-      for (int j = n_landed; j < n_issued; ++j) mbar_wait(&bars[j & 1], (j >> 1) & 1, nullptr);
-      if (s_iss >= 0) mbar_wait(sdone, s_iss & 1, nullptr);
-      if (p_iss >= 0) mbar_wait(pdone, p_iss & 1, nullptr);
+    // ---- the last split, then out = o / l
+    if (ok) {
+      const int i = ntiles - 1;
+      ok = __all_sync(kFull, mbar_wait(&pdone[i & 1], (i >> 1) & 1, p.err, &s_abort));
+      if (ok) {
+        tc_fence_after();
+        fold(m, l, ((i * kTile) / S) * S);
+      }
     }
-  } else if (tid < kPfRows) {
-    // ---- out = o / l of the merged state, bf16 (and fp32)
-    const int64_t orow = ((int64_t)(q_begin + tok0 + tk) * p.Hq + h * G + r % G) * D;
+    if (hk == 1) xl[r] = mg_l;
+    if (lane == 0) xok[(2 * 2 + hk) * 4 + q4] = ok;
+    pair_sync(bar_id);
+    ok = xok[(2 * 2 + 0) * 4 + q4] && xok[(2 * 2 + 1) * 4 + q4];
+    if (ok) {
+      tc_fence_after();
+      const float lv = xl[r];
+      const int64_t orow =
+          ((int64_t)(q_begin + tok0 + tk) * p.Hq + h * G + r % G) * D + hk * DH;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t v[32];
-      tmem_ld32(trow + Gm::kColM + 32 * c, v);  // the whole warp loads
-      if (pos < 0) continue;
-      float o[32];
+      for (int c = 0; c < DH / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tl + Gm::kColM + hk * DH + 32 * c, v);  // the whole warp loads
+        if (pos < 0) continue;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) o[e] = __fdiv_rn(__uint_as_float(v[e]), mg_l);
+        for (int e = 0; e < 32; e += 8) {
+          float o[8];
 #pragma unroll
-      for (int e = 0; e < 32; e += 8) {
-        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + 32 * c + e) =
-            make_uint4(pack_bf16x2(o[e], o[e + 1]), pack_bf16x2(o[e + 2], o[e + 3]),
-                       pack_bf16x2(o[e + 4], o[e + 5]), pack_bf16x2(o[e + 6], o[e + 7]));
-        if (p.out_f32) {
-          *reinterpret_cast<float4*>(p.out_f32 + orow + 32 * c + e) =
-              make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-          *reinterpret_cast<float4*>(p.out_f32 + orow + 32 * c + e + 4) =
-              make_float4(o[e + 4], o[e + 5], o[e + 6], o[e + 7]);
+          for (int u = 0; u < 8; ++u) o[u] = __fdiv_rn(__uint_as_float(v[e + u]), lv);
+          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + 32 * c + e) =
+              make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                         pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+          if (p.out_f32) {
+            *reinterpret_cast<float4*>(p.out_f32 + orow + 32 * c + e) =
+                make_float4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<float4*>(p.out_f32 + orow + 32 * c + e + 4) =
+                make_float4(o[4], o[5], o[6], o[7]);
+          }
         }
       }
     }
