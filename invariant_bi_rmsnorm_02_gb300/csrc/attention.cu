@@ -17,7 +17,9 @@
 // Decode runs a small plan kernel (the list of (sequence, split) units), a
 // persistent split kernel whose blocks walk that list, and a merge kernel;
 // prefill runs one block per (query block, kv head, sequence) and folds its
-// splits as it goes.  Both call the same tile step and the same fold, so a
+// splits as it goes.  Decode (mma.sync) and prefill (tcgen05) perform the
+// same per-element arithmetic in the same order, and the two instructions
+// give bit-identical fp32 results for the same operands and k order, so a
 // prefill row at position p is bit-identical to a decode with L = p + 1,
 // whatever the chunking.
 //
@@ -27,7 +29,7 @@
 // P^T comes from the S^T accumulators by an in-register 8x8 transpose
 // (movmatrix).  A decode row group (the G query heads of one kv head) fills
 // one 8-wide n-tile, so padding costs at most half of an n-tile.  Scores are
-// scaled by sm_scale*log2(e) and exponentiated with exp2f; P is split into a
+// scaled by sm_scale*log2(e) and exponentiated with ex2.approx; P is split into a
 // bf16 high part and a bf16 low part (P - hi), both multiplied with V, so the
 // probabilities keep ~16 significant bits.  Column max / sum use a fixed
 // shuffle tree.  Explicit __fmul_rn/__fadd_rn keep the compiler from
@@ -70,6 +72,15 @@ template <int D>
 __device__ __forceinline__ uint32_t tile_off(int n, int d) {
   const int p = n >> 4, r = n & 15, hf = d >> 6, chunk = (d & 63) >> 3;
   return (uint32_t)((p * TileGeom<D>::kHalves + hf) * 2048 + r * 128 + ((chunk ^ (r & 7)) << 4));
+}
+
+// 2^x on the special function unit (ex2.approx.ftz: relative error about
+// 2^-22, results below 2^-126 flushed to zero).  Decode and prefill use it
+// for the probabilities and the rescale factors.
+__device__ __forceinline__ float exp2_sfu(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // ----------------------------------------------------------- warp MMA helpers
@@ -198,7 +209,7 @@ __device__ __forceinline__ void tile_step(SplitState<D, NQ>& st,
       } else {
         mnew[cc] = fmaxf(st.m[nq][cc], mx[nq][cc]);
         alpha[nq][cc] =
-            st.m[nq][cc] == -CUDART_INF_F ? 0.0f : exp2f(__fsub_rn(st.m[nq][cc], mnew[cc]));
+            st.m[nq][cc] == -CUDART_INF_F ? 0.0f : exp2_sfu(__fsub_rn(st.m[nq][cc], mnew[cc]));
       }
     }
     float cs[2] = {0.0f, 0.0f};
@@ -208,7 +219,7 @@ __device__ __forceinline__ void tile_step(SplitState<D, NQ>& st,
       for (int c = 0; c < 4; ++c) {
         const int cc = c & 1;
         const float x = s[mt][nq][c];
-        const float pv = x == -CUDART_INF_F ? 0.0f : exp2f(__fsub_rn(x, mnew[cc]));
+        const float pv = x == -CUDART_INF_F ? 0.0f : exp2_sfu(__fsub_rn(x, mnew[cc]));
         s[mt][nq][c] = pv;
         cs[cc] = __fadd_rn(cs[cc], pv);
       }
@@ -1172,11 +1183,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       const int nvis = pos >= lo ? min(min(lo + S, pos + 1) - key0, kTile) : 0;
       float x[32];
       float pm = -CUDART_INF_F;
+      if (all_vis) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float sj = __fmul_rn(__uint_as_float(sv[j]), p.scale_log2);
-        x[j] = (all_vis || 32 * hk + j < nvis) ? sj : -CUDART_INF_F;
-        pm = fmaxf(pm, x[j]);
+        for (int j = 0; j < 32; ++j) {
+          x[j] = __fmul_rn(__uint_as_float(sv[j]), p.scale_log2);
+          pm = fmaxf(pm, x[j]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          x[j] = 32 * hk + j < nvis ? __fmul_rn(__uint_as_float(sv[j]), p.scale_log2)
+                                    : -CUDART_INF_F;
+          pm = fmaxf(pm, x[j]);
+        }
       }
       xmax[hk * kPfRows + r] = pm;
       if (lane == 0) xok[(0 * 2 + hk) * 4 + q4] = okw;
@@ -1191,19 +1210,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
         mnew = m;
       } else {
         mnew = fmaxf(m, mx);
-        alpha = m == -CUDART_INF_F ? 0.0f : exp2f(__fsub_rn(m, mnew));
+        alpha = m == -CUDART_INF_F ? 0.0f : exp2_sfu(__fsub_rn(m, mnew));
       }
       // probabilities; key j of the tile adds to partial sum j % 8, each in
       // increasing key order, the first warp's four keys before the second's
       float cs[8];
 #pragma unroll
       for (int g8 = 0; g8 < 8; ++g8) cs[g8] = 0.0f;
+      if (all_vis) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float pj =
-            (all_vis || x[j] != -CUDART_INF_F) ? exp2f(__fsub_rn(x[j], mnew)) : 0.0f;
-        x[j] = pj;
-        if (hk == 0) cs[j & 7] = __fadd_rn(cs[j & 7], pj);
+        for (int j = 0; j < 32; ++j) x[j] = exp2_sfu(__fsub_rn(x[j], mnew));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          x[j] = x[j] != -CUDART_INF_F ? exp2_sfu(__fsub_rn(x[j], mnew)) : 0.0f;
+      }
+      if (hk == 0) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) cs[j & 7] = __fadd_rn(cs[j & 7], x[j]);
       }
       if (hk == 0) {
 #pragma unroll
