@@ -880,17 +880,22 @@ __global__ void __launch_bounds__(D / 2) attn_decode_merge_kernel(const KernelPa
 // operands and k order, so every output row equals the decode of its
 // position bit for bit.
 // Warps 0-7 run the softmax: warps q and q+4 share rows 32q..32q+31 (TMEM
-// lanes of quadrant q); warp q takes keys 0-31 of each tile and the first D/2
-// output columns, warp q+4 keys 32-63 and the other columns.  The pair
-// exchanges the row maximum, and the first warp's partial key sums seed the
-// second warp's, so the summation order is the decode's.  Warp 8 is the
-// producer: TMA copies into a three-stage ring, MMA issue.  The S MMA of the
-// next tile and the PV MMA of this one run while the softmax works.  The
-// split state is folded into the merged state (a second TMEM region) at each
-// split end.  Blocks are started longest first.
+// lanes of quadrant q) and take the tiles alternately, warp q the even ones.
+// A warp hands the running maximum of its tile to its partner as soon as it
+// is known, and the sums and merged state when the tile is done (through
+// shared memory, one mbarrier phase per tile: a waiter never counts as an
+// arrival, so the handoffs cannot pair up wrongly), and the partner's score
+// load, maximum and exponentials for the next tile overlap this tile's wait
+// for PV and its rescale.  Warp 8 is the
+// producer: TMA copies into a three-stage ring, MMA issue; the S MMA of the
+// next tile goes to the tensor core ahead of the PV of this one.  The split
+// state is folded into the merged state (a second TMEM region) at each split
+// end.  Blocks are started longest first.
 constexpr int kPfRows = 128;
 constexpr int kPfSoftmaxWarps = 8;
-constexpr int kPfThreads = (kPfSoftmaxWarps + 1) * 32;
+constexpr int kPfThreads = (kPfSoftmaxWarps + 2) * 32;  // + MMA warp + TMA warp
+constexpr int kPfMmaWarp = kPfSoftmaxWarps, kPfTmaWarp = kPfSoftmaxWarps + 1;
+constexpr int kPfPageCache = 2048;  // page ids held in shared memory (32768 keys)
 constexpr int kPfStages = 3;
 
 template <int D>
@@ -898,30 +903,29 @@ struct PfGeom {
   static constexpr int kHalves = D / 64;
   static constexpr int kQBytes = kHalves * kPfRows * 128;  // [half][row][128 B]
   static constexpr int kKBytes = kHalves * kTile * 128;     // [half][key][128 B]
-  static constexpr int kStageBytes = 2 * kKBytes;           // K then V
+  static constexpr int kStageBytes = 2 * kKBytes;           // one K and one V tile
   static constexpr int kPBytes = kPfRows * 128;             // one part of P: [row][64 keys]
   static constexpr int kStageOff = kQBytes;
   static constexpr int kPOff = kStageOff + kPfStages * kStageBytes;  // [buffer][hi, lo]
   static constexpr int kXOff = kPOff + 4 * kPBytes;
-  static constexpr int kXFloats = 2 * kPfRows + 8 * kPfRows + kPfRows + 32;
-  static constexpr int kBarOff = kXOff + kXFloats * 4;
-  static constexpr int kNumBars = kPfStages + 8;  // full[], sfull[2], sfree[2], pready[2], pdone[2]
+  static constexpr int kXFloats = 5 * kPfRows;
+  static constexpr int kPidOff = kXOff + kXFloats * 4;
+  static constexpr int kBarOff = kPidOff + kPfPageCache * 4;
+  // kfull[], vfull[], kfree[], vfree[], sfull[2], sfree[2], pready[2], pdone[2],
+  // hm[4], hst[4]
+  static constexpr int kNumBars = 4 * kPfStages + 16;
   static constexpr int kSmem = 1024 + kBarOff + kNumBars * 8;
   static constexpr uint32_t kTmemCols = D == 128 ? 512 : 256;
   // S buffers at columns 0 and 64, the split's o at 128, the merged o after it
   static constexpr uint32_t kColS = 0, kColO = 128, kColM = 128 + D;
 };
 
-__device__ __forceinline__ void pair_sync(int id) {
-  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
-}
 
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const KernelParams p) {
   using Gm = PfGeom<D>;
-  constexpr int DH = D / 2;  // output columns per softmax warp
   constexpr uint32_t kIdescS = umma_idesc_bf16(kPfRows, kTile, false, false);
   constexpr uint32_t kIdescPV = umma_idesc_bf16(kPfRows, D, false, true);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -930,15 +934,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   uint8_t* qs = smem;
   uint8_t* stages = smem + Gm::kStageOff;
   uint8_t* pbuf = smem + Gm::kPOff;
-  float* xmax = reinterpret_cast<float*>(smem + Gm::kXOff);  // [2][128] row max per key half
-  float* xcs = xmax + 2 * kPfRows;                             // [8][128] partial key sums
-  float* xl = xcs + 8 * kPfRows;                               // [128] merged l
-  int* xok = reinterpret_cast<int*>(xl + kPfRows);             // [3 points][2 halves][4 pairs]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Gm::kBarOff);
-  uint64_t* sfull = full + kPfStages;
+  float* xm = reinterpret_cast<float*>(smem + Gm::kXOff);  // [128] running max, to the next tile
+  float* xst = xm + kPfRows;  // [4][128] l, merged m, merged l, merged-yet, to the next tile
+  uint8_t* kst = stages;                            // K ring: kPfStages tiles
+  uint8_t* vst = stages + kPfStages * Gm::kKBytes;  // V ring: kPfStages tiles
+  int* pid_s = reinterpret_cast<int*>(smem + Gm::kPidOff);  // page ids of this sequence
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + Gm::kBarOff);
+  uint64_t* vfull = kfull + kPfStages;
+  uint64_t* kfree = vfull + kPfStages;  // the S that read the K stage is done
+  uint64_t* vfree = kfree + kPfStages;  // the PV that read the V stage is done
+  uint64_t* sfull = vfree + kPfStages;
   uint64_t* sfree = sfull + 2;
   uint64_t* pready = sfree + 2;
   uint64_t* pdone = pready + 2;
+  uint64_t* hm = pdone + 2;   // per row quadrant: the running max of a tile is written
+  uint64_t* hst = hm + 4;     // per row quadrant: the sums and merged state of a tile are written
   __shared__ uint32_t tmem_slot;
   __shared__ int s_abort;
 
@@ -961,8 +971,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   const int32_t* bt_row = p.block_table + (int64_t)b * p.max_blocks;
   const int ntiles = (p_last + kTile) / kTile;  // tiles 0 .. covering key p_last
   {
-    const int loaded_hi = min(kvl, ntiles * kTile);  // keys a tile copy may read
-    bool ok = pages_ok(bt_row, 0, loaded_hi, p.num_pages, tid, blockDim.x);
+    // check every page a tile copy may read, and keep the first ids at hand
+    const int loaded_hi = min(kvl, ntiles * kTile);
+    bool ok = true;
+    for (int pg = tid; pg * kPage < loaded_hi; pg += kPfThreads) {
+      const int v = bt_row[pg];
+      if (v < 0 || v >= p.num_pages) ok = false;
+      if (pg < kPfPageCache) pid_s[pg] = v;
+    }
     ok = __syncthreads_and(ok);
     if (!ok) {
       if (tid == 0) record_error(p.err, BI_ERR_DEVICE_BOUNDS);
@@ -974,12 +990,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     s_abort = 0;
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
-    for (int i = 0; i < kPfStages; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < kPfStages; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&vfull[i], 1);
+      mbar_init(&kfree[i], 1);
+      mbar_init(&vfree[i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sfull[i], 1);
-      mbar_init(&sfree[i], kPfSoftmaxWarps);
-      mbar_init(&pready[i], kPfSoftmaxWarps);
+      mbar_init(&sfree[i], kPfSoftmaxWarps / 2);   // the four warps of that tile parity
+      mbar_init(&pready[i], kPfSoftmaxWarps / 2);
       mbar_init(&pdone[i], 1);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&hm[i], 32);  // every lane of the warp that wrote its rows
+      mbar_init(&hst[i], 32);
     }
     fence_mbar_init();
   }
@@ -1000,139 +1025,163 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == kPfSoftmaxWarps) {
-    // ================================================================ producer
-    auto issue_tile = [&](int i) {  // lane 0
+  if (warp == kPfTmaWarp) {
+    // ================================================================ copies
+    // K and V tiles of 64 keys stream through separate rings of kPfStages
+    // stages: a K stage is free once the S that read it is done, a V stage
+    // once its PV is.  Copies go out in the order they are needed (K of tile
+    // i, V of tile i-1), which is also the order in which stages free up.
+    auto issue_copy = [&](int i, bool is_v) {  // lane 0
       const int stg = i % kPfStages;
-      uint8_t* st = stages + stg * Gm::kStageBytes;
+      uint8_t* dst = (is_v ? vst : kst) + stg * Gm::kKBytes;
+      uint64_t* bar = is_v ? &vfull[stg] : &kfull[stg];
       const int key0 = i * kTile;
       const int np = pages_below(key0, kvl);
-      mbar_arrive_expect_tx(&full[stg], np * 2 * Gm::kHalves * 2048);
+      mbar_arrive_expect_tx(bar, np * Gm::kHalves * 2048);
       for (int pp = 0; pp < np; ++pp) {
-        const int y = (bt_row[(key0 >> 4) + pp] * p.Hkv + h) * kPage;
+        const int pg = (key0 >> 4) + pp;
+        const int y = ((pg < kPfPageCache ? pid_s[pg] : bt_row[pg]) * p.Hkv + h) * kPage;
 #pragma unroll
-        for (int hf = 0; hf < Gm::kHalves; ++hf) {
-          const int off = hf * (kTile * 128) + pp * 2048;
-          tma_load_2d(st + off, &kmap, hf * 64, y, &full[stg]);
-          tma_load_2d(st + Gm::kKBytes + off, &vmap, hf * 64, y, &full[stg]);
-        }
+        for (int hf = 0; hf < Gm::kHalves; ++hf)
+          tma_load_2d(dst + hf * (kTile * 128) + pp * 2048, is_v ? &vmap : &kmap, hf * 64, y,
+                      bar);
       }
     };
-    int issued = min(kPfStages, ntiles), landed = 0;
+    const int n0 = min(kPfStages, ntiles);
+    int k_issued = n0, v_issued = n0;
+    if (lane == 0) {
+      for (int i = 0; i < n0; ++i) issue_copy(i, false);
+      for (int i = 0; i < n0; ++i) issue_copy(i, true);
+    }
+    bool ok = true;
+    for (int i = kPfStages; i <= ntiles && ok; ++i) {
+      if (i < ntiles) {
+        ok = __all_sync(kFull, mbar_wait(&kfree[i % kPfStages], (i / kPfStages - 1) & 1,
+                                         p.err, &s_abort));
+        if (!ok) break;
+        if (lane == 0) issue_copy(i, false);
+        k_issued = i + 1;
+      }
+      const int iv = i - 1;
+      if (iv >= kPfStages && iv < ntiles) {
+        ok = __all_sync(kFull, mbar_wait(&vfree[iv % kPfStages], (iv / kPfStages - 1) & 1,
+                                         p.err, &s_abort));
+        if (!ok) break;
+        if (lane == 0) issue_copy(iv, true);
+        v_issued = iv + 1;
+      }
+    }
+    if (lane == 0) {
+      // every copy lands before the block exits (bounded waits)
+      for (int j = max(0, k_issued - kPfStages); j < k_issued; ++j)
+        mbar_wait(&kfull[j % kPfStages], (j / kPfStages) & 1, ok ? p.err : nullptr,
+                  ok ? &s_abort : nullptr);
+      for (int j = max(0, v_issued - kPfStages); j < v_issued; ++j)
+        mbar_wait(&vfull[j % kPfStages], (j / kPfStages) & 1, ok ? p.err : nullptr,
+                  ok ? &s_abort : nullptr);
+    }
+  } else if (warp == kPfMmaWarp) {
+    // ================================================================ MMA
+    // descriptors: the tile bases once, offsets added in the 16-byte units of
+    // the address field
+    const uint64_t qd = umma_desc_sw128(smem_u32(qs), 16, 1024);
+    const uint64_t kd = umma_desc_sw128(smem_u32(kst), 16, 1024);
+    const uint64_t vd = umma_desc_sw128(smem_u32(vst), kTile * 128, 1024);
+    const uint64_t pd = umma_desc_sw128(smem_u32(pbuf), 16, 1024);
     uint64_t* last_bar = nullptr;  // the latest MMA commit
     uint32_t last_par = 0;
-    if (lane == 0)
-      for (int i = 0; i < issued; ++i) issue_tile(i);
-    // S of tile i once its copy landed and its TMEM buffer is free; the V
-    // rows past the end of the sequence are zeroed before any PV reads them
+    // S of tile i once its K landed and its TMEM buffer is free
     auto issue_s = [&](int i) -> bool {
       const int b2 = i & 1;
       const int stg = i % kPfStages;
-      uint8_t* st = stages + stg * Gm::kStageBytes;
-      bool w = mbar_wait(&full[stg], (i / kPfStages) & 1, p.err, &s_abort);
+      bool w = mbar_wait(&kfull[stg], (i / kPfStages) & 1, p.err, &s_abort);
       if (i >= 2) w = w && mbar_wait(&sfree[b2], ((i - 2) >> 1) & 1, p.err, &s_abort);
       if (!__all_sync(kFull, w)) return false;
-      landed = i + 1;
       tc_fence_after();
       if (lane == 0) {
+        const uint64_t kb = kd + static_cast<uint64_t>(stg * (Gm::kKBytes >> 4));
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t ad = umma_desc_sw128(
-              smem_u32(qs) + (ks >> 2) * (kPfRows * 128) + (ks & 3) * 32, 16, 1024);
-          const uint64_t bd = umma_desc_sw128(
-              smem_u32(st) + (ks >> 2) * (kTile * 128) + (ks & 3) * 32, 16, 1024);
-          tc_mma(tmem + Gm::kColS + 64 * b2, ad, bd, kIdescS, ks > 0 ? 1u : 0u);
-        }
+        for (int ks = 0; ks < D / 16; ++ks)
+          tc_mma(tmem + Gm::kColS + 64 * b2,
+                 qd + static_cast<uint64_t>((ks >> 2) * (kPfRows * 8) + (ks & 3) * 2),
+                 kb + static_cast<uint64_t>((ks >> 2) * (kTile * 8) + (ks & 3) * 2), kIdescS,
+                 ks > 0 ? 1u : 0u);
         tc_commit(&sfull[b2]);
+        tc_commit(&kfree[stg]);
       }
       last_bar = &sfull[b2];
       last_par = (i >> 1) & 1;
-      const int key0 = i * kTile;
-      if (key0 + kTile > kvl) {
-        const int first = kvl - key0;
-        for (int idx = lane; idx < (kTile - first) * Gm::kHalves * 8; idx += 32) {
-          const int n = first + idx / (Gm::kHalves * 8);
-          const int rem = idx % (Gm::kHalves * 8);
-          *reinterpret_cast<uint4*>(st + Gm::kKBytes + (rem >> 3) * (kTile * 128) + n * 128 +
-                                    (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
       return true;
     };
     bool ok = issue_s(0);
     for (int i = 0; i < ntiles && ok; ++i) {
       const int b2 = i & 1;
       const uint32_t ph2 = (i >> 1) & 1;
-      uint8_t* st = stages + (i % kPfStages) * Gm::kStageBytes;
-      const bool split_first = (i * kTile) % S == 0;
+      const int stg = i % kPfStages;
+      uint8_t* vt = vst + stg * Gm::kKBytes;
+      const int key0 = i * kTile;
+      const bool split_first = key0 % S == 0;
       // the next tile's S goes to the tensor core ahead of this tile's PV,
       // so that the softmax of tile i + 1 overlaps PV(i)
       if (i + 1 < ntiles && !issue_s(i + 1)) {
         ok = false;
         break;
       }
-      ok = mbar_wait(&pready[b2], ph2, p.err, &s_abort);
-      if (!__all_sync(kFull, ok)) {
-        ok = false;
-        break;
+      ok = __all_sync(kFull, mbar_wait(&vfull[stg], (i / kPfStages) & 1, p.err, &s_abort) &&
+                                 mbar_wait(&pready[b2], ph2, p.err, &s_abort));
+      if (!ok) break;
+      if (key0 + kTile > kvl) {  // keys past the end: zero their V rows before PV
+        const int first = kvl - key0;
+        for (int idx = lane; idx < (kTile - first) * Gm::kHalves * 8; idx += 32) {
+          const int n = first + idx / (Gm::kHalves * 8);
+          const int rem = idx % (Gm::kHalves * 8);
+          *reinterpret_cast<uint4*>(vt + (rem >> 3) * (kTile * 128) + n * 128 + (rem & 7) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
       }
       tc_fence_after();
       if (lane == 0) {  // ---- O += P V, per 16-key chunk the hi part then the lo part
-        const uint32_t pa = smem_u32(pbuf + b2 * 2 * Gm::kPBytes);
+        const uint64_t vb = vd + static_cast<uint64_t>(stg * (Gm::kKBytes >> 4));
+        const uint64_t ph = pd + static_cast<uint64_t>(b2 * (2 * Gm::kPBytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t bd =
-              umma_desc_sw128(smem_u32(st + Gm::kKBytes) + kk * 2048, kTile * 128, 1024);
-          const uint64_t adh = umma_desc_sw128(pa + kk * 32, 16, 1024);
-          const uint64_t adl = umma_desc_sw128(pa + Gm::kPBytes + kk * 32, 16, 1024);
-          tc_mma(tmem + Gm::kColO, adh, bd, kIdescPV, (split_first && kk == 0) ? 0u : 1u);
-          tc_mma(tmem + Gm::kColO, adl, bd, kIdescPV, 1u);
+          const uint64_t bd = vb + static_cast<uint64_t>(kk * 128);
+          tc_mma(tmem + Gm::kColO, ph + static_cast<uint64_t>(kk * 2), bd, kIdescPV,
+                 (split_first && kk == 0) ? 0u : 1u);
+          tc_mma(tmem + Gm::kColO, ph + static_cast<uint64_t>((Gm::kPBytes >> 4) + kk * 2), bd,
+                 kIdescPV, 1u);
         }
         tc_commit(&pdone[b2]);
+        tc_commit(&vfree[stg]);
       }
       last_bar = &pdone[b2];
       last_par = ph2;
-      if (i >= 1) {  // PV of the previous tile done: its stage takes a new copy
-        ok = mbar_wait(&pdone[(i - 1) & 1], ((i - 1) >> 1) & 1, p.err, &s_abort);
-        if (!__all_sync(kFull, ok)) {
-          ok = false;
-          break;
-        }
-        if (i - 1 + kPfStages < ntiles) {
-          if (lane == 0) issue_tile(i - 1 + kPfStages);
-          issued = i - 1 + kPfStages + 1;
-        }
-      }
     }
-    if (!ok && lane == 0) {
-      // a wait ran out: bounded waits for the copies and MMAs still in flight
-      for (int j = landed; j < issued; ++j)
-        mbar_wait(&full[j % kPfStages], (j / kPfStages) & 1, nullptr);
-      if (last_bar) mbar_wait(last_bar, last_par, nullptr);
-    }
+    if (!ok && lane == 0 && last_bar) mbar_wait(last_bar, last_par, nullptr);  // MMAs in flight
   } else {
     // ================================================================= softmax
-    const int q4 = warp & 3, hk = warp >> 2;  // row quadrant, key / column half
+    const int q4 = warp & 3, par = warp >> 2;  // row quadrant, parity of the tiles taken
     const int r = q4 * 32 + lane;
     const int tk = r / G;
     const int pos = (r < TPB * G && tk < ntok) ? start + tok0 + tk : -1;
     const uint32_t tl = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
-    const int bar_id = 1 + q4;
-    float m = -CUDART_INF_F, l = 0.0f;        // split state (l kept by the second warp)
+    // state handed from the warp of tile t-1 to the warp of tile t
+    float m = -CUDART_INF_F, l = 0.0f;        // split state after the tile
     float mg_m = -CUDART_INF_F, mg_l = 0.0f;  // merged state
     bool have = false;
+    bool live = true;  // no wait has run out
     // fold the finished split (m_s, l_s, o in TMEM) into the merged state
     auto fold = [&](float m_s, float l_s, int lo_s) {
       const bool part = pos >= lo_s;
       float mn = 0.0f, ca = 0.0f, cb = 0.0f;
       if (part && have) lse_coeffs(mg_m, m_s, mn, ca, cb);
 #pragma unroll
-      for (int c = 0; c < DH / 32; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t vo[32], vm[32];
-        tmem_ld32_nowait(tl + Gm::kColO + hk * DH + 32 * c, vo);
-        tmem_ld32_nowait(tl + Gm::kColM + hk * DH + 32 * c, vm);
+        tmem_ld32_nowait(tl + Gm::kColO + 32 * c, vo);
+        tmem_ld32_nowait(tl + Gm::kColM + 32 * c, vm);
         tmem_wait_ld();
         if (part) {
 #pragma unroll
@@ -1141,7 +1190,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
                                                    __uint_as_float(vo[e]), cb))
                          : vo[e];
         }
-        tmem_st32(tl + Gm::kColM + hk * DH + 32 * c, vm);
+        tmem_st32(tl + Gm::kColM + 32 * c, vm);
       }
       tmem_wait_st();
       if (part) {
@@ -1155,193 +1204,181 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
         }
       }
     };
-    bool ok = true;
-    for (int i = 0; i < ntiles; ++i) {
+    for (int i = par; i < ntiles && live; i += 2) {
       const int b2 = i & 1;
       const uint32_t ph2 = (i >> 1) & 1;
       const int key0 = i * kTile;
       const int lo = (key0 / S) * S;  // split start
       const bool split_first = key0 == lo;
-      float m_s = 0.0f, l_s = 0.0f;  // the split that ended with the previous tile
-      if (split_first && i > 0) {
-        m_s = m;
-        l_s = l;
-        m = -CUDART_INF_F;
-        l = 0.0f;
-      }
-      // ---- this warp's 32 keys of the tile
-      bool okw = __all_sync(kFull, mbar_wait(&sfull[b2], ph2, p.err, &s_abort));
-      uint32_t sv[32];
-      if (okw) {
+      // ---- scores of the tile
+      live = __all_sync(kFull, live && mbar_wait(&sfull[b2], ph2, p.err, &s_abort));
+      // The row is read from TMEM twice, 32 columns at a time: once for the
+      // maximum, once for the probabilities (the same scaled values both
+      // times), so that only 32 scores are live in registers.
+      const bool all_vis = key0 + kTile - 1 <= start + tok0;  // every row sees the tile
+      const int nvis = pos >= lo ? min(lo + S, pos + 1) - key0 : 0;
+      auto scores = [&](int hf, float (&x)[32]) {
+        uint32_t sv[32];
+        tmem_ld32(tl + Gm::kColS + 64 * b2 + 32 * hf, sv);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float sj = __fmul_rn(__uint_as_float(sv[j]), p.scale_log2);
+          x[j] = (all_vis || 32 * hf + j < nvis) ? sj : -CUDART_INF_F;
+        }
+      };
+      float mh[2] = {-CUDART_INF_F, -CUDART_INF_F};
+      if (live) {
         tc_fence_after();
-        tmem_ld32(tl + Gm::kColS + 64 * b2 + 32 * hk, sv);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float x[32];
+          scores(hf, x);
+          float t[16];  // the row maximum is exact in any order: a tree
+#pragma unroll
+          for (int j = 0; j < 16; ++j) t[j] = fmaxf(x[2 * j], x[2 * j + 1]);
+#pragma unroll
+          for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+            for (int j = 0; j < w; ++j) t[j] = fmaxf(t[2 * j], t[2 * j + 1]);
+          mh[hf] = t[0];
+        }
+      }
+      const float mx = fmaxf(mh[0], mh[1]);
+      // ---- running maximum of the previous tile
+      float m_prev = -CUDART_INF_F;
+      if (i > 0) {
+        live = __all_sync(kFull, live && mbar_wait(&hm[q4], (i - 1) & 1, p.err, &s_abort));
+        m_prev = xm[r];
+      }
+      const float m_in = split_first ? -CUDART_INF_F : m_prev;
+      float mnew, alpha = 1.0f;
+      if (mx == -CUDART_INF_F) {  // no visible key: exact no-op for this row
+        mnew = m_in;
+      } else {
+        mnew = fmaxf(m_in, mx);
+        alpha = m_in == -CUDART_INF_F ? 0.0f : exp2_sfu(__fsub_rn(m_in, mnew));
+      }
+      if (i + 1 < ntiles) {
+        xm[r] = mnew;
+        mbar_arrive(&hm[q4]);
+      }
+      // ---- probabilities into P = hi + lo (buffer b2, once the PV of two
+      // tiles ago has read it); key j adds to partial sum j % 8 in increasing
+      // key order, then the tree ((0+1)+(2+3))+((4+5)+(6+7))
+      if (i >= 2)
+        live = __all_sync(kFull, live && mbar_wait(&pdone[b2], ((i - 2) >> 1) & 1, p.err,
+                                                   &s_abort));
+      float cs[8];
+#pragma unroll
+      for (int g8 = 0; g8 < 8; ++g8) cs[g8] = 0.0f;
+      if (live) {
+        uint8_t* ph = pbuf + b2 * 2 * Gm::kPBytes;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float x[32];
+          scores(hf, x);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            x[j] = x[j] != -CUDART_INF_F ? exp2_sfu(__fsub_rn(x[j], mnew)) : 0.0f;
+            cs[j & 7] = __fadd_rn(cs[j & 7], x[j]);
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t wh[4], wl[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float p0 = x[8 * c + 2 * e], p1 = x[8 * c + 2 * e + 1];
+              const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
+              __nv_bfloat162 hh;
+              hh.x = h0;
+              hh.y = h1;
+              wh[e] = *reinterpret_cast<uint32_t*>(&hh);
+              wl[e] = pack_bf16x2(__fsub_rn(p0, __bfloat162float(h0)),
+                                  __fsub_rn(p1, __bfloat162float(h1)));
+            }
+            const uint32_t off = sw128_off(r, 4 * hf + c);
+            *reinterpret_cast<uint4*>(ph + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+            *reinterpret_cast<uint4*>(ph + Gm::kPBytes + off) =
+                make_uint4(wl[0], wl[1], wl[2], wl[3]);
+          }
+        }
+        fence_proxy_async_smem();
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sfree[b2]);
-      const bool all_vis = key0 + kTile - 1 <= start + tok0;  // every row sees the tile
-      const int nvis = pos >= lo ? min(min(lo + S, pos + 1) - key0, kTile) : 0;
-      float x[32];
-      float pm = -CUDART_INF_F;
-      if (all_vis) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          x[j] = __fmul_rn(__uint_as_float(sv[j]), p.scale_log2);
-          pm = fmaxf(pm, x[j]);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          x[j] = 32 * hk + j < nvis ? __fmul_rn(__uint_as_float(sv[j]), p.scale_log2)
-                                    : -CUDART_INF_F;
-          pm = fmaxf(pm, x[j]);
-        }
+      const float csum = __fadd_rn(__fadd_rn(__fadd_rn(cs[0], cs[1]), __fadd_rn(cs[2], cs[3])),
+                                   __fadd_rn(__fadd_rn(cs[4], cs[5]), __fadd_rn(cs[6], cs[7])));
+      // ---- sum and merged state of the previous tile
+      float l_prev = 0.0f;
+      if (i > 0) {
+        live = __all_sync(kFull, live && mbar_wait(&hst[q4], (i - 1) & 1, p.err, &s_abort));
+        l_prev = xst[r];
+        mg_m = xst[kPfRows + r];
+        mg_l = xst[2 * kPfRows + r];
+        have = xst[3 * kPfRows + r] != 0.0f;
       }
-      xmax[hk * kPfRows + r] = pm;
-      if (lane == 0) xok[(0 * 2 + hk) * 4 + q4] = okw;
-      pair_sync(bar_id);
-      if (!(xok[(0 * 2 + 0) * 4 + q4] && xok[(0 * 2 + 1) * 4 + q4])) {
-        ok = false;
-        break;
-      }
-      const float mx = fmaxf(xmax[r], xmax[kPfRows + r]);
-      float mnew, alpha = 1.0f;
-      if (mx == -CUDART_INF_F) {  // no visible key: exact no-op for this row
-        mnew = m;
-      } else {
-        mnew = fmaxf(m, mx);
-        alpha = m == -CUDART_INF_F ? 0.0f : exp2_sfu(__fsub_rn(m, mnew));
-      }
-      // probabilities; key j of the tile adds to partial sum j % 8, each in
-      // increasing key order, the first warp's four keys before the second's
-      float cs[8];
-#pragma unroll
-      for (int g8 = 0; g8 < 8; ++g8) cs[g8] = 0.0f;
-      if (all_vis) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = exp2_sfu(__fsub_rn(x[j], mnew));
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          x[j] = x[j] != -CUDART_INF_F ? exp2_sfu(__fsub_rn(x[j], mnew)) : 0.0f;
-      }
-      if (hk == 0) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) cs[j & 7] = __fadd_rn(cs[j & 7], x[j]);
-      }
-      if (hk == 0) {
-#pragma unroll
-        for (int g8 = 0; g8 < 8; ++g8) xcs[g8 * kPfRows + r] = cs[g8];
-      }
-      // P = hi + lo into buffer b2, once the PV of two tiles ago has read it
-      if (i >= 2) okw = __all_sync(kFull, mbar_wait(&pdone[b2], ((i - 2) >> 1) & 1, p.err,
-                                                    &s_abort));
-      if (okw) {
-        uint8_t* ph = pbuf + b2 * 2 * Gm::kPBytes;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t wh[4], wl[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p0 = x[8 * cc + 2 * e], p1 = x[8 * cc + 2 * e + 1];
-            const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
-            __nv_bfloat162 hh;
-            hh.x = h0;
-            hh.y = h1;
-            wh[e] = *reinterpret_cast<uint32_t*>(&hh);
-            wl[e] = pack_bf16x2(__fsub_rn(p0, __bfloat162float(h0)),
-                                __fsub_rn(p1, __bfloat162float(h1)));
-          }
-          const uint32_t off = sw128_off(r, 4 * hk + cc);
-          *reinterpret_cast<uint4*>(ph + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-          *reinterpret_cast<uint4*>(ph + Gm::kPBytes + off) =
-              make_uint4(wl[0], wl[1], wl[2], wl[3]);
-        }
-        fence_proxy_async_smem();
-      }
-      if (lane == 0) xok[(1 * 2 + hk) * 4 + q4] = okw;
-      pair_sync(bar_id);
-      if (!(xok[(1 * 2 + 0) * 4 + q4] && xok[(1 * 2 + 1) * 4 + q4])) {
-        ok = false;
-        break;
-      }
-      if (hk == 1) {
-#pragma unroll
-        for (int g8 = 0; g8 < 8; ++g8) {
-          float c8 = xcs[g8 * kPfRows + r];
-#pragma unroll
-          for (int t4 = 0; t4 < 4; ++t4) c8 = __fadd_rn(c8, x[g8 + 8 * t4]);
-          cs[g8] = c8;
-        }
-        const float csum =
-            __fadd_rn(__fadd_rn(__fadd_rn(cs[0], cs[1]), __fadd_rn(cs[2], cs[3])),
-                      __fadd_rn(__fadd_rn(cs[4], cs[5]), __fadd_rn(cs[6], cs[7])));
-        l = __fadd_rn(__fmul_rn(l, alpha), csum);
-      }
+      l = __fadd_rn(__fmul_rn(split_first ? 0.0f : l_prev, alpha), csum);
       m = mnew;
       // ---- the previous tile's PV is done: fold a finished split, or o *= alpha
       if (i >= 1)
-        okw = __all_sync(kFull, mbar_wait(&pdone[(i - 1) & 1], ((i - 1) >> 1) & 1, p.err,
-                                          &s_abort));
-      if (okw) {
+        live = __all_sync(kFull, live && mbar_wait(&pdone[(i - 1) & 1], ((i - 1) >> 1) & 1,
+                                                   p.err, &s_abort));
+      if (live) {
         tc_fence_after();
         if (split_first && i > 0) {
-          fold(m_s, l_s, lo - S);
+          fold(m_prev, l_prev, lo - S);
         } else if (!split_first && __any_sync(kFull, alpha != 1.0f)) {
 #pragma unroll
-          for (int c = 0; c < DH / 32; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             uint32_t v[32];
-            tmem_ld32(tl + Gm::kColO + hk * DH + 32 * c, v);
+            tmem_ld32(tl + Gm::kColO + 32 * c, v);
 #pragma unroll
             for (int e = 0; e < 32; ++e)
               v[e] = __float_as_uint(__fmul_rn(__uint_as_float(v[e]), alpha));
-            tmem_st32(tl + Gm::kColO + hk * DH + 32 * c, v);
+            tmem_st32(tl + Gm::kColO + 32 * c, v);
           }
           tmem_wait_st();
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&pready[b2]);
-      } else {
-        ok = false;  // the next pair check stops both warps
       }
+      if (i + 1 < ntiles) {
+        xst[r] = l;
+        xst[kPfRows + r] = mg_m;
+        xst[2 * kPfRows + r] = mg_l;
+        xst[3 * kPfRows + r] = have ? 1.0f : 0.0f;
+        mbar_arrive(&hst[q4]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (live && lane == 0) mbar_arrive(&pready[b2]);
     }
-    // ---- the last split, then out = o / l
-    if (ok) {
+    // ---- the warp of the last tile folds the last split and writes out = o / l
+    if (((ntiles - 1) & 1) == par) {
       const int i = ntiles - 1;
-      ok = __all_sync(kFull, mbar_wait(&pdone[i & 1], (i >> 1) & 1, p.err, &s_abort));
-      if (ok) {
+      live = __all_sync(kFull, live && mbar_wait(&pdone[i & 1], (i >> 1) & 1, p.err, &s_abort));
+      if (live && !s_abort) {
         tc_fence_after();
         fold(m, l, ((i * kTile) / S) * S);
-      }
-    }
-    if (hk == 1) xl[r] = mg_l;
-    if (lane == 0) xok[(2 * 2 + hk) * 4 + q4] = ok;
-    pair_sync(bar_id);
-    ok = xok[(2 * 2 + 0) * 4 + q4] && xok[(2 * 2 + 1) * 4 + q4];
-    if (ok) {
-      tc_fence_after();
-      const float lv = xl[r];
-      const int64_t orow =
-          ((int64_t)(q_begin + tok0 + tk) * p.Hq + h * G + r % G) * D + hk * DH;
+        const int64_t orow = ((int64_t)(q_begin + tok0 + tk) * p.Hq + h * G + r % G) * D;
 #pragma unroll
-      for (int c = 0; c < DH / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tl + Gm::kColM + hk * DH + 32 * c, v);  // the whole warp loads
-        if (pos < 0) continue;
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tl + Gm::kColM + 32 * c, v);  // the whole warp loads
+          if (pos < 0) continue;
 #pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          float o[8];
+          for (int e = 0; e < 32; e += 8) {
+            float o[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) o[u] = __fdiv_rn(__uint_as_float(v[e + u]), lv);
-          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + 32 * c + e) =
-              make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
-                         pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
-          if (p.out_f32) {
-            *reinterpret_cast<float4*>(p.out_f32 + orow + 32 * c + e) =
-                make_float4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<float4*>(p.out_f32 + orow + 32 * c + e + 4) =
-                make_float4(o[4], o[5], o[6], o[7]);
+            for (int u = 0; u < 8; ++u) o[u] = __fdiv_rn(__uint_as_float(v[e + u]), mg_l);
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + 32 * c + e) =
+                make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                           pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+            if (p.out_f32) {
+              *reinterpret_cast<float4*>(p.out_f32 + orow + 32 * c + e) =
+                  make_float4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<float4*>(p.out_f32 + orow + 32 * c + e + 4) =
+                  make_float4(o[4], o[5], o[6], o[7]);
+            }
           }
         }
       }

@@ -63,14 +63,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Nanoseconds of the global timer.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 // Wait for the phase with the given parity to complete.  Returns false (and
-// records BI_ERR_TIMEOUT) if it did not complete within kWaitLimit polls, or
-// if *abort becomes non-zero meanwhile (another role gave up).
+// records BI_ERR_TIMEOUT) if it did not complete within kWaitNs nanoseconds
+// (or kWaitLimit polls), or if *abort becomes non-zero meanwhile (another
+// role gave up).  try_wait may suspend the thread for a while, so the bound
+// is on time, not only on the number of polls.
+constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err,
                                           volatile int* abort = nullptr) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
   for (uint32_t i = 0; i < kWaitLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (abort && *abort) return false;
+    if ((i & 63) == 63 && global_ns() - t0 > kWaitNs) break;
   }
   record_error(err, BI_ERR_TIMEOUT);
   if (abort) *abort = 1;
