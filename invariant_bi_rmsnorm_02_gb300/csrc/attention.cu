@@ -895,56 +895,54 @@ constexpr int kPfRows = 128;
 constexpr int kPfSoftmaxWarps = 8;
 constexpr int kPfThreads = (kPfSoftmaxWarps + 2) * 32;  // + MMA warp + TMA warp
 constexpr int kPfMmaWarp = kPfSoftmaxWarps, kPfTmaWarp = kPfSoftmaxWarps + 1;
-constexpr int kPfPageCache = 2048;  // page ids held in shared memory (32768 keys)
+constexpr int kPfPageCache = 1024;  // page ids held in shared memory (16384 keys)
 constexpr int kPfStages = 3;
 
 template <int D>
 struct PfGeom {
   static constexpr int kHalves = D / 64;
-  static constexpr int kQBytes = kHalves * kPfRows * 128;  // [half][row][128 B]
-  static constexpr int kKBytes = kHalves * kTile * 128;     // [half][key][128 B]
-  static constexpr int kStageBytes = 2 * kKBytes;           // one K and one V tile
-  static constexpr int kPBytes = kPfRows * 128;             // one part of P: [row][64 keys]
-  static constexpr int kStageOff = kQBytes;
-  static constexpr int kPOff = kStageOff + kPfStages * kStageBytes;  // [buffer][hi, lo]
+  static constexpr int kQBytes = kHalves * kPfRows * 128;    // [half][row][128 B]
+  static constexpr int kKBytes = kHalves * kTile * 128;       // one tile: [half][key][128 B]
+  static constexpr int kKPairBytes = 2 * kKBytes;             // two tiles: [half][128 keys][128 B]
+  static constexpr int kKOff = kQBytes;                       // K ring: 2 stages of tile pairs
+  static constexpr int kVOff = kKOff + 2 * kKPairBytes;       // V ring: kPfStages tiles
+  static constexpr int kPBytes = kPfRows * 128;               // one part of P: [row][64 keys]
+  static constexpr int kPOff = kVOff + kPfStages * kKBytes;   // [buffer][hi, lo]
   static constexpr int kXOff = kPOff + 4 * kPBytes;
   static constexpr int kXFloats = 5 * kPfRows;
   static constexpr int kPidOff = kXOff + kXFloats * 4;
   static constexpr int kBarOff = kPidOff + kPfPageCache * 4;
-  // kfull[], vfull[], kfree[], vfree[], sfull[2], sfree[2], pready[2], pdone[2],
-  // hm[4], hst[4]
-  static constexpr int kNumBars = 4 * kPfStages + 16;
+  // kfull[2], kfree[2], vfull[], vfree[], sfull[2], sfree[2], pready[2], pdone[2], hm[4], hst[4]
+  static constexpr int kNumBars = 4 + 2 * kPfStages + 8 + 8;
   static constexpr int kSmem = 1024 + kBarOff + kNumBars * 8;
-  static constexpr uint32_t kTmemCols = D == 128 ? 512 : 256;
-  // S buffers at columns 0 and 64, the split's o at 128, the merged o after it
-  static constexpr uint32_t kColS = 0, kColO = 128, kColM = 128 + D;
+  static constexpr uint32_t kTmemCols = 512;
+  // two S buffers of 128 columns (a tile pair each), the split's o, the merged o
+  static constexpr uint32_t kColS = 0, kColO = 256, kColM = 256 + D;
 };
-
 
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const KernelParams p) {
   using Gm = PfGeom<D>;
-  constexpr uint32_t kIdescS = umma_idesc_bf16(kPfRows, kTile, false, false);
+  constexpr uint32_t kIdescS = umma_idesc_bf16(kPfRows, 2 * kTile, false, false);
   constexpr uint32_t kIdescPV = umma_idesc_bf16(kPfRows, D, false, true);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* qs = smem;
-  uint8_t* stages = smem + Gm::kStageOff;
+  uint8_t* kst = smem + Gm::kKOff;  // K ring: 2 tile pairs
+  uint8_t* vst = smem + Gm::kVOff;  // V ring: kPfStages tiles
   uint8_t* pbuf = smem + Gm::kPOff;
   float* xm = reinterpret_cast<float*>(smem + Gm::kXOff);  // [128] running max, to the next tile
   float* xst = xm + kPfRows;  // [4][128] l, merged m, merged l, merged-yet, to the next tile
-  uint8_t* kst = stages;                            // K ring: kPfStages tiles
-  uint8_t* vst = stages + kPfStages * Gm::kKBytes;  // V ring: kPfStages tiles
   int* pid_s = reinterpret_cast<int*>(smem + Gm::kPidOff);  // page ids of this sequence
-  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + Gm::kBarOff);
-  uint64_t* vfull = kfull + kPfStages;
-  uint64_t* kfree = vfull + kPfStages;  // the S that read the K stage is done
-  uint64_t* vfree = kfree + kPfStages;  // the PV that read the V stage is done
-  uint64_t* sfull = vfree + kPfStages;
-  uint64_t* sfree = sfull + 2;
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + Gm::kBarOff);  // K pair landed
+  uint64_t* kfree = kfull + 2;          // the S that read the K pair is done
+  uint64_t* vfull = kfree + 2;          // V tile landed
+  uint64_t* vfree = vfull + kPfStages;  // the PV that read the V stage is done
+  uint64_t* sfull = vfree + kPfStages;  // S of a tile pair computed
+  uint64_t* sfree = sfull + 2;          // both tiles' scores read
   uint64_t* pready = sfree + 2;
   uint64_t* pdone = pready + 2;
   uint64_t* hm = pdone + 2;   // per row quadrant: the running max of a tile is written
@@ -991,15 +989,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
     for (int i = 0; i < kPfStages; ++i) {
-      mbar_init(&kfull[i], 1);
       mbar_init(&vfull[i], 1);
-      mbar_init(&kfree[i], 1);
       mbar_init(&vfree[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&kfree[i], 1);
       mbar_init(&sfull[i], 1);
-      mbar_init(&sfree[i], kPfSoftmaxWarps / 2);   // the four warps of that tile parity
-      mbar_init(&pready[i], kPfSoftmaxWarps / 2);
+      mbar_init(&sfree[i], kPfSoftmaxWarps);       // all eight warps read a pair
+      mbar_init(&pready[i], kPfSoftmaxWarps / 2);  // the four warps of that tile parity
       mbar_init(&pdone[i], 1);
     }
     for (int i = 0; i < 4; ++i) {
@@ -1027,56 +1025,71 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
 
   if (warp == kPfTmaWarp) {
     // ================================================================ copies
-    // K and V tiles of 64 keys stream through separate rings of kPfStages
-    // stages: a K stage is free once the S that read it is done, a V stage
-    // once its PV is.  Copies go out in the order they are needed (K of tile
-    // i, V of tile i-1), which is also the order in which stages free up.
-    auto issue_copy = [&](int i, bool is_v) {  // lane 0
-      const int stg = i % kPfStages;
-      uint8_t* dst = (is_v ? vst : kst) + stg * Gm::kKBytes;
-      uint64_t* bar = is_v ? &vfull[stg] : &kfull[stg];
+    // K goes in pairs of tiles (one S MMA covers 128 keys) through two pair
+    // stages, V tile by tile through kPfStages stages.  A K stage is free once
+    // the S that read it is done, a V stage once its PV is.  Copies go out in
+    // the order they are needed: the K pair k at the MMA warp's tile 2(k-1),
+    // V of tile i at tile i.
+    const int npairs = (ntiles + 1) / 2;
+    auto issue_copy = [&](int i, bool is_v) {  // tile i; lane 0
+      uint8_t* dst;
+      uint64_t* bar;
+      if (is_v) {
+        dst = vst + (i % kPfStages) * Gm::kKBytes;
+        bar = &vfull[i % kPfStages];
+      } else {  // rows 64 (i & 1) .. of each half of the pair stage
+        dst = kst + ((i >> 1) & 1) * Gm::kKPairBytes + (i & 1) * (kTile * 128);
+        bar = &kfull[(i >> 1) & 1];
+      }
       const int key0 = i * kTile;
       const int np = pages_below(key0, kvl);
-      mbar_arrive_expect_tx(bar, np * Gm::kHalves * 2048);
       for (int pp = 0; pp < np; ++pp) {
         const int pg = (key0 >> 4) + pp;
         const int y = ((pg < kPfPageCache ? pid_s[pg] : bt_row[pg]) * p.Hkv + h) * kPage;
 #pragma unroll
         for (int hf = 0; hf < Gm::kHalves; ++hf)
-          tma_load_2d(dst + hf * (kTile * 128) + pp * 2048, is_v ? &vmap : &kmap, hf * 64, y,
-                      bar);
+          tma_load_2d(dst + hf * (is_v ? kTile * 128 : 2 * kTile * 128) + pp * 2048,
+                      is_v ? &vmap : &kmap, hf * 64, y, bar);
       }
     };
-    const int n0 = min(kPfStages, ntiles);
-    int k_issued = n0, v_issued = n0;
+    auto issue_kpair = [&](int k) {  // lane 0
+      const int t1 = 2 * k + 1 < ntiles;
+      const int bytes = (pages_below(2 * k * kTile, kvl) +
+                         (t1 ? pages_below((2 * k + 1) * kTile, kvl) : 0)) *
+                        Gm::kHalves * 2048;
+      mbar_arrive_expect_tx(&kfull[k & 1], bytes);
+      issue_copy(2 * k, false);
+      if (t1) issue_copy(2 * k + 1, false);
+    };
+    auto issue_v = [&](int i) {  // lane 0
+      mbar_arrive_expect_tx(&vfull[i % kPfStages], pages_below(i * kTile, kvl) * Gm::kHalves * 2048);
+      issue_copy(i, true);
+    };
+    int nk = min(2, npairs), nv = min(kPfStages, ntiles);
     if (lane == 0) {
-      for (int i = 0; i < n0; ++i) issue_copy(i, false);
-      for (int i = 0; i < n0; ++i) issue_copy(i, true);
+      for (int k = 0; k < nk; ++k) issue_kpair(k);
+      for (int i = 0; i < nv; ++i) issue_v(i);
     }
     bool ok = true;
-    for (int i = kPfStages; i <= ntiles && ok; ++i) {
-      if (i < ntiles) {
-        ok = __all_sync(kFull, mbar_wait(&kfree[i % kPfStages], (i / kPfStages - 1) & 1,
+    while (ok && (nk < npairs || nv < ntiles)) {
+      if (nk < npairs && (nv >= ntiles || 2 * (nk - 1) <= nv)) {
+        ok = __all_sync(kFull, mbar_wait(&kfree[nk & 1], ((nk - 2) >> 1) & 1, p.err, &s_abort));
+        if (!ok) break;
+        if (lane == 0) issue_kpair(nk);
+        ++nk;
+      } else {
+        ok = __all_sync(kFull, mbar_wait(&vfree[nv % kPfStages], (nv / kPfStages - 1) & 1,
                                          p.err, &s_abort));
         if (!ok) break;
-        if (lane == 0) issue_copy(i, false);
-        k_issued = i + 1;
-      }
-      const int iv = i - 1;
-      if (iv >= kPfStages && iv < ntiles) {
-        ok = __all_sync(kFull, mbar_wait(&vfree[iv % kPfStages], (iv / kPfStages - 1) & 1,
-                                         p.err, &s_abort));
-        if (!ok) break;
-        if (lane == 0) issue_copy(iv, true);
-        v_issued = iv + 1;
+        if (lane == 0) issue_v(nv);
+        ++nv;
       }
     }
     if (lane == 0) {
       // every copy lands before the block exits (bounded waits)
-      for (int j = max(0, k_issued - kPfStages); j < k_issued; ++j)
-        mbar_wait(&kfull[j % kPfStages], (j / kPfStages) & 1, ok ? p.err : nullptr,
-                  ok ? &s_abort : nullptr);
-      for (int j = max(0, v_issued - kPfStages); j < v_issued; ++j)
+      for (int k = max(0, nk - 2); k < nk; ++k)
+        mbar_wait(&kfull[k & 1], (k >> 1) & 1, ok ? p.err : nullptr, ok ? &s_abort : nullptr);
+      for (int j = max(0, nv - kPfStages); j < nv; ++j)
         mbar_wait(&vfull[j % kPfStages], (j / kPfStages) & 1, ok ? p.err : nullptr,
                   ok ? &s_abort : nullptr);
     }
@@ -1090,27 +1103,27 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     const uint64_t pd = umma_desc_sw128(smem_u32(pbuf), 16, 1024);
     uint64_t* last_bar = nullptr;  // the latest MMA commit
     uint32_t last_par = 0;
-    // S of tile i once its K landed and its TMEM buffer is free
-    auto issue_s = [&](int i) -> bool {
-      const int b2 = i & 1;
-      const int stg = i % kPfStages;
-      bool w = mbar_wait(&kfull[stg], (i / kPfStages) & 1, p.err, &s_abort);
-      if (i >= 2) w = w && mbar_wait(&sfree[b2], ((i - 2) >> 1) & 1, p.err, &s_abort);
+    // S of tile pair k (128 keys) once its K landed and its TMEM buffer is free
+    const int npairs = (ntiles + 1) / 2;
+    auto issue_s = [&](int k) -> bool {
+      const int kb2 = k & 1;
+      bool w = mbar_wait(&kfull[kb2], (k >> 1) & 1, p.err, &s_abort);
+      if (k >= 2) w = w && mbar_wait(&sfree[kb2], ((k - 2) >> 1) & 1, p.err, &s_abort);
       if (!__all_sync(kFull, w)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint64_t kb = kd + static_cast<uint64_t>(stg * (Gm::kKBytes >> 4));
+        const uint64_t kb = kd + static_cast<uint64_t>(kb2 * (Gm::kKPairBytes >> 4));
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          tc_mma(tmem + Gm::kColS + 64 * b2,
+          tc_mma(tmem + Gm::kColS + 128 * kb2,
                  qd + static_cast<uint64_t>((ks >> 2) * (kPfRows * 8) + (ks & 3) * 2),
-                 kb + static_cast<uint64_t>((ks >> 2) * (kTile * 8) + (ks & 3) * 2), kIdescS,
+                 kb + static_cast<uint64_t>((ks >> 2) * (2 * kTile * 8) + (ks & 3) * 2), kIdescS,
                  ks > 0 ? 1u : 0u);
-        tc_commit(&sfull[b2]);
-        tc_commit(&kfree[stg]);
+        tc_commit(&sfull[kb2]);
+        tc_commit(&kfree[kb2]);
       }
-      last_bar = &sfull[b2];
-      last_par = (i >> 1) & 1;
+      last_bar = &sfull[kb2];
+      last_par = (k >> 1) & 1;
       return true;
     };
     bool ok = issue_s(0);
@@ -1121,9 +1134,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       uint8_t* vt = vst + stg * Gm::kKBytes;
       const int key0 = i * kTile;
       const bool split_first = key0 % S == 0;
-      // the next tile's S goes to the tensor core ahead of this tile's PV,
-      // so that the softmax of tile i + 1 overlaps PV(i)
-      if (i + 1 < ntiles && !issue_s(i + 1)) {
+      // the next pair's S goes to the tensor core ahead of this tile's PV,
+      // so that the softmax of the next tiles overlaps the PVs
+      if ((i & 1) == 0 && (i >> 1) + 1 < npairs && !issue_s((i >> 1) + 1)) {
         ok = false;
         break;
       }
@@ -1206,20 +1219,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     };
     for (int i = par; i < ntiles && live; i += 2) {
       const int b2 = i & 1;
-      const uint32_t ph2 = (i >> 1) & 1;
       const int key0 = i * kTile;
       const int lo = (key0 / S) * S;  // split start
       const bool split_first = key0 == lo;
       // ---- scores of the tile
-      live = __all_sync(kFull, live && mbar_wait(&sfull[b2], ph2, p.err, &s_abort));
-      // The row is read from TMEM twice, 32 columns at a time: once for the
-      // maximum, once for the probabilities (the same scaled values both
-      // times), so that only 32 scores are live in registers.
+      live = __all_sync(kFull, live && mbar_wait(&sfull[(i >> 1) & 1], (i >> 2) & 1, p.err,
+                                                 &s_abort));
+      // The row is read from TMEM 32 columns at a time; the second half's
+      // scaled scores stay in registers from the maximum to the
+      // probabilities, the first half is read again (the same values).
       const bool all_vis = key0 + kTile - 1 <= start + tok0;  // every row sees the tile
       const int nvis = pos >= lo ? min(lo + S, pos + 1) - key0 : 0;
       auto scores = [&](int hf, float (&x)[32]) {
         uint32_t sv[32];
-        tmem_ld32(tl + Gm::kColS + 64 * b2 + 32 * hf, sv);
+        tmem_ld32(tl + Gm::kColS + 128 * ((i >> 1) & 1) + 64 * (i & 1) + 32 * hf, sv);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const float sj = __fmul_rn(__uint_as_float(sv[j]), p.scale_log2);
@@ -1227,6 +1240,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
         }
       };
       float mh[2] = {-CUDART_INF_F, -CUDART_INF_F};
+      float x1[32];  // scaled scores of keys 32..63
       if (live) {
         tc_fence_after();
 #pragma unroll
@@ -1241,6 +1255,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
 #pragma unroll
             for (int j = 0; j < w; ++j) t[j] = fmaxf(t[2 * j], t[2 * j + 1]);
           mh[hf] = t[0];
+          if (hf == 1) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x1[j] = x[j];
+          }
         }
       }
       const float mx = fmaxf(mh[0], mh[1]);
@@ -1276,7 +1294,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           float x[32];
-          scores(hf, x);
+          if (hf == 0) {
+            scores(0, x);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = x1[j];
+          }
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             x[j] = x[j] != -CUDART_INF_F ? exp2_sfu(__fsub_rn(x[j], mnew)) : 0.0f;
@@ -1306,7 +1329,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sfree[b2]);
+      if (lane == 0) mbar_arrive(&sfree[(i >> 1) & 1]);
       const float csum = __fadd_rn(__fadd_rn(__fadd_rn(cs[0], cs[1]), __fadd_rn(cs[2], cs[3])),
                                    __fadd_rn(__fadd_rn(cs[4], cs[5]), __fadd_rn(cs[6], cs[7])));
       // ---- sum and merged state of the previous tile
@@ -1330,13 +1353,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
           fold(m_prev, l_prev, lo - S);
         } else if (!split_first && __any_sync(kFull, alpha != 1.0f)) {
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tl + Gm::kColO + 32 * c, v);
+          for (int c = 0; c < D / 32; c += 2) {  // two chunks per TMEM round trip
+            uint32_t v0[32], v1[32];
+            tmem_ld32_nowait(tl + Gm::kColO + 32 * c, v0);
+            tmem_ld32_nowait(tl + Gm::kColO + 32 * (c + 1), v1);
+            tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              v[e] = __float_as_uint(__fmul_rn(__uint_as_float(v[e]), alpha));
-            tmem_st32(tl + Gm::kColO + 32 * c, v);
+            for (int e = 0; e < 32; ++e) {
+              v0[e] = __float_as_uint(__fmul_rn(__uint_as_float(v0[e]), alpha));
+              v1[e] = __float_as_uint(__fmul_rn(__uint_as_float(v1[e]), alpha));
+            }
+            tmem_st32(tl + Gm::kColO + 32 * c, v0);
+            tmem_st32(tl + Gm::kColO + 32 * (c + 1), v1);
           }
           tmem_wait_st();
         }
