@@ -80,10 +80,10 @@ def source_hash(*names):
 
 
 KERNEL_SOURCES = {
-    "gemm_tc_kernel": ("gemm.cu", "device_common.cuh"),
+    "gemm_tc_kernel": ("gemm.cu", "device_common.cuh", "tcgen05.cuh"),
     "rmsnorm_row_kernel": ("rmsnorm.cu",),
-    "attn_decode_split_kernel": ("attention.cu", "device_common.cuh"),
-    "attn_prefill_kernel": ("attention.cu", "device_common.cuh"),
+    "attn_decode_split_kernel": ("attention.cu", "device_common.cuh", "tcgen05.cuh"),
+    "attn_prefill_kernel": ("attention.cu", "device_common.cuh", "tcgen05.cuh"),
 }
 
 
