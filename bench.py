@@ -21,7 +21,9 @@ batch-variant mode to report the cost of invariance (t_invariant / t_variant
 - 1 per kernel).  L2 is flushed (a 256 MB write, then a 256 MB read so the dirty
 lines drain outside the timed region) before every kernel of the step, so
 each kernel is timed on a cold, clean L2 and none pays for the write-back of
-its predecessor's output; the step time is the sum of the kernels' times.
+its predecessor's output; a short device-side sleep after the flush keeps the
+host's launch latency out of the kernel's events.  The step time is the sum of
+the kernels' times.
 Inputs are resident in HBM when the timed region starts.  The end-to-end
 line runs the same kernels back to back with host copies around them.
 
@@ -50,6 +52,7 @@ if ROOT not in sys.path:
 import torch  # noqa: E402
 
 M, H, N_QKV, N_UP = 8192, 4096, 6144, 14336
+HOST_LEAD_CYCLES = 200_000  # ~0.1 ms at the SM clock
 EPS = 1e-6
 DEC = dict(B=64, Hq=32, Hkv=8, D=128, page=16, S=256, max_len=32768)
 PRE = dict(T=8192, chunk=2048, start=6144)
@@ -284,6 +287,10 @@ def timed_steps(wl, mode, steps, warmup, flush, stream, dist_barrier):
         for s in range(steps):
             for i, (_, fn, _) in enumerate(ops):
                 flush.zero_()
+                # a short device-side wait so that the host has enqueued the
+                # kernel before the start event fires: host launch latency
+                # stays out of the kernel's time (the e2e line measures it)
+                torch.cuda._sleep(HOST_LEAD_CYCLES)
                 ev[s][2 * i].record(stream)
                 fn()
                 ev[s][2 * i + 1].record(stream)

@@ -249,6 +249,15 @@ bi_status bi_kv_write(const void* k_new, const void* v_new, const int32_t* seq,
  * word.  Returns BI_OK, the first recorded device error, or BI_ERR_CUDA. */
 bi_status bi_check_device_errors(void* stream);
 
+/* Diagnostic of the failure path: launches one thread that waits on a
+ * barrier nothing arrives on, with the bounded wait every kernel of this
+ * library uses, given up after timeout_us microseconds (1 .. 2,000,000).
+ * The kernel records BI_ERR_TIMEOUT in the device error word and returns;
+ * the context stays usable.  Returns the launch status (BI_ERR_INVALID_ARG
+ * for an out-of-range timeout); read the recorded status with
+ * bi_check_device_errors. */
+bi_status bi_selftest_wait_timeout(uint32_t timeout_us, void* stream);
+
 /* Static English description of a status code (never NULL). */
 const char* bi_status_string(bi_status status);
 

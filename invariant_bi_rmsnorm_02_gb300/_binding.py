@@ -30,7 +30,8 @@ __all__ = [
     "bi_rmsnorm", "bi_rmsnorm_workspace_size", "bi_gemm", "bi_gemm_workspace_size",
     "bi_gemm_variant_splits", "bi_attn_decode", "bi_attn_decode_workspace_size",
     "bi_attn_prefill_chunk", "bi_kv_write", "bi_check_device_errors", "bi_status_string",
-    "bi_version", "bi_attn_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "rmsnorm", "gemm", "attn_decode", "attn_prefill_chunk", "kv_write",
+    "bi_version", "bi_attn_decode_noalloc", "bi_selftest_wait_timeout", "NOALLOC_SCRATCH_BYTES",
+    "rmsnorm", "gemm", "attn_decode", "attn_prefill_chunk", "kv_write",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -39,7 +40,7 @@ EXPORTED_SYMBOLS = (
     "bi_rmsnorm", "bi_rmsnorm_workspace_size", "bi_gemm", "bi_gemm_workspace_size",
     "bi_gemm_variant_splits", "bi_attn_decode", "bi_attn_decode_workspace_size",
     "bi_attn_prefill_chunk", "bi_kv_write", "bi_check_device_errors", "bi_status_string",
-    "bi_version", "bi_attn_decode_noalloc",
+    "bi_version", "bi_attn_decode_noalloc", "bi_selftest_wait_timeout",
 )
 
 
@@ -93,6 +94,7 @@ def load(build_if_missing: bool = True):
                                               _i32, _i32, _i32, _i64, _i32, _i32, _i32, _f32,
                                               _vp]),
             "bi_check_device_errors": (_i32, [_vp]),
+            "bi_selftest_wait_timeout": (_i32, [ctypes.c_uint32, _vp]),
             "bi_status_string": (ctypes.c_char_p, [_i32]),
             "bi_version": (ctypes.c_char_p, []),
         }
@@ -240,6 +242,12 @@ def bi_kv_write(k_new, v_new, seq, pos, k_cache, v_cache, block_table, stream=No
 
 def bi_check_device_errors(stream=None) -> int:
     return int(load().bi_check_device_errors(_stream(stream)))
+
+
+def bi_selftest_wait_timeout(timeout_us: int, stream=None) -> int:
+    """Launch the bounded-wait diagnostic (see include/bi.h); returns the
+    launch status, the recorded one comes from bi_check_device_errors."""
+    return int(load().bi_selftest_wait_timeout(int(timeout_us), _stream(stream)))
 
 
 def bi_status_string(status: int) -> str:

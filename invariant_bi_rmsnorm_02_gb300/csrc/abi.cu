@@ -10,6 +10,7 @@
 
 #include "bi.h"
 #include "bi_internal.h"
+#include "device_common.cuh"
 
 namespace bi {
 
@@ -119,6 +120,25 @@ bi_status bi_check_device_errors(void* stream) {
       return BI_ERR_CUDA;
   }
   return static_cast<bi_status>(v);
+}
+
+// --------------------------------------------------------------- self-test
+// One thread waits on an mbarrier that nothing arrives on; the bounded wait
+// gives up after limit_ns, records BI_ERR_TIMEOUT and the kernel returns.
+static __global__ void wait_timeout_kernel(int* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  mbar_wait(&bar, 0, err, nullptr, limit_ns);
+}
+
+bi_status bi_selftest_wait_timeout(uint32_t timeout_us, void* stream) {
+  if (timeout_us == 0 || timeout_us > 2000000u) return BI_ERR_INVALID_ARG;
+  int* err = device_error_word();
+  if (!err) return BI_ERR_CUDA;
+  wait_timeout_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(
+      err, static_cast<uint64_t>(timeout_us) * 1000u);
+  return cuda_status(cudaGetLastError());
 }
 
 // ------------------------------------------------------------------ RMSNorm

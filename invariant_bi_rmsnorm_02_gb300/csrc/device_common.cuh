@@ -77,13 +77,14 @@ __device__ __forceinline__ uint64_t global_ns() {
 // is on time, not only on the number of polls.
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err,
-                                          volatile int* abort = nullptr) {
+                                          volatile int* abort = nullptr,
+                                          uint64_t limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 0; i < kWaitLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (abort && *abort) return false;
-    if ((i & 63) == 63 && global_ns() - t0 > kWaitNs) break;
+    if ((i & 63) == 63 && global_ns() - t0 > limit_ns) break;
   }
   record_error(err, BI_ERR_TIMEOUT);
   if (abort) *abort = 1;
