@@ -44,6 +44,7 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include <type_traits>
 #include <utility>
 
 #include "bi_internal.h"
@@ -1225,28 +1226,28 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       // ---- scores of the tile
       live = __all_sync(kFull, live && mbar_wait(&sfull[(i >> 1) & 1], (i >> 2) & 1, p.err,
                                                  &s_abort));
-      // The row is read from TMEM 32 columns at a time; the second half's
-      // scaled scores stay in registers from the maximum to the
-      // probabilities, the first half is read again (the same values).
-      const bool all_vis = key0 + kTile - 1 <= start + tok0;  // every row sees the tile
+      // The row is read from TMEM 32 columns at a time, twice: once for the
+      // maximum, once for the probabilities (the same scaled values both
+      // times), so that only 32 scores are live in registers.  Tiles that
+      // every row of the block sees whole take a path without masking.
+      const bool all_vis = key0 + kTile - 1 <= start + tok0;
       const int nvis = pos >= lo ? min(lo + S, pos + 1) - key0 : 0;
-      auto scores = [&](int hf, float (&x)[32]) {
+      auto scores = [&](int hf, float (&x)[32], auto all_tag) {
+        constexpr bool kAll = decltype(all_tag)::value;
         uint32_t sv[32];
         tmem_ld32(tl + Gm::kColS + 128 * ((i >> 1) & 1) + 64 * (i & 1) + 32 * hf, sv);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const float sj = __fmul_rn(__uint_as_float(sv[j]), p.scale_log2);
-          x[j] = (all_vis || 32 * hf + j < nvis) ? sj : -CUDART_INF_F;
+          x[j] = (kAll || 32 * hf + j < nvis) ? sj : -CUDART_INF_F;
         }
       };
       float mh[2] = {-CUDART_INF_F, -CUDART_INF_F};
-      float x1[32];  // scaled scores of keys 32..63
-      if (live) {
-        tc_fence_after();
+      auto row_max = [&](auto all_tag) {
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           float x[32];
-          scores(hf, x);
+          scores(hf, x, all_tag);
           float t[16];  // the row maximum is exact in any order: a tree
 #pragma unroll
           for (int j = 0; j < 16; ++j) t[j] = fmaxf(x[2 * j], x[2 * j + 1]);
@@ -1255,11 +1256,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
 #pragma unroll
             for (int j = 0; j < w; ++j) t[j] = fmaxf(t[2 * j], t[2 * j + 1]);
           mh[hf] = t[0];
-          if (hf == 1) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) x1[j] = x[j];
-          }
         }
+      };
+      if (live) {
+        tc_fence_after();
+        if (all_vis)
+          row_max(std::true_type{});
+        else
+          row_max(std::false_type{});
       }
       const float mx = fmaxf(mh[0], mh[1]);
       // ---- running maximum of the previous tile
@@ -1289,20 +1293,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       float cs[8];
 #pragma unroll
       for (int g8 = 0; g8 < 8; ++g8) cs[g8] = 0.0f;
-      if (live) {
+      auto probs = [&](auto all_tag) {
+        constexpr bool kAll = decltype(all_tag)::value;
         uint8_t* ph = pbuf + b2 * 2 * Gm::kPBytes;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           float x[32];
-          if (hf == 0) {
-            scores(0, x);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] = x1[j];
-          }
+          scores(hf, x, all_tag);
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            x[j] = x[j] != -CUDART_INF_F ? exp2_sfu(__fsub_rn(x[j], mnew)) : 0.0f;
+            x[j] = (kAll || x[j] != -CUDART_INF_F) ? exp2_sfu(__fsub_rn(x[j], mnew)) : 0.0f;
             cs[j & 7] = __fadd_rn(cs[j & 7], x[j]);
           }
 #pragma unroll
@@ -1326,6 +1326,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
           }
         }
         fence_proxy_async_smem();
+      };
+      if (live) {
+        if (all_vis)
+          probs(std::true_type{});
+        else
+          probs(std::false_type{});
       }
       tc_fence_before();
       __syncwarp();
