@@ -84,6 +84,22 @@ bi_status bi_rmsnorm(const void* x, const void* w, void* y, float* y_f32, int64_
                      int64_t H, float eps, bi_mode mode, void* workspace,
                      size_t workspace_bytes, void* stream);
 
+/* Residual add fused with RMSNorm (the pre-norm step of a decoder layer).
+ * The pages define only RMSNorm ("Your Answer Depends on Who Else Is in the
+ * Batch", "A Concrete Example"); the fused add is this library's addition:
+ *   h = bf16(x + residual)   (each element: fp32 add, rounded once to bf16),
+ *       written over residual (the updated residual stream);
+ *   y = RMSNorm(h) * w        exactly as bi_rmsnorm(h, w, y, ...).
+ * The bytes equal a bf16 add followed by bi_rmsnorm, in both modes; the
+ * invariant mode reads x and residual once (one row per CTA, the RMSNorm
+ * row reduction above).  Layouts, alignment and errors as bi_rmsnorm; x and
+ * residual must not overlap.  BI_MODE_VARIANT runs the add, then the split
+ * RMSNorm, and needs bi_rmsnorm_workspace_size(M, H, BI_MODE_VARIANT)
+ * bytes. */
+bi_status bi_add_rmsnorm(const void* x, void* residual, const void* w, void* y, float* y_f32,
+                         int64_t M, int64_t H, float eps, bi_mode mode, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
 /* Bytes of workspace bi_rmsnorm needs: 0 for BI_MODE_INVARIANT; for
  * BI_MODE_VARIANT an upper bound (M * 64 * 4).  Host arithmetic only. */
 size_t bi_rmsnorm_workspace_size(int64_t M, int64_t H, bi_mode mode);

@@ -30,8 +30,9 @@ __all__ = [
     "bi_rmsnorm", "bi_rmsnorm_workspace_size", "bi_gemm", "bi_gemm_workspace_size",
     "bi_gemm_variant_splits", "bi_attn_decode", "bi_attn_decode_workspace_size",
     "bi_attn_prefill_chunk", "bi_kv_write", "bi_check_device_errors", "bi_status_string",
-    "bi_version", "bi_attn_decode_noalloc", "bi_selftest_wait_timeout", "NOALLOC_SCRATCH_BYTES",
-    "rmsnorm", "gemm", "attn_decode", "attn_prefill_chunk", "kv_write",
+    "bi_version", "bi_attn_decode_noalloc", "bi_selftest_wait_timeout", "bi_add_rmsnorm",
+    "NOALLOC_SCRATCH_BYTES", "rmsnorm", "add_rmsnorm", "gemm", "attn_decode",
+    "attn_prefill_chunk", "kv_write",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -40,7 +41,7 @@ EXPORTED_SYMBOLS = (
     "bi_rmsnorm", "bi_rmsnorm_workspace_size", "bi_gemm", "bi_gemm_workspace_size",
     "bi_gemm_variant_splits", "bi_attn_decode", "bi_attn_decode_workspace_size",
     "bi_attn_prefill_chunk", "bi_kv_write", "bi_check_device_errors", "bi_status_string",
-    "bi_version", "bi_attn_decode_noalloc", "bi_selftest_wait_timeout",
+    "bi_version", "bi_attn_decode_noalloc", "bi_selftest_wait_timeout", "bi_add_rmsnorm",
 )
 
 
@@ -76,6 +77,8 @@ def load(build_if_missing: bool = True):
         lib = ctypes.CDLL(LIB_PATH)
         sig = {
             "bi_rmsnorm": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _f32, _i32, _vp, _sz, _vp]),
+            "bi_add_rmsnorm": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, _i32, _vp, _sz,
+                                      _vp]),
             "bi_rmsnorm_workspace_size": (_sz, [_i64, _i64, _i32]),
             "bi_gemm": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp, _sz, _vp]),
             "bi_gemm_workspace_size": (_sz, [_i64, _i64, _i64, _i32, _i32]),
@@ -152,6 +155,20 @@ def bi_rmsnorm(x, w, y, eps, mode=INVARIANT, workspace=None, stream=None, y_f32=
                              _ptr(y, torch.bfloat16, "y"), _ptr(y_f32, torch.float32, "y_f32"),
                              M, H, float(eps), int(mode), wp, wb, _stream(stream)),
            "bi_rmsnorm")
+
+
+def bi_add_rmsnorm(x, residual, w, y, eps, mode=INVARIANT, workspace=None, stream=None,
+                   y_f32=None):
+    """residual <- bf16(x + residual); y <- RMSNorm(residual) * w (include/bi.h)."""
+    M, H = x.shape
+    if tuple(residual.shape) != (M, H) or tuple(y.shape) != (M, H):
+        raise ValueError("x, residual and y must have the same shape")
+    wp, wb = _ws(workspace)
+    _check(load().bi_add_rmsnorm(_ptr(x, torch.bfloat16, "x"),
+                                 _ptr(residual, torch.bfloat16, "residual"),
+                                 _ptr(w, torch.bfloat16, "w"), _ptr(y, torch.bfloat16, "y"),
+                                 _ptr(y_f32, torch.float32, "y_f32"), M, H, float(eps),
+                                 int(mode), wp, wb, _stream(stream)), "bi_add_rmsnorm")
 
 
 def bi_rmsnorm_workspace_size(M, H, mode=INVARIANT) -> int:
@@ -272,6 +289,16 @@ def rmsnorm(x, w, eps=1e-6, mode=INVARIANT, want_f32=False, stream=None):
     y32 = torch.empty(x.shape, dtype=torch.float32, device=x.device) if want_f32 else None
     ws = _workspace(bi_rmsnorm_workspace_size(x.shape[0], x.shape[1], mode), x.device)
     bi_rmsnorm(x, w, y, eps, mode, ws, stream, y_f32=y32)
+    return (y, y32) if want_f32 else y
+
+
+def add_rmsnorm(x, residual, w, eps=1e-6, mode=INVARIANT, want_f32=False, stream=None):
+    """Updates residual in place (residual <- bf16(x + residual)) and returns
+    RMSNorm(residual) * w (and its fp32 values with want_f32)."""
+    y = torch.empty_like(x)
+    y32 = torch.empty(x.shape, dtype=torch.float32, device=x.device) if want_f32 else None
+    ws = _workspace(bi_rmsnorm_workspace_size(x.shape[0], x.shape[1], mode), x.device)
+    bi_add_rmsnorm(x, residual, w, y, eps, mode, ws, stream, y_f32=y32)
     return (y, y32) if want_f32 else y
 
 

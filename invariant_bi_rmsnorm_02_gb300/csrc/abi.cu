@@ -175,6 +175,27 @@ bi_status bi_rmsnorm(const void* x, const void* w, void* y, float* y_f32, int64_
                                 static_cast<float*>(workspace), err, s);
 }
 
+bi_status bi_add_rmsnorm(const void* x, void* residual, const void* w, void* y, float* y_f32,
+                         int64_t M, int64_t H, float eps, bi_mode mode, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (M < 0 || H <= 0) return BI_ERR_INVALID_ARG;
+  if (mode != BI_MODE_INVARIANT && mode != BI_MODE_VARIANT) return BI_ERR_INVALID_ARG;
+  if (H % 8 != 0 || H < 8 || H > 65536) return BI_ERR_UNSUPPORTED;
+  if (M > 0x7fffffff) return BI_ERR_UNSUPPORTED;
+  if (M == 0) return BI_OK;
+  if (!x || !residual || !w || !y) return BI_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(residual) || !aligned16(w) || !aligned16(y))
+    return BI_ERR_INVALID_ARG;
+  if (y_f32 && !aligned16(y_f32)) return BI_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f)) return BI_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (mode == BI_MODE_INVARIANT)
+    return launch_add_rmsnorm_invariant(x, residual, w, y, y_f32, M, H, eps, s);
+  const bi_status st = launch_add_bf16(x, residual, M * H, s);
+  if (st != BI_OK) return st;
+  return bi_rmsnorm(residual, w, y, y_f32, M, H, eps, mode, workspace, workspace_bytes, stream);
+}
+
 // --------------------------------------------------------------------- GEMM
 int bi_gemm_variant_splits(int64_t M, int64_t N, int64_t K, int num_sms) {
   if (M <= 0 || N <= 0 || K <= 0 || num_sms <= 0) return 1;

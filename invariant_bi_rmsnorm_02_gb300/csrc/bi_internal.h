@@ -27,6 +27,10 @@ inline bi_status cuda_status(cudaError_t e) { return e == cudaSuccess ? BI_OK : 
 // ---- RMSNorm (rmsnorm.cu) ---------------------------------------------------
 bi_status launch_rmsnorm_invariant(const void* x, const void* w, void* y, float* y_f32,
                                    int64_t M, int64_t H, float eps, int* err, cudaStream_t s);
+bi_status launch_add_rmsnorm_invariant(const void* x, void* res, const void* w, void* y,
+                                       float* y_f32, int64_t M, int64_t H, float eps,
+                                       cudaStream_t s);
+bi_status launch_add_bf16(const void* x, void* res, int64_t elems, cudaStream_t s);
 int rmsnorm_variant_splits(int64_t M, int64_t H, int num_sms);
 bi_status launch_rmsnorm_variant(const void* x, const void* w, void* y, float* y_f32, int64_t M,
                                  int64_t H, float eps, int splits, float* ws, int* err,

@@ -113,6 +113,60 @@ __global__ void __launch_bounds__(1024) rmsnorm_row_kernel(const uint4* __restri
   }
 }
 
+// Residual add fused in front: h = bf16(x + res) (an fp32 add, rounded once)
+// overwrites res, and y = RMSNorm(h) * w with exactly the row reduction of
+// rmsnorm_row_kernel, so the result equals a bf16 add followed by RMSNorm.
+__device__ __forceinline__ uint4 add_bf16x8(const uint4& a, const uint4& b) {
+  const uint32_t as[4] = {a.x, a.y, a.z, a.w}, bs[4] = {b.x, b.y, b.z, b.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    o[i] = pack_bf16x2(__fadd_rn(bf16_lo(as[i]), bf16_lo(bs[i])),
+                       __fadd_rn(bf16_hi(as[i]), bf16_hi(bs[i])));
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(1024) add_rmsnorm_row_kernel(
+    const uint4* __restrict__ x, uint4* __restrict__ res, const uint4* __restrict__ w,
+    uint4* __restrict__ y, float* __restrict__ yf, int nvec, float inv_h, float eps) {
+  __shared__ float red[32];
+  const int64_t row = blockIdx.x;
+  const uint4* xr = x + row * nvec;
+  uint4* rr = res + row * nvec;
+  uint4 hv[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = threadIdx.x + k * blockDim.x;
+    hv[k] = v < nvec ? add_bf16x8(__ldcs(xr + v), __ldcs(rr + v)) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = threadIdx.x + k * blockDim.x;
+    if (v < nvec) __stcs(rr + v, hv[k]);
+  }
+  float ss = 0.0f;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) ss = sum_squares8(hv[k], ss);
+  const float r = inv_rms(block_sum(ss, red), inv_h, eps);
+  uint4* yr = y + row * nvec;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = threadIdx.x + k * blockDim.x;
+    if (v < nvec)
+      __stcs(yr + v, scale_row8(hv[k], __ldg(w + v), r, yf ? yf + (row * nvec + v) * 8 : nullptr));
+  }
+}
+
+// The add alone, for the batch-variant path (which then runs the split
+// RMSNorm over h).
+__global__ void add_bf16_kernel(const uint4* __restrict__ x, uint4* __restrict__ res,
+                                int64_t nvec_total) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nvec_total;
+       i += (int64_t)gridDim.x * blockDim.x)
+    res[i] = add_bf16x8(x[i], res[i]);
+}
+
 // Block shape as a function of H only: VPT vectors of 8 elements per thread,
 // T threads (a multiple of 32, at most 1024).
 struct RowShape {
@@ -187,6 +241,38 @@ bi_status launch_rmsnorm_invariant(const void* x, const void* w, void* y, float*
     case 8: rmsnorm_row_kernel<8><<<grid, sh.threads, 0, s>>>(xp, wp, yp, y_f32, nvec, inv_h, eps); break;
     default: return BI_ERR_UNSUPPORTED;
   }
+  return cuda_status(cudaGetLastError());
+}
+
+bi_status launch_add_rmsnorm_invariant(const void* x, void* res, const void* w, void* y,
+                                       float* y_f32, int64_t M, int64_t H, float eps,
+                                       cudaStream_t s) {
+  if (M == 0) return BI_OK;
+  const RowShape sh = row_shape(H);
+  const int nvec = static_cast<int>(H / 8);
+  const float inv_h = 1.0f / static_cast<float>(H);
+  const dim3 grid(static_cast<unsigned>(M));
+  const auto* xp = static_cast<const uint4*>(x);
+  auto* rp = static_cast<uint4*>(res);
+  const auto* wp = static_cast<const uint4*>(w);
+  auto* yp = static_cast<uint4*>(y);
+  switch (sh.vpt) {
+    case 1: add_rmsnorm_row_kernel<1><<<grid, sh.threads, 0, s>>>(xp, rp, wp, yp, y_f32, nvec, inv_h, eps); break;
+    case 2: add_rmsnorm_row_kernel<2><<<grid, sh.threads, 0, s>>>(xp, rp, wp, yp, y_f32, nvec, inv_h, eps); break;
+    case 4: add_rmsnorm_row_kernel<4><<<grid, sh.threads, 0, s>>>(xp, rp, wp, yp, y_f32, nvec, inv_h, eps); break;
+    case 8: add_rmsnorm_row_kernel<8><<<grid, sh.threads, 0, s>>>(xp, rp, wp, yp, y_f32, nvec, inv_h, eps); break;
+    default: return BI_ERR_UNSUPPORTED;
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+bi_status launch_add_bf16(const void* x, void* res, int64_t elems, cudaStream_t s) {
+  const int64_t nvec = elems / 8;
+  if (nvec == 0) return BI_OK;
+  int64_t blocks = (nvec + 255) / 256;
+  if (blocks > 65535) blocks = 65535;
+  add_bf16_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const uint4*>(x),
+                                                               static_cast<uint4*>(res), nvec);
   return cuda_status(cudaGetLastError());
 }
 

@@ -59,6 +59,8 @@ def _load():
             lib.oracle_default_threads.restype = _i32
             lib.oracle_rmsnorm.argtypes = [_vp, _vp, _i64, _i64, _dbl, _vp, _vp, _i32]
             lib.oracle_rmsnorm.restype = _i32
+            lib.oracle_add_bf16.argtypes = [_vp, _vp, _i64, _vp]
+            lib.oracle_add_bf16.restype = _i32
             lib.oracle_gemm.argtypes = [_vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _i32]
             lib.oracle_gemm.restype = _i32
             lib.oracle_attention.argtypes = [_vp, _i64, _i32, _i32, _vp, _vp, _vp, _vp,
@@ -116,6 +118,26 @@ def rmsnorm(x, w, eps: float, nthreads: int = 0, return_mean_sq: bool = False):
     if rc:
         raise RuntimeError("oracle_rmsnorm failed: %d" % rc)
     return (y, ms) if return_mean_sq else y
+
+
+def add_bf16(x, r) -> np.ndarray:
+    """The bf16 residual stream after an add: round_bf16(float32(x) + float32(r))
+    element by element; returns the uint16 bit patterns, shape of x."""
+    xb, rb = _bits(x), _bits(r)
+    if xb.shape != rb.shape:
+        raise ValueError("x and r differ in shape")
+    h = np.empty(xb.shape, np.uint16)
+    rc = _load().oracle_add_bf16(_p(xb), _p(rb), xb.size, _p(h))
+    if rc:
+        raise RuntimeError("oracle_add_bf16 failed: %d" % rc)
+    return h
+
+
+def add_rmsnorm(x, r, w, eps: float, nthreads: int = 0):
+    """Pre-norm step of a decoder layer: h = add_bf16(x, r), y = rmsnorm(h, w).
+    Returns (h as uint16 bf16 bits, y float64)."""
+    h = add_bf16(x, r)
+    return h, rmsnorm(h, w, eps, nthreads)
 
 
 def gemm(A, W, rows=None, nthreads: int = 0) -> np.ndarray:

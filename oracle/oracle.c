@@ -130,6 +130,32 @@ int oracle_rmsnorm(const uint16_t* x, const uint16_t* w, int64_t M, int64_t H,
 }
 
 /* ------------------------------------------------------------------ */
+/* Residual add (the step in front of a pre-norm RMSNorm)              */
+/* ------------------------------------------------------------------ */
+/* The residual stream is kept in bf16: h = round_bf16(float(x) + float(r)),
+ * the sum of the two bf16 values in IEEE single precision (round to nearest
+ * even), then rounded once more to bf16, nearest even.  The library's fused
+ * add-RMSNorm normalises this h; the RMSNorm itself is oracle_rmsnorm. */
+static uint16_t bf16_round_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7f800000u) == 0x7f800000u) /* inf or nan: keep, quiet the nan */
+    return (uint16_t)((u >> 16) | ((u & 0xffffu) ? 0x40u : 0u));
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+int oracle_add_bf16(const uint16_t* x, const uint16_t* r, int64_t n, uint16_t* h) {
+  if (n < 0 || (n > 0 && (!x || !r || !h))) return -1;
+  for (int64_t i = 0; i < n; ++i) {
+    const float a = (float)bf16_val(x[i]), b = (float)bf16_val(r[i]);
+    volatile float s = a + b; /* one single-precision rounding, no wider intermediate */
+    h[i] = bf16_round_rne(s);
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------ */
 /* GEMM                                                                */
 /* ------------------------------------------------------------------ */
 /* The linear layer: every output element is one dot product over the

@@ -364,3 +364,50 @@ def test_oracle_thread_count_does_not_change_results():
     A = synth.normal_bf16((33, 64), 111)
     W = synth.normal_bf16((40, 64), 112)
     np.testing.assert_array_equal(oracle.gemm(A, W, nthreads=1), oracle.gemm(A, W, nthreads=7))
+
+
+# ------------------------------------------------- residual add (bf16 stream)
+def _bf(vals):
+    return torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16)
+
+
+def _val(bits):
+    return torch.from_numpy(bits.astype(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+
+
+def test_oracle_add_bf16_zero_and_negation():
+    x = synth.normal_bf16((3, 64), 9100)
+    h0 = oracle.add_bf16(x, torch.zeros_like(x))              # x + 0 = x, bit for bit
+    assert np.array_equal(h0, x.view(torch.int16).numpy().astype(np.uint16))
+    hz = oracle.add_bf16(x, -x)                                 # x + (-x) = +0
+    assert (hz == 0).all()
+
+
+def test_oracle_add_bf16_exact_small_integers():
+    g = torch.Generator().manual_seed(9101)
+    a = torch.randint(-64, 65, (500,), generator=g)
+    b = torch.randint(-64, 65, (500,), generator=g)
+    h = _val(oracle.add_bf16(a.to(torch.bfloat16), b.to(torch.bfloat16)))
+    assert np.array_equal(h, (a + b).to(torch.float64).numpy())  # |sum| <= 128: exact in bf16
+
+
+def test_oracle_add_bf16_rounds_to_nearest_even():
+    # bf16 has 8 significant bits: the spacing at 1 is 2^-7
+    x = _bf([1.0, 1.0, 1.0, 1.0 + 2 ** -7, -1.0])
+    r = _bf([2 ** -8, 3 * 2 ** -8, 2 ** -9, 2 ** -8, -(2 ** -8)])
+    h = _val(oracle.add_bf16(x, r))
+    # 1 + 2^-8 is a tie between 1 and 1 + 2^-7: the even one (1) wins;
+    # 1 + 3*2^-8 ties between 1 + 2^-7 and 1 + 2^-6: 1 + 2^-6 is even;
+    # 1 + 2^-9 rounds down; (1 + 2^-7) + 2^-8 ties and goes up to 1 + 2^-6;
+    # -1 - 2^-8 ties and keeps -1
+    assert list(h) == [1.0, 1.0 + 2 ** -6, 1.0, 1.0 + 2 ** -6, -1.0]
+
+
+def test_oracle_add_rmsnorm_is_rmsnorm_of_the_sum():
+    x = synth.normal_bf16((5, 256), 9102)
+    r = synth.normal_bf16((5, 256), 9103)
+    w = synth.normal_bf16((256,), 9104, std=0.1, mean=1.0)
+    h, y = oracle.add_rmsnorm(x, r, w, 1e-6)
+    hv = _val(h)
+    want = hv / np.sqrt((hv * hv).mean(axis=1, keepdims=True) + 1e-6) * f64(w)
+    assert np.allclose(y, want, rtol=1e-12, atol=0)
