@@ -74,6 +74,13 @@ def _load():
             lib.oracle_split_starts_fixed_size.restype = _i64
             lib.oracle_split_starts_fixed_count.argtypes = [_i64, _i64, _vp, _i64]
             lib.oracle_split_starts_fixed_count.restype = _i64
+            lib.oracle_philox4x64.argtypes = [_vp, _vp, _vp]
+            lib.oracle_philox4x64.restype = None
+            lib.oracle_sample_uniform.argtypes = [ctypes.c_uint64, ctypes.c_uint64, _i64, _i64,
+                                                  _vp]
+            lib.oracle_sample_uniform.restype = _i32
+            lib.oracle_sample_scores.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _i32]
+            lib.oracle_sample_scores.restype = _i32
             _lib = lib
     return _lib
 
@@ -230,3 +237,46 @@ def split_starts_fixed_count(L: int, count: int) -> list:
     if n < 0:
         raise ValueError("bad split plan arguments")
     return [int(v) for v in buf[: n + 1]]
+
+
+# --------------------------------------------------------------------------
+# seeded sampling
+# --------------------------------------------------------------------------
+def philox4x64(counter, key) -> np.ndarray:
+    """Philox4x64-10 (Salmon et al., SC 2011) of a 4-word counter under a
+    2-word key: the four 64-bit output words."""
+    c = np.ascontiguousarray(counter, dtype=np.uint64)
+    k = np.ascontiguousarray(key, dtype=np.uint64)
+    if c.shape != (4,) or k.shape != (2,):
+        raise ValueError("counter has 4 words, key 2")
+    out = np.empty(4, np.uint64)
+    _load().oracle_philox4x64(_p(c), _p(k), _p(out))
+    return out
+
+
+def sample_uniform(seed: int, step: int, v0: int, n: int) -> np.ndarray:
+    """The uniforms in (0, 1) of vocabulary entries v0 .. v0+n-1 for one
+    (seed, step) -- the random numbers behind the Gumbel noise."""
+    u = np.empty(n, np.float64)
+    rc = _load().oracle_sample_uniform(int(seed), int(step), int(v0), int(n), _p(u))
+    if rc:
+        raise RuntimeError("oracle_sample_uniform failed: %d" % rc)
+    return u
+
+
+def sample(logits, temperature, seed, step, nthreads: int = 0):
+    """Seeded Gumbel-max sampling (P1 §9.3; §9.2 for temperature 0): for each
+    row b, token = argmax_v score[b, v] with score = z / T_b - log(-log(u))
+    when T_b > 0 and score = z otherwise; ties go to the lowest index.
+    logits [B, V] bf16; temperature float32 [B]; seed, step uint64 [B].
+    Returns (tokens int64 [B], scores float64 [B, V])."""
+    zb = _bits(logits)
+    B, V = zb.shape
+    T = np.ascontiguousarray(np.asarray(temperature, dtype=np.float32).reshape(B))
+    sd = np.ascontiguousarray(np.asarray(seed, dtype=np.uint64).reshape(B))
+    st = np.ascontiguousarray(np.asarray(step, dtype=np.uint64).reshape(B))
+    scores = np.empty((B, V), np.float64)
+    rc = _load().oracle_sample_scores(_p(zb), B, V, _p(T), _p(sd), _p(st), _p(scores), nthreads)
+    if rc:
+        raise RuntimeError("oracle_sample_scores failed: %d" % rc)
+    return np.argmax(scores, axis=1).astype(np.int64), scores

@@ -414,3 +414,96 @@ int oracle_attention_splits(const uint16_t* q, int64_t R, int Hq, int D,
   parallel_rows(attn_split_row, &c, R, nthreads);
   return c.status;
 }
+
+/* ------------------------------------------------------------------ */
+/* Seeded sampling ([P1] §9.2, §9.3)                                   */
+/* ------------------------------------------------------------------ */
+/* [P1] §9.3: a sampler that is deterministic under batching perturbs the
+ * logits with Gumbel noise drawn from a seeded hash and takes the argmax
+ * (the Gumbel-max construction: argmax_v (z_v / T + G_v) with G_v i.i.d.
+ * standard Gumbel is a draw from softmax(z / T)); §9.2: temperature 0 is the
+ * plain argmax.  The pages name no hash; this oracle and the kernel each
+ * implement Philox4x64-10 from its publication (Salmon, Moraes, Dror and
+ * Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3", SC 2011): a 4 x 64-bit
+ * counter and a 2 x 64-bit key, ten rounds of two 64 x 64 -> 128-bit
+ * products, the key advanced by two Weyl constants between rounds. */
+static void philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]) {
+  uint64_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+  uint64_t k0 = key[0], k1 = key[1];
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k0 += 0x9E3779B97F4A7C15ull;   /* golden ratio */
+      k1 += 0xBB67AE8584CAA73Bull;   /* sqrt(3) - 1 */
+    }
+    unsigned __int128 p0 = (unsigned __int128)0xD2E7470EE14C6C93ull * c0;
+    unsigned __int128 p1 = (unsigned __int128)0xCA5A826395121157ull * c2;
+    uint64_t hi0 = (uint64_t)(p0 >> 64), lo0 = (uint64_t)p0;
+    uint64_t hi1 = (uint64_t)(p1 >> 64), lo1 = (uint64_t)p1;
+    c0 = hi1 ^ c1 ^ k0;
+    c1 = lo1;
+    c2 = hi0 ^ c3 ^ k1;
+    c3 = lo0;
+  }
+  out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+void oracle_philox4x64(const uint64_t* ctr, const uint64_t* key, uint64_t* out) {
+  philox4x64_10(ctr, key, out);
+}
+
+/* The uniform of vocabulary entry v for (seed, step): one Philox block per 8
+ * entries (counter {v / 8, step, 0, 0}, key {seed, 0}); entry v takes 32-bit
+ * half v % 2 (0 = low) of 64-bit word (v / 2) % 4, keeps its top 23 bits k
+ * and maps them to u = (k + 1/2) 2^-23, strictly inside (0, 1). */
+static double sample_uniform(uint64_t seed, uint64_t step, int64_t v) {
+  const uint64_t ctr[4] = {(uint64_t)v >> 3, step, 0, 0}, key[2] = {seed, 0};
+  uint64_t out[4];
+  philox4x64_10(ctr, key, out);
+  const uint64_t w = out[(v >> 1) & 3];
+  const uint32_t half = (v & 1) ? (uint32_t)(w >> 32) : (uint32_t)w;
+  return ((double)(half >> 9) + 0.5) * 0x1p-23;
+}
+
+int oracle_sample_uniform(uint64_t seed, uint64_t step, int64_t v0, int64_t n, double* u) {
+  if (v0 < 0 || n < 0 || (n && !u)) return -1;
+  for (int64_t i = 0; i < n; ++i) u[i] = sample_uniform(seed, step, v0 + i);
+  return 0;
+}
+
+typedef struct {
+  const uint16_t* logits;
+  int64_t V;
+  const float* temperature;
+  const uint64_t* seed;
+  const uint64_t* step;
+  double* scores;
+} sample_ctx;
+
+/* Score of entry v of row b: z / T + G with G = -log(-log(u)) for T > 0,
+ * else the logit itself (greedy). */
+static void sample_row(void* p, int64_t b) {
+  sample_ctx* c = (sample_ctx*)p;
+  const uint16_t* z = c->logits + b * c->V;
+  double* s = c->scores + b * c->V;
+  const double T = (double)c->temperature[b];
+  for (int64_t v = 0; v < c->V; ++v) {
+    const double x = bf16_val(z[v]);
+    if (T > 0.0) {
+      const double u = sample_uniform(c->seed[b], c->step[b], v);
+      s[v] = x / T - log(-log(u));
+    } else {
+      s[v] = x;
+    }
+  }
+}
+
+int oracle_sample_scores(const uint16_t* logits, int64_t B, int64_t V, const float* temperature,
+                         const uint64_t* seed, const uint64_t* step, double* scores,
+                         int nthreads) {
+  if (B < 0 || V <= 0) return -1;
+  if (B == 0) return 0;
+  if (!logits || !temperature || !seed || !step || !scores) return -1;
+  sample_ctx c = {logits, V, temperature, seed, step, scores};
+  parallel_rows(sample_row, &c, B, nthreads);
+  return 0;
+}

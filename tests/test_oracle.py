@@ -411,3 +411,92 @@ def test_oracle_add_rmsnorm_is_rmsnorm_of_the_sum():
     hv = _val(h)
     want = hv / np.sqrt((hv * hv).mean(axis=1, keepdims=True) + 1e-6) * f64(w)
     assert np.allclose(y, want, rtol=1e-12, atol=0)
+
+
+# ------------------------------------------------------------ seeded sampling
+U64 = (1 << 64) - 1
+
+
+def _numpy_philox_words(counter, key, nwords):
+    """numpy's Philox4x64-10 stream: it advances the counter before each
+    block, so starting one below gives the block of `counter` first."""
+    whole = sum(int(w) << (64 * i) for i, w in enumerate(counter)) - 1   # 256-bit, borrows
+    whole &= (1 << 256) - 1
+    c = np.array([(whole >> (64 * i)) & U64 for i in range(4)], dtype=np.uint64)
+    bg = np.random.Philox(counter=c, key=np.array(key, dtype=np.uint64))
+    return bg.random_raw(nwords)
+
+
+@pytest.mark.parametrize("counter,key", [([0, 0, 0, 0], [0, 0]),
+                                         ([5, 7, 0, 0], [0x1234567890ABCDEF, 42]),
+                                         ([U64, 3, 9, 1], [0xFEDCBA9876543210, U64]),
+                                         ([1 << 63, U64, 0, U64], [1, 2])])
+def test_philox_matches_numpy(counter, key):
+    got = oracle.philox4x64(counter, key)
+    assert np.array_equal(got, _numpy_philox_words(counter, key, 4))
+
+
+def test_philox_known_answer_zero_counter_and_key():
+    # the published known-answer vector of Philox4x64-10 for an all-zero
+    # counter and key (Random123 distribution)
+    got = [int(v) for v in oracle.philox4x64([0, 0, 0, 0], [0, 0])]
+    assert got == [0x16554D9ECA36314C, 0xDB20FE9D672D0FDC, 0xD7E772CEE186176B,
+                   0x7E68B68AEC7BA23B]
+
+
+@pytest.mark.parametrize("seed,step", [(0, 0), (2024, 17), (U64, 1 << 40)])
+def test_sample_uniforms_are_the_philox_stream(seed, step):
+    # entry v's uniform comes from the 32-bit word v of the little-endian
+    # stream of blocks {0, step}, {1, step}, ... under key {seed, 0}
+    n = 1000
+    words = _numpy_philox_words([0, step, 0, 0], [seed, 0], n // 2 + 8)
+    halves = words.astype("<u8").view("<u4")[:n].astype(np.float64)
+    want = (np.floor(halves / 512) + 0.5) * 2.0 ** -23
+    assert np.array_equal(oracle.sample_uniform(seed, step, 0, n), want)
+    # an offset start reads the same stream
+    assert np.array_equal(oracle.sample_uniform(seed, step, 333, 100), want[333:433])
+
+
+def test_gumbel_noise_moments():
+    # G = -log(-log u) is standard Gumbel: mean = Euler's constant,
+    # variance = pi^2 / 6
+    u = oracle.sample_uniform(99, 5, 0, 1 << 20)
+    assert u.min() > 0 and u.max() < 1
+    g = -np.log(-np.log(u))
+    se = math.sqrt(math.pi ** 2 / 6 / u.size)
+    assert abs(g.mean() - 0.5772156649015329) < 5 * se
+    assert abs(g.var() - math.pi ** 2 / 6) < 0.02
+
+
+def test_gumbel_max_draws_follow_softmax():
+    # Gumbel-max: argmax(z / T + G) is distributed as softmax(z / T)
+    z = bf([0.0, 1.0, 2.0, -1.0, 1.0])
+    T, n = 0.75, 40000
+    logits = z.repeat(n, 1)
+    tok, _ = oracle.sample(logits, np.full(n, T, np.float32), np.full(n, 7, np.uint64),
+                           np.arange(n, dtype=np.uint64))
+    p = np.exp(f64(z) / T)
+    p /= p.sum()
+    freq = np.bincount(tok, minlength=5) / n
+    assert np.all(np.abs(freq - p) < 5 * np.sqrt(p * (1 - p) / n)), (freq, p)
+
+
+def test_sample_greedy_and_limits():
+    z = bf([[0.5, 3.0, -1.0, 3.0, 2.0], [-2.0, -2.0, -2.0, -2.0, -2.0]])
+    seed = np.array([1, 2], np.uint64)
+    step = np.array([0, 0], np.uint64)
+    # temperature 0 (and below): the plain argmax, lowest index on ties
+    for T in (0.0, -1.0):
+        tok, sc = oracle.sample(z, np.full(2, T, np.float32), seed, step)
+        assert list(tok) == [1, 0]
+        assert np.array_equal(sc, f64(z))
+    # a tiny temperature: the logit gaps dwarf the noise
+    tok, _ = oracle.sample(bf([[0.5, 3.0, -1.0, 2.0]]), np.float32([1e-3]), seed[:1], step[:1])
+    assert list(tok) == [1]
+    # the same (logits, seed, step) always gives the same token; the seed matters
+    zz = synth.normal_bf16((64, 300), 9120)
+    T = np.full(64, 1.0, np.float32)
+    a, _ = oracle.sample(zz, T, np.arange(64, dtype=np.uint64), np.zeros(64, np.uint64))
+    b, _ = oracle.sample(zz, T, np.arange(64, dtype=np.uint64), np.zeros(64, np.uint64))
+    c, _ = oracle.sample(zz, T, np.arange(64, dtype=np.uint64) + 1000, np.zeros(64, np.uint64))
+    assert np.array_equal(a, b) and not np.array_equal(a, c)
