@@ -259,6 +259,35 @@ bi_status bi_kv_write(const void* k_new, const void* v_new, const int32_t* seq,
                       int64_t num_pages, int max_blocks_per_seq, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Next-token selection  (P1 §9.2, §9.3)                                    */
+/* ------------------------------------------------------------------------ */
+/* One token per request from its row of logits, deterministic for given
+ * (logits row, temperature, seed, step) whatever the batch around it.
+ *   logits [B][V] bf16 (row-major, e.g. the LM-head output of bi_gemm);
+ *   temperature [B] float, seed [B] and step [B] uint64, tokens [B] int32:
+ *   all device pointers, caller-owned; logits aligned to 2 bytes, the
+ *   others to their element size.
+ * temperature[b] > 0: Gumbel-max sampling (P1 §9.3: the logits perturbed by
+ *   Gumbel noise from a seeded hash), tokens[b] = argmax_v z_v / T + G_v with
+ *   G_v = -log(-log(u_v)), computed in fp32 (z * (1/T), then + G).  u_v is
+ *   drawn by Philox4x64-10 (Salmon et al., SC 2011) under key {seed[b], 0}
+ *   at counter {v / 8, step[b], 0, 0}: 32-bit half v % 2 (low half first) of
+ *   output word (v / 2) % 4, top 23 bits k, u = (k + 1/2) 2^-23.  The draw
+ *   follows softmax(z / T); step is the caller's per-request counter (e.g.
+ *   the position of the token being chosen), so successive tokens of one
+ *   request get fresh noise.
+ * temperature[b] <= 0 (or NaN): greedy, tokens[b] = argmax_v z_v (P1 §9.2).
+ * Ties go to the lowest index; -0 equals +0; a NaN score never wins (an
+ *   all-NaN or all -inf row gives token 0).
+ * The argmax is a reduction under a total order, so its result does not
+ *   depend on how the row is split; one launch, a cluster of 8 CTAs per row.
+ * Requirements: 0 <= B <= 65535, 1 <= V < 2^31.  Needs no workspace.
+ * Errors: BI_ERR_INVALID_ARG (null, misaligned, B < 0, V < 1),
+ *   BI_ERR_UNSUPPORTED (B or V too large), BI_ERR_CUDA (launch). */
+bi_status bi_sample(const void* logits, int64_t B, int64_t V, const float* temperature,
+                    const uint64_t* seed, const uint64_t* step, int32_t* tokens, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Errors and introspection                                                 */
 /* ------------------------------------------------------------------------ */
 /* Synchronises `stream`, then reads and clears the current device's error

@@ -31,8 +31,8 @@ __all__ = [
     "bi_gemm_variant_splits", "bi_attn_decode", "bi_attn_decode_workspace_size",
     "bi_attn_prefill_chunk", "bi_kv_write", "bi_check_device_errors", "bi_status_string",
     "bi_version", "bi_attn_decode_noalloc", "bi_selftest_wait_timeout", "bi_add_rmsnorm",
-    "NOALLOC_SCRATCH_BYTES", "rmsnorm", "add_rmsnorm", "gemm", "attn_decode",
-    "attn_prefill_chunk", "kv_write",
+    "bi_sample", "NOALLOC_SCRATCH_BYTES", "rmsnorm", "add_rmsnorm", "gemm", "attn_decode",
+    "attn_prefill_chunk", "kv_write", "sample",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -42,6 +42,7 @@ EXPORTED_SYMBOLS = (
     "bi_gemm_variant_splits", "bi_attn_decode", "bi_attn_decode_workspace_size",
     "bi_attn_prefill_chunk", "bi_kv_write", "bi_check_device_errors", "bi_status_string",
     "bi_version", "bi_attn_decode_noalloc", "bi_selftest_wait_timeout", "bi_add_rmsnorm",
+    "bi_sample",
 )
 
 
@@ -96,6 +97,7 @@ def load(build_if_missing: bool = True):
             "bi_attn_decode_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32,
                                               _i32, _i32, _i32, _i64, _i32, _i32, _i32, _f32,
                                               _vp]),
+            "bi_sample": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
             "bi_check_device_errors": (_i32, [_vp]),
             "bi_selftest_wait_timeout": (_i32, [ctypes.c_uint32, _vp]),
             "bi_status_string": (ctypes.c_char_p, [_i32]),
@@ -257,6 +259,20 @@ def bi_kv_write(k_new, v_new, seq, pos, k_cache, v_cache, block_table, stream=No
         block_table.shape[1], _stream(stream)), "bi_kv_write")
 
 
+def bi_sample(logits, temperature, seed, step, tokens, stream=None):
+    """tokens[b] <- the token of row b of logits (include/bi.h).  seed and step
+    are int64 tensors whose bits are read as uint64."""
+    B, V = logits.shape
+    for t, name in ((temperature, "temperature"), (seed, "seed"), (step, "step"),
+                    (tokens, "tokens")):
+        if tuple(t.shape) != (B,):
+            raise ValueError("%s must have shape [B]" % name)
+    _check(load().bi_sample(_ptr(logits, torch.bfloat16, "logits"), B, V,
+                            _ptr(temperature, torch.float32, "temperature"),
+                            _ptr(seed, torch.int64, "seed"), _ptr(step, torch.int64, "step"),
+                            _ptr(tokens, torch.int32, "tokens"), _stream(stream)), "bi_sample")
+
+
 def bi_check_device_errors(stream=None) -> int:
     return int(load().bi_check_device_errors(_stream(stream)))
 
@@ -337,6 +353,13 @@ def attn_prefill_chunk(q, cu_q, q_start_pos, k_cache, v_cache, block_table, kv_l
                           split_size=split_size, sm_scale=sm_scale, mode=mode,
                           variant_splits=variant_splits, stream=stream)
     return (out, out32) if want_f32 else out
+
+
+def sample(logits, temperature, seed, step, stream=None):
+    """One token per row: seeded Gumbel-max at temperature > 0, argmax at 0."""
+    tokens = torch.empty(logits.shape[0], dtype=torch.int32, device=logits.device)
+    bi_sample(logits, temperature, seed, step, tokens, stream)
+    return tokens
 
 
 def kv_write(k_new, v_new, seq, pos, k_cache, v_cache, block_table, stream=None):

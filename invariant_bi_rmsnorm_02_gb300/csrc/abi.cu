@@ -383,4 +383,19 @@ bi_status bi_kv_write(const void* k_new, const void* v_new, const int32_t* seq,
                          static_cast<cudaStream_t>(stream));
 }
 
+// ------------------------------------------------------------------ sampling
+bi_status bi_sample(const void* logits, int64_t B, int64_t V, const float* temperature,
+                    const uint64_t* seed, const uint64_t* step, int32_t* tokens, void* stream) {
+  if (B < 0 || V <= 0) return BI_ERR_INVALID_ARG;
+  if (B > 65535 || V >= (int64_t(1) << 31)) return BI_ERR_UNSUPPORTED;
+  if (B == 0) return BI_OK;
+  if (!logits || !temperature || !seed || !step || !tokens) return BI_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(logits) & 1u) || (reinterpret_cast<uintptr_t>(seed) & 7u) ||
+      (reinterpret_cast<uintptr_t>(step) & 7u) || (reinterpret_cast<uintptr_t>(temperature) & 3u) ||
+      (reinterpret_cast<uintptr_t>(tokens) & 3u))
+    return BI_ERR_INVALID_ARG;
+  return launch_sample(logits, B, V, temperature, seed, step, tokens,
+                       static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

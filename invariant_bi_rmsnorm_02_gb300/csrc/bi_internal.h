@@ -31,6 +31,9 @@ bi_status launch_add_rmsnorm_invariant(const void* x, void* res, const void* w, 
                                        float* y_f32, int64_t M, int64_t H, float eps,
                                        cudaStream_t s);
 bi_status launch_add_bf16(const void* x, void* res, int64_t elems, cudaStream_t s);
+bi_status launch_sample(const void* logits, int64_t B, int64_t V, const float* temperature,
+                        const uint64_t* seed, const uint64_t* step, int32_t* tokens,
+                        cudaStream_t s);
 int rmsnorm_variant_splits(int64_t M, int64_t H, int num_sms);
 bi_status launch_rmsnorm_variant(const void* x, const void* w, void* y, float* y_f32, int64_t M,
                                  int64_t H, float eps, int splits, float* ws, int* err,
