@@ -280,3 +280,54 @@ def sample(logits, temperature, seed, step, nthreads: int = 0):
     if rc:
         raise RuntimeError("oracle_sample_scores failed: %d" % rc)
     return np.argmax(scores, axis=1).astype(np.int64), scores
+
+
+# --------------------------------------------------------------------------
+# element-wise decoder-layer steps (numpy, float64)
+# --------------------------------------------------------------------------
+def _widen(t) -> np.ndarray:
+    """bf16 (torch tensor or uint16 bits) -> float64, exactly."""
+    b = _bits(t).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def gather_rows(src, idx) -> np.ndarray:
+    """Row gather (token embedding lookup): the bf16 bit patterns of
+    src[idx[i], :] for each i."""
+    return _bits(src)[np.asarray(idx, dtype=np.int64)]
+
+
+def rope(x, pos, theta: float) -> np.ndarray:
+    """Rotary position embedding of x [T, H, D] at positions pos [T], in the
+    rotate-half arrangement of the Llama family (the pages fix no positional
+    encoding): pair i < D/2 of a head holds elements i and i + D/2 and turns
+    by the angle pos * theta^(-2i/D) (counter-clockwise, element i as the real
+    part)."""
+    xv = _widen(x)
+    D = xv.shape[-1]
+    half = D // 2
+    i = np.arange(half, dtype=np.float64)
+    ang = np.asarray(pos, dtype=np.float64)[:, None] * theta ** (-2.0 * i / D)
+    c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    x1, x2 = xv[..., :half], xv[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def rope_qkv(qkv, pos, Hq: int, Hkv: int, D: int, theta: float):
+    """Split a stacked QKV projection [T, (Hq + 2 Hkv) D] into q, k, v and
+    rotate q and k (see rope); v is returned unrotated (float64)."""
+    T = qkv.shape[0]
+    bits = _bits(qkv).reshape(T, Hq + 2 * Hkv, D)
+    q = rope(bits[:, :Hq], pos, theta)
+    k = rope(bits[:, Hq:Hq + Hkv], pos, theta)
+    v = _widen(bits[:, Hq + Hkv:])
+    return q, k, v
+
+
+def silu_mul(gate_up) -> np.ndarray:
+    """SwiGLU product of a stacked [T, 2F] gate/up projection:
+    silu(g) * u with silu(g) = g / (1 + exp(-g)) (float64)."""
+    gu = _widen(gate_up)
+    F = gu.shape[1] // 2
+    g, u = gu[:, :F], gu[:, F:]
+    return g / (1.0 + np.exp(-g)) * u

@@ -500,3 +500,92 @@ def test_sample_greedy_and_limits():
     b, _ = oracle.sample(zz, T, np.arange(64, dtype=np.uint64), np.zeros(64, np.uint64))
     c, _ = oracle.sample(zz, T, np.arange(64, dtype=np.uint64) + 1000, np.zeros(64, np.uint64))
     assert np.array_equal(a, b) and not np.array_equal(a, c)
+
+
+# ------------------------------------------------- element-wise decoder steps
+def test_rope_position_zero_is_identity_and_pairs_keep_their_norm():
+    x = synth.normal_bf16((5, 3, 64), 9130)
+    pos = np.array([0, 1, 17, 4095, 100000])
+    y = oracle.rope(x, pos, 500000.0)
+    xv = f64(x)
+    assert np.array_equal(y[0], xv[0])
+    n_in = xv[..., :32] ** 2 + xv[..., 32:] ** 2
+    n_out = y[..., :32] ** 2 + y[..., 32:] ** 2
+    assert np.allclose(n_in, n_out, rtol=1e-12, atol=1e-12)
+
+
+def test_rope_is_complex_multiplication_by_the_phase():
+    # pairs (x_i, x_{i+D/2}) as complex numbers x_i + j x_{i+D/2}, multiplied
+    # by exp(j pos theta^(-2i/D))
+    D, theta = 16, 10000.0
+    x = synth.normal_bf16((4, 2, D), 9131)
+    pos = np.array([3, 10, 250, 7])
+    xv = f64(x)
+    z = xv[..., :D // 2] + 1j * xv[..., D // 2:]
+    freq = np.array([theta ** (-2.0 * i / D) for i in range(D // 2)])
+    w = z * np.exp(1j * pos[:, None, None] * freq[None, None, :])
+    y = oracle.rope(x, pos, theta)
+    assert np.allclose(y[..., :D // 2], w.real, atol=1e-12)
+    assert np.allclose(y[..., D // 2:], w.imag, atol=1e-12)
+
+
+def test_rope_hand_worked_pair():
+    # D = 4: pair 0 turns by pos radians, pair 1 by pos / sqrt(theta)
+    x = bf([[[1.0, 2.0, 0.0, -1.0]]])
+    y = oracle.rope(x, np.array([1]), 100.0)[0, 0]
+    a0, a1 = 1.0, 0.1
+    want = [1.0 * math.cos(a0) - 0.0 * math.sin(a0), 2.0 * math.cos(a1) + 1.0 * math.sin(a1),
+            0.0 * math.cos(a0) + 1.0 * math.sin(a0), -1.0 * math.cos(a1) + 2.0 * math.sin(a1)]
+    assert np.allclose(y, want, atol=1e-15)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    q = synth.normal_bf16((1, 1, 128), 9132)
+    k = synth.normal_bf16((1, 1, 128), 9133)
+
+    def score(m, n):
+        return float((oracle.rope(q, [m], 500000.0) * oracle.rope(k, [n], 500000.0)).sum())
+
+    for m, n, s in ((5, 2, 1000), (300, 299, 7), (0, 40, 8000)):
+        assert abs(score(m, n) - score(m + s, n + s)) < 1e-9
+
+
+def test_rope_qkv_splits_heads_in_order():
+    Hq, Hkv, D = 4, 2, 16
+    qkv = synth.normal_bf16((3, (Hq + 2 * Hkv) * D), 9134)
+    pos = np.array([0, 0, 0])
+    q, k, v = oracle.rope_qkv(qkv, pos, Hq, Hkv, D, 10000.0)
+    flat = f64(qkv)
+    assert np.array_equal(q.reshape(3, -1), flat[:, :Hq * D])
+    assert np.array_equal(k.reshape(3, -1), flat[:, Hq * D:(Hq + Hkv) * D])
+    assert np.array_equal(v.reshape(3, -1), flat[:, (Hq + Hkv) * D:])
+
+
+def test_silu_mul_closed_forms():
+    g = np.array([0.0, math.log(3.0), -math.log(3.0), 20.0, -20.0, 1.5])
+    gu = bf(np.concatenate([g, np.ones(6)])[None, :])
+    gb = f64(gu)[0, :6]
+    y = oracle.silu_mul(gu)[0]
+    assert y[0] == 0.0
+    # sigmoid(ln 3) = 3/4, so silu(ln 3) = 0.75 ln 3; g holds ln 3 rounded to
+    # bf16, and silu' < 1 near ln 3 bounds what that rounding moves
+    assert abs(y[1] - 0.75 * math.log(3.0)) <= abs(gb[1] - math.log(3.0)) + 1e-15
+    assert abs(y[2] - (y[1] - gb[1])) < 1e-15          # silu(-x) = silu(x) - x
+    # silu(-x) = silu(x) - x
+    xs = f64(synth.normal_bf16((1, 50), 9135))[0]
+    pos = oracle.silu_mul(bf(np.concatenate([xs, np.ones(50)])[None, :]))[0]
+    neg = oracle.silu_mul(bf(np.concatenate([-xs, np.ones(50)])[None, :]))[0]
+    assert np.allclose(neg, pos - xs, atol=1e-14)
+    assert abs(y[3] - gb[3]) < 1e-7 and abs(y[4]) < 1e-7
+    # the up half multiplies
+    u = f64(synth.normal_bf16((1, 6), 9136))[0]
+    y2 = oracle.silu_mul(bf(np.concatenate([gb, u])[None, :]))[0]
+    assert np.allclose(y2, y * u, rtol=1e-15, atol=0)
+
+
+def test_gather_rows_copies_bits():
+    src = synth.normal_bf16((10, 24), 9137)
+    idx = np.array([3, 3, 0, 9])
+    got = oracle.gather_rows(src, idx)
+    bits = src.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, bits[[3, 3, 0, 9]])
