@@ -259,6 +259,39 @@ bi_status bi_kv_write(const void* k_new, const void* v_new, const int32_t* seq,
                       int64_t num_pages, int max_blocks_per_seq, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Element-wise decoder-layer steps (P1 §5.4: batch-invariant by nature)    */
+/* ------------------------------------------------------------------------ */
+/* Row gather: dst[i, :] = src[idx[i], :] for i < n (token embedding lookup,
+ * or picking the rows that need logits).  src [rows][H] bf16, idx int32 [n]
+ * (device), dst [n][H] bf16.  H % 8 == 0.  An index outside [0, rows) is
+ * recorded in the device error word (BI_ERR_DEVICE_BOUNDS) and its row is
+ * written as zeros.  Pure data movement. */
+bi_status bi_gather_rows(const void* src, int64_t rows, int64_t H, const int32_t* idx, int64_t n,
+                         void* dst, void* stream);
+
+/* Rotary position embedding fused with the split of a QKV projection.
+ *   qkv [T][(Hq + 2 Hkv) D] bf16: per token the Hq query heads, then the Hkv
+ *   key heads, then the Hkv value heads, D elements each (the output of
+ *   bi_gemm with the stacked q/k/v weight); pos int32 [T] (device): each
+ *   token's absolute position.
+ *   q [T][Hq][D], k [T][Hkv][D]: rotated; v [T][Hkv][D]: copied.
+ * Rotation (the rotate-half arrangement): for pair i < D/2 of a head,
+ *   angle = pos * theta^(-2i/D),
+ *   y[i] = x[i] cos - x[i + D/2] sin,  y[i + D/2] = x[i + D/2] cos + x[i] sin.
+ * The angle is formed in fp64 and reduced modulo 2 pi; sine, cosine and the
+ * rotation are fp32, rounded once to bf16.  The pages fix no positional
+ * encoding; this is the one of the Llama family.
+ * Requirements: D % 16 == 0, D <= 1024, theta > 1.  Errors: as bi_rmsnorm. */
+bi_status bi_rope_qkv(const void* qkv, const int32_t* pos, int64_t T, int Hq, int Hkv, int D,
+                      double theta, void* q, void* k, void* v, void* stream);
+
+/* SwiGLU product: out[t, j] = bf16(silu(g) * u) with g = gate_up[t, j],
+ * u = gate_up[t, F + j] (the gate and up projections stacked in one GEMM
+ * output [T][2F] bf16), silu(g) = g / (1 + exp(-g)), fp32.  out [T][F] bf16.
+ * F % 8 == 0.  Errors: as bi_rmsnorm. */
+bi_status bi_silu_mul(const void* gate_up, int64_t T, int64_t F, void* out, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Next-token selection  (P1 §9.2, §9.3)                                    */
 /* ------------------------------------------------------------------------ */
 /* One token per request from its row of logits, deterministic for given

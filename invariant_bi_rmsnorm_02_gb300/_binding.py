@@ -31,8 +31,8 @@ __all__ = [
     "bi_gemm_variant_splits", "bi_attn_decode", "bi_attn_decode_workspace_size",
     "bi_attn_prefill_chunk", "bi_kv_write", "bi_check_device_errors", "bi_status_string",
     "bi_version", "bi_attn_decode_noalloc", "bi_selftest_wait_timeout", "bi_add_rmsnorm",
-    "bi_sample", "NOALLOC_SCRATCH_BYTES", "rmsnorm", "add_rmsnorm", "gemm", "attn_decode",
-    "attn_prefill_chunk", "kv_write", "sample",
+    "bi_sample", "bi_gather_rows", "bi_rope_qkv", "bi_silu_mul", "NOALLOC_SCRATCH_BYTES", "rmsnorm", "add_rmsnorm", "gemm", "attn_decode",
+    "attn_prefill_chunk", "kv_write", "sample", "gather_rows", "rope_qkv", "silu_mul",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -42,7 +42,7 @@ EXPORTED_SYMBOLS = (
     "bi_gemm_variant_splits", "bi_attn_decode", "bi_attn_decode_workspace_size",
     "bi_attn_prefill_chunk", "bi_kv_write", "bi_check_device_errors", "bi_status_string",
     "bi_version", "bi_attn_decode_noalloc", "bi_selftest_wait_timeout", "bi_add_rmsnorm",
-    "bi_sample",
+    "bi_sample", "bi_gather_rows", "bi_rope_qkv", "bi_silu_mul",
 )
 
 
@@ -98,6 +98,10 @@ def load(build_if_missing: bool = True):
                                               _i32, _i32, _i32, _i64, _i32, _i32, _i32, _f32,
                                               _vp]),
             "bi_sample": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
+            "bi_gather_rows": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
+            "bi_rope_qkv": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, ctypes.c_double, _vp, _vp,
+                                   _vp, _vp]),
+            "bi_silu_mul": (_i32, [_vp, _i64, _i64, _vp, _vp]),
             "bi_check_device_errors": (_i32, [_vp]),
             "bi_selftest_wait_timeout": (_i32, [ctypes.c_uint32, _vp]),
             "bi_status_string": (ctypes.c_char_p, [_i32]),
@@ -273,6 +277,37 @@ def bi_sample(logits, temperature, seed, step, tokens, stream=None):
                             _ptr(tokens, torch.int32, "tokens"), _stream(stream)), "bi_sample")
 
 
+def bi_gather_rows(src, idx, dst, stream=None):
+    rows, H = src.shape
+    n = idx.shape[0]
+    if tuple(dst.shape) != (n, H):
+        raise ValueError("dst must be [len(idx), H]")
+    _check(load().bi_gather_rows(_ptr(src, torch.bfloat16, "src"), rows, H,
+                                 _ptr(idx, torch.int32, "idx"), n,
+                                 _ptr(dst, torch.bfloat16, "dst"), _stream(stream)),
+           "bi_gather_rows")
+
+
+def bi_rope_qkv(qkv, pos, Hq, Hkv, D, theta, q, k, v, stream=None):
+    T = qkv.shape[0]
+    if qkv.shape[1] != (Hq + 2 * Hkv) * D or pos.shape != (T,):
+        raise ValueError("qkv must be [T, (Hq + 2 Hkv) D] and pos [T]")
+    if q.shape != (T, Hq, D) or k.shape != (T, Hkv, D) or v.shape != (T, Hkv, D):
+        raise ValueError("q, k, v must be [T, H, D]")
+    _check(load().bi_rope_qkv(_ptr(qkv, torch.bfloat16, "qkv"), _ptr(pos, torch.int32, "pos"), T,
+                              Hq, Hkv, D, float(theta), _ptr(q, torch.bfloat16, "q"),
+                              _ptr(k, torch.bfloat16, "k"), _ptr(v, torch.bfloat16, "v"),
+                              _stream(stream)), "bi_rope_qkv")
+
+
+def bi_silu_mul(gate_up, out, stream=None):
+    T, F2 = gate_up.shape
+    if F2 % 2 or tuple(out.shape) != (T, F2 // 2):
+        raise ValueError("gate_up must be [T, 2F] and out [T, F]")
+    _check(load().bi_silu_mul(_ptr(gate_up, torch.bfloat16, "gate_up"), T, F2 // 2,
+                              _ptr(out, torch.bfloat16, "out"), _stream(stream)), "bi_silu_mul")
+
+
 def bi_check_device_errors(stream=None) -> int:
     return int(load().bi_check_device_errors(_stream(stream)))
 
@@ -360,6 +395,28 @@ def sample(logits, temperature, seed, step, stream=None):
     tokens = torch.empty(logits.shape[0], dtype=torch.int32, device=logits.device)
     bi_sample(logits, temperature, seed, step, tokens, stream)
     return tokens
+
+
+def gather_rows(src, idx, stream=None):
+    dst = torch.empty(idx.shape[0], src.shape[1], dtype=src.dtype, device=src.device)
+    bi_gather_rows(src, idx, dst, stream)
+    return dst
+
+
+def rope_qkv(qkv, pos, Hq, Hkv, D, theta=500000.0, stream=None):
+    T = qkv.shape[0]
+    q = torch.empty(T, Hq, D, dtype=qkv.dtype, device=qkv.device)
+    k = torch.empty(T, Hkv, D, dtype=qkv.dtype, device=qkv.device)
+    v = torch.empty(T, Hkv, D, dtype=qkv.dtype, device=qkv.device)
+    bi_rope_qkv(qkv, pos, Hq, Hkv, D, theta, q, k, v, stream)
+    return q, k, v
+
+
+def silu_mul(gate_up, stream=None):
+    out = torch.empty(gate_up.shape[0], gate_up.shape[1] // 2, dtype=gate_up.dtype,
+                      device=gate_up.device)
+    bi_silu_mul(gate_up, out, stream)
+    return out
 
 
 def kv_write(k_new, v_new, seq, pos, k_cache, v_cache, block_table, stream=None):

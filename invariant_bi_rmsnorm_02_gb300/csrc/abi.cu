@@ -383,6 +383,38 @@ bi_status bi_kv_write(const void* k_new, const void* v_new, const int32_t* seq,
                          static_cast<cudaStream_t>(stream));
 }
 
+// ------------------------------------------------------- element-wise layer ops
+bi_status bi_gather_rows(const void* src, int64_t rows, int64_t H, const int32_t* idx, int64_t n,
+                         void* dst, void* stream) {
+  if (rows < 0 || H <= 0 || n < 0) return BI_ERR_INVALID_ARG;
+  if (H % 8 != 0) return BI_ERR_UNSUPPORTED;
+  if (n == 0) return BI_OK;
+  if (!src || !idx || !dst || !aligned16(src) || !aligned16(dst)) return BI_ERR_INVALID_ARG;
+  return launch_gather_rows(src, rows, H, idx, n, dst, device_error_word(),
+                            static_cast<cudaStream_t>(stream));
+}
+
+bi_status bi_rope_qkv(const void* qkv, const int32_t* pos, int64_t T, int Hq, int Hkv, int D,
+                      double theta, void* q, void* k, void* v, void* stream) {
+  if (T < 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return BI_ERR_INVALID_ARG;
+  if (!(theta > 1.0) || !(theta < 1e300)) return BI_ERR_INVALID_ARG;
+  if (D % 16 != 0 || D > 1024 || Hq + 2 * Hkv > 65535) return BI_ERR_UNSUPPORTED;
+  if (T == 0) return BI_OK;
+  if (!qkv || !pos || !q || !k || !v) return BI_ERR_INVALID_ARG;
+  if (!aligned16(qkv) || !aligned16(q) || !aligned16(k) || !aligned16(v))
+    return BI_ERR_INVALID_ARG;
+  return launch_rope_qkv(qkv, pos, T, Hq, Hkv, D, theta, q, k, v,
+                         static_cast<cudaStream_t>(stream));
+}
+
+bi_status bi_silu_mul(const void* gate_up, int64_t T, int64_t F, void* out, void* stream) {
+  if (T < 0 || F <= 0) return BI_ERR_INVALID_ARG;
+  if (F % 8 != 0) return BI_ERR_UNSUPPORTED;
+  if (T == 0) return BI_OK;
+  if (!gate_up || !out || !aligned16(gate_up) || !aligned16(out)) return BI_ERR_INVALID_ARG;
+  return launch_silu_mul(gate_up, T, F, out, static_cast<cudaStream_t>(stream));
+}
+
 // ------------------------------------------------------------------ sampling
 bi_status bi_sample(const void* logits, int64_t B, int64_t V, const float* temperature,
                     const uint64_t* seed, const uint64_t* step, int32_t* tokens, void* stream) {

@@ -31,6 +31,11 @@ bi_status launch_add_rmsnorm_invariant(const void* x, void* res, const void* w, 
                                        float* y_f32, int64_t M, int64_t H, float eps,
                                        cudaStream_t s);
 bi_status launch_add_bf16(const void* x, void* res, int64_t elems, cudaStream_t s);
+bi_status launch_gather_rows(const void* src, int64_t rows, int64_t H, const int32_t* idx,
+                             int64_t n, void* dst, int* err, cudaStream_t s);
+bi_status launch_rope_qkv(const void* qkv, const int32_t* pos, int64_t T, int Hq, int Hkv, int D,
+                          double theta, void* q, void* k, void* v, cudaStream_t s);
+bi_status launch_silu_mul(const void* gu, int64_t T, int64_t F, void* out, cudaStream_t s);
 bi_status launch_sample(const void* logits, int64_t B, int64_t V, const float* temperature,
                         const uint64_t* seed, const uint64_t* step, int32_t* tokens,
                         cudaStream_t s);

@@ -1,0 +1,160 @@
+// layer_ops.cu -- the element-wise steps of a Llama-style decoder layer
+// around the reductions: a row gather (token embedding, selecting the rows
+// that need logits), rotary position embedding fused with the split of the
+// QKV projection into q / k / v, and the SwiGLU product silu(gate) * up.
+// None of them reduces across a row of the batch, so each output element is
+// a function of its own inputs only ("Reproducible LLM Inference - Batch
+// Invariance, the Cost of Determinism, and Where Bitwise Identity Is Actually
+// Required", §5.4: element-wise operations are batch-invariant by nature).
+#include <cuda_runtime.h>
+
+#include "bi_internal.h"
+#include "device_common.cuh"
+
+namespace bi {
+namespace {
+
+constexpr int kThreads = 256;
+
+unsigned blocks_for(int64_t work, int64_t cap = 152 * 32) {
+  int64_t b = (work + kThreads - 1) / kThreads;
+  if (b > cap) b = cap;
+  return static_cast<unsigned>(b < 1 ? 1 : b);
+}
+
+// ------------------------------------------------------------ gather rows
+// dst[i, :] = src[idx[i], :], 16-byte vectors; an index outside [0, rows) is
+// recorded and its row is written as zeros.
+__global__ void __launch_bounds__(kThreads) gather_rows_kernel(
+    const uint4* __restrict__ src, int64_t rows, int64_t vec_per_row,
+    const int32_t* __restrict__ idx, int64_t n, uint4* __restrict__ dst, int* err) {
+  const int64_t total = n * vec_per_row;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int64_t i = e / vec_per_row, c = e - i * vec_per_row;
+    const int64_t r = idx[i];
+    if (r < 0 || r >= rows) {
+      if (c == 0) record_error(err, BI_ERR_DEVICE_BOUNDS);
+      dst[e] = make_uint4(0, 0, 0, 0);
+    } else {
+      dst[e] = __ldg(src + r * vec_per_row + c);
+    }
+  }
+}
+
+// --------------------------------------------------------------- rotary
+// One thread per (token, group of 8 frequency pairs).  Pair i (0 <= i < D/2)
+// of a head rotates elements i and i + D/2 (the rotate-half arrangement) by
+// the angle pos * theta^(-2i/D).  The angle is formed in fp64 and reduced
+// modulo 2 pi before the fp32 sine and cosine, so it is accurate at any
+// position; the rotation itself is fp32 with one rounding to bf16.
+__global__ void __launch_bounds__(kThreads) rope_qkv_kernel(
+    const uint4* __restrict__ qkv, const int32_t* __restrict__ pos, int64_t T, int Hq, int Hkv,
+    int D, double log2_theta, uint4* __restrict__ q, uint4* __restrict__ k,
+    uint4* __restrict__ v) {
+  const int groups = D / 16;               // groups of 8 pairs per head
+  const int vec_head = D / 8;              // 16-byte vectors per head
+  const int64_t vec_row = static_cast<int64_t>(Hq + 2 * Hkv) * vec_head;
+  const int64_t total = T * groups;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int64_t t = e / groups;
+    const int g = static_cast<int>(e - t * groups);
+    const double p = static_cast<double>(pos[t]);
+    float cs[8], sn[8];
+    // theta^(-2i/D) for i = 8g .. 8g+7: the first power directly, the rest
+    // by the constant ratio theta^(-2/D)
+    const double ratio = exp2(-2.0 / D * log2_theta);
+    double f = exp2(-2.0 * (8 * g) / D * log2_theta);
+    constexpr double kTwoPi = 6.283185307179586476925286766559;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const double a = p * f;
+      const double r = fma(-kTwoPi, rint(a / kTwoPi), a);
+      sincosf(static_cast<float>(r), &sn[j], &cs[j]);
+      f *= ratio;
+    }
+    const uint4* row = qkv + t * vec_row;
+    for (int h = 0; h < Hq + Hkv; ++h) {
+      const uint4 lo = __ldg(row + h * vec_head + g);
+      const uint4 hi = __ldg(row + h * vec_head + groups + g);
+      const uint32_t a[4] = {lo.x, lo.y, lo.z, lo.w}, b[4] = {hi.x, hi.y, hi.z, hi.w};
+      uint32_t ol[4], oh[4];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        float x1[2] = {bf16_lo(a[w]), bf16_hi(a[w])}, x2[2] = {bf16_lo(b[w]), bf16_hi(b[w])};
+        float y1[2], y2[2];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          const float c = cs[2 * w + s], si = sn[2 * w + s];
+          y1[s] = __fsub_rn(__fmul_rn(x1[s], c), __fmul_rn(x2[s], si));
+          y2[s] = __fadd_rn(__fmul_rn(x2[s], c), __fmul_rn(x1[s], si));
+        }
+        ol[w] = pack_bf16x2(y1[0], y1[1]);
+        oh[w] = pack_bf16x2(y2[0], y2[1]);
+      }
+      uint4* dst = h < Hq ? q + (t * Hq + h) * vec_head : k + (t * Hkv + (h - Hq)) * vec_head;
+      dst[g] = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+      dst[groups + g] = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+    }
+    for (int h = 0; h < Hkv; ++h) {
+      const uint4* src = row + (Hq + Hkv + h) * vec_head;
+      uint4* dst = v + (t * Hkv + h) * vec_head;
+      dst[g] = __ldg(src + g);
+      dst[groups + g] = __ldg(src + groups + g);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- SwiGLU
+// out[t, j] = bf16(silu(gate) * up), gate = gu[t, j], up = gu[t, F + j],
+// silu(x) = x / (1 + exp(-x)), all in fp32.
+__device__ __forceinline__ float silu_mul1(float g, float u) {
+  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
+__global__ void __launch_bounds__(kThreads) silu_mul_kernel(const uint4* __restrict__ gu,
+                                                            int64_t T, int64_t vec_f,
+                                                            uint4* __restrict__ out) {
+  const int64_t total = T * vec_f;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int64_t t = e / vec_f, c = e - t * vec_f;
+    const uint4 gv = __ldcs(gu + t * 2 * vec_f + c);
+    const uint4 uv = __ldcs(gu + t * 2 * vec_f + vec_f + c);
+    const uint32_t g[4] = {gv.x, gv.y, gv.z, gv.w}, u[4] = {uv.x, uv.y, uv.z, uv.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      o[w] = pack_bf16x2(silu_mul1(bf16_lo(g[w]), bf16_lo(u[w])),
+                         silu_mul1(bf16_hi(g[w]), bf16_hi(u[w])));
+    out[e] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+}  // namespace
+
+bi_status launch_gather_rows(const void* src, int64_t rows, int64_t H, const int32_t* idx,
+                             int64_t n, void* dst, int* err, cudaStream_t s) {
+  const int64_t vpr = H / 8;
+  gather_rows_kernel<<<blocks_for(n * vpr), kThreads, 0, s>>>(
+      static_cast<const uint4*>(src), rows, vpr, idx, n, static_cast<uint4*>(dst), err);
+  return cuda_status(cudaGetLastError());
+}
+
+bi_status launch_rope_qkv(const void* qkv, const int32_t* pos, int64_t T, int Hq, int Hkv, int D,
+                          double theta, void* q, void* k, void* v, cudaStream_t s) {
+  rope_qkv_kernel<<<blocks_for(T * (D / 16)), kThreads, 0, s>>>(
+      static_cast<const uint4*>(qkv), pos, T, Hq, Hkv, D, log2(theta), static_cast<uint4*>(q),
+      static_cast<uint4*>(k), static_cast<uint4*>(v));
+  return cuda_status(cudaGetLastError());
+}
+
+bi_status launch_silu_mul(const void* gu, int64_t T, int64_t F, void* out, cudaStream_t s) {
+  const int64_t vf = F / 8;
+  silu_mul_kernel<<<blocks_for(T * vf), kThreads, 0, s>>>(static_cast<const uint4*>(gu), T, vf,
+                                                          static_cast<uint4*>(out));
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace bi

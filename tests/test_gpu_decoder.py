@@ -1,0 +1,121 @@
+"""The decoder stepped through libbi on the GPU: logits of a small model
+against the fp64 oracle of the whole forward pass, chunking invariance of the
+logits, and the serving check -- every request's greedy tokens identical under
+every batch mix (continuous batching with different slot counts, token
+budgets, prefill chunk caps and arrival patterns), at toy size and at the
+Llama-3-8B shape."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import invariant_bi_rmsnorm_02_gb300 as bi
+from invariant_bi_rmsnorm_02_gb300.decoder import (LLAMA3_8B, TINY, Decoder, DecoderWeights,
+                                                   StepPlan)
+from invariant_bi_rmsnorm_02_gb300.serving import (Scheduler, assert_reproducible,
+                                                   synthetic_requests)
+from oracle.decoder import forward_logits
+from gpu_util import f64, same_bytes
+
+pytestmark = pytest.mark.gpu
+
+
+def chunk_plan(prompt, start, n, table_row, sample_all=True):
+    """Plan for one sequence: its tokens start .. start+n-1 as a prefill chunk,
+    logits for every one of them."""
+    toks = np.asarray(prompt[start:start + n], np.int32)
+    rows = np.arange(n, dtype=np.int32) if sample_all else np.array([n - 1], np.int32)
+    return StepPlan(tokens=toks, pos=np.arange(start, start + n, dtype=np.int32),
+                    row_seq=np.zeros(n, np.int32), table=table_row[None, :],
+                    kv_lens=np.array([start + n], np.int32), n_dec=0,
+                    cu_q=np.array([0, n], np.int32), q_start=np.array([start], np.int32),
+                    sample_rows=rows, temperature=np.zeros(len(rows), np.float32),
+                    seed=np.zeros(len(rows), np.uint64), counter=np.zeros(len(rows), np.uint64))
+
+
+def decode_plan(token, p, table_row):
+    return StepPlan(tokens=np.array([token], np.int32), pos=np.array([p], np.int32),
+                    row_seq=np.zeros(1, np.int32), table=table_row[None, :],
+                    kv_lens=np.array([p + 1], np.int32), n_dec=1, cu_q=np.zeros(1, np.int32),
+                    q_start=np.zeros(0, np.int32), sample_rows=np.zeros(1, np.int32),
+                    temperature=np.zeros(1, np.float32), seed=np.zeros(1, np.uint64),
+                    counter=np.zeros(1, np.uint64))
+
+
+def test_tiny_decoder_logits_match_oracle_and_chunking(cuda):
+    cfg = TINY
+    w = DecoderWeights(cfg, 11, cuda, gen_device="cpu")
+    w_cpu = DecoderWeights(cfg, 11, "cpu")
+    T = 40
+    prompt = np.random.default_rng(12).integers(0, cfg.vocab, T).astype(np.int32)
+    mb = 8
+    table = np.array([5, 2, 7, 0, 1, 3, 4, 6], np.int32)      # shuffled pages
+    dec = Decoder(cfg, w, num_pages=8, max_tokens=64, max_seqs=64, max_blocks=mb, device=cuda)
+    tok = dec.step(chunk_plan(prompt, 0, T, table))
+    logits = dec.logits[:T].clone()
+    assert bi.bi_check_device_errors() == bi.OK
+    ref = forward_logits(w_cpu, cfg, prompt)
+    g = f64(logits)
+    err = np.abs(g - ref)
+    scale = ref.std()
+    # storage rounding differs only where fp32 and fp64 values straddle a bf16
+    # rounding boundary; a wiring mistake (positions, heads, residual order)
+    # moves logits by O(scale)
+    assert err.max() <= 0.1 * scale and err.mean() <= 0.02 * scale, (err.max(), err.mean(), scale)
+    assert np.array_equal(tok, np.argmax(g, axis=1))
+    # the same positions as three chunks, then token by token: identical bytes
+    dec2 = Decoder(cfg, w, num_pages=8, max_tokens=64, max_seqs=64, max_blocks=mb, device=cuda)
+    parts = []
+    for a, n in ((0, 13), (13, 13), (26, 7)):
+        dec2.step(chunk_plan(prompt, a, n, table))
+        parts.append(dec2.logits[:n].clone())
+    for p in range(33, T):
+        dec2.step(decode_plan(prompt[p], p, table))
+        parts.append(dec2.logits[:1].clone())
+    assert same_bytes(torch.cat(parts), logits)
+
+
+def serve(dec, cfg, reqs, **kw):
+    sch = Scheduler(dec.step, page_size=cfg.page_size, max_blocks=dec.max_blocks,
+                    num_pages=dec.num_pages, **kw)
+    out = sch.run(reqs)
+    assert bi.bi_check_device_errors() == bi.OK
+    return out, sch.records
+
+
+def test_tiny_decoder_tokens_identical_under_every_batch_mix(cuda):
+    cfg = TINY
+    w = DecoderWeights(cfg, 21, cuda)
+    dec = Decoder(cfg, w, num_pages=400, max_tokens=512, max_seqs=16, max_blocks=32,
+                  device=cuda)
+    reqs = synthetic_requests(12, 16, 200, 24, cfg.vocab, seed=22, mean_gap=2.0)
+    burst = [dataclasses.replace(r, arrival=0) for r in reqs]
+    runs, mixes = {}, {}
+    for name, rq, kw in (("one at a time", reqs, dict(max_seqs=1, token_budget=16)),
+                         ("4 slots, chunks of 32", reqs,
+                          dict(max_seqs=4, token_budget=64, prefill_chunk=32)),
+                         ("16 slots, burst", burst, dict(max_seqs=16, token_budget=512)),
+                         ("16 slots, budget 40", burst, dict(max_seqs=16, token_budget=40))):
+        runs[name], rec = serve(dec, cfg, rq, **kw)
+        mixes[name] = sorted({(r.decode_tokens, r.prefill_tokens) for r in rec})
+    assert_reproducible(runs)
+    assert all(len(t) == 24 for t in runs["one at a time"].values())
+    assert len(mixes["16 slots, burst"]) > 3        # the batches really differed
+
+
+def test_llama3_8b_shaped_tokens_identical_under_every_batch_mix(cuda):
+    cfg = LLAMA3_8B
+    w = DecoderWeights(cfg, 31, cuda)
+    dec = Decoder(cfg, w, num_pages=1200, max_tokens=1024, max_seqs=8, max_blocks=48,
+                  device=cuda)
+    reqs = synthetic_requests(8, 16, 600, 16, cfg.vocab, seed=32, mean_gap=3.0)
+    burst = [dataclasses.replace(r, arrival=0) for r in reqs]
+    runs = {}
+    runs["alone"], _ = serve(dec, cfg, reqs, max_seqs=1, token_budget=1024)
+    runs["8 slots, chunks of 256"], _ = serve(dec, cfg, burst, max_seqs=8, token_budget=1024,
+                                              prefill_chunk=256)
+    runs["4 slots, budget 100"], _ = serve(dec, cfg, reqs, max_seqs=4, token_budget=100)
+    assert_reproducible(runs)
+    toks = np.concatenate([np.asarray(t) for t in runs["alone"].values()])
+    assert len(np.unique(toks)) > 8                  # not a degenerate constant output

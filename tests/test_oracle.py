@@ -589,3 +589,47 @@ def test_gather_rows_copies_bits():
     got = oracle.gather_rows(src, idx)
     bits = src.view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(got, bits[[3, 3, 0, 9]])
+
+
+# ------------------------------------------------------- decoder forward pass
+def test_to_bf16_is_round_to_nearest_even():
+    from oracle.decoder import to_bf16
+    # float32 inputs: torch's float32 -> bfloat16 conversion rounds to nearest even
+    x = torch.randn(100000, generator=torch.Generator().manual_seed(9140)) * 37.0
+    want = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(to_bf16(x.double().numpy()), want)
+    # from float64 it rounds once: 1 + 2^-8 + 2^-40 is above the tie
+    assert to_bf16(np.array([1 + 2.0 ** -8 + 2.0 ** -40]))[0] == 0x3F81
+    assert to_bf16(np.array([1 + 2.0 ** -8, 0.0, -3.0]))[0] == 0x3F80
+    assert list(to_bf16(np.array([0.0, -3.0]))) == [0x0000, 0xC040]
+
+
+def _tiny_weights(layers):
+    from invariant_bi_rmsnorm_02_gb300.decoder import TINY, DecoderWeights
+    import dataclasses
+    cfg = dataclasses.replace(TINY, layers=layers)
+    return cfg, DecoderWeights(cfg, 3, "cpu")
+
+
+def test_decoder_without_layers_is_norm_then_lm_head():
+    from oracle.decoder import forward_logits
+    cfg, w = _tiny_weights(0)
+    tok = [5, 0, 511, 5]
+    got = forward_logits(w, cfg, tok)
+    e = f64(w.embed)[tok]
+    y = e / np.sqrt((e * e).mean(axis=1, keepdims=True) + cfg.eps)
+    y = f64(torch.from_numpy(y).to(torch.bfloat16))
+    assert np.allclose(got, y @ f64(w.lm_head).T, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(got[0], got[3])            # same token, no context
+
+
+def test_decoder_is_causal():
+    from oracle.decoder import forward_logits
+    cfg, w = _tiny_weights(2)
+    tok = list(np.random.default_rng(9141).integers(0, cfg.vocab, 37))
+    full = forward_logits(w, cfg, tok)
+    part = forward_logits(w, cfg, tok[:20])
+    assert np.array_equal(full[:20], part)
+    # and the last token's logits do depend on the first token
+    tok2 = [(tok[0] + 1) % cfg.vocab] + tok[1:]
+    assert not np.array_equal(forward_logits(w, cfg, tok2)[-1], full[-1])
