@@ -149,6 +149,15 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[NQ][D / 16][2],
     }
 }
 
+// The running reference maximum of a row moves only when a tile's maximum
+// exceeds it by more than this many powers of two (and on the first tile
+// with a visible key); otherwise the tile's probabilities are taken against
+// the old reference (so they are at most 2^8) and the accumulated sum and o
+// are left as they are.  The split's m is this reference; the merge rule is
+// exact for any reference.  Decode and prefill apply the same rule to the
+// same values, so they stay bit-identical.
+constexpr float kRescaleLog2 = 8.0f;
+
 // One tile of 64 keys (absolute indices key0 .. key0+63).  Query column
 // (nq, cc) sees key k iff lo <= k < hi[nq][cc].  A column that sees no key
 // of the tile is left exactly as it was.
@@ -204,13 +213,17 @@ __device__ __forceinline__ void tile_step(SplitState<D, NQ>& st,
     float mnew[2];
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
-      if (mx[nq][cc] == -CUDART_INF_F) {  // no visible key: exact no-op for this column
-        alpha[nq][cc] = 1.0f;
-        mnew[cc] = st.m[nq][cc];
-      } else {
-        mnew[cc] = fmaxf(st.m[nq][cc], mx[nq][cc]);
-        alpha[nq][cc] =
-            st.m[nq][cc] == -CUDART_INF_F ? 0.0f : exp2_sfu(__fsub_rn(st.m[nq][cc], mnew[cc]));
+      const float m_in = st.m[nq][cc], t = mx[nq][cc];
+      alpha[nq][cc] = 1.0f;
+      mnew[cc] = m_in;
+      if (t == -CUDART_INF_F) {
+        // no visible key: exact no-op for this column
+      } else if (m_in == -CUDART_INF_F) {
+        mnew[cc] = t;
+        alpha[nq][cc] = 0.0f;
+      } else if (__fsub_rn(t, m_in) > kRescaleLog2) {
+        mnew[cc] = t;
+        alpha[nq][cc] = exp2_sfu(__fsub_rn(m_in, t));
       }
     }
     float cs[2] = {0.0f, 0.0f};
@@ -898,6 +911,7 @@ constexpr int kPfThreads = (kPfSoftmaxWarps + 2) * 32;  // + MMA warp + TMA warp
 constexpr int kPfMmaWarp = kPfSoftmaxWarps, kPfTmaWarp = kPfSoftmaxWarps + 1;
 constexpr int kPfPageCache = 1024;  // page ids held in shared memory (16384 keys)
 constexpr int kPfStages = 3;
+constexpr int kPvRing = 8;  // PV-done barriers, one phase per tile
 
 template <int D>
 struct PfGeom {
@@ -913,8 +927,9 @@ struct PfGeom {
   static constexpr int kXFloats = 5 * kPfRows;
   static constexpr int kPidOff = kXOff + kXFloats * 4;
   static constexpr int kBarOff = kPidOff + kPfPageCache * 4;
-  // kfull[2], kfree[2], vfull[], vfree[], sfull[2], sfree[2], pready[2], pdone[2], hm[4], hst[4]
-  static constexpr int kNumBars = 4 + 2 * kPfStages + 8 + 8;
+  // kfull[2], kfree[2], vfull[], vfree[], sfull[2], sfree[2], pready[2], pdone[2], hm[4], hst[4],
+  // pvd[kPvRing]
+  static constexpr int kNumBars = 4 + 2 * kPfStages + 8 + 8 + kPvRing;
   static constexpr int kSmem = 1024 + kBarOff + kNumBars * 8;
   static constexpr uint32_t kTmemCols = 512;
   // two S buffers of 128 columns (a tile pair each), the split's o, the merged o
@@ -948,6 +963,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   uint64_t* pdone = pready + 2;
   uint64_t* hm = pdone + 2;   // per row quadrant: the running max of a tile is written
   uint64_t* hst = hm + 4;     // per row quadrant: the sums and merged state of a tile are written
+  // PV of tile t done, phase t / kPvRing of barrier t % kPvRing.  Waited only
+  // when a softmax warp must change o; a wait for tile i-1 there comes after
+  // the unconditional wait (pdone) that saw the PV of tile i-2 complete, and
+  // the PV of tile i is issued only after it, so the barrier is never more
+  // than one phase from the one waited for.
+  uint64_t* pvd = hst + 4;
   __shared__ uint32_t tmem_slot;
   __shared__ int s_abort;
 
@@ -1005,6 +1026,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       mbar_init(&hm[i], 32);  // every lane of the warp that wrote its rows
       mbar_init(&hst[i], 32);
     }
+    for (int i = 0; i < kPvRing; ++i) mbar_init(&pvd[i], 1);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&tmem_slot, Gm::kTmemCols);
@@ -1169,6 +1191,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
         }
         tc_commit(&pdone[b2]);
         tc_commit(&vfree[stg]);
+        tc_commit(&pvd[i % kPvRing]);
       }
       last_bar = &pdone[b2];
       last_par = ph2;
@@ -1273,12 +1296,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
         m_prev = xm[r];
       }
       const float m_in = split_first ? -CUDART_INF_F : m_prev;
-      float mnew, alpha = 1.0f;
-      if (mx == -CUDART_INF_F) {  // no visible key: exact no-op for this row
-        mnew = m_in;
-      } else {
-        mnew = fmaxf(m_in, mx);
-        alpha = m_in == -CUDART_INF_F ? 0.0f : exp2_sfu(__fsub_rn(m_in, mnew));
+      float mnew = m_in, alpha = 1.0f;  // the decode's reference rule (kRescaleLog2)
+      if (mx == -CUDART_INF_F) {
+        // no visible key: exact no-op for this row
+      } else if (m_in == -CUDART_INF_F) {
+        mnew = mx;
+        alpha = 0.0f;
+      } else if (__fsub_rn(mx, m_in) > kRescaleLog2) {
+        mnew = mx;
+        alpha = exp2_sfu(__fsub_rn(m_in, mx));
       }
       if (i + 1 < ntiles) {
         xm[r] = mnew;
@@ -1349,15 +1375,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       }
       l = __fadd_rn(__fmul_rn(split_first ? 0.0f : l_prev, alpha), csum);
       m = mnew;
-      // ---- the previous tile's PV is done: fold a finished split, or o *= alpha
-      if (i >= 1)
-        live = __all_sync(kFull, live && mbar_wait(&pdone[(i - 1) & 1], ((i - 1) >> 1) & 1,
-                                                   p.err, &s_abort));
+      // ---- fold a finished split, or o *= alpha where a reference moved:
+      // both need the previous tile's PV done; otherwise this tile's PV may
+      // be issued while that one still runs (the tensor core accumulates in
+      // issue order)
+      const bool fold_now = split_first && i > 0;
+      const bool rescale = !split_first && __any_sync(kFull, alpha != 1.0f);
+      if (fold_now || rescale)
+        live = __all_sync(kFull, live && mbar_wait(&pvd[(i - 1) % kPvRing],
+                                                   ((i - 1) / kPvRing) & 1, p.err, &s_abort));
       if (live) {
         tc_fence_after();
-        if (split_first && i > 0) {
+        if (fold_now) {
           fold(m_prev, l_prev, lo - S);
-        } else if (!split_first && __any_sync(kFull, alpha != 1.0f)) {
+        } else if (rescale) {
 #pragma unroll
           for (int c = 0; c < D / 32; c += 2) {  // two chunks per TMEM round trip
             uint32_t v0[32], v1[32];
