@@ -310,10 +310,12 @@ bi_status bi_silu_mul(const void* gate_up, int64_t T, int64_t F, void* out, void
  *   the position of the token being chosen), so successive tokens of one
  *   request get fresh noise.
  * temperature[b] <= 0 (or NaN): greedy, tokens[b] = argmax_v z_v (P1 §9.2).
- * Ties go to the lowest index; -0 equals +0; a NaN score never wins (an
+ * Ties go to the lowest index; -0 equals +0; a NaN score counts as -inf (it
+ *   is chosen only when no entry scores above -inf, lowest index first: an
  *   all-NaN or all -inf row gives token 0).
  * The argmax is a reduction under a total order, so its result does not
- *   depend on how the row is split; one launch, a cluster of 8 CTAs per row.
+ *   depend on how the row is split; one launch: a cluster of 8 CTAs per row
+ *   below 128 rows (one row keeps several SMs busy), one CTA per row above.
  * Requirements: 0 <= B <= 65535, 1 <= V < 2^31.  Needs no workspace.
  * Errors: BI_ERR_INVALID_ARG (null, misaligned, B < 0, V < 1),
  *   BI_ERR_UNSUPPORTED (B or V too large), BI_ERR_CUDA (launch). */

@@ -23,22 +23,21 @@ unsigned blocks_for(int64_t work, int64_t cap = 152 * 32) {
 }
 
 // ------------------------------------------------------------ gather rows
-// dst[i, :] = src[idx[i], :], 16-byte vectors; an index outside [0, rows) is
-// recorded and its row is written as zeros.
+// dst[i, :] = src[idx[i], :], 16-byte vectors, one block per row (rows taken
+// in a grid-stride loop); an index outside [0, rows) is recorded and its row
+// is written as zeros.
 __global__ void __launch_bounds__(kThreads) gather_rows_kernel(
-    const uint4* __restrict__ src, int64_t rows, int64_t vec_per_row,
+    const uint4* __restrict__ src, int64_t rows, int vec_per_row,
     const int32_t* __restrict__ idx, int64_t n, uint4* __restrict__ dst, int* err) {
-  const int64_t total = n * vec_per_row;
-  for (int64_t e = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; e < total;
-       e += static_cast<int64_t>(gridDim.x) * kThreads) {
-    const int64_t i = e / vec_per_row, c = e - i * vec_per_row;
+  for (int64_t i = blockIdx.x; i < n; i += gridDim.x) {
     const int64_t r = idx[i];
-    if (r < 0 || r >= rows) {
-      if (c == 0) record_error(err, BI_ERR_DEVICE_BOUNDS);
-      dst[e] = make_uint4(0, 0, 0, 0);
-    } else {
-      dst[e] = __ldg(src + r * vec_per_row + c);
-    }
+    const bool ok = r >= 0 && r < rows;
+    if (!ok && threadIdx.x == 0) record_error(err, BI_ERR_DEVICE_BOUNDS);
+    const uint4* s = src + (ok ? r : 0) * vec_per_row;
+    uint4* d = dst + i * vec_per_row;
+#pragma unroll 4
+    for (int c = threadIdx.x; c < vec_per_row; c += kThreads)
+      __stcs(d + c, ok ? __ldg(s + c) : make_uint4(0, 0, 0, 0));
   }
 }
 
@@ -67,41 +66,71 @@ __global__ void __launch_bounds__(kThreads) rope_qkv_kernel(
     const double ratio = exp2(-2.0 / D * log2_theta);
     double f = exp2(-2.0 * (8 * g) / D * log2_theta);
     constexpr double kTwoPi = 6.283185307179586476925286766559;
+    constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const double a = p * f;
-      const double r = fma(-kTwoPi, rint(a / kTwoPi), a);
+      const double r = fma(-kTwoPi, rint(a * kInvTwoPi), a);  // |r| <= pi (+ a few ulps)
       sincosf(static_cast<float>(r), &sn[j], &cs[j]);
       f *= ratio;
     }
     const uint4* row = qkv + t * vec_row;
-    for (int h = 0; h < Hq + Hkv; ++h) {
-      const uint4 lo = __ldg(row + h * vec_head + g);
-      const uint4 hi = __ldg(row + h * vec_head + groups + g);
-      const uint32_t a[4] = {lo.x, lo.y, lo.z, lo.w}, b[4] = {hi.x, hi.y, hi.z, hi.w};
-      uint32_t ol[4], oh[4];
+    // heads in groups of kHeadBatch: all loads of a group before its stores,
+    // so that many loads are in flight per thread
+    constexpr int kHeadBatch = 4;
+    for (int h0 = 0; h0 < Hq + Hkv; h0 += kHeadBatch) {
+      uint4 lo[kHeadBatch], hi[kHeadBatch];
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        float x1[2] = {bf16_lo(a[w]), bf16_hi(a[w])}, x2[2] = {bf16_lo(b[w]), bf16_hi(b[w])};
-        float y1[2], y2[2];
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          const float c = cs[2 * w + s], si = sn[2 * w + s];
-          y1[s] = __fsub_rn(__fmul_rn(x1[s], c), __fmul_rn(x2[s], si));
-          y2[s] = __fadd_rn(__fmul_rn(x2[s], c), __fmul_rn(x1[s], si));
+      for (int u = 0; u < kHeadBatch; ++u) {
+        const int h = h0 + u;
+        if (h < Hq + Hkv) {
+          lo[u] = __ldg(row + h * vec_head + g);
+          hi[u] = __ldg(row + h * vec_head + groups + g);
         }
-        ol[w] = pack_bf16x2(y1[0], y1[1]);
-        oh[w] = pack_bf16x2(y2[0], y2[1]);
       }
-      uint4* dst = h < Hq ? q + (t * Hq + h) * vec_head : k + (t * Hkv + (h - Hq)) * vec_head;
-      dst[g] = make_uint4(ol[0], ol[1], ol[2], ol[3]);
-      dst[groups + g] = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+#pragma unroll
+      for (int u = 0; u < kHeadBatch; ++u) {
+        const int h = h0 + u;
+        if (h >= Hq + Hkv) break;
+        const uint32_t a[4] = {lo[u].x, lo[u].y, lo[u].z, lo[u].w};
+        const uint32_t b[4] = {hi[u].x, hi[u].y, hi[u].z, hi[u].w};
+        uint32_t ol[4], oh[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          float x1[2] = {bf16_lo(a[w]), bf16_hi(a[w])}, x2[2] = {bf16_lo(b[w]), bf16_hi(b[w])};
+          float y1[2], y2[2];
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            const float c = cs[2 * w + s], si = sn[2 * w + s];
+            y1[s] = __fsub_rn(__fmul_rn(x1[s], c), __fmul_rn(x2[s], si));
+            y2[s] = __fadd_rn(__fmul_rn(x2[s], c), __fmul_rn(x1[s], si));
+          }
+          ol[w] = pack_bf16x2(y1[0], y1[1]);
+          oh[w] = pack_bf16x2(y2[0], y2[1]);
+        }
+        uint4* dst =
+            h < Hq ? q + (t * Hq + h) * vec_head : k + (t * Hkv + (h - Hq)) * vec_head;
+        __stcs(dst + g, make_uint4(ol[0], ol[1], ol[2], ol[3]));
+        __stcs(dst + groups + g, make_uint4(oh[0], oh[1], oh[2], oh[3]));
+      }
     }
-    for (int h = 0; h < Hkv; ++h) {
-      const uint4* src = row + (Hq + Hkv + h) * vec_head;
-      uint4* dst = v + (t * Hkv + h) * vec_head;
-      dst[g] = __ldg(src + g);
-      dst[groups + g] = __ldg(src + groups + g);
+    for (int h0 = 0; h0 < Hkv; h0 += kHeadBatch) {
+      uint4 lo[kHeadBatch], hi[kHeadBatch];
+#pragma unroll
+      for (int u = 0; u < kHeadBatch; ++u) {
+        const uint4* src = row + (Hq + Hkv + h0 + u) * vec_head;
+        if (h0 + u < Hkv) {
+          lo[u] = __ldg(src + g);
+          hi[u] = __ldg(src + groups + g);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kHeadBatch; ++u) {
+        if (h0 + u >= Hkv) break;
+        uint4* dst = v + (t * Hkv + h0 + u) * vec_head;
+        __stcs(dst + g, lo[u]);
+        __stcs(dst + groups + g, hi[u]);
+      }
     }
   }
 }
@@ -136,9 +165,10 @@ __global__ void __launch_bounds__(kThreads) silu_mul_kernel(const uint4* __restr
 
 bi_status launch_gather_rows(const void* src, int64_t rows, int64_t H, const int32_t* idx,
                              int64_t n, void* dst, int* err, cudaStream_t s) {
-  const int64_t vpr = H / 8;
-  gather_rows_kernel<<<blocks_for(n * vpr), kThreads, 0, s>>>(
-      static_cast<const uint4*>(src), rows, vpr, idx, n, static_cast<uint4*>(dst), err);
+  const int vpr = static_cast<int>(H / 8);
+  const unsigned grid = static_cast<unsigned>(n < 152 * 16 ? n : 152 * 16);
+  gather_rows_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint4*>(src), rows, vpr, idx, n,
+                                               static_cast<uint4*>(dst), err);
   return cuda_status(cudaGetLastError());
 }
 

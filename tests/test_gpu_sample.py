@@ -69,21 +69,32 @@ def test_sample_shapes_match_oracle(cuda, V):
 
 def test_greedy_ties_signed_zero_and_special_values(cuda):
     V = 1000
-    z = torch.full((5, V), -1.0)
+    z = torch.full((7, V), -1.0)
     z[0, [17, 400, 999]] = 2.5                  # three-way tie: lowest index
     z[1, 3] = -0.0
     z[1, 5] = 0.0                               # -0 == +0: index 3
     z[2] = float("-inf")                        # every entry -inf: index 0
     z[3, 10] = float("nan")
-    z[3, 11] = 7.0                              # a NaN never wins
+    z[3, 11] = 7.0                              # a NaN counts as -inf
     z[4, V - 1] = 1.0                           # the last entry
+    z[5] = float("-inf")
+    z[5, 300] = float("nan")                    # NaN and -inf tie: lowest index
+    z[5, 301:] = float("nan")
+    z[5, :300] = float("nan")
+    z[5, 299] = float("-inf")
+    z[6] = float("nan")                         # every entry NaN: index 0
     logits = z.to(torch.bfloat16).to(cuda)
-    T = torch.zeros(5, device=cuda)
-    tok = bi.sample(logits, T, u64([1] * 5, cuda), u64([0] * 5, cuda))
-    assert tok.cpu().tolist() == [17, 3, 0, 11, V - 1]
+    T = torch.zeros(7, device=cuda)
+    tok = bi.sample(logits, T, u64([1] * 7, cuda), u64([0] * 7, cuda))
+    assert tok.cpu().tolist() == [17, 3, 0, 11, V - 1, 0, 0]
     # a negative or NaN temperature is greedy too
-    T2 = torch.tensor([-1.0, float("nan"), 0.0, -0.0, -5.0], device=cuda)
-    assert same_bytes(bi.sample(logits, T2, u64([9] * 5, cuda), u64([4] * 5, cuda)), tok)
+    T2 = torch.tensor([-1.0, float("nan"), 0.0, -0.0, -5.0, 0.0, -2.0], device=cuda)
+    assert same_bytes(bi.sample(logits, T2, u64([9] * 7, cuda), u64([4] * 7, cuda)), tok)
+    # the same rows at an odd 2-byte offset take the per-entry load path
+    store = torch.empty(7 * V + 1, dtype=torch.bfloat16, device=cuda)
+    shifted = store[1:].view(7, V)
+    shifted.copy_(logits)
+    assert same_bytes(bi.sample(shifted, T, u64([1] * 7, cuda), u64([0] * 7, cuda)), tok)
 
 
 def test_sample_is_batch_invariant_and_repeatable(cuda):
