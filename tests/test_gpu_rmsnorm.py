@@ -144,3 +144,25 @@ def test_rmsnorm_empty_batch(cuda):
     x = torch.empty(0, 4096, dtype=torch.bfloat16, device=cuda)
     w = torch.ones(4096, dtype=torch.bfloat16, device=cuda)
     assert bi.rmsnorm(x, w).shape == (0, 4096)
+
+
+@pytest.mark.parametrize("H", [256, 4096])
+@pytest.mark.parametrize("mode", [bi.INVARIANT, bi.VARIANT])
+def test_rmsnorm_exact_row_is_bit_exact(cuda, H, mode):
+    # entries +-1/2, +-1, +-2 in counts 4:3:1 have mean square exactly 1: every
+    # partial sum of squares is a multiple of 1/4 (exact in fp32), rsqrt(1) = 1
+    # and each output is a weight times a power of two, so with eps = 0 the
+    # kernel's result is the exact value, bit for bit, in any reduction order
+    n_half, n_one, n_two = H // 2, 3 * H // 8, H // 8
+    mags = np.concatenate([np.full(n_half, 0.5), np.full(n_one, 1.0), np.full(n_two, 2.0)])
+    g = np.random.default_rng(H + 17 * mode)
+    rows = []
+    for _ in range(6):
+        rows.append(g.permutation(mags) * g.choice([-1.0, 1.0], H))
+    x = torch.tensor(np.stack(rows), dtype=torch.float32).to(torch.bfloat16)
+    assert float((x.double() ** 2).mean(dim=1).max()) == 1.0
+    w = synth.normal_bf16((H,), 2600 + H, std=0.1, mean=1.0)
+    y = bi.rmsnorm(x.to(cuda), w.to(cuda), 0.0, mode)
+    want = torch.from_numpy(oracle.rmsnorm(x, w, 0.0)).to(torch.bfloat16)
+    assert same_bytes(y.cpu(), want)
+    assert same_bytes(want.float(), (x.float() * w.float()).to(torch.bfloat16).float())
