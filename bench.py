@@ -420,6 +420,21 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------- main arm
+def max_over_ranks(vals, dist=None, device="cpu"):
+    """The max over ranks of each timed quantity (every rank gets the result;
+    one process: the values themselves)."""
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def whole_job_tflops(world, flops_per_rank, ms_max):
+    """Throughput of the whole job: every rank's work over the slowest rank's
+    time (replicas process the same amount each: weak scaling)."""
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -468,21 +483,16 @@ def main():
     gemm_flops = work["gemm_qkv"]["flops"] + work["gemm_up"]["flops"]
     gemm_ms = inv["gemm_qkv"] + inv["gemm_up"]
     # max over ranks of the timed quantities
-    t = torch.tensor([gemm_ms, inv_step], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    gemm_ms_max, step_ms_max = float(t[0]), float(t[1])
-    value = world * gemm_flops / (gemm_ms_max * 1e-3) / 1e12
+    gemm_ms_max, step_ms_max = max_over_ranks([gemm_ms, inv_step], dist, dev)
+    value = whole_job_tflops(world, gemm_flops, gemm_ms_max)
 
     e2e = None
     if not args.no_e2e:
         e2e_ms, h2d, d2h = e2e_steps(wl, max(3, args.steps // 2), args.warmup, stream)
-        te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        if dist is not None:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        e2e = {"value": world * gemm_flops / (float(te[0]) * 1e-3) / 1e12, "unit": "TFLOP/s",
+        (e2e_ms_max,) = max_over_ranks([e2e_ms], dist, dev)
+        e2e = {"value": whole_job_tflops(world, gemm_flops, e2e_ms_max), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": float(te[0])}
+               "ms_per_step": e2e_ms_max}
 
     comps = {}
     for n in inv:
