@@ -24,6 +24,15 @@ the decode kernel) and prefill chunks after them (the chunked-prefill kernel),
 so both attention kernels write contiguous slices of one output.  The two
 kernels give bit-identical results for the same position, so which one serves
 a token never changes its bytes.
+
+Decode-only steps can be replayed from CUDA graphs (``use_graphs``): a step
+is a few hundred short launches, so at small batch the host, not the GPU, sets
+its pace ("Reproducible LLM Inference - Batch Invariance, the Cost of
+Determinism, and Where Bitwise Identity Is Actually Required", §8.5: graphs
+recover much of what deterministic mode costs).  Every call takes its shapes
+from host arguments that are fixed per (batch size, KV-length bucket) and
+reads lengths, positions and page tables on the device, so a captured step
+replays the same kernels on the step's uploaded arrays.
 """
 from __future__ import annotations
 
@@ -165,7 +174,8 @@ class Decoder:
 
     def __init__(self, cfg: DecoderConfig, weights: DecoderWeights, *, num_pages: int,
                  max_tokens: int, max_seqs: int, max_blocks: int, device,
-                 mode: int = bi.INVARIANT):
+                 mode: int = bi.INVARIANT, use_graphs: bool = False,
+                 graph_kv_bucket: int = 1024, max_graphs: int = 32):
         self.cfg, self.w, self.mode, self.device = cfg, weights, mode, device
         self.max_tokens, self.max_seqs, self.max_blocks = max_tokens, max_seqs, max_blocks
         c = cfg
@@ -189,6 +199,19 @@ class Decoder:
         words = 4 * T + max_seqs * (max_blocks + 8) + 64
         self.pack = _Pack(4 * words + 8 * 2 * max_seqs + 16 * 16, device)
         self.sm_scale = c.head_dim ** -0.5
+        # decode-step graphs: captured on the second step of a shape, kept
+        # (at most max_graphs, oldest dropped) per (decode rows, KV bucket)
+        self.use_graphs = use_graphs and mode == bi.INVARIANT
+        self.graph_kv_bucket = graph_kv_bucket
+        self.max_graphs = max_graphs
+        self.graphs, self.seen = {}, set()
+        self.graph_replays = 0
+        if self.use_graphs:
+            # the decode workspace at its largest, so that no captured step
+            # ever sees it move
+            ctx = max_blocks * c.page_size
+            self._workspace(bi.bi_attn_decode_workspace_size(
+                max_seqs, c.heads, c.kv_heads, c.head_dim, ctx, c.split_size, mode))
 
     # workspace: one growing device buffer shared by all calls of a step (the
     # calls run in stream order, so they never overlap)
@@ -215,7 +238,7 @@ class Decoder:
     def step(self, plan: StepPlan) -> np.ndarray:
         """Run one forward step; returns the chosen tokens of plan.sample_rows
         (host int32)."""
-        c, w, mode = self.cfg, self.w, self.mode
+        c = self.cfg
         T, n_seq, n_dec = len(plan.tokens), len(plan.kv_lens), plan.n_dec
         n_pre, n_s = n_seq - n_dec, len(plan.sample_rows)
         if T == 0 or T > self.max_tokens or n_seq > self.max_seqs or n_s > self.max_seqs:
@@ -234,10 +257,41 @@ class Decoder:
         p.add(plan.temperature.astype(np.float32), torch.float32)
         p.add(plan.seed.astype(np.uint64).view(np.int64), torch.int64)
         p.add(plan.counter.astype(np.uint64).view(np.int64), torch.int64)
-        (tok, pos, row_seq, table, kv_lens, cu_q, q_start, rows, temp, seed,
-         counter) = p.upload()
-
+        views = p.upload()
         kv_max = int(plan.kv_lens.max())
+        max_q = int(np.diff(plan.cu_q).max()) if n_pre else 0
+        if self.use_graphs and n_pre == 0:
+            bucket = min(-(-kv_max // self.graph_kv_bucket) * self.graph_kv_bucket,
+                         self.max_blocks * c.page_size)
+            key = (n_dec, bucket)
+            g = self.graphs.get(key)
+            if g is None and key in self.seen:
+                if len(self.graphs) >= self.max_graphs:
+                    self.graphs.pop(next(iter(self.graphs)))
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    self._forward(T, n_dec, n_pre, n_s, views, bucket, max_q)
+                self.graphs[key] = g
+            self.seen.add(key)
+            if g is not None:
+                g.replay()
+                self.graph_replays += 1
+            else:
+                self._forward(T, n_dec, n_pre, n_s, views, bucket, max_q)
+        else:
+            self._forward(T, n_dec, n_pre, n_s, views, kv_max, max_q)
+        if n_s == 0:
+            return np.empty(0, np.int32)
+        out = self.tokens_host[:n_s]
+        out.copy_(self.tokens_out[:n_s])      # synchronous: the step's one read-back
+        return out.numpy().copy()
+
+    def _forward(self, T, n_dec, n_pre, n_s, views, kv_max, max_q):
+        """Enqueue one step's kernels (no host synchronisation, no allocation
+        once the workspace has its size); kv_max is a host bound on the KV
+        lengths."""
+        c, w, mode = self.cfg, self.w, self.mode
+        (tok, pos, row_seq, table, kv_lens, cu_q, q_start, rows, temp, seed, counter) = views
         h, y = self.h[:T], self.y[:T]
         bi.bi_gather_rows(w.embed, tok, h)
         bi.bi_rmsnorm(h, w.attn_norm[0], y, c.eps, mode, self._ws_norm(T))
@@ -261,7 +315,7 @@ class Decoder:
             if n_pre:
                 bi.bi_attn_prefill_chunk(q[n_dec:], cu_q, q_start, kc, vc, table[n_dec:],
                                          kv_lens[n_dec:], att[n_dec:],
-                                         max_q_len=int(np.diff(plan.cu_q).max()),
+                                         max_q_len=max_q,
                                          max_kv_len=kv_max, split_size=c.split_size,
                                          sm_scale=self.sm_scale, mode=mode)
             o = self.o[:T]
@@ -273,11 +327,8 @@ class Decoder:
             self._gemm(act, w.wdown[layer], delta)
         bi.bi_add_rmsnorm(delta, h, w.final_norm, y, c.eps, mode, self._ws_norm(T))
         if n_s == 0:
-            return np.empty(0, np.int32)
+            return
         ys, logits = self.ys[:n_s], self.logits[:n_s]
         bi.bi_gather_rows(y, rows, ys)
         self._gemm(ys, w.lm_head, logits)
         bi.bi_sample(logits, temp, seed, counter, self.tokens_out[:n_s])
-        out = self.tokens_host[:n_s]
-        out.copy_(self.tokens_out[:n_s])      # synchronous: the step's one read-back
-        return out.numpy().copy()

