@@ -309,7 +309,12 @@ def timed_steps(wl, mode, steps, warmup, flush, stream, dist_barrier):
 
 def e2e_steps(wl, steps, warmup, stream):
     """The GEMM metric end to end through the public API with host buffers:
-    pinned host inputs copied in, the path run, the results copied out."""
+    pinned host inputs copied in, the path run, the results copied out.  Each
+    result is copied out on its own stream as soon as its kernel is done, and
+    each input of the next step is copied in on another as soon as the op
+    that read the current one is done, so copies overlap kernels; an op waits
+    for its input to arrive and for the previous copy of its output to leave.
+    Every step's inputs and results cross the link inside the timed region."""
     bi = wl.bi
     hx = wl.x.cpu().pin_memory()
     hq = wl.q.cpu().pin_memory()
@@ -322,31 +327,65 @@ def e2e_steps(wl, steps, warmup, stream):
     h2d = sum(t.numel() * t.element_size() for t in (hx, hq, hk, hv, hpq))
     d2h = sum(t.numel() * t.element_size() for t in (hqkv, hup, hdec, hpre))
     ops = wl.ops(bi.INVARIANT)
+    inputs = {"kv_write": ((wl.k_new, hk), (wl.v_new, hv)), "rmsnorm": ((wl.x, hx),),
+              "decode": ((wl.q, hq),), "prefill": ((wl.pq, hpq),)}
+    outputs = {"gemm_qkv": (wl.qkv, hqkv), "gemm_up": (wl.up, hup),
+               "decode": (wl.dec_out, hdec), "prefill": (wl.pout, hpre)}
+    copy_in = torch.cuda.Stream(stream.device)
+    copy_out = torch.cuda.Stream(stream.device)
+    loaded = {n: None for n in inputs}     # event: this step's copy of the input is in
+    consumed = {n: None for n in inputs}   # event: the last op that read the input is done
+    copied = {n: None for n in outputs}    # event: the last copy of the output is out
 
-    def one():
-        wl.x.copy_(hx, non_blocking=True)
-        wl.q.copy_(hq, non_blocking=True)
-        wl.k_new.copy_(hk, non_blocking=True)
-        wl.v_new.copy_(hv, non_blocking=True)
-        wl.pq.copy_(hpq, non_blocking=True)
-        for _, fn, _ in ops:
+    def load_inputs():
+        # each input of the next step goes in once the op that read the
+        # previous one is done
+        for n, pairs in inputs.items():
+            if consumed[n] is not None:
+                copy_in.wait_event(consumed[n])
+            with torch.cuda.stream(copy_in):
+                for dev_t, host_t in pairs:
+                    dev_t.copy_(host_t, non_blocking=True)
+            loaded[n] = torch.cuda.Event()
+            loaded[n].record(copy_in)
+
+    def one(last):
+        for n, fn, _ in ops:
+            if n in inputs:
+                stream.wait_event(loaded[n])
+            if n in outputs and copied[n] is not None:
+                stream.wait_event(copied[n])   # the previous copy of this buffer is out
             fn()
-        hqkv.copy_(wl.qkv, non_blocking=True)
-        hup.copy_(wl.up, non_blocking=True)
-        hdec.copy_(wl.dec_out, non_blocking=True)
-        hpre.copy_(wl.pout, non_blocking=True)
+            if n in inputs:
+                consumed[n] = torch.cuda.Event()
+                consumed[n].record(stream)
+            if n in outputs:
+                ready = torch.cuda.Event()
+                ready.record(stream)
+                copy_out.wait_event(ready)
+                dev_t, host_t = outputs[n]
+                with torch.cuda.stream(copy_out):
+                    host_t.copy_(dev_t, non_blocking=True)
+                copied[n] = torch.cuda.Event()
+                copied[n].record(copy_out)
+        if not last:
+            load_inputs()
 
     wl.reset_lengths()
     with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            one()
-        stream.synchronize()
+        load_inputs()
+        for i in range(warmup):
+            one(i == warmup - 1)
+        torch.cuda.synchronize()
         wl.reset_lengths()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        for _ in range(steps):
-            one()
+        copy_in.wait_stream(stream)            # the first step's inputs are timed too
+        load_inputs()
+        for i in range(steps):
+            one(i == steps - 1)
+        stream.wait_stream(copy_out)           # every result is on the host
         t1.record(stream)
     torch.cuda.synchronize()
     return t0.elapsed_time(t1) / steps, h2d, d2h
