@@ -198,7 +198,8 @@ class Workload:
         self.pkl = torch.tensor([PRE["start"] + PRE["chunk"]], dtype=torch.int32, device=dev)
         self.rms_ws = torch.empty(bi.bi_rmsnorm_workspace_size(M, H, bi.VARIANT) // 4 + 4,
                                   dtype=torch.float32, device=dev)
-        gws = max(bi.bi_gemm_workspace_size(M, n, H, bi.VARIANT) for n in (N_QKV, N_UP))
+        gws = max(bi.bi_gemm_workspace_size(m, n, H, bi.VARIANT)
+                  for n in (N_QKV, N_UP) for m in set(GEMM_M_SWEEP) | {M})
         self.gemm_ws = torch.empty(gws // 4 + 4, dtype=torch.float32, device=dev)
 
     def reset_lengths(self):
@@ -458,6 +459,41 @@ def run_reference(args):
     return 0
 
 
+GEMM_M_SWEEP = (1, 3, 16, 64, 256, 1024, 8192)
+
+
+def gemm_m_sweep(wl, flush, stream, reps=3):
+    """The cost of invariance across batch sizes: the QKV and MLP-up GEMMs at
+    every M of the projection workload, invariant and batch-variant (split-K),
+    L2 clean before each call; returns {M: {...}} of median times and the
+    invariant slowdown t_inv / t_var - 1."""
+    bi = wl.bi
+    out = {}
+    with torch.cuda.stream(stream):
+        for m in GEMM_M_SWEEP:
+            row = {}
+            for name, W, C in (("qkv", wl.Wqkv, wl.qkv), ("up", wl.Wup, wl.up)):
+                ms = {}
+                for mode in (bi.INVARIANT, bi.VARIANT):
+                    ts = []
+                    for r in range(reps + 1):
+                        flush.zero_()
+                        torch.cuda._sleep(HOST_LEAD_CYCLES)
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        bi.bi_gemm(wl.y[:m], W, C[:m], mode, 0, wl.gemm_ws)
+                        e1.record(stream)
+                        stream.synchronize()
+                        if r:
+                            ts.append(e0.elapsed_time(e1))
+                    ms[mode] = statistics.median(ts)
+                row[name] = {"ms": ms[bi.INVARIANT], "ms_variant": ms[bi.VARIANT],
+                             "slowdown": ms[bi.INVARIANT] / ms[bi.VARIANT] - 1.0}
+            out[m] = row
+    return out
+
+
 # ----------------------------------------------------------------- main arm
 def max_over_ranks(vals, dist=None, device="cpu"):
     """The max over ranks of each timed quantity (every rank gets the result;
@@ -515,6 +551,7 @@ def main():
         inv, inv_step = timed_steps(wl, bi.INVARIANT, args.steps, args.warmup, flush, stream,
                                     barrier)
     var, var_step = timed_steps(wl, bi.VARIANT, args.steps, args.warmup, flush, stream, barrier)
+    sweep = gemm_m_sweep(wl, flush, stream)
     status = bi.bi_check_device_errors()
     if status != bi.OK:
         raise RuntimeError("device error during the bench: %s" % bi.bi_status_string(status))
@@ -575,7 +612,8 @@ def main():
         "components": comps,
         "invariant_slowdown": {"step": inv_step / var_step - 1.0,
                                "gemm": gemm_ms / (var["gemm_qkv"] + var["gemm_up"]) - 1.0,
-                               "ms_per_step_variant": var_step},
+                               "ms_per_step_variant": var_step,
+                               "gemm_by_m": sweep},
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }
