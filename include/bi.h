@@ -137,6 +137,26 @@ size_t bi_gemm_workspace_size(int64_t M, int64_t N, int64_t K, bi_mode mode,
  * with num_sms SMs (1 = no split).  Host arithmetic only. */
 int bi_gemm_variant_splits(int64_t M, int64_t N, int64_t K, int num_sms);
 
+/* Gate/up projection with the SwiGLU product in the GEMM epilogue (P1 §5.4:
+ * element-wise work is batch-invariant by nature, so fusing it into the
+ * invariant GEMM keeps every row's bytes).
+ *   out[i,j] = bf16( silu(g) * u ),  silu(x) = x / (1 + exp(-x)) in fp32,
+ *   g = bf16((A W^T)[i, 256*(j/128) + j%128]),
+ *   u = bf16((A W^T)[i, 256*(j/128) + 128 + j%128]).
+ *   A [M,K] bf16, W [2F,K] bf16 with the gate and up rows stacked in blocks
+ *   of 128 features (rows 256b .. 256b+127: gate of features 128b ..
+ *   128b+127; rows 256b+128 .. 256b+255: up of the same features), out [M,F]
+ *   bf16.  The GEMM arithmetic (tile, instruction, K order, both modes) is
+ *   bi_gemm's on (M, 2F, K), so out holds exactly the bytes of bi_gemm into a
+ *   [M,2F] buffer followed by bi_silu_mul with block = 128, with no [M,2F]
+ *   tensor written.
+ * Workspace: bi_gemm_workspace_size(M, 2F, K, mode, variant_splits) bytes.
+ * Requirements: F % 128 == 0, K % 8 == 0, 2F and K < 2^31; pointers 16-byte
+ *   aligned.  Errors: as bi_gemm. */
+bi_status bi_gemm_swiglu(const void* A, const void* W, void* out, int64_t M, int64_t F,
+                         int64_t K, bi_mode mode, int variant_splits, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Attention over a paged KV cache  (P1 §5.5; P3 "The attention detail that */
 /* gets missed")                                                            */
@@ -285,11 +305,17 @@ bi_status bi_gather_rows(const void* src, int64_t rows, int64_t H, const int32_t
 bi_status bi_rope_qkv(const void* qkv, const int32_t* pos, int64_t T, int Hq, int Hkv, int D,
                       double theta, void* q, void* k, void* v, void* stream);
 
-/* SwiGLU product: out[t, j] = bf16(silu(g) * u) with g = gate_up[t, j],
- * u = gate_up[t, F + j] (the gate and up projections stacked in one GEMM
- * output [T][2F] bf16), silu(g) = g / (1 + exp(-g)), fp32.  out [T][F] bf16.
- * F % 8 == 0.  Errors: as bi_rmsnorm. */
-bi_status bi_silu_mul(const void* gate_up, int64_t T, int64_t F, void* out, void* stream);
+/* SwiGLU product: out[t, j] = bf16(silu(g) * u), silu(g) = g / (1 + exp(-g))
+ * in fp32, out [T][F] bf16, from the gate and up projections stacked in one
+ * GEMM output gate_up [T][2F] bf16 in blocks of `block` features:
+ *   g = gate_up[t, 2*block*(j/block) + j%block],  u = the element block
+ *   columns further on.
+ * block = F: all gate columns, then all up columns.  block = 128: the layout
+ * bi_gemm writes with bi_gemm_swiglu's weight, so that this kernel after
+ * bi_gemm gives the bytes of bi_gemm_swiglu.
+ * Requirements: F % block == 0, block % 8 == 0.  Errors: as bi_rmsnorm. */
+bi_status bi_silu_mul(const void* gate_up, int64_t T, int64_t F, int64_t block, void* out,
+                      void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Next-token selection  (P1 §9.2, §9.3)                                    */

@@ -14,6 +14,7 @@ import ctypes
 import os
 import threading
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -31,9 +32,10 @@ __all__ = [
     "bi_gemm_variant_splits", "bi_attn_decode", "bi_attn_decode_workspace_size",
     "bi_attn_prefill_chunk", "bi_kv_write", "bi_check_device_errors", "bi_status_string",
     "bi_version", "bi_attn_decode_noalloc", "bi_selftest_wait_timeout", "bi_add_rmsnorm",
-    "bi_sample", "bi_gather_rows", "bi_rope_qkv", "bi_silu_mul", "NOALLOC_SCRATCH_BYTES", "rmsnorm", "add_rmsnorm", "gemm", "attn_decode",
-    "attn_prefill_chunk", "kv_write", "sample", "gather_rows", "rope_qkv", "silu_mul",
-    "EXPORTED_SYMBOLS",
+    "bi_sample", "bi_gather_rows", "bi_rope_qkv", "bi_silu_mul", "bi_gemm_swiglu",
+    "NOALLOC_SCRATCH_BYTES", "rmsnorm", "add_rmsnorm", "gemm", "gemm_swiglu",
+    "swiglu_interleave", "attn_decode", "attn_prefill_chunk", "kv_write", "sample",
+    "gather_rows", "rope_qkv", "silu_mul", "EXPORTED_SYMBOLS",
 ]
 
 # every function include/bi.h declares
@@ -42,7 +44,7 @@ EXPORTED_SYMBOLS = (
     "bi_gemm_variant_splits", "bi_attn_decode", "bi_attn_decode_workspace_size",
     "bi_attn_prefill_chunk", "bi_kv_write", "bi_check_device_errors", "bi_status_string",
     "bi_version", "bi_attn_decode_noalloc", "bi_selftest_wait_timeout", "bi_add_rmsnorm",
-    "bi_sample", "bi_gather_rows", "bi_rope_qkv", "bi_silu_mul",
+    "bi_sample", "bi_gather_rows", "bi_rope_qkv", "bi_silu_mul", "bi_gemm_swiglu",
 )
 
 
@@ -84,6 +86,8 @@ def load(build_if_missing: bool = True):
             "bi_gemm": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp, _sz, _vp]),
             "bi_gemm_workspace_size": (_sz, [_i64, _i64, _i64, _i32, _i32]),
             "bi_gemm_variant_splits": (_i32, [_i64, _i64, _i64, _i32]),
+            "bi_gemm_swiglu": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp, _sz,
+                                      _vp]),
             "bi_attn_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                       _i32, _i64, _i32, _i32, _i32, _f32, _i32, _i32, _vp, _sz,
                                       _vp]),
@@ -101,7 +105,7 @@ def load(build_if_missing: bool = True):
             "bi_gather_rows": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _vp]),
             "bi_rope_qkv": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, ctypes.c_double, _vp, _vp,
                                    _vp, _vp]),
-            "bi_silu_mul": (_i32, [_vp, _i64, _i64, _vp, _vp]),
+            "bi_silu_mul": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp]),
             "bi_check_device_errors": (_i32, [_vp]),
             "bi_selftest_wait_timeout": (_i32, [ctypes.c_uint32, _vp]),
             "bi_status_string": (ctypes.c_char_p, [_i32]),
@@ -196,6 +200,17 @@ def bi_gemm_workspace_size(M, N, K, mode=INVARIANT, variant_splits=0) -> int:
 
 def bi_gemm_variant_splits(M, N, K, num_sms) -> int:
     return int(load().bi_gemm_variant_splits(M, N, K, int(num_sms)))
+
+
+def bi_gemm_swiglu(A, W, out, mode=INVARIANT, variant_splits=0, workspace=None, stream=None):
+    M, K = A.shape
+    F = W.shape[0] // 2
+    if W.shape[0] % 2 or tuple(out.shape) != (M, F):
+        raise ValueError("W must be [2F, K] and out [M, F]")
+    wp, wb = _ws(workspace)
+    _check(load().bi_gemm_swiglu(_ptr(A, torch.bfloat16, "A"), _ptr(W, torch.bfloat16, "W"),
+                                 _ptr(out, torch.bfloat16, "out"), M, F, K, int(mode),
+                                 int(variant_splits), wp, wb, _stream(stream)), "bi_gemm_swiglu")
 
 
 def bi_attn_decode(q, k_cache, v_cache, block_table, kv_lens, out, out_f32=None, *,
@@ -300,11 +315,15 @@ def bi_rope_qkv(qkv, pos, Hq, Hkv, D, theta, q, k, v, stream=None):
                               _stream(stream)), "bi_rope_qkv")
 
 
-def bi_silu_mul(gate_up, out, stream=None):
+def bi_silu_mul(gate_up, out, block=None, stream=None):
+    """block: features per gate/up block (None: F, i.e. the gate half then
+    the up half; 128: the layout bi_gemm writes with bi_gemm_swiglu's
+    weight)."""
     T, F2 = gate_up.shape
     if F2 % 2 or tuple(out.shape) != (T, F2 // 2):
         raise ValueError("gate_up must be [T, 2F] and out [T, F]")
-    _check(load().bi_silu_mul(_ptr(gate_up, torch.bfloat16, "gate_up"), T, F2 // 2,
+    blk = F2 // 2 if block is None else int(block)
+    _check(load().bi_silu_mul(_ptr(gate_up, torch.bfloat16, "gate_up"), T, F2 // 2, blk,
                               _ptr(out, torch.bfloat16, "out"), _stream(stream)), "bi_silu_mul")
 
 
@@ -412,10 +431,29 @@ def rope_qkv(qkv, pos, Hq, Hkv, D, theta=500000.0, stream=None):
     return q, k, v
 
 
-def silu_mul(gate_up, stream=None):
+def gemm_swiglu(A, W, mode=INVARIANT, variant_splits=0, stream=None):
+    out = torch.empty(A.shape[0], W.shape[0] // 2, dtype=torch.bfloat16, device=A.device)
+    ws = _workspace(bi_gemm_workspace_size(A.shape[0], W.shape[0], A.shape[1], mode,
+                                           variant_splits), A.device)
+    bi_gemm_swiglu(A, W, out, mode, variant_splits, ws, stream)
+    return out
+
+
+def swiglu_interleave(F: int) -> np.ndarray:
+    """Row order of bi_gemm_swiglu's weight: entry r is the row of a [gate;
+    up] stacked weight (gate rows 0..F-1, up rows F..2F-1) that goes to row r
+    (blocks of 128 features, the gate rows of a block before its up rows)."""
+    if F % 128:
+        raise ValueError("F must be a multiple of 128")
+    j = np.arange(2 * F)
+    blk, r = j // 256, j % 256
+    return np.where(r < 128, blk * 128 + r, F + blk * 128 + (r - 128)).astype(np.int32)
+
+
+def silu_mul(gate_up, block=None, stream=None):
     out = torch.empty(gate_up.shape[0], gate_up.shape[1] // 2, dtype=gate_up.dtype,
                       device=gate_up.device)
-    bi_silu_mul(gate_up, out, stream)
+    bi_silu_mul(gate_up, out, block, stream)
     return out
 
 

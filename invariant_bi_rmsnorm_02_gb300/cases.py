@@ -10,11 +10,15 @@ flush between runs -- the unit a profiler capture or a quick timing needs.
     python -m invariant_bi_rmsnorm_02_gb300.cases rope --M 8192
     python -m invariant_bi_rmsnorm_02_gb300.cases silu --M 8192 --F 14336
     python -m invariant_bi_rmsnorm_02_gb300.cases gather --M 8192 --H 4096
+    python -m invariant_bi_rmsnorm_02_gb300.cases gemm_swiglu --M 8192 --F 14336 --K 4096
+    python -m invariant_bi_rmsnorm_02_gb300.cases gemm_silu --M 8192 --F 14336 --K 4096
 
 Prints one line per run with the CUDA-event time of the call (the device is
 kept busy while the call is queued, so host launch latency is not in the
 time) and, for the element-wise and sampling ops, the algorithmic bytes moved
-per second.
+per second; for the GEMMs, the flops per second.  gemm_swiglu is the gate/up
+projection with SwiGLU in the GEMM epilogue, gemm_silu the same work as two
+calls (the GEMM into [M, 2F], then the SwiGLU kernel).
 """
 from __future__ import annotations
 
@@ -29,7 +33,8 @@ from . import synth
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("op", choices=["rmsnorm", "gemm", "decode", "prefill", "add_rmsnorm",
-                                   "sample", "rope", "silu", "gather"])
+                                   "sample", "rope", "silu", "gather", "gemm_swiglu",
+                                   "gemm_silu"])
     ap.add_argument("--mode", type=int, default=bi.INVARIANT)
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--M", type=int, default=8192)
@@ -46,6 +51,7 @@ def main(argv=None):
     ap.add_argument("--temp", type=float, default=0.0)
     a = ap.parse_args(argv)
     nbytes = 0  # algorithmic bytes of one call (element-wise and sampling ops)
+    flops = 0   # algorithmic flops of one call (GEMMs)
     dev = torch.device("cuda", 0)
     bi.load()
     # L2 flush: write 256 MB, then read another 256 MB so that the written
@@ -60,6 +66,15 @@ def main(argv=None):
         A = synth.normal_bf16((a.M, a.K), 1, device=dev)
         W = synth.normal_bf16((a.N, a.K), 2, std=0.02, device=dev)
         fn = lambda: bi.gemm(A, W, a.mode)
+        flops = 2 * a.M * a.N * a.K
+    elif a.op in ("gemm_swiglu", "gemm_silu"):
+        A = synth.normal_bf16((a.M, a.K), 1, device=dev)
+        W = synth.normal_bf16((2 * a.F, a.K), 2, std=0.02, device=dev)
+        if a.op == "gemm_swiglu":
+            fn = lambda: bi.gemm_swiglu(A, W, a.mode)
+        else:
+            fn = lambda: bi.silu_mul(bi.gemm(A, W, a.mode), block=128)
+        flops = 2 * a.M * 2 * a.F * a.K
     elif a.op == "decode":
         lens = synth.loguniform_int(a.B, 1, a.max_len, 3).tolist()
         kv = synth.paged_kv(lens, 8, 128, 16, 4, device=dev)
@@ -112,6 +127,8 @@ def main(argv=None):
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1)
         extra = "  %.1f GB/s" % (nbytes / ms / 1e6) if nbytes else ""
+        if flops:
+            extra = "  %.1f TFLOP/s" % (flops / ms / 1e9)
         print("%s run %d: %.3f ms%s" % (a.op, i, ms, extra))
     status = bi.bi_check_device_errors()
     if status != bi.OK:

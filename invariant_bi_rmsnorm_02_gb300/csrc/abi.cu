@@ -251,6 +251,38 @@ bi_status bi_gemm(const void* A, const void* W, void* C, int64_t M, int64_t N, i
   return launch_gemm(A, W, C, M, N, K, splits, static_cast<float*>(workspace), err, s);
 }
 
+bi_status bi_gemm_swiglu(const void* A, const void* W, void* out, int64_t M, int64_t F,
+                         int64_t K, bi_mode mode, int variant_splits, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (M < 0 || F <= 0 || K <= 0) return BI_ERR_INVALID_ARG;
+  if (mode != BI_MODE_INVARIANT && mode != BI_MODE_VARIANT) return BI_ERR_INVALID_ARG;
+  if (F % (kGemmBN / 2) != 0 || K % 8 != 0) return BI_ERR_UNSUPPORTED;
+  const int64_t N = 2 * F;
+  if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+    return BI_ERR_UNSUPPORTED;
+  if (M == 0) return BI_OK;
+  if (!A || !W || !out) return BI_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(W) || !aligned16(out)) return BI_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int splits = 1;
+  if (mode == BI_MODE_VARIANT) {
+    splits = variant_splits;
+    if (splits <= 0) {
+      const int sms = device_sm_count();
+      if (sms <= 0) return BI_ERR_CUDA;
+      splits = bi_gemm_variant_splits(M, N, K, sms);
+    }
+    const int64_t kblocks = (K + kGemmBK - 1) / kGemmBK;
+    if (splits > kblocks) splits = static_cast<int>(kblocks);
+    if (splits > 1) {
+      const size_t need = static_cast<size_t>(splits) * M * N * sizeof(float);
+      if (!workspace || workspace_bytes < need || !aligned16(workspace)) return BI_ERR_WORKSPACE;
+    }
+  }
+  return launch_gemm(A, W, out, M, N, K, splits, static_cast<float*>(workspace),
+                     device_error_word(), s, /*swiglu=*/true);
+}
+
 // ---------------------------------------------------------------- attention
 static bi_status attn_common_checks(const void* q, const void* k, const void* v,
                                     const int32_t* bt, const int32_t* kl, const void* out,
@@ -407,12 +439,13 @@ bi_status bi_rope_qkv(const void* qkv, const int32_t* pos, int64_t T, int Hq, in
                          static_cast<cudaStream_t>(stream));
 }
 
-bi_status bi_silu_mul(const void* gate_up, int64_t T, int64_t F, void* out, void* stream) {
-  if (T < 0 || F <= 0) return BI_ERR_INVALID_ARG;
-  if (F % 8 != 0) return BI_ERR_UNSUPPORTED;
+bi_status bi_silu_mul(const void* gate_up, int64_t T, int64_t F, int64_t block, void* out,
+                      void* stream) {
+  if (T < 0 || F <= 0 || block <= 0) return BI_ERR_INVALID_ARG;
+  if (block % 8 != 0 || F % block != 0) return BI_ERR_UNSUPPORTED;
   if (T == 0) return BI_OK;
   if (!gate_up || !out || !aligned16(gate_up) || !aligned16(out)) return BI_ERR_INVALID_ARG;
-  return launch_silu_mul(gate_up, T, F, out, static_cast<cudaStream_t>(stream));
+  return launch_silu_mul(gate_up, T, F, block, out, static_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------------ sampling

@@ -35,7 +35,8 @@ bi_status launch_gather_rows(const void* src, int64_t rows, int64_t H, const int
                              int64_t n, void* dst, int* err, cudaStream_t s);
 bi_status launch_rope_qkv(const void* qkv, const int32_t* pos, int64_t T, int Hq, int Hkv, int D,
                           double theta, void* q, void* k, void* v, cudaStream_t s);
-bi_status launch_silu_mul(const void* gu, int64_t T, int64_t F, void* out, cudaStream_t s);
+bi_status launch_silu_mul(const void* gu, int64_t T, int64_t F, int64_t block, void* out,
+                          cudaStream_t s);
 bi_status launch_sample(const void* logits, int64_t B, int64_t V, const float* temperature,
                         const uint64_t* seed, const uint64_t* step, int32_t* tokens,
                         cudaStream_t s);
@@ -48,8 +49,9 @@ bi_status launch_rmsnorm_variant(const void* x, const void* w, void* y, float* y
 constexpr int kGemmBM = 128;
 constexpr int kGemmBN = 256;
 constexpr int kGemmBK = 64;
+// swiglu: C is [M, N/2], the SwiGLU product of each tile's two column halves
 bi_status launch_gemm(const void* A, const void* W, void* C, int64_t M, int64_t N, int64_t K,
-                      int splits, float* ws, int* err, cudaStream_t s);
+                      int splits, float* ws, int* err, cudaStream_t s, bool swiglu = false);
 
 // ---- attention (attention.cu) -------------------------------------------------
 struct AttnArgs {

@@ -144,5 +144,18 @@ __device__ __forceinline__ float bf16_lo(uint32_t v) {
 __device__ __forceinline__ float bf16_hi(uint32_t v) {
   return __uint_as_float(v & 0xffff0000u);
 }
+// x rounded to bf16 (nearest, ties to even) and widened back: the value a
+// bf16 store of x followed by a load gives.
+__device__ __forceinline__ float bf16_round(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// -------------------------------------------------------------- SwiGLU
+// silu(g) * u = g / (1 + exp(-g)) * u in fp32, one rounding per operation;
+// the standalone SwiGLU kernel and the fused GEMM epilogue both use it, so
+// the fused projection gives the bytes of the unfused pair.
+__device__ __forceinline__ float silu_mul_f32(float g, float u) {
+  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
 
 }  // namespace bi

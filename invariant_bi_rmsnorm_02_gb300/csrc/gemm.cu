@@ -18,6 +18,14 @@
 // the k-blocks, writes fp32 partial tiles, and sums them in slice order in a
 // second kernel.
 //
+// SwiGLU epilogue: for a gate/up weight whose rows come in blocks of 128
+// features (the gate rows of the block, then its up rows), each 256-column
+// tile holds the gate and up values of the same 128 features, so the
+// epilogue rounds both to bf16 (as a stored projection would be), applies
+// silu(g) * u and writes 128 columns of the product: the bytes of the GEMM
+// followed by the standalone SwiGLU kernel, without the round trip of the
+// [M, 2F] projection through memory.
+//
 // Structure: persistent blocks (one per SM), 6 warps:
 //   warp 0    : TMA producer, fills a 4-stage ring of (A 128x64, W 256x64)
 //               tiles, 128-byte swizzled, completion on mbarriers;
@@ -98,7 +106,13 @@ __device__ __forceinline__ Unit unit_of(int u, const GemmParams& p) {
   return w;
 }
 
-template <bool kF32Out>
+enum Epilogue : int {
+  kEpiBf16 = 0,    // C [M, N] bf16
+  kEpiF32 = 1,     // fp32 split-K partials ws [split][M][N]
+  kEpiSwiglu = 2,  // C [M, N/2] bf16 = silu(gate) * up of the interleaved tile halves
+};
+
+template <int kEpi>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(
     const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
     const GemmParams p) {
@@ -230,30 +244,56 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(
       const int row = w.m_tile * BM + wq * 32 + lane;
       const uint32_t tbase =
           tmem_base + (static_cast<uint32_t>(wq * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      if constexpr (kEpi == kEpiSwiglu) {
+        // gate in accumulator columns 0 .. BN/2-1, up in BN/2 .. BN-1
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tbase + c * 32, v);
-        const int col0 = w.n_tile * BN + c * 32;
-        if (row < p.M) {
-          if constexpr (kF32Out) {
-            float* dst = p.ws + (static_cast<int64_t>(w.split) * p.M + row) * p.N + col0;
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              if (col0 + 4 * q < p.N)
-                *reinterpret_cast<uint4*>(dst + 4 * q) =
-                    make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-          } else {
-            __nv_bfloat16* dst = p.C + static_cast<int64_t>(row) * p.N + col0;
+        for (int c = 0; c < BN / 64; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld32_nowait(tbase + c * 32, g);
+          tmem_ld32_nowait(tbase + BN / 2 + c * 32, u);
+          tmem_wait_ld();
+          if (row < p.M) {
+            __nv_bfloat16* dst = p.C + static_cast<int64_t>(row) * (p.N / 2) +
+                                 w.n_tile * (BN / 2) + c * 32;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              if (col0 + 8 * q < p.N) {
-                uint4 o;
-                o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
-                o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
-                o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
-                o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
-                *reinterpret_cast<uint4*>(dst + 8 * q) = o;
+              float y[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                y[e] = silu_mul_f32(bf16_round(__uint_as_float(g[8 * q + e])),
+                                    bf16_round(__uint_as_float(u[8 * q + e])));
+              *reinterpret_cast<uint4*>(dst + 8 * q) =
+                  make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                             pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tbase + c * 32, v);
+          const int col0 = w.n_tile * BN + c * 32;
+          if (row < p.M) {
+            if constexpr (kEpi == kEpiF32) {
+              float* dst = p.ws + (static_cast<int64_t>(w.split) * p.M + row) * p.N + col0;
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                if (col0 + 4 * q < p.N)
+                  *reinterpret_cast<uint4*>(dst + 4 * q) =
+                      make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            } else {
+              __nv_bfloat16* dst = p.C + static_cast<int64_t>(row) * p.N + col0;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                if (col0 + 8 * q < p.N) {
+                  uint4 o;
+                  o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+                  o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+                  o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+                  o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+                  *reinterpret_cast<uint4*>(dst + 8 * q) = o;
+                }
               }
             }
           }
@@ -294,10 +334,53 @@ __global__ void splitk_reduce_kernel(const float4* __restrict__ ws, uint2* __res
   }
 }
 
+// out[i, j] = bf16(silu(g) * u), g and u the slice-ordered sums of the gate
+// and up partials of output feature j (columns 256 (j / 128) + j % 128 and
+// 128 more of ws), each rounded to bf16 first: the bytes of
+// splitk_reduce_kernel followed by the standalone SwiGLU kernel.  Four
+// features per thread.
+__global__ void splitk_reduce_swiglu_kernel(const float* __restrict__ ws, uint2* __restrict__ out,
+                                            int64_t M, int64_t F, int splits) {
+  const int64_t f4 = F / 4, n4 = M * f4, N = 2 * F, slice = M * N;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = i / f4, j = (i - row * f4) * 4;
+    const float* gp = ws + row * N + (j / 128) * 256 + j % 128;
+    float4 g = *reinterpret_cast<const float4*>(gp);
+    float4 u = *reinterpret_cast<const float4*>(gp + 128);
+    for (int s = 1; s < splits; ++s) {
+      const float4 b = *reinterpret_cast<const float4*>(gp + s * slice);
+      const float4 c = *reinterpret_cast<const float4*>(gp + s * slice + 128);
+      g.x = __fadd_rn(g.x, b.x);
+      g.y = __fadd_rn(g.y, b.y);
+      g.z = __fadd_rn(g.z, b.z);
+      g.w = __fadd_rn(g.w, b.w);
+      u.x = __fadd_rn(u.x, c.x);
+      u.y = __fadd_rn(u.y, c.y);
+      u.z = __fadd_rn(u.z, c.z);
+      u.w = __fadd_rn(u.w, c.w);
+    }
+    out[i] = make_uint2(pack_bf16x2(silu_mul_f32(bf16_round(g.x), bf16_round(u.x)),
+                                    silu_mul_f32(bf16_round(g.y), bf16_round(u.y))),
+                        pack_bf16x2(silu_mul_f32(bf16_round(g.z), bf16_round(u.z)),
+                                    silu_mul_f32(bf16_round(g.w), bf16_round(u.w))));
+  }
+}
+
+template <int kEpi>
+bi_status launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int grid,
+                    cudaStream_t s) {
+  if (cudaFuncSetAttribute(gemm_tc_kernel<kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemBytes)) != cudaSuccess)
+    return BI_ERR_CUDA;
+  gemm_tc_kernel<kEpi><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, p);
+  return cuda_status(cudaGetLastError());
+}
+
 }  // namespace
 
 bi_status launch_gemm(const void* A, const void* W, void* C, int64_t M, int64_t N, int64_t K,
-                      int splits, float* ws, int* err, cudaStream_t s) {
+                      int splits, float* ws, int* err, cudaStream_t s, bool swiglu) {
   const int sms = device_sm_count();
   if (sms <= 0) return BI_ERR_CUDA;
   CUtensorMap ta, tb;
@@ -329,21 +412,17 @@ bi_status launch_gemm(const void* A, const void* W, void* C, int64_t M, int64_t 
   const int64_t units = static_cast<int64_t>(p.m_tiles) * p.n_tiles * p.splits;
   if (units > 0x7fffffff) return BI_ERR_UNSUPPORTED;
   const int grid = static_cast<int>(units < sms ? units : sms);
-  if (p.splits == 1) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes)) != cudaSuccess)
-      return BI_ERR_CUDA;
-    gemm_tc_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, p);
-    return cuda_status(cudaGetLastError());
-  }
-  if (cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSmemBytes)) != cudaSuccess)
-    return BI_ERR_CUDA;
-  gemm_tc_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, p);
-  const int64_t mn4 = M * N / 4;
-  const int rb = static_cast<int>((mn4 + 255) / 256 < 4 * sms ? (mn4 + 255) / 256 : 4 * sms);
-  splitk_reduce_kernel<<<rb, 256, 0, s>>>(reinterpret_cast<const float4*>(ws),
-                                          static_cast<uint2*>(C), mn4, p.splits);
+  if (p.splits == 1)
+    return swiglu ? launch_tc<kEpiSwiglu>(ta, tb, p, grid, s) : launch_tc<kEpiBf16>(ta, tb, p, grid, s);
+  const bi_status st = launch_tc<kEpiF32>(ta, tb, p, grid, s);
+  if (st != BI_OK) return st;
+  const int64_t n4 = swiglu ? M * N / 8 : M * N / 4;  // threads of the reduction
+  const int rb = static_cast<int>((n4 + 255) / 256 < 4 * sms ? (n4 + 255) / 256 : 4 * sms);
+  if (swiglu)
+    splitk_reduce_swiglu_kernel<<<rb, 256, 0, s>>>(ws, static_cast<uint2*>(C), M, N / 2, p.splits);
+  else
+    splitk_reduce_kernel<<<rb, 256, 0, s>>>(reinterpret_cast<const float4*>(ws),
+                                            static_cast<uint2*>(C), n4, p.splits);
   return cuda_status(cudaGetLastError());
 }
 

@@ -136,27 +136,28 @@ __global__ void __launch_bounds__(kThreads) rope_qkv_kernel(
 }
 
 // ---------------------------------------------------------------- SwiGLU
-// out[t, j] = bf16(silu(gate) * up), gate = gu[t, j], up = gu[t, F + j],
-// silu(x) = x / (1 + exp(-x)), all in fp32.
-__device__ __forceinline__ float silu_mul1(float g, float u) {
-  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
-}
+// out[t, j] = bf16(silu(gate) * up), silu(x) = x / (1 + exp(-x)) in fp32
+// (silu_mul_f32); gate and up come in blocks of vb 16-byte vectors (8 features
+// each): gate vector c at 2 vb (c / vb) + c % vb of the row, up vb after it.
 
 __global__ void __launch_bounds__(kThreads) silu_mul_kernel(const uint4* __restrict__ gu,
                                                             int64_t T, int64_t vec_f,
+                                                            int64_t vb,
                                                             uint4* __restrict__ out) {
   const int64_t total = T * vec_f;
   for (int64_t e = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; e < total;
        e += static_cast<int64_t>(gridDim.x) * kThreads) {
     const int64_t t = e / vec_f, c = e - t * vec_f;
-    const uint4 gv = __ldcs(gu + t * 2 * vec_f + c);
-    const uint4 uv = __ldcs(gu + t * 2 * vec_f + vec_f + c);
+    const int64_t cb = c / vb;
+    const uint4* src = gu + t * 2 * vec_f + cb * 2 * vb + (c - cb * vb);
+    const uint4 gv = __ldcs(src);
+    const uint4 uv = __ldcs(src + vb);
     const uint32_t g[4] = {gv.x, gv.y, gv.z, gv.w}, u[4] = {uv.x, uv.y, uv.z, uv.w};
     uint32_t o[4];
 #pragma unroll
     for (int w = 0; w < 4; ++w)
-      o[w] = pack_bf16x2(silu_mul1(bf16_lo(g[w]), bf16_lo(u[w])),
-                         silu_mul1(bf16_hi(g[w]), bf16_hi(u[w])));
+      o[w] = pack_bf16x2(silu_mul_f32(bf16_lo(g[w]), bf16_lo(u[w])),
+                         silu_mul_f32(bf16_hi(g[w]), bf16_hi(u[w])));
     out[e] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
@@ -180,10 +181,11 @@ bi_status launch_rope_qkv(const void* qkv, const int32_t* pos, int64_t T, int Hq
   return cuda_status(cudaGetLastError());
 }
 
-bi_status launch_silu_mul(const void* gu, int64_t T, int64_t F, void* out, cudaStream_t s) {
+bi_status launch_silu_mul(const void* gu, int64_t T, int64_t F, int64_t block, void* out,
+                          cudaStream_t s) {
   const int64_t vf = F / 8;
   silu_mul_kernel<<<blocks_for(T * vf), kThreads, 0, s>>>(static_cast<const uint4*>(gu), T, vf,
-                                                          static_cast<uint4*>(out));
+                                                          block / 8, static_cast<uint4*>(out));
   return cuda_status(cudaGetLastError());
 }
 

@@ -12,7 +12,7 @@ which other requests share a step.  Each layer is
     K/V cache <- k, v                                bi_kv_write
     a   = attention(q, cache)                        bi_attn_decode / bi_attn_prefill_chunk
     h  += a W_o^T;  y = RMSNorm(h) * w_mlp            bi_gemm, bi_add_rmsnorm
-    h  += (silu(y W_gate^T) * y W_up^T) W_down^T      bi_gemm, bi_silu_mul, bi_gemm
+    h  += (silu(y W_gate^T) * y W_up^T) W_down^T      bi_gemm_swiglu, bi_gemm
 
 followed by a final RMSNorm, the LM-head GEMM on the rows that need a token
 and bi_sample (greedy at temperature 0, seeded Gumbel-max above).  Weights are
@@ -74,11 +74,22 @@ TINY = DecoderConfig(layers=2, hidden=256, heads=4, kv_heads=2, head_dim=64, ffn
 """A two-layer decoder small enough for the fp64 oracle."""
 
 
+# Below one full 128-row tile the fused SwiGLU epilogue is slower than the
+# two-kernel form: its element work falls on the few warps that own valid
+# rows, after the tile's last MMA, with nothing to overlap (GB300, gate/up
+# 2 x 14336 by 4096: 55 against 50 us at 16 rows, 53 against 54 at 128, 90
+# against 99 at 512, 1.05 against 1.21 ms at 8192).
+SWIGLU_FUSE_MIN_ROWS = 128
+
+
 class DecoderWeights:
     """Random bf16 weights N(0, init_std^2), norm weights 1.  Linear weights
     are [out, in] (the GEMM's W [N, K]); the q/k/v and gate/up projections are
-    stacked into one matrix each.  ``gen_device`` is where the numbers are
-    drawn (CPU for configurations an oracle also reads, the GPU for speed)."""
+    stacked into one matrix each, the gate/up one in blocks of 128 features
+    (the block's gate rows, then its up rows: the layout bi_gemm_swiglu reads,
+    so the SwiGLU product comes out of the GEMM epilogue).  ``gen_device`` is
+    where the numbers are drawn (CPU for configurations an oracle also reads,
+    the GPU for speed)."""
 
     def __init__(self, cfg: DecoderConfig, seed: int, device, gen_device=None):
         gd = device if gen_device is None else gen_device
@@ -191,7 +202,9 @@ class Decoder:
         self.q, self.k, self.v = (buf(T, c.heads, c.head_dim), buf(T, c.kv_heads, c.head_dim),
                                   buf(T, c.kv_heads, c.head_dim))
         self.att, self.o = buf(T, c.heads, c.head_dim), buf(T, H)
-        self.gu, self.act, self.delta = buf(T, 2 * c.ffn), buf(T, c.ffn), buf(T, H)
+        self.act, self.delta = buf(T, c.ffn), buf(T, H)
+        # the gate/up projection of steps below SWIGLU_FUSE_MIN_ROWS tokens
+        self.gu = buf(min(T, SWIGLU_FUSE_MIN_ROWS - 1), 2 * c.ffn)
         self.ys, self.logits = buf(max_seqs, H), buf(max_seqs, c.vocab)
         self.tokens_out = buf(max_seqs, dtype=torch.int32)
         self.tokens_host = torch.empty(max_seqs, dtype=torch.int32, pin_memory=True)
@@ -234,6 +247,21 @@ class Decoder:
             ws = self._workspace(bi.bi_gemm_workspace_size(A.shape[0], W.shape[0], A.shape[1],
                                                            self.mode))
         bi.bi_gemm(A, W, C, self.mode, 0, ws)
+
+    def _gemm_swiglu(self, A, W, out):
+        """out = SwiGLU of the gate/up projection A W^T: in the GEMM epilogue
+        from SWIGLU_FUSE_MIN_ROWS rows on, else as the GEMM then the SwiGLU
+        kernel (the same bytes either way)."""
+        T = A.shape[0]
+        if T < SWIGLU_FUSE_MIN_ROWS:
+            gu = self.gu[:T]
+            self._gemm(A, W, gu)
+            bi.bi_silu_mul(gu, out, block=128)
+            return
+        ws = None
+        if self.mode != bi.INVARIANT:
+            ws = self._workspace(bi.bi_gemm_workspace_size(T, W.shape[0], A.shape[1], self.mode))
+        bi.bi_gemm_swiglu(A, W, out, self.mode, 0, ws)
 
     def step(self, plan: StepPlan) -> np.ndarray:
         """Run one forward step; returns the chosen tokens of plan.sample_rows
@@ -321,9 +349,8 @@ class Decoder:
             o = self.o[:T]
             self._gemm(att.view(T, c.heads * c.head_dim), w.wo[layer], o)
             bi.bi_add_rmsnorm(o, h, w.mlp_norm[layer], y, c.eps, mode, self._ws_norm(T))
-            gu, act = self.gu[:T], self.act[:T]
-            self._gemm(y, w.wgu[layer], gu)
-            bi.bi_silu_mul(gu, act)
+            act = self.act[:T]
+            self._gemm_swiglu(y, w.wgu[layer], act)
             self._gemm(act, w.wdown[layer], delta)
         bi.bi_add_rmsnorm(delta, h, w.final_norm, y, c.eps, mode, self._ws_norm(T))
         if n_s == 0:

@@ -13,6 +13,10 @@ to even) where the model stores it:
                 h = bf16(h + (silu(y W_gate^T) * y W_up^T) W_down^T)
     logits = (RMSNorm(h) * w_final) W_lm^T        (float64, not rounded)
 
+W_gate and W_up are stacked into one weight in blocks of 128 features: rows
+256b .. 256b+127 are the gate rows of features 128b .. 128b+127 and the next
+128 rows the up rows of the same features.
+
 Sources: "Reproducible LLM Inference - Batch Invariance, the Cost of
 Determinism, and Where Bitwise Identity Is Actually Required" (§5.3-5.5: the
 three reductions; §6: the serving loop) and "Your Answer Depends on Who Else
@@ -34,6 +38,16 @@ def to_bf16(x) -> np.ndarray:
     m, e = np.frexp(x)                       # x = m 2^e, 1/2 <= |m| < 1
     q = np.ldexp(np.rint(m * 256.0), e - 8)  # rint rounds half to even
     return (q.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def gate_up_halves(gu) -> np.ndarray:
+    """[T, 2F] projection in the blocked gate/up column order -> [T, 2F] with
+    all gate columns first, then all up columns (silu_mul's layout)."""
+    gu = np.asarray(gu)
+    T, F2 = gu.shape
+    blocks = gu.reshape(T, F2 // 256, 2, 128)
+    return np.concatenate([blocks[:, :, 0, :].reshape(T, -1), blocks[:, :, 1, :].reshape(T, -1)],
+                          axis=1)
 
 
 def forward_logits(weights, cfg, tokens) -> np.ndarray:
@@ -63,7 +77,7 @@ def forward_logits(weights, cfg, tokens) -> np.ndarray:
         o = to_bf16(gemm(to_bf16(a).reshape(T, Hq * D), weights.wo[layer]))
         h = add_bf16(o, h)
         y = to_bf16(rmsnorm(h, weights.mlp_norm[layer], cfg.eps))
-        act = to_bf16(silu_mul(to_bf16(gemm(y, weights.wgu[layer]))))
+        act = to_bf16(silu_mul(gate_up_halves(to_bf16(gemm(y, weights.wgu[layer])))))
         d = to_bf16(gemm(act, weights.wdown[layer]))
         h = add_bf16(d, h)
     y = to_bf16(rmsnorm(h, weights.final_norm, cfg.eps))

@@ -102,6 +102,30 @@ def test_gemm_argument_checks(lib):
     assert g(None, None, None, 0, 128, 64, 0, 0, None, 0, None) == bi.OK
 
 
+def test_gemm_swiglu_argument_checks(lib):
+    p = 1 << 20
+    g = lambda *a: lib.bi_gemm_swiglu(*a)
+    assert g(p, p, p, 4, 192, 64, 0, 0, None, 0, None) == bi.ERR_UNSUPPORTED   # F % 128
+    assert g(p, p, p, 4, 128, 60, 0, 0, None, 0, None) == bi.ERR_UNSUPPORTED   # K % 8
+    assert g(p, p, p, 4, 0, 64, 0, 0, None, 0, None) == bi.ERR_INVALID_ARG
+    assert g(p, p, p, 4, 128, 64, 5, 0, None, 0, None) == bi.ERR_INVALID_ARG   # mode
+    assert g(p, None, p, 4, 128, 64, 0, 0, None, 0, None) == bi.ERR_INVALID_ARG
+    assert g(p, p, p + 8, 4, 128, 64, 0, 0, None, 0, None) == bi.ERR_INVALID_ARG
+    # variant with an explicit split count and no workspace: refused, host-side
+    assert g(p, p, p, 4, 128, 256, 1, 2, None, 0, None) == bi.ERR_WORKSPACE
+    assert g(None, None, None, 0, 128, 64, 0, 0, None, 0, None) == bi.OK
+
+
+def test_silu_mul_argument_checks(lib):
+    p = 1 << 20
+    f = lambda T, F, block, out=p: lib.bi_silu_mul(p, T, F, block, out, None)
+    assert f(4, 256, 0) == bi.ERR_INVALID_ARG
+    assert f(4, 256, 12) == bi.ERR_UNSUPPORTED          # block % 8
+    assert f(4, 384, 256) == bi.ERR_UNSUPPORTED         # F % block
+    assert f(4, 256, 128, out=p + 4) == bi.ERR_INVALID_ARG
+    assert f(0, 256, 128) == bi.OK
+
+
 def _decode(lib, **kw):
     p = 1 << 20
     a = dict(q=p, k=p, v=p, bt=p, kl=p, out=p, o32=None, B=2, Hq=4, Hkv=2, D=64, page=16,
@@ -140,3 +164,20 @@ def test_product_package_never_imports_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
                 assert "liboracle" not in text, f
+
+
+@pytest.mark.parametrize("F", [128, 256, 1024, 14336])
+def test_swiglu_interleave_inverts_the_oracle_layout(F):
+    """bi.swiglu_interleave (the row order bi_gemm_swiglu's weight takes) and
+    the oracle's reading of that layout (gate_up_halves) undo each other."""
+    import numpy as np
+    from oracle.decoder import gate_up_halves
+    perm = bi.swiglu_interleave(F)
+    assert sorted(perm.tolist()) == list(range(2 * F))
+    x = np.random.default_rng(F).standard_normal((3, 2 * F))
+    assert np.array_equal(gate_up_halves(x[:, perm]), x)
+
+
+def test_swiglu_interleave_rejects_unaligned_widths():
+    with pytest.raises(ValueError):
+        bi.swiglu_interleave(192)

@@ -78,3 +78,22 @@ def test_silu_mul_matches_oracle(cuda, T, F):
     check_close(g, r, bf16_half_ulp(g) + 2.0 ** -20 * np.abs(r) + 1e-30, "silu_mul")
     if T > 1:
         assert same_bytes(bi.silu_mul(gu[1:2].contiguous()), out[1:2])
+    assert same_bytes(bi.silu_mul(gu, block=F), out)        # block = F: the halves layout
+
+
+@pytest.mark.parametrize("T,F,block", [(3, 14336, 128), (70, 384, 128), (2, 64, 8),
+                                       (5, 96, 32)])
+def test_silu_mul_blocked_layout_matches_oracle(cuda, T, F, block):
+    gu = synth.normal_bf16((T, 2 * F), 11400 + F + block, std=2.0, device=cuda)
+    out = bi.silu_mul(gu, block=block)
+    assert bi.bi_check_device_errors() == bi.OK
+    # the oracle reads the stacked halves: gather block b's gate and up
+    # columns (2 block b .. and block after) into them
+    x = gu.cpu().view(torch.int16).numpy().view(np.uint16).reshape(T, F // block, 2, block)
+    halves = np.concatenate([x[:, :, 0, :].reshape(T, F), x[:, :, 1, :].reshape(T, F)], axis=1)
+    r = oracle.silu_mul(halves)
+    g = f64(out)
+    check_close(g, r, bf16_half_ulp(g) + 2.0 ** -20 * np.abs(r) + 1e-30, "silu_mul blocked")
+    # the same elements through the halves layout: identical bytes
+    h = torch.from_numpy(halves.view(np.int16)).view(torch.bfloat16).to(cuda)
+    assert same_bytes(bi.silu_mul(h), out)

@@ -583,6 +583,20 @@ def test_silu_mul_closed_forms():
     assert np.allclose(y2, y * u, rtol=1e-15, atol=0)
 
 
+def test_gate_up_halves_reads_the_blocked_layout():
+    from oracle.decoder import gate_up_halves
+    # F = 256: two blocks of 128 features; columns 0-127 gate of features
+    # 0-127, 128-255 their up, 256-383 gate of features 128-255, 384-511 up
+    x = np.arange(512, dtype=np.float64)[None, :].repeat(2, axis=0)
+    y = gate_up_halves(x)
+    want = np.concatenate([np.arange(0, 128), np.arange(256, 384), np.arange(128, 256),
+                           np.arange(384, 512)])
+    assert np.array_equal(y[0], want) and np.array_equal(y[1], want)
+    # one block: the layout is already gate-then-up
+    z = np.arange(256, dtype=np.float64)[None, :]
+    assert np.array_equal(gate_up_halves(z), z)
+
+
 def test_gather_rows_copies_bits():
     src = synth.normal_bf16((10, 24), 9137)
     idx = np.array([3, 3, 0, 9])
