@@ -298,13 +298,16 @@ template <int D>
 __device__ __forceinline__ void issue_pages(uint8_t* buf, uint64_t* bar, const CUtensorMap* km,
                                             const CUtensorMap* vm, const int (&pid)[4], int np,
                                             int Hkv, int h) {
+  // each cached K/V byte is read once per call: evict it first, so that the
+  // split partials written meanwhile are still in L2 for the merge
+  const uint64_t pol = l2_policy_evict_first();
   for (int p = 0; p < np; ++p) {
     const int y = (pid[p] * Hkv + h) * kPage;
 #pragma unroll
     for (int hf = 0; hf < TileGeom<D>::kHalves; ++hf) {
       const int off = (p * TileGeom<D>::kHalves + hf) * 2048;
-      tma_load_2d(buf + off, km, hf * 64, y, bar);
-      tma_load_2d(buf + TileGeom<D>::kKBytes + off, vm, hf * 64, y, bar);
+      tma_load_2d_hint(buf + off, km, hf * 64, y, bar, pol);
+      tma_load_2d_hint(buf + TileGeom<D>::kKBytes + off, vm, hf * 64, y, bar, pol);
     }
   }
 }
@@ -752,25 +755,31 @@ __global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
 }
 
 // ------------------------------------------------------------ decode merge
-// Block (qh, b), D/2 threads (two output columns each): left fold over the
-// splits in index order, then o / l.  Empty splits are skipped; a split
-// marked l = -1 (bad pages) makes the whole row zero.  The partial rows and
-// their {m, l} pairs are staged by bulk copies in chunks of kMergeChunk
-// splits, merge_slots chunks in flight, so the fold (strictly in split order)
-// runs from shared memory while later chunks are still arriving.
+// Block (qh, b): D/2 fold threads (two output columns each) and one
+// coefficient warp.  The left fold over the splits in index order, then
+// o / l.  Empty splits are skipped; a split marked l = -1 (bad pages) makes
+// the whole row zero.  The partial rows and their {m, l} pairs are staged by
+// bulk copies in chunks of kMergeChunk splits, merge_slots chunks in flight.
+// The fold's data dependences are split apart: the running maximum before
+// each split is a prefix maximum (exact in any order), so the coefficient
+// warp derives the coefficients of a whole chunk at once, a chunk or more
+// ahead of the fold threads; the fold proper is then a chain of products and
+// sums with one select per split and no branch, bit-identical to folding one
+// split at a time.  Per chunk and slot: `landed` (the copies), `ready` (its
+// coefficients), `consumed` (every fold thread is done with the slot).
 constexpr int kMergeChunk = 16;
 constexpr int kMergeSlots = 4;
 
 template <int D>
-__global__ void __launch_bounds__(D / 2) attn_decode_merge_kernel(const KernelParams p) {
+__global__ void __launch_bounds__(D / 2 + 32) attn_decode_merge_kernel(const KernelParams p) {
+  constexpr int kFold = D / 2;  // fold threads; the coefficient warp follows them
   extern __shared__ __align__(16) float mo[];  // [slot][kMergeChunk][D]
   __shared__ __align__(16) float2 sml[kMergeSlots][kMergeChunk];
-  __shared__ float2 scoef[kMergeChunk];  // ca, cb of each split of the chunk
-  __shared__ int skind[kMergeChunk];     // 0 empty, 1 first non-empty, 2 fold in
-  __shared__ uint64_t bars[kMergeSlots];
+  __shared__ float2 scoef[kMergeSlots][kMergeChunk];  // ca, cb of each split of the chunk
+  __shared__ int skind[kMergeSlots][kMergeChunk];     // 0 empty, 1 first non-empty, 2 fold in
+  __shared__ uint64_t landed[kMergeSlots], ready[kMergeSlots], consumed[kMergeSlots];
   __shared__ int s_abort, s_bad;
   const int qh = blockIdx.x, tid = threadIdx.x;
-  const int d = tid * 2;
   grid_dependency_wait();  // every split kernel block has finished
   const int b = p.order ? p.order[blockIdx.y] : blockIdx.y;
   const int64_t row = (int64_t)b * p.Hq + qh;
@@ -782,46 +791,52 @@ __global__ void __launch_bounds__(D / 2) attn_decode_merge_kernel(const KernelPa
   const int slots = p.merge_slots;
   const float2* mlrow = reinterpret_cast<const float2*>(p.ml) + row * p.ml_stride;
   const float* orow = p.o + row * p.max_splits * D;
-  auto issue = [&](int c) {  // thread 0: chunk c into slot c % slots
+  auto issue = [&](int c) {  // one thread: chunk c into slot c % slots
     const int j0 = c * kMergeChunk, cnt = min(kMergeChunk, ns - j0), slot = c % slots;
     const uint32_t ob = cnt * D * 4, mb = ((cnt + 1) & ~1) * 8;  // the row stride is even
-    mbar_arrive_expect_tx(&bars[slot], ob + mb);
-    bulk_load(mo + slot * kMergeChunk * D, orow + (int64_t)j0 * D, ob, &bars[slot]);
-    bulk_load(&sml[slot][0], mlrow + j0, mb, &bars[slot]);
+    mbar_arrive_expect_tx(&landed[slot], ob + mb);
+    bulk_load(mo + slot * kMergeChunk * D, orow + (int64_t)j0 * D, ob, &landed[slot]);
+    bulk_load(&sml[slot][0], mlrow + j0, mb, &landed[slot]);
   };
   if (tid == 0) {
     s_abort = 0;
     s_bad = 0;
-    for (int i = 0; i < slots; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < slots; ++i) {
+      mbar_init(&landed[i], 1);
+      mbar_init(&ready[i], 1);
+      mbar_init(&consumed[i], kFold);
+    }
     fence_mbar_init();
-    for (int c = 0; c < nch && c < slots; ++c) issue(c);
   }
   __syncthreads();
-  // The left fold in split order, with its data dependences split apart: the
-  // running max before each split is a prefix max (exact in any order), so
-  // warp 0 derives every split's coefficients of a chunk at once, and the
-  // fold proper is a chain of products and sums, bit-identical to folding
-  // one split at a time.
-  float run_m = -CUDART_INF_F;  // warp 0: max over the splits folded so far
-  bool have = false;            // warp 0: a non-empty split was folded
-  float o0 = 0.0f, o1 = 0.0f, l = 0.0f;
-  bool ok = true;
-  for (int c = 0; c < nch; ++c) {
-    const int slot = c % slots;
-    const int cnt = min(kMergeChunk, ns - c * kMergeChunk);
-    const bool landed = mbar_wait(&bars[slot], (c / slots) & 1, p.err, &s_abort);
-    if (__syncthreads_or(!landed)) {
-      // a copy never arrived: bounded waits for the ones still in flight
-      if (tid == 0)
-        for (int i = c; i < nch && i < c + slots; ++i)
-          mbar_wait(&bars[i % slots], (i / slots) & 1, nullptr);
-      ok = false;
-      break;
-    }
-    if (tid < 32) {
+  if (tid >= kFold) {
+    // ================================================= coefficient warp
+    // A slot is refilled once every fold thread has consumed it, so no
+    // barrier here is ever more than one phase ahead of its waiter.
+    const int lane = tid - kFold;
+    float run_m = -CUDART_INF_F;  // max over the splits folded so far
+    bool have = false;            // a non-empty split was folded
+    const int first = min(nch, slots);
+    if (lane == 0)
+      for (int c = 0; c < first; ++c) issue(c);
+    int issued = first, waited = 0;
+    bool ok = true;
+    for (int c = 0; c < nch; ++c) {
+      const int slot = c % slots;
+      if (c >= slots) {
+        ok = __all_sync(kFull, mbar_wait(&consumed[slot], ((c - slots) / slots) & 1, p.err,
+                                         &s_abort));
+        if (!ok) break;
+        if (lane == 0) issue(c);
+        ++issued;
+      }
+      ok = __all_sync(kFull, mbar_wait(&landed[slot], (c / slots) & 1, p.err, &s_abort));
+      if (!ok) break;
+      ++waited;
+      const int cnt = min(kMergeChunk, ns - c * kMergeChunk);
       float m = -CUDART_INF_F, lj = 0.0f;
-      if (tid < cnt) {
-        const float2 v = sml[slot][tid];
+      if (lane < cnt) {
+        const float2 v = sml[slot][lane];
         m = v.x;
         lj = v.y;
       }
@@ -830,45 +845,63 @@ __global__ void __launch_bounds__(D / 2) attn_decode_merge_kernel(const KernelPa
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const float t = __shfl_up_sync(kFull, pm, o);
-        if (tid >= o) pm = fmaxf(pm, t);
+        if (lane >= o) pm = fmaxf(pm, t);
       }
       float before = __shfl_up_sync(kFull, pm, 1);
-      before = fmaxf(run_m, tid == 0 ? -CUDART_INF_F : before);
+      before = fmaxf(run_m, lane == 0 ? -CUDART_INF_F : before);
       const unsigned ne = __ballot_sync(kFull, nonempty);
-      const bool had = have || (ne & ((1u << tid) - 1u)) != 0;
-      if (__any_sync(kFull, lj < 0.0f) && tid == 0) s_bad = 1;
-      if (tid < cnt) {
+      const bool had = have || (ne & ((1u << lane) - 1u)) != 0;
+      if (__any_sync(kFull, lj < 0.0f) && lane == 0) s_bad = 1;
+      if (lane < cnt) {
         float ca = 0.0f, cb = 0.0f;
         if (nonempty && had) {
           float mn;
           lse_coeffs(before, m, mn, ca, cb);
         }
-        scoef[tid] = make_float2(ca, cb);
-        skind[tid] = nonempty ? (had ? 2 : 1) : 0;
+        scoef[slot][lane] = make_float2(ca, cb);
+        skind[slot][lane] = nonempty ? (had ? 2 : 1) : 0;
       }
       run_m = fmaxf(run_m, __shfl_sync(kFull, pm, 31));
       have = have || ne != 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ready[slot]);
     }
-    __syncthreads();
+    if (!ok && lane == 0)
+      // a wait gave up: the copies still in flight land before the block exits
+      for (int i = waited; i < issued; ++i) mbar_wait(&landed[i % slots], (i / slots) & 1, nullptr);
+    return;
+  }
+  // ===================================================== fold threads
+  const int d = tid * 2;
+  float o0 = 0.0f, o1 = 0.0f, l = 0.0f;
+  bool ok = true;
+  for (int c = 0; c < nch; ++c) {
+    const int slot = c % slots;
+    // `ready` follows `landed`; waiting on both makes the copied bytes this
+    // thread's own observation (neither barrier can be a phase ahead here)
+    if (!mbar_wait(&ready[slot], (c / slots) & 1, p.err, &s_abort) ||
+        !mbar_wait(&landed[slot], (c / slots) & 1, p.err, &s_abort)) {
+      ok = false;
+      break;
+    }
+    const int cnt = min(kMergeChunk, ns - c * kMergeChunk);
     const float* ms = mo + slot * kMergeChunk * D + d;
-#pragma unroll 4
-    for (int j = 0; j < cnt; ++j) {
-      const int kind = skind[j];
+    // every entry of the slot is read (stale ones past cnt are discarded by
+    // the select), so the loads of later splits need not wait for earlier ones
+#pragma unroll
+    for (int j = 0; j < kMergeChunk; ++j) {
+      const int kind = j < cnt ? skind[slot][j] : 0;
       const float2 oj = *reinterpret_cast<const float2*>(ms + j * D);
       const float lj = sml[slot][j].y;
-      if (kind == 1) {
-        o0 = oj.x;
-        o1 = oj.y;
-        l = lj;
-      } else if (kind == 2) {
-        const float2 cf = scoef[j];
-        l = lse_mix(l, cf.x, lj, cf.y);
-        o0 = lse_mix(o0, cf.x, oj.x, cf.y);
-        o1 = lse_mix(o1, cf.x, oj.y, cf.y);
-      }
+      const float2 cf = scoef[slot][j];
+      const float nl = lse_mix(l, cf.x, lj, cf.y);
+      const float n0 = lse_mix(o0, cf.x, oj.x, cf.y);
+      const float n1 = lse_mix(o1, cf.x, oj.y, cf.y);
+      l = kind == 2 ? nl : (kind == 1 ? lj : l);
+      o0 = kind == 2 ? n0 : (kind == 1 ? oj.x : o0);
+      o1 = kind == 2 ? n1 : (kind == 1 ? oj.y : o1);
     }
-    __syncthreads();  // slot and coefficients free again
-    if (tid == 0 && c + slots < nch) issue(c + slots);
+    mbar_arrive(&consumed[slot]);
   }
   float r0 = 0.0f, r1 = 0.0f;
   if (ok && ns > 0 && !s_bad && l > 0.0f) {
@@ -1597,7 +1630,7 @@ bi_status decode_impl(const AttnArgs& a, cudaStream_t s) {
   }
   // at most 32 KB: under the default dynamic shared memory limit
   const size_t msm = static_cast<size_t>(p.merge_slots) * kMergeChunk * D * sizeof(float);
-  if (launch_pdl(attn_decode_merge_kernel<D>, dim3(a.Hq, a.B), dim3(D / 2), msm, s, p) !=
+  if (launch_pdl(attn_decode_merge_kernel<D>, dim3(a.Hq, a.B), dim3(D / 2 + 32), msm, s, p) !=
       cudaSuccess)
     return BI_ERR_CUDA;
   return BI_OK;
