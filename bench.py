@@ -117,7 +117,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             threading.Thread(target=self._read, daemon=True).start()
         except OSError:
@@ -547,11 +547,13 @@ def main():
     flush = L2Flush(dev)
     stream = torch.cuda.Stream(dev)
 
+    # clocks over every timed region of the device-side measurement
     with ClockSampler(local) as clk:
         inv, inv_step = timed_steps(wl, bi.INVARIANT, args.steps, args.warmup, flush, stream,
                                     barrier)
-    var, var_step = timed_steps(wl, bi.VARIANT, args.steps, args.warmup, flush, stream, barrier)
-    sweep = gemm_m_sweep(wl, flush, stream)
+        var, var_step = timed_steps(wl, bi.VARIANT, args.steps, args.warmup, flush, stream,
+                                    barrier)
+        sweep = gemm_m_sweep(wl, flush, stream)
     status = bi.bi_check_device_errors()
     if status != bi.OK:
         raise RuntimeError("device error during the bench: %s" % bi.bi_status_string(status))
