@@ -104,6 +104,31 @@ def profiled_traffic(kernel):
     return e.get("dram_bytes_per_launch")
 
 
+def fingerprint(dev, rank):
+    """What a result was measured with: device, driver and toolchain, the
+    library's sources, the fixed tile shapes, the seeds and the host."""
+    import invariant_bi_rmsnorm_02_gb300 as bi
+    driver = None
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", str(dev.index), "--query-gpu=driver_version",
+                              "--format=csv,noheader"], capture_output=True, text=True, timeout=20)
+        driver = out.stdout.strip() or None
+    except (OSError, subprocess.SubprocessError):
+        pass
+    csrc = os.path.join(ROOT, "invariant_bi_rmsnorm_02_gb300", "csrc")
+    return {
+        "gpu": torch.cuda.get_device_name(dev), "sm_count":
+            torch.cuda.get_device_properties(dev).multi_processor_count,
+        "driver": driver, "cuda_runtime": torch.version.cuda, "torch": torch.__version__,
+        "libbi": bi.bi_version(), "libbi_sources_sha": source_hash(
+            *sorted(f for f in os.listdir(csrc) if os.path.isfile(os.path.join(csrc, f)))),
+        "gemm_tile": "128x256, k-block 64, tcgen05 kind::f16 128x256x16",
+        "attention_key_tile": 64, "split_size": DEC["S"], "page_size": DEC["page"],
+        "seeds": "workload seeds 100000*rank + 1..11 (rank %d)" % rank,
+        "host_cores": os.cpu_count(),
+    }
+
+
 class ClockSampler:
     """Samples SM clock and throttle reasons with nvidia-smi while running."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
@@ -618,6 +643,7 @@ def main():
                                "gemm_by_m": sweep},
         "gpu_launches": launches,
         "clocks": clk.summary(),
+        "fingerprint": fingerprint(dev, rank),
     }
     if e2e is not None:
         line["e2e"] = e2e
