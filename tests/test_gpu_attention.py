@@ -353,3 +353,24 @@ def test_kv_write_places_rows_in_pages(cuda):
         vc[page, :, p % 16] = vn[i]
     assert same_bytes(kv.k_cache, kc) and same_bytes(kv.v_cache, vc)
     assert bi.bi_check_device_errors() == bi.OK
+
+
+def test_attention_run_to_run(cuda):
+    # the same call twice gives the same bytes (a race between the roles of
+    # a block, or an order that depends on timing, would show up here):
+    # GQA decode over log-uniform lengths and a long causal prefill chunk
+    lens = synth.loguniform_int(24, 1, 9000, 5100).tolist()
+    kv = to_dev(synth.paged_kv(lens, 8, 128, 16, 5101), cuda)
+    q = synth.normal_bf16((24, 32, 128), 5102, device=cuda)
+    d1 = decode(q, kv, 9000, 256)
+    d2 = decode(q, kv, 9000, 256)
+    assert same_bytes(d1[0], d2[0]) and same_bytes(d1[1], d2[1])
+    T, C = 3000, 1000
+    pkv = to_dev(synth.paged_kv([T], 8, 128, 16, 5103), cuda)
+    pq = synth.normal_bf16((C, 32, 128), 5104, device=cuda)
+    cu = torch.tensor([0, C], dtype=torch.int32, device=cuda)
+    st = torch.tensor([T - C], dtype=torch.int32, device=cuda)
+    p1 = prefill(pq, cu, st, pkv, pkv.kv_lens, C, T, 256)
+    p2 = prefill(pq, cu, st, pkv, pkv.kv_lens, C, T, 256)
+    assert same_bytes(p1[0], p2[0]) and same_bytes(p1[1], p2[1])
+    assert bi.bi_check_device_errors() == bi.OK
