@@ -23,7 +23,6 @@ import json
 import sys
 import time
 
-import numpy as np
 import torch
 
 from . import _binding as bi

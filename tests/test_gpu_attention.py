@@ -3,7 +3,6 @@ Parity with the fp64 oracle (2e-3 absolute on the fp32 result; the bf16
 output is that result rounded once), bitwise invariance across batch size,
 batch position, neighbours, KV growth, grid size and prefill chunking, and
 the fixed split-count mode as a negative control."""
-import math
 
 import numpy as np
 import pytest

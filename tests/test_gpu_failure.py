@@ -2,7 +2,6 @@
 out is reported through the device error word, and the context stays
 usable afterwards."""
 import pytest
-import torch
 
 import invariant_bi_rmsnorm_02_gb300 as bi
 import oracle

@@ -3,7 +3,6 @@ memory (an engine that has given all of HBM to its KV-cache pool, a plugin
 whose host framework owns the allocator).  Its scratch is a fixed array inside
 the library instead of a caller workspace.  This file is collected last, so a
 run that stops at the first failure has run every other test before it."""
-import numpy as np
 import pytest
 import torch
 
