@@ -313,7 +313,7 @@ bi_status bi_rope_qkv(const void* qkv, const int32_t* pos, int64_t T, int Hq, in
  * block = F: all gate columns, then all up columns.  block = 128: the layout
  * bi_gemm writes with bi_gemm_swiglu's weight, so that this kernel after
  * bi_gemm gives the bytes of bi_gemm_swiglu.
- * Requirements: F % block == 0, block % 8 == 0.  Errors: as bi_rmsnorm. */
+ * Requirements: F % block == 0, block % 8 == 0, F < 2^31.  Errors: as bi_rmsnorm. */
 bi_status bi_silu_mul(const void* gate_up, int64_t T, int64_t F, int64_t block, void* out,
                       void* stream);
 

@@ -442,7 +442,7 @@ bi_status bi_rope_qkv(const void* qkv, const int32_t* pos, int64_t T, int Hq, in
 bi_status bi_silu_mul(const void* gate_up, int64_t T, int64_t F, int64_t block, void* out,
                       void* stream) {
   if (T < 0 || F <= 0 || block <= 0) return BI_ERR_INVALID_ARG;
-  if (block % 8 != 0 || F % block != 0) return BI_ERR_UNSUPPORTED;
+  if (block % 8 != 0 || F % block != 0 || F >= (int64_t(1) << 31)) return BI_ERR_UNSUPPORTED;
   if (T == 0) return BI_OK;
   if (!gate_up || !out || !aligned16(gate_up) || !aligned16(out)) return BI_ERR_INVALID_ARG;
   return launch_silu_mul(gate_up, T, F, block, out, static_cast<cudaStream_t>(stream));

@@ -147,9 +147,12 @@ __global__ void __launch_bounds__(kThreads) silu_mul_kernel(const uint4* __restr
   const int64_t total = T * vec_f;
   for (int64_t e = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; e < total;
        e += static_cast<int64_t>(gridDim.x) * kThreads) {
-    const int64_t t = e / vec_f, c = e - t * vec_f;
-    const int64_t cb = c / vb;
-    const uint4* src = gu + t * 2 * vec_f + cb * 2 * vb + (c - cb * vb);
+    const int64_t t = e / vec_f;
+    // c, vb < vec_f < 2^31 (16-byte vectors of one row): 32-bit arithmetic;
+    // one block (vb == vec_f) is the stacked-halves layout
+    const int c = static_cast<int>(e - t * vec_f), v = static_cast<int>(vb);
+    const int cb = v == static_cast<int>(vec_f) ? 0 : c / v;
+    const uint4* src = gu + t * 2 * vec_f + static_cast<int64_t>(cb) * 2 * v + (c - cb * v);
     const uint4 gv = __ldcs(src);
     const uint4 uv = __ldcs(src + vb);
     const uint32_t g[4] = {gv.x, gv.y, gv.z, gv.w}, u[4] = {uv.x, uv.y, uv.z, uv.w};
