@@ -647,3 +647,205 @@ def test_decoder_is_causal():
     # and the last token's logits do depend on the first token
     tok2 = [(tok[0] + 1) % cfg.vocab] + tok[1:]
     assert not np.array_equal(forward_logits(w, cfg, tok2)[-1], full[-1])
+
+
+# ------------------------------------------- one decoder layer, pinned by hand
+# The decoder oracle's per-layer body (pre-norm attention block, then the
+# SwiGLU MLP block, each added to the bf16 residual stream) is fixed below by
+# cases that do not reuse its code: a pure-Python forward pass with math.fsum
+# dot products and an independent bf16 rounding, and closed forms that follow
+# when an output projection is zero.
+
+def _bf16_round(v: float) -> float:
+    """Nearest bf16 value of a Python float, ties to even (normal range):
+    math.frexp gives v = m 2^e with 1/2 <= |m| < 1, and Python's round() of
+    the exact m * 256 rounds half to even."""
+    if v == 0.0 or not math.isfinite(v):
+        return v
+    m, e = math.frexp(v)
+    return math.ldexp(round(m * 256.0), e - 8)
+
+
+def _f32(v: float) -> float:
+    import struct
+    return struct.unpack("f", struct.pack("f", v))[0]
+
+
+def _hand_forward(w, cfg, tokens):
+    """Logits of a Llama-style pre-norm decoder whose activations are stored
+    in bf16, with scalar Python loops (fsum dot products, math.exp/cos/sin);
+    shares no code with oracle/decoder.py."""
+    H, Hq, Hkv, D, F = cfg.hidden, cfg.heads, cfg.kv_heads, cfg.head_dim, cfg.ffn
+    G = Hq // Hkv
+    mat = lambda t: t.to(torch.float64).tolist()
+    emb, lm, fn = mat(w.embed), mat(w.lm_head), mat(w.final_norm)
+
+    def norm(x, g):
+        r = math.sqrt(math.fsum(v * v for v in x) / len(x) + cfg.eps)
+        return [_bf16_round(v / r * gi) for v, gi in zip(x, g)]
+
+    def lin(x, W, rnd=True):
+        out = [math.fsum(a * b for a, b in zip(x, row)) for row in W]
+        return [_bf16_round(v) for v in out] if rnd else out
+
+    def add(x, r):   # the residual add: one float32 rounding, then bf16
+        return [_bf16_round(_f32(a + b)) for a, b in zip(x, r)]
+
+    def rope(vec, p):
+        half = D // 2
+        out = list(vec)
+        for i in range(half):
+            ang = p * cfg.rope_theta ** (-2.0 * i / D)
+            c, s = math.cos(ang), math.sin(ang)
+            a, b = vec[i], vec[i + half]
+            out[i], out[i + half] = a * c - b * s, b * c + a * s
+        return [_bf16_round(v) for v in out]
+
+    h = [list(emb[t]) for t in tokens]
+    for layer in range(cfg.layers):
+        wqkv, wo = mat(w.wqkv[layer]), mat(w.wo[layer])
+        wgu, wd = mat(w.wgu[layer]), mat(w.wdown[layer])
+        an, mn = mat(w.attn_norm[layer]), mat(w.mlp_norm[layer])
+        qs, ks, vs = [], [], []
+        for p, x in enumerate(h):
+            qkv = lin(norm(x, an), wqkv)
+            qs.append([rope(qkv[j * D:(j + 1) * D], p) for j in range(Hq)])
+            ks.append([rope(qkv[(Hq + j) * D:(Hq + j + 1) * D], p) for j in range(Hkv)])
+            vs.append([qkv[(Hq + Hkv + j) * D:(Hq + Hkv + j + 1) * D] for j in range(Hkv)])
+        new_h = []
+        for p, x in enumerate(h):
+            att = []
+            for j in range(Hq):
+                kvh = j // G
+                sc = [math.fsum(a * b for a, b in zip(qs[p][j], ks[t][kvh])) / math.sqrt(D)
+                      for t in range(p + 1)]
+                mx = max(sc)
+                e = [math.exp(s - mx) for s in sc]
+                z = math.fsum(e)
+                att += [_bf16_round(math.fsum(e[t] * vs[t][kvh][d] for t in range(p + 1)) / z)
+                        for d in range(D)]
+            h1 = add(lin(att, wo), x)
+            gu = lin(norm(h1, mn), wgu)
+            act = []
+            for f in range(F):
+                blk, i = divmod(f, 128)
+                g, u = gu[256 * blk + i], gu[256 * blk + 128 + i]
+                act.append(_bf16_round(g / (1.0 + math.exp(-g)) * u))
+            new_h.append(add(lin(act, wd), h1))
+        h = new_h
+    return np.array([lin(norm(x, fn), lm, rnd=False) for x in h])
+
+
+def _small_decoder(layers, seed=5):
+    import dataclasses
+    from invariant_bi_rmsnorm_02_gb300.decoder import TINY, DecoderWeights
+    # two gate/up blocks of 128 features, two query heads sharing one KV head
+    cfg = dataclasses.replace(TINY, layers=layers, hidden=64, heads=2, kv_heads=1,
+                              head_dim=32, ffn=256, vocab=40)
+    w = DecoderWeights(cfg, seed, "cpu")
+    # non-trivial norm weights, so that each norm's weight is read
+    for k, lst in enumerate((w.attn_norm, w.mlp_norm)):
+        for layer in range(layers):
+            lst[layer] = synth.normal_bf16((cfg.hidden,), 9150 + 10 * layer + k, std=0.2,
+                                           mean=1.0)
+    w.final_norm = synth.normal_bf16((cfg.hidden,), 9149, std=0.2, mean=1.0)
+    return cfg, w
+
+
+@pytest.mark.parametrize("layers,tokens", [(1, [7]), (1, [3, 39, 3]), (2, [0, 17, 17, 5, 21])])
+def test_decoder_layer_matches_a_hand_computed_forward_pass(layers, tokens):
+    from oracle.decoder import forward_logits
+    cfg, w = _small_decoder(layers)
+    got = forward_logits(w, cfg, tokens)
+    want = _hand_forward(w, cfg, tokens)
+    # the two differ only in fp64 summation order (fsum is exactly rounded),
+    # far below a bf16 step of any stored activation
+    np.testing.assert_allclose(got, want, rtol=1e-9, atol=1e-12)
+
+
+def test_decoder_hand_forward_detects_a_dropped_term():
+    """The hand pass is sensitive to every branch: zeroing the O projection
+    or the down projection, or one norm weight entry, moves the logits."""
+    cfg, w = _small_decoder(1)
+    tok = [3, 39, 3]
+    base = _hand_forward(w, cfg, tok)
+    for attr in ("wo", "wdown"):
+        saved = getattr(w, attr)[0]
+        getattr(w, attr)[0] = torch.zeros_like(saved)
+        assert np.abs(_hand_forward(w, cfg, tok) - base).max() > 1e-4, attr
+        getattr(w, attr)[0] = saved
+
+
+def _zero_layers_closed_form(w, cfg, tok):
+    e = f64(w.embed)[tok]
+    y = e / np.sqrt((e * e).mean(axis=1, keepdims=True) + cfg.eps) * f64(w.final_norm)
+    y = f64(torch.from_numpy(y).to(torch.bfloat16))
+    return y @ f64(w.lm_head).T
+
+
+def test_decoder_layers_with_zero_output_projections_are_the_identity():
+    """W_o = 0 and W_down = 0: both branches add exact zeros to the residual
+    stream, so every layer passes h through and the logits are those of the
+    embedding's final norm and LM head alone."""
+    from oracle.decoder import forward_logits
+    cfg, w = _tiny_weights(2)
+    for layer in range(cfg.layers):
+        w.wo[layer] = torch.zeros_like(w.wo[layer])
+        w.wdown[layer] = torch.zeros_like(w.wdown[layer])
+    tok = list(np.random.default_rng(9143).integers(0, cfg.vocab, 21))
+    got = forward_logits(w, cfg, tok)
+    np.testing.assert_allclose(got, _zero_layers_closed_form(w, cfg, tok), rtol=1e-12,
+                               atol=1e-12)
+
+
+def test_decoder_attention_block_alone():
+    """W_down = 0: one layer is h1 = bf16(h0 + bf16(bf16(attn) W_o^T)) with attn
+    the causal attention of the rotated q, k (bf16) over the bf16 v; over 37
+    tokens (three pages of the private cache)."""
+    from oracle.decoder import forward_logits, to_bf16
+    cfg, w = _tiny_weights(1)
+    w.wdown[0] = torch.zeros_like(w.wdown[0])
+    tok = list(np.random.default_rng(9144).integers(0, cfg.vocab, 37))
+    T, Hq, Hkv, D = len(tok), cfg.heads, cfg.kv_heads, cfg.head_dim
+    h0 = oracle.gather_rows(w.embed, tok)
+    y = to_bf16(oracle.rmsnorm(h0, w.attn_norm[0], cfg.eps))
+    q, k, v = oracle.rope_qkv(to_bf16(oracle.gemm(y, w.wqkv[0])), np.arange(T), Hq, Hkv, D,
+                              cfg.rope_theta)
+    # attention directly in float64 from the widened bf16 operands
+    qf = f64(torch.from_numpy(to_bf16(q).view(np.int16)).view(torch.bfloat16))
+    kf = f64(torch.from_numpy(to_bf16(k).view(np.int16)).view(torch.bfloat16))
+    vf = f64(torch.from_numpy(to_bf16(v).view(np.int16)).view(torch.bfloat16))
+    att = np.zeros((T, Hq, D))
+    G = Hq // Hkv
+    for hh in range(Hq):
+        s = qf[:, hh] @ kf[:, hh // G].T / math.sqrt(D)
+        s[np.triu_indices(T, 1)] = -np.inf
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        att[:, hh] = (p / p.sum(axis=1, keepdims=True)) @ vf[:, hh // G]
+    o = to_bf16(oracle.gemm(to_bf16(att).reshape(T, Hq * D), w.wo[0]))
+    h1 = oracle.add_bf16(o, h0)
+    yf = to_bf16(oracle.rmsnorm(h1, w.final_norm, cfg.eps))
+    want = oracle.gemm(yf, w.lm_head)
+    np.testing.assert_allclose(forward_logits(w, cfg, tok), want, rtol=1e-9, atol=1e-12)
+
+
+def test_decoder_mlp_block_alone():
+    """W_o = 0: one layer is h1 = bf16(h0 + bf16(act W_down^T)) with act =
+    bf16(silu(g) u), g and u the bf16 gate and up halves of the projection
+    of RMSNorm(h0); attention contributes nothing."""
+    from oracle.decoder import forward_logits, to_bf16
+    cfg, w = _tiny_weights(1)
+    w.wo[0] = torch.zeros_like(w.wo[0])
+    tok = list(np.random.default_rng(9145).integers(0, cfg.vocab, 19))
+    h0 = oracle.gather_rows(w.embed, tok)
+    y = to_bf16(oracle.rmsnorm(h0, w.mlp_norm[0], cfg.eps))
+    gu = f64(torch.from_numpy(to_bf16(oracle.gemm(y, w.wgu[0])).view(np.int16))
+             .view(torch.bfloat16))
+    F = cfg.ffn
+    blocks = gu.reshape(len(tok), F // 128, 2, 128)
+    g, u = blocks[:, :, 0].reshape(len(tok), F), blocks[:, :, 1].reshape(len(tok), F)
+    act = to_bf16(g / (1.0 + np.exp(-g)) * u)
+    h1 = oracle.add_bf16(to_bf16(oracle.gemm(act, w.wdown[0])), h0)
+    yf = to_bf16(oracle.rmsnorm(h1, w.final_norm, cfg.eps))
+    want = oracle.gemm(yf, w.lm_head)
+    np.testing.assert_allclose(forward_logits(w, cfg, tok), want, rtol=1e-9, atol=1e-12)
