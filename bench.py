@@ -259,10 +259,13 @@ class Workload:
         return sum(n for _, _, n in self.ops(self.bi.INVARIANT))
 
     # algorithmic work per launch
-    def work(self):
+    def work(self, steps):
+        """Algorithmic bytes / flops of each op of one step; the decode's at the
+        mean KV length of the timed steps (step s, counted from 0, attends
+        over lens0 + s + 1 keys after its KV write)."""
         d = DEC
-        lens = self.lens.double()
-        kv_bytes = float(lens.sum()) * d["Hkv"] * d["D"] * 2 * 2  # at the step's mean length
+        lens = self.lens0.double() + (steps + 1) / 2.0
+        kv_bytes = float(lens.sum()) * d["Hkv"] * d["D"] * 2 * 2
         qo = d["B"] * d["Hq"] * d["D"] * 2 * 2
         T0, C = PRE["start"], PRE["chunk"]
         causal_keys = sum(p + 1 for p in range(T0, T0 + C))
@@ -420,37 +423,76 @@ def e2e_steps(wl, steps, warmup, stream):
 def oracle_gemm_sample(rows, seed=0):
     """The oracle's GEMM rows of both projections on a row sample; returns
     (flops, seconds, threads)."""
-    import numpy as np
     import oracle
     from invariant_bi_rmsnorm_02_gb300 import synth
     x = synth.normal_bf16((rows, H), seed + 1)
-    w = synth.normal_bf16((H,), seed + 2, std=0.1, mean=1.0)
     Wq = synth.normal_bf16((N_QKV, H), seed + 3, std=0.02)
     Wu = synth.normal_bf16((N_UP, H), seed + 4, std=0.02)
-    y = oracle.rmsnorm(x, w, EPS)
-    yb = torch.from_numpy(y).to(torch.bfloat16)
     t = time.perf_counter()
-    oracle.gemm(yb, Wq)
-    oracle.gemm(yb, Wu)
+    oracle.gemm(x, Wq)
+    oracle.gemm(x, Wu)
     dt = time.perf_counter() - t
     flops = 2.0 * rows * H * (N_QKV + N_UP)
     return flops, dt, oracle.default_threads()
 
 
-def cpu_baseline(min_seconds=10.0):
+def _repeat(fn, min_seconds, max_reps):
+    """Runs fn until min_seconds have passed (at least once, at most max_reps
+    times); returns (reps, total seconds)."""
+    reps, tot = 0, 0.0
+    while reps < max_reps and (reps == 0 or tot < min_seconds):
+        t = time.perf_counter()
+        fn()
+        tot += time.perf_counter() - t
+        reps += 1
+    return reps, tot
+
+
+def cpu_baseline(wl, per_op_seconds=4.0):
+    """The fp64 oracle on the host cores, op by op, on the step's own inputs
+    (copied to the host): RMSNorm of all 8192 rows, the two GEMMs on a row
+    sample, the decode of all 64 requests and the prefill chunk on a sample of
+    its query tokens.  Each op is repeated until about per_op_seconds have
+    passed; the headline value is the GEMM's TFLOP/s (the bench's metric)."""
     import oracle
     oracle.build()
-    rows = max(1, oracle.default_threads())
-    f, dt, th = oracle_gemm_sample(rows)
-    reps, tot_f, tot_t = 1, f, dt
-    while tot_t < min_seconds and reps < 8:
-        f, dt, _ = oracle_gemm_sample(rows, seed=reps)
-        tot_f += f
-        tot_t += dt
-        reps += 1
-    return {"value": tot_f / tot_t / 1e12, "unit": "TFLOP/s", "cores": th, "kind": "oracle",
-            "sample": "%d x %d rows (one per oracle thread) of the QKV and MLP-up GEMMs "
-                      "(K=4096, N=6144+14336), fp64, %.1f s" % (reps, rows, tot_t)}
+    th = oracle.default_threads()
+    d = DEC
+    x, w = wl.x.cpu(), wl.w.cpu()
+    ops = {}
+    reps, t = _repeat(lambda: oracle.rmsnorm(x, w, EPS), per_op_seconds, 20)
+    ops["rmsnorm"] = {"s_per_call": t / reps, "gbs": (2 * M * H * 2 + H * 2) / (t / reps) / 1e9,
+                      "sample": "all %d rows" % M}
+    rows = 4 * th
+    A, Wq, Wu = wl.x[:rows].cpu(), wl.Wqkv.cpu(), wl.Wup.cpu()
+    reps, t = _repeat(lambda: (oracle.gemm(A, Wq), oracle.gemm(A, Wu)), per_op_seconds, 20)
+    gf = 2.0 * rows * H * (N_QKV + N_UP)
+    ops["gemm"] = {"s_per_call": t / reps, "tflops": gf / (t / reps) / 1e12,
+                   "sample": "%d of %d rows, QKV + MLP-up" % (rows, M)}
+    q, kc, vc = wl.q.cpu(), wl.kv.k_cache.cpu(), wl.kv.v_cache.cpu()
+    bt, lens = wl.kv.block_table.cpu(), wl.lens0.cpu()
+    reps, t = _repeat(lambda: oracle.decode_attention(q, kc, vc, bt, lens, d["D"] ** -0.5),
+                      per_op_seconds, 20)
+    kvb = float(lens.double().sum()) * d["Hkv"] * d["D"] * 4
+    ops["decode"] = {"s_per_call": t / reps, "gbs": kvb / (t / reps) / 1e9,
+                     "sample": "all %d requests" % d["B"]}
+    T0, C = PRE["start"], PRE["chunk"]
+    idx = torch.arange(0, C, C // 32)
+    pq, pkc, pvc = wl.pq.cpu()[idx], wl.pkv.k_cache.cpu(), wl.pkv.v_cache.cpu()
+    pbt = wl.pkv.block_table.cpu()
+    pos = (idx + T0).to(torch.int32)
+    reps, t = _repeat(lambda: oracle.prefill_attention(pq, 0, pos, pkc, pvc, pbt,
+                                                       d["D"] ** -0.5), per_op_seconds, 20)
+    pf = 4.0 * d["Hq"] * d["D"] * float((pos + 1).double().sum())
+    ops["prefill"] = {"s_per_call": t / reps, "tflops": pf / (t / reps) / 1e12,
+                      "sample": "%d of the %d chunk tokens" % (len(idx), C)}
+    return {"value": ops["gemm"]["tflops"], "unit": "TFLOP/s", "cores": th, "kind": "oracle",
+            "sample": "fp64 oracle on the step's inputs: RMSNorm %s, GEMM %s, decode %s, "
+                      "prefill %s; each op repeated ~%.0f s" % (
+                          ops["rmsnorm"]["sample"], ops["gemm"]["sample"],
+                          ops["decode"]["sample"], ops["prefill"]["sample"], per_op_seconds),
+            "per_op": {k: {kk: vv for kk, vv in v.items() if kk != "sample"}
+                       for k, v in ops.items()}}
 
 
 def run_reference(args):
@@ -518,6 +560,132 @@ def gemm_m_sweep(wl, flush, stream, reps=3):
     return out
 
 
+def _median_ms(fn, stream, flush=None, reps=3):
+    """Median CUDA-event time of fn on ``stream`` (L2 flushed before each rep
+    when ``flush`` is given; one untimed rep first)."""
+    ts = []
+    with torch.cuda.stream(stream):
+        for r in range(reps + 1):
+            if flush is not None:
+                flush.zero_()
+            torch.cuda._sleep(HOST_LEAD_CYCLES)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            stream.synchronize()
+            if r:
+                ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def tiny_layer(dev, stream, reps=20):
+    """The tiny-layer workload (RMSNorm over 256, GEMM 256->512, decode with
+    4/2 heads of 64 over 8 requests of KV 1..512, page 16, split 64) at batch
+    1 and 8: microseconds per op and for the three back to back (launch-latency
+    bound: no roofline fraction is meaningful at this size)."""
+    import invariant_bi_rmsnorm_02_gb300 as bi
+    from invariant_bi_rmsnorm_02_gb300 import synth
+    c = synth.TINY
+    x = synth.normal_bf16((c["B"], c["H"]), 1001, device=dev)
+    w = synth.normal_bf16((c["H"],), 1002, std=0.1, mean=1.0, device=dev)
+    W = synth.normal_bf16((c["N"], c["H"]), 1003, std=0.02, device=dev)
+    lens = synth.uniform_int(c["B"], 1, c["max_len"], 1004).tolist()
+    kv = synth.paged_kv(lens, c["Hkv"], c["D"], c["page"], 1005, device=dev)
+    q = synth.normal_bf16((c["B"], c["Hq"], c["D"]), 1006, device=dev)
+    y, C, out = torch.empty_like(x), torch.empty(c["B"], c["N"], dtype=torch.bfloat16,
+                                                 device=dev), torch.empty_like(q)
+    ws = torch.empty(bi.bi_attn_decode_workspace_size(c["B"], c["Hq"], c["Hkv"], c["D"],
+                                                      c["max_len"], c["split"]) // 4 + 4,
+                     dtype=torch.float32, device=dev)
+    res = {}
+    for m in (1, c["B"]):
+        ops = [lambda: bi.bi_rmsnorm(x[:m], w, y[:m], c["eps"]),
+               lambda: bi.bi_gemm(y[:m], W, C[:m]),
+               lambda: bi.bi_attn_decode(q[:m], kv.k_cache, kv.v_cache, kv.block_table[:m],
+                                         kv.kv_lens[:m], out[:m], max_kv_len=c["max_len"],
+                                         split_size=c["split"], sm_scale=c["D"] ** -0.5,
+                                         workspace=ws)]
+        per = [1000.0 * _median_ms(f, stream, reps=reps) for f in ops]
+        layer = 1000.0 * _median_ms(lambda: [f() for f in ops], stream, reps=reps)
+        res["b%d" % m] = {"rmsnorm_us": per[0], "gemm_us": per[1], "decode_us": per[2],
+                          "layer_us": layer}
+    return res
+
+
+def prefill_schedules(dev, stream, flush):
+    """The chunked-prefill workload: one 8192-token prompt (32/8 heads, D=128,
+    split 256) as chunks of 512, 2048 and 8192 and as token-by-token decode;
+    milliseconds for the whole prompt's attention under each schedule (L2
+    flushed before the first call of each) and TFLOP/s of the causal work."""
+    import invariant_bi_rmsnorm_02_gb300 as bi
+    from invariant_bi_rmsnorm_02_gb300 import synth
+    c = synth.CHUNKED_PREFILL
+    T, d = c["T"], DEC
+    kv = synth.paged_kv([T], c["Hkv"], c["D"], c["page"], 4001, device=dev)
+    q = synth.normal_bf16((T, c["Hq"], c["D"]), 4002, device=dev)
+    out = torch.empty_like(q)
+    scale = c["D"] ** -0.5
+    flops = 4.0 * c["Hq"] * c["D"] * T * (T + 1) / 2.0
+    res = {}
+    for chunk in c["chunks"]:
+        cus = [torch.tensor([0, chunk], dtype=torch.int32, device=dev)]
+        starts = [torch.tensor([a], dtype=torch.int32, device=dev) for a in range(0, T, chunk)]
+        kls = [torch.tensor([a + chunk], dtype=torch.int32, device=dev)
+               for a in range(0, T, chunk)]
+
+        def run(chunk=chunk, starts=starts, kls=kls):
+            for i, a in enumerate(range(0, T, chunk)):
+                bi.bi_attn_prefill_chunk(q[a:a + chunk], cus[0], starts[i], kv.k_cache,
+                                         kv.v_cache, kv.block_table, kls[i],
+                                         out[a:a + chunk], None, max_q_len=chunk,
+                                         max_kv_len=a + chunk, split_size=c["split"],
+                                         sm_scale=scale)
+        ms = _median_ms(run, stream, flush, reps=2)
+        res["chunk%d" % chunk] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+                                  "calls": T // chunk}
+    ws = torch.empty(bi.bi_attn_decode_workspace_size(1, c["Hq"], c["Hkv"], c["D"], T,
+                                                      c["split"]) // 4 + 4,
+                     dtype=torch.float32, device=dev)
+    kl = torch.arange(1, T + 1, dtype=torch.int32, device=dev)
+
+    def tokens():
+        for p in range(T):
+            bi.bi_attn_decode(q[p:p + 1], kv.k_cache, kv.v_cache, kv.block_table,
+                              kl[p:p + 1], out[p:p + 1], max_kv_len=p + 1,
+                              split_size=c["split"], sm_scale=scale, workspace=ws)
+    ms = _median_ms(tokens, stream, flush, reps=1)
+    res["token_by_token"] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12, "calls": T}
+    return res
+
+
+def rmsnorm_beyond_l2(dev, stream, flush, peaks, rows=32768):
+    """RMSNorm at 32768 x 4096: input and output (268 MB each) both exceed
+    the 129 MB L2, so the output's bytes are written to HBM inside the
+    timed region, not left dirty in L2."""
+    import invariant_bi_rmsnorm_02_gb300 as bi
+    from invariant_bi_rmsnorm_02_gb300 import synth
+    x = synth.normal_bf16((rows, H), 5001, device=dev)
+    w = synth.normal_bf16((H,), 5002, std=0.1, mean=1.0, device=dev)
+    y = torch.empty_like(x)
+    ms = _median_ms(lambda: bi.bi_rmsnorm(x, w, y, EPS), stream, flush, reps=5)
+    gbs = (2 * rows * H * 2 + H * 2) / (ms * 1e-3) / 1e9
+    return {"rows": rows, "us": 1000.0 * ms, "gbs": gbs, "frac_hbm": gbs / peaks["hbm"]}
+
+
+def sig(v, n=3):
+    """Floats rounded to n significant digits, recursively (a short line)."""
+    if isinstance(v, float):
+        return v if (v == 0.0 or v != v or v in (float("inf"), float("-inf"))) else float(
+            "%.*g" % (n, v))
+    if isinstance(v, dict):
+        return {k: sig(x, n) for k, x in v.items()}
+    if isinstance(v, (list, tuple)):
+        return [sig(x, n) for x in v]
+    return v
+
+
 # ----------------------------------------------------------------- main arm
 def max_over_ranks(vals, dist=None, device="cpu"):
     """The max over ranks of each timed quantity (every rank gets the result;
@@ -542,6 +710,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the tiny-layer, prefill-schedule and large-RMSNorm figures")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -564,7 +734,6 @@ def main():
 
     import invariant_bi_rmsnorm_02_gb300 as bi
     bi.load()
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     peaks = load_peaks()
     reserve = 2 * (args.warmup + args.steps) + 8
     wl = Workload(dev, rank, reserve)
@@ -578,10 +747,15 @@ def main():
         var, var_step = timed_steps(wl, bi.VARIANT, args.steps, args.warmup, flush, stream,
                                     barrier)
         sweep = gemm_m_sweep(wl, flush, stream)
+        extra = {}
+        if not args.no_extras:
+            extra["tiny_layer"] = tiny_layer(dev, stream)
+            extra["prefill_8192"] = prefill_schedules(dev, stream, flush)
+            extra["rmsnorm_32768"] = rmsnorm_beyond_l2(dev, stream, flush, peaks)
     status = bi.bi_check_device_errors()
     if status != bi.OK:
         raise RuntimeError("device error during the bench: %s" % bi.bi_status_string(status))
-    work = wl.work()
+    work = wl.work(args.steps)
     gemm_flops = work["gemm_qkv"]["flops"] + work["gemm_up"]["flops"]
     gemm_ms = inv["gemm_qkv"] + inv["gemm_up"]
     # max over ranks of the timed quantities
@@ -592,40 +766,45 @@ def main():
     if not args.no_e2e:
         e2e_ms, h2d, d2h = e2e_steps(wl, max(3, args.steps // 2), args.warmup, stream)
         (e2e_ms_max,) = max_over_ranks([e2e_ms], dist, dev)
-        e2e = {"value": whole_job_tflops(world, gemm_flops, e2e_ms_max), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_ms_max}
+        e2e = {"value": round(whole_job_tflops(world, gemm_flops, e2e_ms_max), 1),
+               "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_ms_max, 4)}
 
+    # kernels are timed one at a time after an L2 flush, at the clock the
+    # chip runs a lone kernel at: the burst tensor peak is their ceiling
     comps = {}
     for n in inv:
         wk = work[n]
-        c = {"ms": inv[n], "ms_variant": var[n], "slowdown": inv[n] / var[n] - 1.0}
+        c = {"us": 1000.0 * inv[n], "us_var": 1000.0 * var[n], "slow": inv[n] / var[n] - 1.0}
         if "flops" in wk and n in ("gemm_qkv", "gemm_up", "prefill"):
             c["tflops"] = wk["flops"] / (inv[n] * 1e-3) / 1e12
-            c["frac_of_bf16_peak"] = c["tflops"] / peaks["bf16_sust"]
-        if "bytes" in wk:
+            c["frac_bf16"] = c["tflops"] / peaks["bf16"]
+        elif "bytes" in wk:
             c["gbs"] = wk["bytes"] / (inv[n] * 1e-3) / 1e9
-            c["frac_of_hbm_peak"] = c["gbs"] / peaks["hbm"]
+            c["frac_hbm"] = c["gbs"] / peaks["hbm"]
         comps[n] = c
     dom = max(inv, key=lambda n: inv[n])
     if dom in ("gemm_qkv", "gemm_up"):
         kname, bound, unit = "gemm_tc_kernel", "tensor", "TFLOP/s"
-        achieved, peak = comps[dom]["tflops"], peaks["bf16_sust"]
+        achieved, peak = comps[dom]["tflops"], peaks["bf16"]
     elif dom == "prefill":
         kname, bound, unit = "attn_prefill_kernel", "tensor", "TFLOP/s"
-        achieved, peak = comps[dom]["tflops"], peaks["bf16_sust"]
+        achieved, peak = comps[dom]["tflops"], peaks["bf16"]
     else:
-        kname = {"rmsnorm": "rmsnorm_row_kernel", "decode": "attn_decode_split_kernel"}.get(dom, dom)
+        kname = {"rmsnorm": "rmsnorm_row_kernel",
+                 "decode": "attn_decode_split_kernel"}.get(dom, dom)
         bound, unit, achieved, peak = "hbm", "GB/s", comps[dom]["gbs"], peaks["hbm"]
     traffic = profiled_traffic(kname) if kname in KERNEL_SOURCES else None
-    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": traffic, "kernel": kname, "op": dom,
-                "peak_source": peaks["src"] + (" sustained bf16" if unit == "TFLOP/s" else " HBM copy")}
+    roofline = {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+                "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kname,
+                "op": dom, "peak_source": peaks["src"] + (
+                    " burst bf16 (cuBLAS, kernel timed alone)" if unit == "TFLOP/s"
+                    else " HBM copy")}
 
     launches = wl.launches() * args.steps
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_max,
+        "metric": METRIC, "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms_max, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, N(0,1) K/V/Q)",
         "config": {"workload": WORKLOAD, "M": M, "hidden": H, "n_qkv": N_QKV, "n_up": N_UP,
@@ -634,20 +813,28 @@ def main():
                    "l2": "flushed before every kernel (256 MB write, then 256 MB read of another "
                          "buffer); step time = sum of the kernels' times",
                    "parallelism": "replicas (dp%d, no collective on the data path)" % world},
-        "roofline": roofline,
-        "components": comps,
-        "invariant_slowdown": {"step": inv_step / var_step - 1.0,
-                               "gemm": gemm_ms / (var["gemm_qkv"] + var["gemm_up"]) - 1.0,
-                               "ms_per_step_variant": var_step,
-                               "gemm_by_m": sweep},
+        "fingerprint": fingerprint(dev, rank),
         "gpu_launches": launches,
         "clocks": clk.summary(),
-        "fingerprint": fingerprint(dev, rank),
+        "roofline": roofline,
     }
     if e2e is not None:
         line["e2e"] = e2e
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline()
+        line["cpu_baseline"] = sig(cpu_baseline(wl))
+    # the per-op figures last and short, so the end of the line carries them
+    line["extra"] = sig(extra)
+    line["components"] = sig(comps)
+    line["invariant_slowdown"] = sig({
+        "step": inv_step / var_step - 1.0,
+        "gemm": gemm_ms / (var["gemm_qkv"] + var["gemm_up"]) - 1.0,
+        "ms_per_step_variant": var_step,
+        "gemm_by_m_us": {str(m): [1000.0 * r["qkv"]["ms"], 1000.0 * r["qkv"]["ms_variant"],
+                                  1000.0 * r["up"]["ms"], 1000.0 * r["up"]["ms_variant"]]
+                         for m, r in sweep.items()},
+        "gemm_by_m_cols": "qkv inv, qkv var, up inv, up var (us)",
+        "gemm_worst_over_m": max(r[k]["slowdown"] for r in sweep.values()
+                                  for k in ("qkv", "up"))})
     if rank == 0:
         print(json.dumps(line))
     if dist is not None:

@@ -231,6 +231,9 @@ size_t bi_attn_decode_workspace_size(int B, int Hq, int Hkv, int D, int max_kv_l
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture begins.
+ * The looked-up address is kept for the life of the process: after a
+ * cudaDeviceReset of that device it is stale, so do not call this entry
+ * point again on a device that has been reset.
  * All calls share the array: calls whose kernels overlap on the GPU race with
  * each other, so order them (e.g. issue them on one stream).
  * Errors: as bi_attn_decode, plus BI_ERR_WORKSPACE for the size limit. */

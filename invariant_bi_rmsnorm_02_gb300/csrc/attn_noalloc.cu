@@ -16,7 +16,9 @@
 // (on the host it names a stand-in object), so the device address is looked
 // up with cudaGetSymbolAddress, once per device, the first time the entry
 // point runs on that device, with that device current.  That first call
-// should therefore happen before any stream capture begins.
+// should therefore happen before any stream capture begins.  The address is
+// kept for the life of the process; a cudaDeviceReset of the device makes it
+// stale, so the entry point must not be used on a device after a reset.
 //
 // All calls share the one array and it keeps whatever the last call left
 // there.  Nothing in it needs to start at zero: every partial result the

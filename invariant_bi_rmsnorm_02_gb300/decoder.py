@@ -219,6 +219,11 @@ class Decoder:
         self.max_graphs = max_graphs
         self.graphs, self.seen = {}, set()
         self.graph_replays = 0
+        # when a list, eager steps append (layer, name, copy) of every stored
+        # activation: the residual stream, each norm's output, q/k/v, the
+        # attention output, the projections and the logits (-1: outside the
+        # layers); for checking a step stage by stage
+        self.capture = None
         if self.use_graphs:
             # the decode workspace at its largest, so that no captured step
             # ever sees it move
@@ -320,6 +325,8 @@ class Decoder:
         lengths."""
         c, w, mode = self.cfg, self.w, self.mode
         (tok, pos, row_seq, table, kv_lens, cu_q, q_start, rows, temp, seed, counter) = views
+        keep = self.capture is not None and not torch.cuda.is_current_stream_capturing()
+        cap = self._keep if keep else (lambda *a: None)
         h, y = self.h[:T], self.y[:T]
         bi.bi_gather_rows(w.embed, tok, h)
         bi.bi_rmsnorm(h, w.attn_norm[0], y, c.eps, mode, self._ws_norm(T))
@@ -327,10 +334,16 @@ class Decoder:
         for layer in range(c.layers):
             if layer:
                 bi.bi_add_rmsnorm(delta, h, w.attn_norm[layer], y, c.eps, mode, self._ws_norm(T))
+            cap(layer, "h", h)
+            cap(layer, "y_attn", y)
             qkv = self.qkv[:T]
             self._gemm(y, w.wqkv[layer], qkv)
             q, k, v = self.q[:T], self.k[:T], self.v[:T]
             bi.bi_rope_qkv(qkv, pos, c.heads, c.kv_heads, c.head_dim, c.rope_theta, q, k, v)
+            cap(layer, "qkv", qkv)
+            cap(layer, "q", q)
+            cap(layer, "k", k)
+            cap(layer, "v", v)
             kc, vc = self.kv[layer, 0], self.kv[layer, 1]
             bi.bi_kv_write(k, v, row_seq, pos, kc, vc, table)
             att = self.att[:T]
@@ -346,16 +359,30 @@ class Decoder:
                                          max_q_len=max_q,
                                          max_kv_len=kv_max, split_size=c.split_size,
                                          sm_scale=self.sm_scale, mode=mode)
+            cap(layer, "att", att)
             o = self.o[:T]
             self._gemm(att.view(T, c.heads * c.head_dim), w.wo[layer], o)
+            cap(layer, "o", o)
             bi.bi_add_rmsnorm(o, h, w.mlp_norm[layer], y, c.eps, mode, self._ws_norm(T))
+            cap(layer, "h_mid", h)
+            cap(layer, "y_mlp", y)
             act = self.act[:T]
             self._gemm_swiglu(y, w.wgu[layer], act)
+            if T < SWIGLU_FUSE_MIN_ROWS:
+                cap(layer, "gate_up", self.gu[:T])
+            cap(layer, "act", act)
             self._gemm(act, w.wdown[layer], delta)
+            cap(layer, "delta", delta)
         bi.bi_add_rmsnorm(delta, h, w.final_norm, y, c.eps, mode, self._ws_norm(T))
+        cap(-1, "h", h)
+        cap(-1, "y_final", y)
         if n_s == 0:
             return
         ys, logits = self.ys[:n_s], self.logits[:n_s]
         bi.bi_gather_rows(y, rows, ys)
         self._gemm(ys, w.lm_head, logits)
+        cap(-1, "logits", logits)
         bi.bi_sample(logits, temp, seed, counter, self.tokens_out[:n_s])
+
+    def _keep(self, layer, name, t):
+        self.capture.append((layer, name, t.clone()))
