@@ -30,9 +30,9 @@
 // (movmatrix).  A decode row group (the G query heads of one kv head) fills
 // one 8-wide n-tile, so padding costs at most half of an n-tile.  Scores are
 // scaled by sm_scale*log2(e) and exponentiated with ex2.approx; P is split into a
-// bf16 high part and a bf16 low part (P - hi), both multiplied with V, so the
-// probabilities keep ~16 significant bits.  Column max / sum use a fixed
-// shuffle tree.  Explicit __fmul_rn/__fadd_rn keep the compiler from
+// bf16 high part and a bf16 low part (P - hi), both taken by truncation and
+// both multiplied with V, so the probabilities keep 16 significant bits.
+// Column max / sum use a fixed shuffle tree.  Explicit __fmul_rn/__fadd_rn keep the compiler from
 // contracting differently in the two kernels.
 //
 // K/V staging: each 16-token page of one kv head is a contiguous [16][D]
@@ -149,6 +149,19 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[NQ][D / 16][2],
     }
 }
 
+// P = hi + lo: the probabilities of keys k, k+1 as two bf16 pairs (key k in
+// the low half).  hi is p with its low 16 bits cleared (bf16 by truncation),
+// lo the exact remainder p - hi truncated the same way, so hi + lo keeps 16
+// significant bits of p (|p - hi - lo| < 2^-14 p) with no conversion
+// instruction; decode and prefill split every probability with this function.
+__device__ __forceinline__ void split_p_bf16(float p0, float p1, uint32_t& hp, uint32_t& lp) {
+  const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+  hp = __byte_perm(b0, b1, 0x7632);
+  const float r0 = __fsub_rn(p0, __uint_as_float(b0 & 0xffff0000u));
+  const float r1 = __fsub_rn(p1, __uint_as_float(b1 & 0xffff0000u));
+  lp = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+}
+
 // The running reference maximum of a row moves only when a tile's maximum
 // exceeds it by more than this many powers of two (and on the first tile
 // with a visible key); otherwise the tile's probabilities are taken against
@@ -226,14 +239,16 @@ __device__ __forceinline__ void tile_step(SplitState<D, NQ>& st,
         alpha[nq][cc] = exp2_sfu(__fsub_rn(m_in, t));
       }
     }
+    // masked keys hold -inf, and 2^(-inf - base) = +0 for any finite base
+    const float mb[2] = {mnew[0] == -CUDART_INF_F ? 0.0f : mnew[0],
+                         mnew[1] == -CUDART_INF_F ? 0.0f : mnew[1]};
     float cs[2] = {0.0f, 0.0f};
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int cc = c & 1;
-        const float x = s[mt][nq][c];
-        const float pv = x == -CUDART_INF_F ? 0.0f : exp2_sfu(__fsub_rn(x, mnew[cc]));
+        const float pv = exp2_sfu(__fsub_rn(s[mt][nq][c], mb[cc]));
         s[mt][nq][c] = pv;
         cs[cc] = __fadd_rn(cs[cc], pv);
       }
@@ -258,14 +273,8 @@ __device__ __forceinline__ void tile_step(SplitState<D, NQ>& st,
     for (int nq = 0; nq < NQ; ++nq)
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        const float p0 = s[kk][nq][2 * half], p1 = s[kk][nq][2 * half + 1];
-        const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
-        __nv_bfloat162 hh;
-        hh.x = h0;
-        hh.y = h1;
-        const uint32_t hp = *reinterpret_cast<uint32_t*>(&hh);
-        const uint32_t lp = pack_bf16x2(__fsub_rn(p0, __bfloat162float(h0)),
-                                        __fsub_rn(p1, __bfloat162float(h1)));
+        uint32_t hp, lp;
+        split_p_bf16(s[kk][nq][2 * half], s[kk][nq][2 * half + 1], hp, lp);
         bh[nq][half] = transpose8x8(hp);
         bl[nq][half] = transpose8x8(lp);
       }
@@ -915,93 +924,126 @@ __global__ void __launch_bounds__(D / 2 + 32) attn_decode_merge_kernel(const Ker
 
 // ---------------------------------------------------- prefill (tcgen05)
 // Block (qb, h, b): 128 query rows -- up to 128 / G tokens times the G heads
-// of kv head h (row r is token r / G, head r % G).  Per tile of 64 keys:
-//   S = Q K^T   tcgen05.mma M=128 N=64, k = d in steps of 16, into one of two
-//               TMEM buffers;
+// of kv head h (row r is token r / G, head r % G).  Per tile i of 64 keys:
+//   S = Q K^T   tcgen05.mma M=128 N=64, k = d in steps of 16, into TMEM
+//               buffer i % 4 (the next tiles' S are computed while this
+//               tile's softmax runs);
 //   softmax     the decode tile step's per-element arithmetic, key summation
-//               tree and P = hi + lo split, row by row; P goes to one of two
-//               shared buffers (K-major, swizzled);
-//   O += P V    tcgen05.mma M=128 N=D, per 16-key chunk the hi part then the
-//               lo part, V read as an MN-major operand.
+//               tree and P = hi + lo split, one row per thread; P (bf16
+//               pairs) is stored back over the tile's own score columns;
+//   O += P V    tcgen05.mma M=128 N=D with A = P read from tensor memory,
+//               per 16-key chunk the hi part then the lo part, V read as an
+//               MN-major operand, into the accumulator of the tile's split
+//               (two accumulators, alternating by split).
 // tcgen05.mma and mma.sync give bit-identical fp32 results for the same
 // operands and k order, so every output row equals the decode of its
 // position bit for bit.
-// Warps 0-7 run the softmax: warps q and q+4 share rows 32q..32q+31 (TMEM
-// lanes of quadrant q) and take the tiles alternately, warp q the even ones.
-// A warp hands the running maximum of its tile to its partner as soon as it
-// is known, and the sums and merged state when the tile is done (through
-// shared memory, one mbarrier phase per tile: a waiter never counts as an
-// arrival, so the handoffs cannot pair up wrongly), and the partner's score
-// load, maximum and exponentials for the next tile overlap this tile's wait
-// for PV and its rescale.  Warp 8 is the
-// producer: TMA copies into a three-stage ring, MMA issue; the S MMA of the
-// next tile goes to the tensor core ahead of the PV of this one.  The split
-// state is folded into the merged state (a second TMEM region) at each split
-// end.  Blocks are started longest first.
+// Roles: warps 0-3 run the softmax (warp w owns rows 32w..32w+31, the TMEM
+// lanes of quadrant w), keeping each row's split state (reference maximum m,
+// sum l) in registers; warps 4-7 fold every finished split into the merged
+// state (in shared memory) while the next split runs, and write out = o / l
+// at the end; warp 8 issues the MMAs; warp 9 the TMA copies (K
+// and V rings, page ids cached in shared memory).  A split's accumulator is
+// reused two splits later, once its fold is done.  The fold and TMA warps
+// sleep in their barrier waits instead of polling, so that they leave the
+// issue slots of their scheduler to the softmax warp beside them.  Blocks
+// are started longest first.
 constexpr int kPfRows = 128;
-constexpr int kPfSoftmaxWarps = 8;
-constexpr int kPfThreads = (kPfSoftmaxWarps + 2) * 32;  // + MMA warp + TMA warp
-constexpr int kPfMmaWarp = kPfSoftmaxWarps, kPfTmaWarp = kPfSoftmaxWarps + 1;
+constexpr int kPfThreads = 10 * 32;
+constexpr int kPfSoftWarp0 = 0, kPfFoldWarp0 = 4, kPfMmaWarp = 8, kPfTmaWarp = 9;
 constexpr int kPfPageCache = 1024;  // page ids held in shared memory (16384 keys)
-constexpr int kPfStages = 3;
-constexpr int kPvRing = 8;  // PV-done barriers, one phase per tile
+constexpr int kPfKStages = 3, kPfVStages = 4;
+constexpr int kPfSBufs = 4;         // S / P buffers in tensor memory
 
 template <int D>
 struct PfGeom {
   static constexpr int kHalves = D / 64;
   static constexpr int kQBytes = kHalves * kPfRows * 128;    // [half][row][128 B]
-  static constexpr int kKBytes = kHalves * kTile * 128;       // one tile: [half][key][128 B]
-  static constexpr int kKPairBytes = 2 * kKBytes;             // two tiles: [half][128 keys][128 B]
-  static constexpr int kKOff = kQBytes;                       // K ring: 2 stages of tile pairs
-  static constexpr int kVOff = kKOff + 2 * kKPairBytes;       // V ring: kPfStages tiles
-  static constexpr int kPBytes = kPfRows * 128;               // one part of P: [row][64 keys]
-  static constexpr int kPOff = kVOff + kPfStages * kKBytes;   // [buffer][hi, lo]
-  static constexpr int kXOff = kPOff + 4 * kPBytes;
-  static constexpr int kXFloats = 5 * kPfRows;
-  static constexpr int kPidOff = kXOff + kXFloats * 4;
+  static constexpr int kTBytes = kHalves * kTile * 128;       // one K or V tile: [half][key][128 B]
+  static constexpr int kKOff = kQBytes;
+  static constexpr int kVOff = kKOff + kPfKStages * kTBytes;
+  // merged o, fp32 [D / 4][128 rows][4]: a row's four consecutive columns
+  // are one 16-byte vector, and a warp's 32 rows a contiguous 512 bytes
+  static constexpr int kMOff = kVOff + kPfVStages * kTBytes;
+  static constexpr int kXOff = kMOff + D * kPfRows * 4;       // split m, l: [parity][2][128]
+  static constexpr int kPidOff = kXOff + 4 * kPfRows * 4;
   static constexpr int kBarOff = kPidOff + kPfPageCache * 4;
-  // kfull[2], kfree[2], vfull[], vfree[], sfull[2], sfree[2], pready[2], pdone[2], hm[4], hst[4],
-  // pvd[kPvRing]
-  static constexpr int kNumBars = 4 + 2 * kPfStages + 8 + 8 + kPvRing;
+  // kfull, kfree [KS]; vfull, vfree [VS]; sfull, pready, pfree [SB]; odone,
+  // sdone, folded [2]
+  static constexpr int kNumBars = 2 * kPfKStages + 2 * kPfVStages + 3 * kPfSBufs + 6;
   static constexpr int kSmem = 1024 + kBarOff + kNumBars * 8;
   static constexpr uint32_t kTmemCols = 512;
-  // two S buffers of 128 columns (a tile pair each), the split's o, the merged o
-  static constexpr uint32_t kColS = 0, kColO = 256, kColM = 256 + D;
+  // four S / P buffers of 64 columns, two split accumulators of D columns
+  static constexpr uint32_t kColS = 0, kColO = kPfSBufs * kTile;
 };
+
+// mbarrier wait for the roles with slack (the fold and TMA warps): the thread
+// suspends in the wait (a hint of 20 us, then it tries again), leaving the
+// issue slots of its scheduler to the softmax warp beside it; bounded in time
+// like mbar_wait.  The MMA and softmax warps, whose waits are on the
+// critical path, use mbar_wait itself.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool pf_wait_lazy(uint64_t* bar, uint32_t parity, int* err,
+                                             volatile int* abort) {
+  if (mbar_try_wait_sleep(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (abort && *abort) return false;
+    if (global_ns() - t0 > kWaitNs) break;
+  }
+  record_error(err, BI_ERR_TIMEOUT);
+  if (abort) *abort = 1;
+  return false;
+}
+
+// D (tmem) += A (tmem) * B (smem descriptor), one CTA, kind::f16.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const KernelParams p) {
   using Gm = PfGeom<D>;
-  constexpr uint32_t kIdescS = umma_idesc_bf16(kPfRows, 2 * kTile, false, false);
+  constexpr uint32_t kIdescS = umma_idesc_bf16(kPfRows, kTile, false, false);
   constexpr uint32_t kIdescPV = umma_idesc_bf16(kPfRows, D, false, true);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* qs = smem;
-  uint8_t* kst = smem + Gm::kKOff;  // K ring: 2 tile pairs
-  uint8_t* vst = smem + Gm::kVOff;  // V ring: kPfStages tiles
-  uint8_t* pbuf = smem + Gm::kPOff;
-  float* xm = reinterpret_cast<float*>(smem + Gm::kXOff);  // [128] running max, to the next tile
-  float* xst = xm + kPfRows;  // [4][128] l, merged m, merged l, merged-yet, to the next tile
-  int* pid_s = reinterpret_cast<int*>(smem + Gm::kPidOff);  // page ids of this sequence
-  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + Gm::kBarOff);  // K pair landed
-  uint64_t* kfree = kfull + 2;          // the S that read the K pair is done
-  uint64_t* vfull = kfree + 2;          // V tile landed
-  uint64_t* vfree = vfull + kPfStages;  // the PV that read the V stage is done
-  uint64_t* sfull = vfree + kPfStages;  // S of a tile pair computed
-  uint64_t* sfree = sfull + 2;          // both tiles' scores read
-  uint64_t* pready = sfree + 2;
-  uint64_t* pdone = pready + 2;
-  uint64_t* hm = pdone + 2;   // per row quadrant: the running max of a tile is written
-  uint64_t* hst = hm + 4;     // per row quadrant: the sums and merged state of a tile are written
-  // PV of tile t done, phase t / kPvRing of barrier t % kPvRing.  Waited only
-  // when a softmax warp must change o; a wait for tile i-1 there comes after
-  // the unconditional wait (pdone) that saw the PV of tile i-2 complete, and
-  // the PV of tile i is issued only after it, so the barrier is never more
-  // than one phase from the one waited for.
-  uint64_t* pvd = hst + 4;
+  uint8_t* kst = smem + Gm::kKOff;
+  uint8_t* vst = smem + Gm::kVOff;
+  float* xsplit = reinterpret_cast<float*>(smem + Gm::kXOff);  // [parity][m, l][128]
+  float4* omg = reinterpret_cast<float4*>(smem + Gm::kMOff);   // merged o [D/4][128]
+  int* pid_s = reinterpret_cast<int*>(smem + Gm::kPidOff);      // page ids of this sequence
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + Gm::kBarOff);  // K tile landed
+  uint64_t* kfree = kfull + kPfKStages;    // the S that read the K stage is done
+  uint64_t* vfull = kfree + kPfKStages;    // V tile landed
+  uint64_t* vfree = vfull + kPfVStages;    // the PV that read the V stage is done
+  uint64_t* sfull = vfree + kPfVStages;    // S of the tile computed
+  uint64_t* pready = sfull + kPfSBufs;     // P of the tile written over it
+  uint64_t* pfree = pready + kPfSBufs;     // PV of the tile done (buffer free)
+  uint64_t* odone = pfree + kPfSBufs;      // the last PV of a split done
+  uint64_t* sdone = odone + 2;             // a split's m, l written
+  uint64_t* folded = sdone + 2;            // a split folded (its accumulator free)
   __shared__ uint32_t tmem_slot;
   __shared__ int s_abort;
 
@@ -1023,6 +1065,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   const int p_last = start + tok0 + ntok - 1;  // last position in this block
   const int32_t* bt_row = p.block_table + (int64_t)b * p.max_blocks;
   const int ntiles = (p_last + kTile) / kTile;  // tiles 0 .. covering key p_last
+  const int S = p.split_size;
+  const int tps = S / kTile;                    // tiles per split
+  const int nsplits = (ntiles + tps - 1) / tps;
   {
     // check every page a tile copy may read, and keep the first ids at hand
     const int loaded_hi = min(kvl, ntiles * kTile);
@@ -1038,28 +1083,28 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       return;
     }
   }
-  const int S = p.split_size;
   if (tid == 0) {
     s_abort = 0;
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
-    for (int i = 0; i < kPfStages; ++i) {
+    for (int i = 0; i < kPfKStages; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&kfree[i], 1);
+    }
+    for (int i = 0; i < kPfVStages; ++i) {
       mbar_init(&vfull[i], 1);
       mbar_init(&vfree[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&kfull[i], 1);
-      mbar_init(&kfree[i], 1);
+    for (int i = 0; i < kPfSBufs; ++i) {
       mbar_init(&sfull[i], 1);
-      mbar_init(&sfree[i], kPfSoftmaxWarps);       // all eight warps read a pair
-      mbar_init(&pready[i], kPfSoftmaxWarps / 2);  // the four warps of that tile parity
-      mbar_init(&pdone[i], 1);
+      mbar_init(&pready[i], 4);  // the four softmax warps
+      mbar_init(&pfree[i], 1);
     }
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&hm[i], 32);  // every lane of the warp that wrote its rows
-      mbar_init(&hst[i], 32);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&odone[i], 1);
+      mbar_init(&sdone[i], 4);
+      mbar_init(&folded[i], 4);  // the four fold warps
     }
-    for (int i = 0; i < kPvRing; ++i) mbar_init(&pvd[i], 1);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&tmem_slot, Gm::kTmemCols);
@@ -1081,254 +1126,182 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
 
   if (warp == kPfTmaWarp) {
     // ================================================================ copies
-    // K goes in pairs of tiles (one S MMA covers 128 keys) through two pair
-    // stages, V tile by tile through kPfStages stages.  A K stage is free once
-    // the S that read it is done, a V stage once its PV is.  Copies go out in
-    // the order they are needed: the K pair k at the MMA warp's tile 2(k-1),
-    // V of tile i at tile i.
-    const int npairs = (ntiles + 1) / 2;
-    auto issue_copy = [&](int i, bool is_v) {  // tile i; lane 0
-      uint8_t* dst;
-      uint64_t* bar;
-      if (is_v) {
-        dst = vst + (i % kPfStages) * Gm::kKBytes;
-        bar = &vfull[i % kPfStages];
-      } else {  // rows 64 (i & 1) .. of each half of the pair stage
-        dst = kst + ((i >> 1) & 1) * Gm::kKPairBytes + (i & 1) * (kTile * 128);
-        bar = &kfull[(i >> 1) & 1];
-      }
-      const int key0 = i * kTile;
-      const int np = pages_below(key0, kvl);
-      for (int pp = 0; pp < np; ++pp) {
-        const int pg = (key0 >> 4) + pp;
-        const int y = ((pg < kPfPageCache ? pid_s[pg] : bt_row[pg]) * p.Hkv + h) * kPage;
-#pragma unroll
-        for (int hf = 0; hf < Gm::kHalves; ++hf)
-          tma_load_2d(dst + hf * (is_v ? kTile * 128 : 2 * kTile * 128) + pp * 2048,
-                      is_v ? &vmap : &kmap, hf * 64, y, bar);
-      }
-    };
-    auto issue_kpair = [&](int k) {  // lane 0
-      const int t1 = 2 * k + 1 < ntiles;
-      const int bytes = (pages_below(2 * k * kTile, kvl) +
-                         (t1 ? pages_below((2 * k + 1) * kTile, kvl) : 0)) *
-                        Gm::kHalves * 2048;
-      mbar_arrive_expect_tx(&kfull[k & 1], bytes);
-      issue_copy(2 * k, false);
-      if (t1) issue_copy(2 * k + 1, false);
-    };
-    auto issue_v = [&](int i) {  // lane 0
-      mbar_arrive_expect_tx(&vfull[i % kPfStages], pages_below(i * kTile, kvl) * Gm::kHalves * 2048);
-      issue_copy(i, true);
-    };
-    int nk = min(2, npairs), nv = min(kPfStages, ntiles);
+    // One thread.  Tile i: K into stage i % KS once the S of tile i - KS is
+    // done, V into stage i % VS once the PV of tile i - VS is.
     if (lane == 0) {
-      for (int k = 0; k < nk; ++k) issue_kpair(k);
-      for (int i = 0; i < nv; ++i) issue_v(i);
-    }
-    bool ok = true;
-    while (ok && (nk < npairs || nv < ntiles)) {
-      if (nk < npairs && (nv >= ntiles || 2 * (nk - 1) <= nv)) {
-        ok = __all_sync(kFull, mbar_wait(&kfree[nk & 1], ((nk - 2) >> 1) & 1, p.err, &s_abort));
+      auto issue_tile = [&](int i, bool is_v) {
+        uint8_t* dst = is_v ? vst + (i % kPfVStages) * Gm::kTBytes
+                            : kst + (i % kPfKStages) * Gm::kTBytes;
+        uint64_t* bar = is_v ? &vfull[i % kPfVStages] : &kfull[i % kPfKStages];
+        const int key0 = i * kTile;
+        const int np = pages_below(key0, kvl);
+        mbar_arrive_expect_tx(bar, np * Gm::kHalves * 2048);
+        for (int pp = 0; pp < np; ++pp) {
+          const int pg = (key0 >> 4) + pp;
+          const int y = ((pg < kPfPageCache ? pid_s[pg] : bt_row[pg]) * p.Hkv + h) * kPage;
+#pragma unroll
+          for (int hf = 0; hf < Gm::kHalves; ++hf)
+            tma_load_2d(dst + hf * (kTile * 128) + pp * 2048, is_v ? &vmap : &kmap, hf * 64, y,
+                        bar);
+        }
+      };
+      bool ok = true;
+      int nk = 0, nv = 0;
+      for (int i = 0; i < ntiles && ok; ++i) {
+        if (i >= kPfKStages)
+          ok = pf_wait_lazy(&kfree[i % kPfKStages], ((i / kPfKStages) - 1) & 1, p.err, &s_abort);
         if (!ok) break;
-        if (lane == 0) issue_kpair(nk);
+        issue_tile(i, false);
         ++nk;
-      } else {
-        ok = __all_sync(kFull, mbar_wait(&vfree[nv % kPfStages], (nv / kPfStages - 1) & 1,
-                                         p.err, &s_abort));
+        if (i >= kPfVStages)
+          ok = pf_wait_lazy(&vfree[i % kPfVStages], ((i / kPfVStages) - 1) & 1, p.err, &s_abort);
         if (!ok) break;
-        if (lane == 0) issue_v(nv);
+        issue_tile(i, true);
         ++nv;
       }
-    }
-    if (lane == 0) {
       // every copy lands before the block exits (bounded waits)
-      for (int k = max(0, nk - 2); k < nk; ++k)
-        mbar_wait(&kfull[k & 1], (k >> 1) & 1, ok ? p.err : nullptr, ok ? &s_abort : nullptr);
-      for (int j = max(0, nv - kPfStages); j < nv; ++j)
-        mbar_wait(&vfull[j % kPfStages], (j / kPfStages) & 1, ok ? p.err : nullptr,
-                  ok ? &s_abort : nullptr);
+      for (int k = max(0, nk - kPfKStages); k < nk; ++k)
+        pf_wait_lazy(&kfull[k % kPfKStages], (k / kPfKStages) & 1, ok ? p.err : nullptr,
+                     ok ? &s_abort : nullptr);
+      for (int j = max(0, nv - kPfVStages); j < nv; ++j)
+        pf_wait_lazy(&vfull[j % kPfVStages], (j / kPfVStages) & 1, ok ? p.err : nullptr,
+                     ok ? &s_abort : nullptr);
     }
+    __syncwarp();
   } else if (warp == kPfMmaWarp) {
     // ================================================================ MMA
-    // descriptors: the tile bases once, offsets added in the 16-byte units of
-    // the address field
-    const uint64_t qd = umma_desc_sw128(smem_u32(qs), 16, 1024);
-    const uint64_t kd = umma_desc_sw128(smem_u32(kst), 16, 1024);
-    const uint64_t vd = umma_desc_sw128(smem_u32(vst), kTile * 128, 1024);
-    const uint64_t pd = umma_desc_sw128(smem_u32(pbuf), 16, 1024);
-    uint64_t* last_bar = nullptr;  // the latest MMA commit
-    uint32_t last_par = 0;
-    // S of tile pair k (128 keys) once its K landed and its TMEM buffer is free
-    const int npairs = (ntiles + 1) / 2;
-    auto issue_s = [&](int k) -> bool {
-      const int kb2 = k & 1;
-      bool w = mbar_wait(&kfull[kb2], (k >> 1) & 1, p.err, &s_abort);
-      if (k >= 2) w = w && mbar_wait(&sfree[kb2], ((k - 2) >> 1) & 1, p.err, &s_abort);
-      if (!__all_sync(kFull, w)) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint64_t kb = kd + static_cast<uint64_t>(kb2 * (Gm::kKPairBytes >> 4));
+    // One thread issues everything: no warp collective sits between two MMA
+    // batches, so the tensor core's short issue queue is refilled as soon as
+    // a batch's inputs are ready.
+    if (lane == 0) {
+      const uint64_t qd = umma_desc_sw128(smem_u32(qs), 16, 1024);
+      const uint64_t kd = umma_desc_sw128(smem_u32(kst), 16, 1024);
+      const uint64_t vd = umma_desc_sw128(smem_u32(vst), kTile * 128, 1024);
+      uint64_t* last_bar = nullptr;  // the latest MMA commit
+      uint32_t last_par = 0;
+      // S of tile i once its K landed and the PV of tile i - 4 (the last
+      // reader of its buffer) is done
+      auto issue_s = [&](int i) -> bool {
+        const int ks_ = i % kPfKStages, sb = i % kPfSBufs;
+        if (!mbar_wait(&kfull[ks_], (i / kPfKStages) & 1, p.err, &s_abort)) return false;
+        if (i >= kPfSBufs && !mbar_wait(&pfree[sb], ((i / kPfSBufs) - 1) & 1, p.err, &s_abort))
+          return false;
+        tc_fence_after();
+        const uint64_t kb = kd + static_cast<uint64_t>(ks_ * (Gm::kTBytes >> 4));
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          tc_mma(tmem + Gm::kColS + 128 * kb2,
+          tc_mma(tmem + Gm::kColS + kTile * sb,
                  qd + static_cast<uint64_t>((ks >> 2) * (kPfRows * 8) + (ks & 3) * 2),
-                 kb + static_cast<uint64_t>((ks >> 2) * (2 * kTile * 8) + (ks & 3) * 2), kIdescS,
+                 kb + static_cast<uint64_t>((ks >> 2) * (kTile * 8) + (ks & 3) * 2), kIdescS,
                  ks > 0 ? 1u : 0u);
-        tc_commit(&sfull[kb2]);
-        tc_commit(&kfree[kb2]);
-      }
-      last_bar = &sfull[kb2];
-      last_par = (k >> 1) & 1;
-      return true;
-    };
-    bool ok = issue_s(0);
-    for (int i = 0; i < ntiles && ok; ++i) {
-      const int b2 = i & 1;
-      const uint32_t ph2 = (i >> 1) & 1;
-      const int stg = i % kPfStages;
-      uint8_t* vt = vst + stg * Gm::kKBytes;
-      const int key0 = i * kTile;
-      const bool split_first = key0 % S == 0;
-      // the next pair's S goes to the tensor core ahead of this tile's PV,
-      // so that the softmax of the next tiles overlaps the PVs
-      if ((i & 1) == 0 && (i >> 1) + 1 < npairs && !issue_s((i >> 1) + 1)) {
-        ok = false;
-        break;
-      }
-      ok = __all_sync(kFull, mbar_wait(&vfull[stg], (i / kPfStages) & 1, p.err, &s_abort) &&
-                                 mbar_wait(&pready[b2], ph2, p.err, &s_abort));
-      if (!ok) break;
-      if (key0 + kTile > kvl) {  // keys past the end: zero their V rows before PV
-        const int first = kvl - key0;
-        for (int idx = lane; idx < (kTile - first) * Gm::kHalves * 8; idx += 32) {
-          const int n = first + idx / (Gm::kHalves * 8);
-          const int rem = idx % (Gm::kHalves * 8);
-          *reinterpret_cast<uint4*>(vt + (rem >> 3) * (kTile * 128) + n * 128 + (rem & 7) * 16) =
-              make_uint4(0, 0, 0, 0);
+        tc_commit(&sfull[sb]);
+        tc_commit(&kfree[ks_]);
+        last_bar = &sfull[sb];
+        last_par = (i / kPfSBufs) & 1;
+        return true;
+      };
+      bool ok = issue_s(0);
+      for (int i = 0; i < ntiles && ok; ++i) {
+        const int sb = i % kPfSBufs;
+        const int stg = i % kPfVStages;
+        uint8_t* vt = vst + stg * Gm::kTBytes;
+        const int key0 = i * kTile;
+        const int j = i / tps;
+        const bool split_first = i % tps == 0;
+        const bool split_last = (i + 1) % tps == 0 || i + 1 == ntiles;
+        // the next tile's S goes to the tensor core ahead of this tile's PV,
+        // so that its softmax can start as soon as this one's ends
+        if (i + 1 < ntiles && !issue_s(i + 1)) {
+          ok = false;
+          break;
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      tc_fence_after();
-      if (lane == 0) {  // ---- O += P V, per 16-key chunk the hi part then the lo part
-        const uint64_t vb = vd + static_cast<uint64_t>(stg * (Gm::kKBytes >> 4));
-        const uint64_t ph = pd + static_cast<uint64_t>(b2 * (2 * Gm::kPBytes >> 4));
+        ok = mbar_wait(&vfull[stg], (i / kPfVStages) & 1, p.err, &s_abort) &&
+             mbar_wait(&pready[sb], (i / kPfSBufs) & 1, p.err, &s_abort);
+        // the split's accumulator was last used two splits ago: its fold must be done
+        if (ok && split_first && j >= 2)
+          ok = mbar_wait(&folded[j & 1], ((j - 2) >> 1) & 1, p.err, &s_abort);
+        if (!ok) break;
+        if (key0 + kTile > kvl) {  // keys past the end: zero their V rows before PV
+          const int first = kvl - key0;
+          for (int idx = 0; idx < (kTile - first) * Gm::kHalves * 8; ++idx) {
+            const int n = first + idx / (Gm::kHalves * 8);
+            const int rem = idx % (Gm::kHalves * 8);
+            *reinterpret_cast<uint4*>(vt + (rem >> 3) * (kTile * 128) + n * 128 +
+                                      (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        tc_fence_after();
+        // ---- O += P V, per 16-key chunk the hi part then the lo part
+        const uint64_t vb = vd + static_cast<uint64_t>(stg * (Gm::kTBytes >> 4));
+        const uint32_t pa = tmem + Gm::kColS + kTile * sb;  // P hi: columns 0-31, lo: 32-63
+        const uint32_t od = tmem + Gm::kColO + D * (j & 1);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint64_t bd = vb + static_cast<uint64_t>(kk * 128);
-          tc_mma(tmem + Gm::kColO, ph + static_cast<uint64_t>(kk * 2), bd, kIdescPV,
-                 (split_first && kk == 0) ? 0u : 1u);
-          tc_mma(tmem + Gm::kColO, ph + static_cast<uint64_t>((Gm::kPBytes >> 4) + kk * 2), bd,
-                 kIdescPV, 1u);
+          tc_mma_ts(od, pa + 8 * kk, bd, kIdescPV, (split_first && kk == 0) ? 0u : 1u);
+          tc_mma_ts(od, pa + 32 + 8 * kk, bd, kIdescPV, 1u);
         }
-        tc_commit(&pdone[b2]);
+        tc_commit(&pfree[sb]);
         tc_commit(&vfree[stg]);
-        tc_commit(&pvd[i % kPvRing]);
+        if (split_last) tc_commit(&odone[j & 1]);
+        last_bar = &pfree[sb];
+        last_par = (i / kPfSBufs) & 1;
       }
-      last_bar = &pdone[b2];
-      last_par = ph2;
+      if (!ok && last_bar) mbar_wait(last_bar, last_par, nullptr);  // MMAs in flight
     }
-    if (!ok && lane == 0 && last_bar) mbar_wait(last_bar, last_par, nullptr);  // MMAs in flight
-  } else {
+    __syncwarp();
+  } else if (warp < kPfFoldWarp0) {
     // ================================================================= softmax
-    const int q4 = warp & 3, par = warp >> 2;  // row quadrant, parity of the tiles taken
-    const int r = q4 * 32 + lane;
+    const int r = (warp - kPfSoftWarp0) * 32 + lane;
     const int tk = r / G;
     const int pos = (r < TPB * G && tk < ntok) ? start + tok0 + tk : -1;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
-    // state handed from the warp of tile t-1 to the warp of tile t
-    float m = -CUDART_INF_F, l = 0.0f;        // split state after the tile
-    float mg_m = -CUDART_INF_F, mg_l = 0.0f;  // merged state
-    bool have = false;
-    bool live = true;  // no wait has run out
-    // fold the finished split (m_s, l_s, o in TMEM) into the merged state
-    auto fold = [&](float m_s, float l_s, int lo_s) {
-      const bool part = pos >= lo_s;
-      float mn = 0.0f, ca = 0.0f, cb = 0.0f;
-      if (part && have) lse_coeffs(mg_m, m_s, mn, ca, cb);
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t vo[32], vm[32];
-        tmem_ld32_nowait(tl + Gm::kColO + 32 * c, vo);
-        tmem_ld32_nowait(tl + Gm::kColM + 32 * c, vm);
-        tmem_wait_ld();
-        if (part) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            vm[e] = have ? __float_as_uint(lse_mix(__uint_as_float(vm[e]), ca,
-                                                   __uint_as_float(vo[e]), cb))
-                         : vo[e];
-        }
-        tmem_st32(tl + Gm::kColM + 32 * c, vm);
-      }
-      tmem_wait_st();
-      if (part) {
-        if (have) {
-          mg_l = lse_mix(mg_l, ca, l_s, cb);
-          mg_m = mn;
-        } else {
-          mg_m = m_s;
-          mg_l = l_s;
-          have = true;
-        }
-      }
-    };
-    for (int i = par; i < ntiles && live; i += 2) {
-      const int b2 = i & 1;
+    const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    float m = -CUDART_INF_F, l = 0.0f;  // the split's reference maximum and sum
+    bool live = true;                   // no wait has run out
+    for (int i = 0; i < ntiles && live; ++i) {
+      const int sb = i % kPfSBufs;
       const int key0 = i * kTile;
-      const int lo = (key0 / S) * S;  // split start
-      const bool split_first = key0 == lo;
-      // ---- scores of the tile
-      live = __all_sync(kFull, live && mbar_wait(&sfull[(i >> 1) & 1], (i >> 2) & 1, p.err,
-                                                 &s_abort));
-      // The row is read from TMEM 32 columns at a time, twice: once for the
-      // maximum, once for the probabilities (the same scaled values both
-      // times), so that only 32 scores are live in registers.  Tiles that
-      // every row of the block sees whole take a path without masking.
-      const bool all_vis = key0 + kTile - 1 <= start + tok0;
-      const int nvis = pos >= lo ? min(lo + S, pos + 1) - key0 : 0;
-      auto scores = [&](int hf, float (&x)[32], auto all_tag) {
-        constexpr bool kAll = decltype(all_tag)::value;
-        uint32_t sv[32];
-        tmem_ld32(tl + Gm::kColS + 128 * ((i >> 1) & 1) + 64 * (i & 1) + 32 * hf, sv);
+      const int j = i / tps;
+      const bool split_first = i % tps == 0;
+      const bool split_last = (i + 1) % tps == 0 || i + 1 == ntiles;
+      const uint32_t sa = tl + Gm::kColS + kTile * sb;
+      // ---- scores of the tile: all 64 in registers
+      live = __all_sync(kFull, mbar_wait(&sfull[sb], (i / kPfSBufs) & 1, p.err, &s_abort));
+      if (!live) break;
+      tc_fence_after();
+      float x[64];
+      {
+        uint32_t sv[64];
+        tmem_ld32_nowait(sa, *reinterpret_cast<uint32_t(*)[32]>(sv));
+        tmem_ld32_nowait(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+        tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float sj = __fmul_rn(__uint_as_float(sv[j]), p.scale_log2);
-          x[j] = (kAll || 32 * hf + j < nvis) ? sj : -CUDART_INF_F;
-        }
-      };
-      float mh[2] = {-CUDART_INF_F, -CUDART_INF_F};
-      auto row_max = [&](auto all_tag) {
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          float x[32];
-          scores(hf, x, all_tag);
-          float t[16];  // the row maximum is exact in any order: a tree
-#pragma unroll
-          for (int j = 0; j < 16; ++j) t[j] = fmaxf(x[2 * j], x[2 * j + 1]);
-#pragma unroll
-          for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-            for (int j = 0; j < w; ++j) t[j] = fmaxf(t[2 * j], t[2 * j + 1]);
-          mh[hf] = t[0];
-        }
-      };
-      if (live) {
-        tc_fence_after();
-        if (all_vis)
-          row_max(std::true_type{});
-        else
-          row_max(std::false_type{});
+        for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(sv[e]);
       }
-      const float mx = fmaxf(mh[0], mh[1]);
-      // ---- running maximum of the previous tile
-      float m_prev = -CUDART_INF_F;
-      if (i > 0) {
-        live = __all_sync(kFull, live && mbar_wait(&hm[q4], (i - 1) & 1, p.err, &s_abort));
-        m_prev = xm[r];
+      // keys key0 .. key0 + nvis - 1 are visible to this row (the tile lies
+      // inside one split, which starts at or before key0)
+      const int nvis = pos >= key0 ? min(kTile, pos + 1 - key0) : 0;
+      if (key0 + kTile - 1 <= start + tok0) {  // every row of the block sees the whole tile
+#pragma unroll
+        for (int e = 0; e < 64; ++e) x[e] = __fmul_rn(x[e], p.scale_log2);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          x[e] = e < nvis ? __fmul_rn(x[e], p.scale_log2) : -CUDART_INF_F;
       }
-      const float m_in = split_first ? -CUDART_INF_F : m_prev;
+      float mx;
+      {
+        float t[32];  // the row maximum is exact in any order: a tree
+#pragma unroll
+        for (int e = 0; e < 32; ++e) t[e] = fmaxf(x[2 * e], x[2 * e + 1]);
+#pragma unroll
+        for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+          for (int e = 0; e < w; ++e) t[e] = fmaxf(t[2 * e], t[2 * e + 1]);
+        mx = t[0];
+      }
+      const float m_in = split_first ? -CUDART_INF_F : m;
       float mnew = m_in, alpha = 1.0f;  // the decode's reference rule (kRescaleLog2)
       if (mx == -CUDART_INF_F) {
         // no visible key: exact no-op for this row
@@ -1339,145 +1312,149 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
         mnew = mx;
         alpha = exp2_sfu(__fsub_rn(m_in, mx));
       }
-      if (i + 1 < ntiles) {
-        xm[r] = mnew;
-        mbar_arrive(&hm[q4]);
-      }
-      // ---- probabilities into P = hi + lo (buffer b2, once the PV of two
-      // tiles ago has read it); key j adds to partial sum j % 8 in increasing
-      // key order, then the tree ((0+1)+(2+3))+((4+5)+(6+7))
-      if (i >= 2)
-        live = __all_sync(kFull, live && mbar_wait(&pdone[b2], ((i - 2) >> 1) & 1, p.err,
-                                                   &s_abort));
+      // ---- probabilities: P = hi + lo as bf16 pairs (column c holds keys
+      // 2c, 2c+1), written over the scores; key e adds to partial sum e % 8
+      // in increasing key order, then the tree ((0+1)+(2+3))+((4+5)+(6+7))
+      // masked keys hold -inf, and 2^(-inf - base) = +0 for any finite base
+      const float mb = mnew == -CUDART_INF_F ? 0.0f : mnew;
       float cs[8];
 #pragma unroll
       for (int g8 = 0; g8 < 8; ++g8) cs[g8] = 0.0f;
-      auto probs = [&](auto all_tag) {
-        constexpr bool kAll = decltype(all_tag)::value;
-        uint8_t* ph = pbuf + b2 * 2 * Gm::kPBytes;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          float x[32];
-          scores(hf, x, all_tag);
+      for (int hf = 0; hf < 2; ++hf) {  // keys 32hf .. 32hf+31: columns 16hf .. 16hf+15
+        uint32_t ph[16], pl[16];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            x[j] = (kAll || x[j] != -CUDART_INF_F) ? exp2_sfu(__fsub_rn(x[j], mnew)) : 0.0f;
-            cs[j & 7] = __fadd_rn(cs[j & 7], x[j]);
+        for (int c = 0; c < 4; ++c) {  // keys 32hf+8c .. 32hf+8c+7
+          const int k0 = 32 * hf + 8 * c;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float pv = exp2_sfu(__fsub_rn(x[k0 + e], mb));
+            x[k0 + e] = pv;
+            cs[e] = __fadd_rn(cs[e], pv);
           }
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t wh[4], wl[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float p0 = x[8 * c + 2 * e], p1 = x[8 * c + 2 * e + 1];
-              const __nv_bfloat16 h0 = __float2bfloat16_rn(p0), h1 = __float2bfloat16_rn(p1);
-              __nv_bfloat162 hh;
-              hh.x = h0;
-              hh.y = h1;
-              wh[e] = *reinterpret_cast<uint32_t*>(&hh);
-              wl[e] = pack_bf16x2(__fsub_rn(p0, __bfloat162float(h0)),
-                                  __fsub_rn(p1, __bfloat162float(h1)));
-            }
-            const uint32_t off = sw128_off(r, 4 * hf + c);
-            *reinterpret_cast<uint4*>(ph + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-            *reinterpret_cast<uint4*>(ph + Gm::kPBytes + off) =
-                make_uint4(wl[0], wl[1], wl[2], wl[3]);
-          }
+          for (int e = 0; e < 4; ++e)
+            split_p_bf16(x[k0 + 2 * e], x[k0 + 2 * e + 1], ph[4 * c + e], pl[4 * c + e]);
         }
-        fence_proxy_async_smem();
-      };
-      if (live) {
-        if (all_vis)
-          probs(std::true_type{});
-        else
-          probs(std::false_type{});
+        tmem_st16(sa + 16 * hf, ph);
+        tmem_st16(sa + 32 + 16 * hf, pl);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sfree[(i >> 1) & 1]);
       const float csum = __fadd_rn(__fadd_rn(__fadd_rn(cs[0], cs[1]), __fadd_rn(cs[2], cs[3])),
                                    __fadd_rn(__fadd_rn(cs[4], cs[5]), __fadd_rn(cs[6], cs[7])));
-      // ---- sum and merged state of the previous tile
-      float l_prev = 0.0f;
-      if (i > 0) {
-        live = __all_sync(kFull, live && mbar_wait(&hst[q4], (i - 1) & 1, p.err, &s_abort));
-        l_prev = xst[r];
-        mg_m = xst[kPfRows + r];
-        mg_l = xst[2 * kPfRows + r];
-        have = xst[3 * kPfRows + r] != 0.0f;
-      }
-      l = __fadd_rn(__fmul_rn(split_first ? 0.0f : l_prev, alpha), csum);
+      l = __fadd_rn(__fmul_rn(split_first ? 0.0f : l, alpha), csum);
       m = mnew;
-      // ---- fold a finished split, or o *= alpha where a reference moved:
-      // both need the previous tile's PV done; otherwise this tile's PV may
-      // be issued while that one still runs (the tensor core accumulates in
-      // issue order)
-      const bool fold_now = split_first && i > 0;
-      const bool rescale = !split_first && __any_sync(kFull, alpha != 1.0f);
-      if (fold_now || rescale)
-        live = __all_sync(kFull, live && mbar_wait(&pvd[(i - 1) % kPvRing],
-                                                   ((i - 1) / kPvRing) & 1, p.err, &s_abort));
-      if (live) {
+      // ---- o *= alpha where a reference moved: after the previous tile's PV,
+      // before this one's (the tensor core accumulates in issue order)
+      if (!split_first && __any_sync(kFull, alpha != 1.0f)) {
+        const int ip = i - 1;
+        live = __all_sync(kFull, mbar_wait(&pfree[ip % kPfSBufs], (ip / kPfSBufs) & 1, p.err,
+                                         &s_abort));
+        if (!live) break;
         tc_fence_after();
-        if (fold_now) {
-          fold(m_prev, l_prev, lo - S);
-        } else if (rescale) {
+        const uint32_t oc = tl + Gm::kColO + D * (j & 1);
 #pragma unroll
-          for (int c = 0; c < D / 32; c += 2) {  // two chunks per TMEM round trip
-            uint32_t v0[32], v1[32];
-            tmem_ld32_nowait(tl + Gm::kColO + 32 * c, v0);
-            tmem_ld32_nowait(tl + Gm::kColO + 32 * (c + 1), v1);
-            tmem_wait_ld();
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v0[32];
+          tmem_ld32(oc + 32 * c, v0);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              v0[e] = __float_as_uint(__fmul_rn(__uint_as_float(v0[e]), alpha));
-              v1[e] = __float_as_uint(__fmul_rn(__uint_as_float(v1[e]), alpha));
-            }
-            tmem_st32(tl + Gm::kColO + 32 * c, v0);
-            tmem_st32(tl + Gm::kColO + 32 * (c + 1), v1);
-          }
-          tmem_wait_st();
+          for (int e = 0; e < 32; ++e)
+            v0[e] = __float_as_uint(__fmul_rn(__uint_as_float(v0[e]), alpha));
+          tmem_st32(oc + 32 * c, v0);
         }
       }
-      if (i + 1 < ntiles) {
-        xst[r] = l;
-        xst[kPfRows + r] = mg_m;
-        xst[2 * kPfRows + r] = mg_l;
-        xst[3 * kPfRows + r] = have ? 1.0f : 0.0f;
-        mbar_arrive(&hst[q4]);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pready[sb]);
+      if (split_last) {
+        // hand the split's m, l to the fold warps (their slot was read when
+        // the fold of split j - 2 finished)
+        if (j >= 2)
+          live = __all_sync(kFull, mbar_wait(&folded[j & 1], ((j - 2) >> 1) & 1, p.err,
+                                           &s_abort));
+        if (!live) break;
+        xsplit[(j & 1) * 2 * kPfRows + r] = m;
+        xsplit[(j & 1) * 2 * kPfRows + kPfRows + r] = l;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sdone[j & 1]);
+      }
+    }
+  } else {
+    // ================================================================ fold
+    // Split j's accumulator (m_s, l_s, o_s) into the merged state, in split
+    // order: the decode merge's left fold, one row per thread.
+    const int r = (warp - kPfFoldWarp0) * 32 + lane;
+    const int tk = r / G;
+    const int pos = (r < TPB * G && tk < ntok) ? start + tok0 + tk : -1;
+    const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    float mg_m = -CUDART_INF_F, mg_l = 0.0f;  // merged state
+    bool have = false;
+    bool live = true;
+    for (int j = 0; j < nsplits && live; ++j) {
+      live = __all_sync(kFull, pf_wait_lazy(&sdone[j & 1], (j >> 1) & 1, p.err, &s_abort) &&
+                                   pf_wait_lazy(&odone[j & 1], (j >> 1) & 1, p.err, &s_abort));
+      if (!live) break;
+      tc_fence_after();
+      const float m_s = xsplit[(j & 1) * 2 * kPfRows + r];
+      const float l_s = xsplit[(j & 1) * 2 * kPfRows + kPfRows + r];
+      const bool part = pos >= j * S;  // the split holds keys this row sees
+      float mn = 0.0f, ca = 0.0f, cb = 0.0f;
+      if (part && have) lse_coeffs(mg_m, m_s, mn, ca, cb);
+      if (__any_sync(kFull, part)) {
+        const uint32_t os = tl + Gm::kColO + D * (j & 1);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t vo[32];
+          tmem_ld32(os + 32 * c, vo);
+          if (part) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              float4* slot = omg + (8 * c + v) * kPfRows + r;
+              const float4 add = make_float4(__uint_as_float(vo[4 * v]),
+                                             __uint_as_float(vo[4 * v + 1]),
+                                             __uint_as_float(vo[4 * v + 2]),
+                                             __uint_as_float(vo[4 * v + 3]));
+              if (have) {
+                const float4 m4 = *slot;
+                *slot = make_float4(lse_mix(m4.x, ca, add.x, cb), lse_mix(m4.y, ca, add.y, cb),
+                                    lse_mix(m4.z, ca, add.z, cb), lse_mix(m4.w, ca, add.w, cb));
+              } else {
+                *slot = add;
+              }
+            }
+          }
+        }
+      }
+      if (part) {
+        if (have) {
+          mg_l = lse_mix(mg_l, ca, l_s, cb);
+          mg_m = mn;
+        } else {
+          mg_m = m_s;
+          mg_l = l_s;
+          have = true;
+        }
       }
       tc_fence_before();
       __syncwarp();
-      if (live && lane == 0) mbar_arrive(&pready[b2]);
+      if (lane == 0) mbar_arrive(&folded[j & 1]);
     }
-    // ---- the warp of the last tile folds the last split and writes out = o / l
-    if (((ntiles - 1) & 1) == par) {
-      const int i = ntiles - 1;
-      live = __all_sync(kFull, live && mbar_wait(&pdone[i & 1], (i >> 1) & 1, p.err, &s_abort));
-      if (live && !s_abort) {
-        tc_fence_after();
-        fold(m, l, ((i * kTile) / S) * S);
-        const int64_t orow = ((int64_t)(q_begin + tok0 + tk) * p.Hq + h * G + r % G) * D;
+    // ---- out = o / l, rounded once
+    if (live && !s_abort && pos >= 0) {
+      const int64_t orow = ((int64_t)(q_begin + tok0 + tk) * p.Hq + h * G + r % G) * D;
+#pragma unroll 4
+      for (int e = 0; e < D; e += 8) {
+        const float4 a4 = omg[(e / 4) * kPfRows + r], b4 = omg[(e / 4 + 1) * kPfRows + r];
+        float o[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tl + Gm::kColM + 32 * c, v);  // the whole warp loads
-          if (pos < 0) continue;
-#pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            float o[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) o[u] = __fdiv_rn(__uint_as_float(v[e + u]), mg_l);
-            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + 32 * c + e) =
-                make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
-                           pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
-            if (p.out_f32) {
-              *reinterpret_cast<float4*>(p.out_f32 + orow + 32 * c + e) =
-                  make_float4(o[0], o[1], o[2], o[3]);
-              *reinterpret_cast<float4*>(p.out_f32 + orow + 32 * c + e + 4) =
-                  make_float4(o[4], o[5], o[6], o[7]);
-            }
-          }
+        for (int u = 0; u < 8; ++u) o[u] = __fdiv_rn(o[u], mg_l);
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + e) =
+            make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                       pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+        if (p.out_f32) {
+          *reinterpret_cast<float4*>(p.out_f32 + orow + e) = make_float4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<float4*>(p.out_f32 + orow + e + 4) =
+              make_float4(o[4], o[5], o[6], o[7]);
         }
       }
     }
