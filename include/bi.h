@@ -181,9 +181,16 @@ bi_status bi_gemm_swiglu(const void* A, const void* W, void* out, int64_t M, int
  *   left fold in chunk order with the log-sum-exp rule, then o/l is rounded.
  *   Boundaries depend on absolute key indices only, never on L, B, the grid
  *   or the chunking of a prompt.
- * BI_MODE_VARIANT (fixed split COUNT, the plan the pages reject): the keys
- *   are cut into c chunks at floor(j*L/c), c = variant_splits if > 0, else
- *   c = min(64, max(ceil(2*#SM / (B*Hkv)), ceil(max_kv_len / 1024))).
+ * BI_MODE_VARIANT (a split plan sized from the batch, the kind of plan the
+ *   pages name as not batch-invariant): one chunk size C for the call,
+ *   C = 64 * max(ceil(Hkv * T / U), ceil(T_max / c)), where T is the sum and
+ *   T_max the largest of the sequences' 64-key tile counts ceil(L/64),
+ *   U = 16 * (resident split-kernel blocks on the device) the target number
+ *   of work units, and c = variant_splits if > 0, else
+ *   c = min(128, ceil(max_kv_len / 256)) the largest number of chunks a
+ *   sequence may get (it sizes the workspace);
+ *   sequence b is cut at multiples of C into ceil(L_b / C) chunks.  Every
+ *   boundary moves with the lengths of the other sequences in the call.
  * A sequence with L == 0 produces zeros.
  * Requirements: D in {64, 128}; Hq % Hkv == 0 and Hq/Hkv <= 16;
  *   page_size == 16; split_size a positive multiple of 64; num_pages >= 1;

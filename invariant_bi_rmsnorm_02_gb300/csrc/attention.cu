@@ -374,6 +374,7 @@ struct KernelParams {
   int local_plan;    // decode: the split kernel works out its units itself
   int merge_slots;   // decode merge: staged chunks in flight
   int* order;        // decode, in-kernel plan: sequences by decreasing split count
+  int target_units;  // decode variant: work units the batch is cut into (about)
   int64_t num_pages;
   float scale_log2;
   bool variant;
@@ -384,16 +385,67 @@ __device__ __forceinline__ bool len_ok(int L, const KernelParams& p) {
 }
 
 // --------------------------------------------------------------- decode plan
-// One block: the list of (sequence, split) units, in sequence order.  The
-// fixed split size gives ceil(L/S) units with boundaries at multiples of S;
-// the variant gives `split_count` units at floor(j*L/c) (some may be empty).
+// The fixed split size gives ceil(L/S) splits with boundaries at multiples of
+// S.  The batch-variant plan (as a throughput-tuned engine plans decode)
+// picks one chunk size C for the whole call from the batch itself: enough
+// chunks over all sequences and kv heads to give every SM several work units
+// (about target_units), and few enough that no sequence has more than
+// split_count (the workspace's capacity); sequence b then gets ceil(L_b / C)
+// chunks with boundaries at multiples of C.  C, and with it every boundary,
+// moves with the batch's lengths: the plan is not batch-invariant.
+__device__ __forceinline__ int variant_chunk_tiles(int64_t total_tiles, int max_tiles,
+                                                   const KernelParams& p) {
+  const int64_t units = total_tiles * p.Hkv;
+  const int64_t by_work = (units + p.target_units - 1) / p.target_units;
+  const int64_t by_cap = (max_tiles + p.split_count - 1) / p.split_count;
+  const int64_t c = by_work > by_cap ? by_work : by_cap;
+  return c < 1 ? 1 : static_cast<int>(c);
+}
+__device__ __forceinline__ int plan_splits(int L, int chunk, const KernelParams& p) {
+  const int c = p.variant ? chunk : p.split_size;
+  return (L + c - 1) / c;
+}
+
+// One block: the list of (sequence, split) units, in sequence order.
 constexpr int kPlanThreads = 1024;
 
 __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const KernelParams p) {
   __shared__ int warp_tot[32];
+  __shared__ long long warp_tiles[32];
+  __shared__ int warp_max[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int chunk = (p.B + kPlanThreads - 1) / kPlanThreads;
   const int b0 = min(p.B, tid * chunk), b1 = min(p.B, b0 + chunk);
+  int csize = 0;  // variant: the call's chunk size in keys
+  if (p.variant) {
+    long long tiles = 0;
+    int tmax = 0;
+    for (int b = b0; b < b1; ++b) {
+      const int L = p.kv_lens[b];
+      if (!len_ok(L, p)) continue;
+      tiles += (L + kTile - 1) / kTile;
+      tmax = max(tmax, (L + kTile - 1) / kTile);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      tiles += __shfl_xor_sync(kFull, tiles, o);
+      tmax = max(tmax, __shfl_xor_sync(kFull, tmax, o));
+    }
+    if (lane == 0) {
+      warp_tiles[warp] = tiles;
+      warp_max[warp] = tmax;
+    }
+    __syncthreads();
+    tiles = warp_tiles[lane];
+    tmax = warp_max[lane];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      tiles += __shfl_xor_sync(kFull, tiles, o);
+      tmax = max(tmax, __shfl_xor_sync(kFull, tmax, o));
+    }
+    csize = kTile * variant_chunk_tiles(tiles, tmax, p);
+    if (tid == 0) p.unit_count[1] = csize;
+  }
   int n = 0;
   for (int b = b0; b < b1; ++b) {
     const int L = p.kv_lens[b];
@@ -401,7 +453,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const KernelPar
       record_error(p.err, BI_ERR_DEVICE_BOUNDS);
       continue;
     }
-    if (L > 0) n += p.variant ? p.split_count : (L + p.split_size - 1) / p.split_size;
+    if (L > 0) n += plan_splits(L, csize, p);
   }
   // block exclusive scan of n
   int incl = n;
@@ -428,18 +480,9 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const KernelPar
   for (int b = b0; b < b1; ++b) {
     const int L = p.kv_lens[b];
     if (!len_ok(L, p) || L == 0) continue;
-    const int ns = p.variant ? p.split_count : (L + p.split_size - 1) / p.split_size;
-    for (int j = 0; j < ns; ++j) {
-      int lo, hi;
-      if (p.variant) {
-        lo = (int)(((int64_t)j * L) / ns);
-        hi = (int)(((int64_t)(j + 1) * L) / ns);
-      } else {
-        lo = j * p.split_size;
-        hi = min(lo + p.split_size, L);
-      }
-      p.units[base++] = make_int4(b, j, lo, hi);
-    }
+    const int ns = plan_splits(L, csize, p);
+    const int c = p.variant ? csize : p.split_size;
+    for (int j = 0; j < ns; ++j) p.units[base++] = make_int4(b, j, j * c, min((j + 1) * c, L));
   }
 }
 
@@ -508,7 +551,28 @@ __global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
   // is <= s, found with one ballot per 32 sequences.
   __shared__ int s_incl[kLocalPlanMax], s_len[kLocalPlanMax];
   int total = 0;
+  int csize = 0;  // variant: the call's chunk size in keys
   if (p.local_plan) {
+    if (p.variant) {
+      long long tiles = 0;
+      int tmax = 0;
+#pragma unroll
+      for (int k = 0; k < kLocalSlabs; ++k) {
+        const int b = lane + 32 * k;
+        const int L = b < p.B ? p.kv_lens[b] : 0;
+        if (b < p.B && len_ok(L, p)) {
+          tiles += (L + kTile - 1) / kTile;
+          tmax = max(tmax, (L + kTile - 1) / kTile);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        tiles += __shfl_xor_sync(kFull, tiles, o);
+        tmax = max(tmax, __shfl_xor_sync(kFull, tmax, o));
+      }
+      csize = kTile * variant_chunk_tiles(tiles, tmax, p);
+      if (blockIdx.x == 0 && lane == 0) p.unit_count[1] = csize;  // for the merge
+    }
 #pragma unroll
     for (int k = 0; k < kLocalSlabs; ++k) {
       const int b = lane + 32 * k;
@@ -519,7 +583,7 @@ __global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
           record_error(p.err, BI_ERR_DEVICE_BOUNDS);
           L = 0;
         }
-        if (L > 0) n = p.variant ? p.split_count : (L + p.split_size - 1) / p.split_size;
+        if (L > 0) n = plan_splits(L, csize, p);
       }
       int v = n;
 #pragma unroll
@@ -561,15 +625,8 @@ __global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
       b += __popc(__ballot_sync(kFull, s_incl[lane + 32 * k] <= s));
     const int L = s_len[b];
     const int j = s - (b > 0 ? s_incl[b - 1] : 0);
-    int lo, hi;
-    if (p.variant) {
-      lo = (int)(((int64_t)j * L) / p.split_count);
-      hi = (int)(((int64_t)(j + 1) * L) / p.split_count);
-    } else {
-      lo = j * p.split_size;
-      hi = min(lo + p.split_size, L);
-    }
-    return make_int4(b, j, lo, hi);
+    const int c = p.variant ? csize : p.split_size;
+    return make_int4(b, j, j * c, min((j + 1) * c, L));
   };
 
   // ---- opening units: one pending (page ids in flight), kQueue opened
@@ -793,9 +850,8 @@ __global__ void __launch_bounds__(D / 2 + 32) attn_decode_merge_kernel(const Ker
   const int b = p.order ? p.order[blockIdx.y] : blockIdx.y;
   const int64_t row = (int64_t)b * p.Hq + qh;
   const int L = p.kv_lens[b];
-  const int ns = (len_ok(L, p) && L > 0)
-                     ? (p.variant ? p.split_count : (L + p.split_size - 1) / p.split_size)
-                     : 0;
+  const int ns = (len_ok(L, p) && L > 0) ? plan_splits(L, p.variant ? p.unit_count[1] : 0, p)
+                                          : 0;
   const int nch = (ns + kMergeChunk - 1) / kMergeChunk;
   const int slots = p.merge_slots;
   const float2* mlrow = reinterpret_cast<const float2*>(p.ml) + row * p.ml_stride;
@@ -1588,7 +1644,6 @@ bi_status decode_impl(const AttnArgs& a, cudaStream_t s) {
     if (p.local_plan) p.order = reinterpret_cast<int*>(base + w.units_off);  // units unused
     const int chunks = (a.max_splits + kMergeChunk - 1) / kMergeChunk;
     p.merge_slots = chunks < kMergeSlots ? chunks : kMergeSlots;
-    if (!p.local_plan) attn_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
     const size_t sm = decode_smem<D, NQ>();
     if (set_smem(attn_decode_split_kernel<D, NQ>, sm) != cudaSuccess) return BI_ERR_CUDA;
     static int per_sm[2][3] = {};
@@ -1600,6 +1655,10 @@ bi_status decode_impl(const AttnArgs& a, cudaStream_t s) {
     if (sms <= 0 || occ <= 0) return BI_ERR_CUDA;
     const int64_t max_units = static_cast<int64_t>(a.B) * a.Hkv * a.max_splits;
     const int64_t cap = static_cast<int64_t>(occ) * sms;
+    // variant: 16 units per resident block (measured on GB300, 64 requests
+    // of 1..32768 keys: 2 -> 111 us, 4 -> 103, 8 -> 100, 16 -> 98 us)
+    p.target_units = static_cast<int>(16 * cap);
+    if (!p.local_plan) attn_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
     const int grid = static_cast<int>(max_units < cap ? max_units : cap);
     if (launch_pdl(attn_decode_split_kernel<D, NQ>, dim3(grid), dim3(32), sm, s, km, vm, p) !=
         cudaSuccess)
@@ -1630,14 +1689,15 @@ bi_status prefill_impl(const AttnArgs& a, cudaStream_t s) {
 }  // namespace
 
 int attn_variant_split_count(int B, int Hkv, int max_kv_len, int num_sms) {
-  // one count for the whole batch: enough units to cover the SMs twice, and
-  // at least one per 1024 keys of the longest sequence
-  const int64_t units = static_cast<int64_t>(B) * Hkv;
-  int64_t c = (2 * static_cast<int64_t>(num_sms) + units - 1) / (units > 0 ? units : 1);
-  const int64_t by_len = (static_cast<int64_t>(max_kv_len) + 1023) / 1024;
-  if (by_len > c) c = by_len;
+  // the largest number of chunks the batch-variant plan may give one
+  // sequence (it sizes the workspace): one per 256 keys of the longest
+  // sequence, at most 128
+  (void)B;
+  (void)Hkv;
+  (void)num_sms;
+  int64_t c = (static_cast<int64_t>(max_kv_len) + 255) / 256;
   if (c < 1) c = 1;
-  if (c > 64) c = 64;
+  if (c > 128) c = 128;
   return static_cast<int>(c);
 }
 

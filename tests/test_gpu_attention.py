@@ -169,7 +169,16 @@ def test_decode_large_batch_plan_matches_small_batches(cuda):
             o, o32 = decode(q[sl].contiguous(), kv, 2048, S, mode, splits=3,
                             kv_lens=kv.kv_lens[sl].contiguous(),
                             bt=kv.block_table[sl].contiguous())
-            assert same_bytes(o32, out32[sl]) and same_bytes(o, out[sl]), (mode, b0)
+            if mode == bi.INVARIANT:
+                assert same_bytes(o32, out32[sl]) and same_bytes(o, out[sl]), b0
+            else:
+                # the variant's chunk size follows the batch: a 100-sequence
+                # slice is planned differently, and only matches the oracle
+                r = [0, 37, 99]
+                ref = oracle.decode_attention(q[sl][r].cpu(), kv.k_cache.cpu(), kv.v_cache.cpu(),
+                                              kv.block_table[sl][r].cpu(),
+                                              kv.kv_lens[sl][r].cpu(), D ** -0.5)
+                check_attn(o[r], o32[r], ref, "decode slice %d variant" % b0)
         assert (out32[7] == 0).all()
         rows = [0, 7, 150, 299, int(torch.argmax(kv.kv_lens))]
         ref = oracle.decode_attention(q[rows].cpu(), kv.k_cache.cpu(), kv.v_cache.cpu(),
@@ -284,16 +293,17 @@ def test_prefill_independent_of_neighbour_sequences(cuda):
 
 
 # ------------------------------------------------------- negative controls
-def test_decode_fixed_split_count_is_not_invariant(cuda):
-    # the fixed split COUNT plan moves its boundaries with L and with B (the
-    # count is chosen to fill the SMs), so a request's bytes change
+def test_decode_variant_plan_is_not_invariant(cuda):
+    # the batch-variant plan sizes its chunks from the whole batch (with at
+    # most 8 chunks a sequence, the longest sequence present sets them), so
+    # a request's boundaries, and its bytes, change with the other requests
     lens = synth.loguniform_int(64, 300, 32000, 5200).tolist()
     kv = to_dev(synth.paged_kv(lens, 8, 128, 16, 5201), cuda)
     q = synth.normal_bf16((64, 32, 128), 5202, device=cuda)
-    ref, _ = decode(q, kv, 32768, 256, bi.VARIANT)
+    ref, _ = decode(q, kv, 32768, 256, bi.VARIANT, splits=8)
     differing = 0
     for B in (1, 2, 4, 16):
-        out, _ = decode(q[:B].contiguous(), kv, 32768, 256, bi.VARIANT,
+        out, _ = decode(q[:B].contiguous(), kv, 32768, 256, bi.VARIANT, splits=8,
                         kv_lens=kv.kv_lens[:B].contiguous(), bt=kv.block_table[:B].contiguous())
         differing += int((out.view(torch.int16) != ref[:B].view(torch.int16)).any(-1).any(-1).sum())
         inv, _ = decode(q[:B].contiguous(), kv, 32768, 256, bi.INVARIANT,
