@@ -29,6 +29,13 @@
 // Structure: persistent blocks (one per SM), 6 warps:
 //   warp 0    : TMA producer, fills a 4-stage ring of (A 128x64, W 256x64)
 //               tiles, 128-byte swizzled, completion on mbarriers;
+//               with at most 32 rows of A (a batch of a few tokens) the A
+//               stages hold 32 rows and the ring has 6 stages: the MMA still
+//               reads 128 rows of A (the rows past 32 are whatever follows in
+//               shared memory, and only reach accumulator rows that are never
+//               stored, since rows do not mix), and the weight, which is what
+//               the block streams at small M, has 192 KB in flight instead of
+//               128 KB;
 //   warp 1    : allocates 512 tensor-memory columns; one thread issues the
 //               MMAs into one of two 256-column accumulators and commits
 //               them to the ring's "empty" barriers;
@@ -50,13 +57,25 @@ namespace bi {
 namespace {
 
 constexpr int BM = kGemmBM, BN = kGemmBN, BK = kGemmBK;
-constexpr int kStages = 4;
-constexpr int kABytes = BM * BK * 2;
 constexpr int kBBytes = BN * BK * 2;
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;  // two BN-column fp32 accumulators
-constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
+constexpr int kSmallRows = 32;       // the A rows of the small-batch ring
+
+// Ring geometry: 4 stages of A (128 rows) and W, or, for at most kSmallRows
+// rows of A, 6 stages of A (kSmallRows rows) and W.
+template <bool kSmall>
+struct Ring {
+  static constexpr int kStages = kSmall ? 6 : 4;
+  static constexpr int kARows = kSmall ? kSmallRows : BM;
+  static constexpr int kABytes = kARows * BK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
+};
+// the MMA reads a 128-row A window from each A stage: it must stay inside
+// the block's shared memory (the W ring follows the A ring)
+static_assert(5 * Ring<true>::kABytes + BM * BK * 2 <= 6 * Ring<true>::kABytes + 6 * kBBytes,
+              "small-batch A window leaves shared memory");
 
 constexpr uint32_t kIdesc = umma_idesc_bf16(BM, BN, false, false);
 
@@ -112,10 +131,13 @@ enum Epilogue : int {
   kEpiSwiglu = 2,  // C [M, N/2] bf16 = silu(gate) * up of the interleaved tile halves
 };
 
-template <int kEpi>
+template <int kEpi, bool kSmall>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(
     const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
     const GemmParams p) {
+  constexpr int kStages = Ring<kSmall>::kStages;
+  constexpr int kABytes = Ring<kSmall>::kABytes;
+  constexpr int kStageBytes = Ring<kSmall>::kStageBytes;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -367,14 +389,22 @@ __global__ void splitk_reduce_swiglu_kernel(const float* __restrict__ ws, uint2*
   }
 }
 
+template <int kEpi, bool kSmall>
+bi_status launch_tc_ring(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+                         int grid, cudaStream_t s) {
+  constexpr size_t smem = Ring<kSmall>::kSmemBytes;
+  if (cudaFuncSetAttribute(gemm_tc_kernel<kEpi, kSmall>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return BI_ERR_CUDA;
+  gemm_tc_kernel<kEpi, kSmall><<<grid, kThreads, smem, s>>>(ta, tb, p);
+  return cuda_status(cudaGetLastError());
+}
 template <int kEpi>
 bi_status launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int grid,
                     cudaStream_t s) {
-  if (cudaFuncSetAttribute(gemm_tc_kernel<kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSmemBytes)) != cudaSuccess)
-    return BI_ERR_CUDA;
-  gemm_tc_kernel<kEpi><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, p);
-  return cuda_status(cudaGetLastError());
+  return p.M <= kSmallRows ? launch_tc_ring<kEpi, true>(ta, tb, p, grid, s)
+                           : launch_tc_ring<kEpi, false>(ta, tb, p, grid, s);
 }
 
 }  // namespace
@@ -384,7 +414,8 @@ bi_status launch_gemm(const void* A, const void* W, void* C, int64_t M, int64_t 
   const int sms = device_sm_count();
   if (sms <= 0) return BI_ERR_CUDA;
   CUtensorMap ta, tb;
-  if (!make_tmap_2d_bf16(&ta, A, static_cast<uint64_t>(M), static_cast<uint64_t>(K), BM, BK) ||
+  const uint32_t a_rows = M <= kSmallRows ? kSmallRows : BM;  // the A box of the ring
+  if (!make_tmap_2d_bf16(&ta, A, static_cast<uint64_t>(M), static_cast<uint64_t>(K), a_rows, BK) ||
       !make_tmap_2d_bf16(&tb, W, static_cast<uint64_t>(N), static_cast<uint64_t>(K), BN, BK))
     return BI_ERR_CUDA;
   GemmParams p{};
