@@ -162,6 +162,30 @@ __device__ __forceinline__ void split_p_bf16(float p0, float p1, uint32_t& hp, u
   lp = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
 }
 
+// Two fp32 operations in one instruction (the packed f32x2 forms of sm_100
+// and later): each lane is the IEEE operation, rounded to nearest, that the
+// scalar form computes, so the results are bit-identical to __fadd_rn /
+// __fmul_rn; the prefill softmax uses them to issue fewer instructions.
+__device__ __forceinline__ void add2_rn(float& r0, float& r1, float a0, float a1, float b0,
+                                        float b1) {
+  asm("{\n\t.reg .b64 a, b, r;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "add.rn.f32x2 r, a, b;\n\tmov.b64 {%0, %1}, r;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void mul2_rn(float& r0, float& r1, float a0, float a1, float b) {
+  asm("{\n\t.reg .b64 a, b, r;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %4};\n\t"
+      "mul.rn.f32x2 r, a, b;\n\tmov.b64 {%0, %1}, r;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b));
+}
+// The largest of three values (exact, as any fmaxf order).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // The running reference maximum of a row moves only when a tile's maximum
 // exceeds it by more than this many powers of two (and on the first tile
 // with a visible key); otherwise the tile's probabilities are taken against
@@ -1008,8 +1032,9 @@ constexpr int kPfRows = 128;
 constexpr int kPfThreads = 10 * 32;
 constexpr int kPfSoftWarp0 = 0, kPfFoldWarp0 = 4, kPfMmaWarp = 8, kPfTmaWarp = 9;
 constexpr int kPfPageCache = 1024;  // page ids held in shared memory (16384 keys)
-constexpr int kPfKStages = 3, kPfVStages = 4;
+constexpr int kPfKStages = 3;
 constexpr int kPfSBufs = 4;         // S / P buffers in tensor memory
+constexpr int kPfVStages = kPfSBufs;  // V stage i % 4 is freed by the same commit as buffer i % 4
 
 template <int D>
 struct PfGeom {
@@ -1024,9 +1049,9 @@ struct PfGeom {
   static constexpr int kXOff = kMOff + D * kPfRows * 4;       // split m, l: [parity][2][128]
   static constexpr int kPidOff = kXOff + 4 * kPfRows * 4;
   static constexpr int kBarOff = kPidOff + kPfPageCache * 4;
-  // kfull, kfree [KS]; vfull, vfree [VS]; sfull, pready, pfree [SB]; odone,
-  // sdone, folded [2]
-  static constexpr int kNumBars = 2 * kPfKStages + 2 * kPfVStages + 3 * kPfSBufs + 6;
+  // kfull, kfree [KS]; vfull [VS]; sfull, pready, pfree [SB]; odone, sdone,
+  // folded [2]
+  static constexpr int kNumBars = 2 * kPfKStages + kPfVStages + 3 * kPfSBufs + 6;
   static constexpr int kSmem = 1024 + kBarOff + kNumBars * 8;
   static constexpr uint32_t kTmemCols = 512;
   // four S / P buffers of 64 columns, two split accumulators of D columns
@@ -1063,6 +1088,19 @@ __device__ __forceinline__ bool pf_wait_lazy(uint64_t* bar, uint32_t parity, int
   return false;
 }
 
+// Wait for up to three barriers: their first tests go out back to back (the
+// common case is that all are complete), then each missing one is waited for.
+__device__ __forceinline__ bool mbar_wait3(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb,
+                                           uint64_t* c, uint32_t pc, int* err,
+                                           volatile int* abort) {
+  const bool ra = mbar_try_wait(a, pa);
+  const bool rb = b == nullptr || mbar_try_wait(b, pb);
+  const bool rc = c == nullptr || mbar_try_wait(c, pc);
+  if (ra && rb && rc) return true;
+  return (ra || mbar_wait(a, pa, err, abort)) && (rb || mbar_wait(b, pb, err, abort)) &&
+         (rc || mbar_wait(c, pc, err, abort));
+}
+
 // D (tmem) += A (tmem) * B (smem descriptor), one CTA, kind::f16.
 __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
                                           uint32_t idesc, uint32_t accumulate) {
@@ -1093,10 +1131,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + Gm::kBarOff);  // K tile landed
   uint64_t* kfree = kfull + kPfKStages;    // the S that read the K stage is done
   uint64_t* vfull = kfree + kPfKStages;    // V tile landed
-  uint64_t* vfree = vfull + kPfVStages;    // the PV that read the V stage is done
-  uint64_t* sfull = vfree + kPfVStages;    // S of the tile computed
+  uint64_t* sfull = vfull + kPfVStages;    // S of the tile computed
   uint64_t* pready = sfull + kPfSBufs;     // P of the tile written over it
-  uint64_t* pfree = pready + kPfSBufs;     // PV of the tile done (buffer free)
+  uint64_t* pfree = pready + kPfSBufs;     // PV of the tile done (buffer and V stage free)
   uint64_t* odone = pfree + kPfSBufs;      // the last PV of a split done
   uint64_t* sdone = odone + 2;             // a split's m, l written
   uint64_t* folded = sdone + 2;            // a split folded (its accumulator free)
@@ -1149,7 +1186,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     }
     for (int i = 0; i < kPfVStages; ++i) {
       mbar_init(&vfull[i], 1);
-      mbar_init(&vfree[i], 1);
     }
     for (int i = 0; i < kPfSBufs; ++i) {
       mbar_init(&sfull[i], 1);
@@ -1183,7 +1219,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   if (warp == kPfTmaWarp) {
     // ================================================================ copies
     // One thread.  Tile i: K into stage i % KS once the S of tile i - KS is
-    // done, V into stage i % VS once the PV of tile i - VS is.
+    // done, V into stage i % VS once the PV of tile i - VS is (pfree).
     if (lane == 0) {
       auto issue_tile = [&](int i, bool is_v) {
         uint8_t* dst = is_v ? vst + (i % kPfVStages) * Gm::kTBytes
@@ -1210,7 +1246,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
         issue_tile(i, false);
         ++nk;
         if (i >= kPfVStages)
-          ok = pf_wait_lazy(&vfree[i % kPfVStages], ((i / kPfVStages) - 1) & 1, p.err, &s_abort);
+          ok = pf_wait_lazy(&pfree[i % kPfVStages], ((i / kPfVStages) - 1) & 1, p.err, &s_abort);
         if (!ok) break;
         issue_tile(i, true);
         ++nv;
@@ -1239,8 +1275,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       // reader of its buffer) is done
       auto issue_s = [&](int i) -> bool {
         const int ks_ = i % kPfKStages, sb = i % kPfSBufs;
-        if (!mbar_wait(&kfull[ks_], (i / kPfKStages) & 1, p.err, &s_abort)) return false;
-        if (i >= kPfSBufs && !mbar_wait(&pfree[sb], ((i / kPfSBufs) - 1) & 1, p.err, &s_abort))
+        if (!mbar_wait3(&kfull[ks_], (i / kPfKStages) & 1, i >= kPfSBufs ? &pfree[sb] : nullptr,
+                        ((i / kPfSBufs) - 1) & 1, nullptr, 0, p.err, &s_abort))
           return false;
         tc_fence_after();
         const uint64_t kb = kd + static_cast<uint64_t>(ks_ * (Gm::kTBytes >> 4));
@@ -1271,11 +1307,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
           ok = false;
           break;
         }
-        ok = mbar_wait(&vfull[stg], (i / kPfVStages) & 1, p.err, &s_abort) &&
-             mbar_wait(&pready[sb], (i / kPfSBufs) & 1, p.err, &s_abort);
-        // the split's accumulator was last used two splits ago: its fold must be done
-        if (ok && split_first && j >= 2)
-          ok = mbar_wait(&folded[j & 1], ((j - 2) >> 1) & 1, p.err, &s_abort);
+        // V landed, P written, and (at a split's first tile) the fold of the
+        // split that last used this accumulator, two splits ago, done
+        ok = mbar_wait3(&vfull[stg], (i / kPfVStages) & 1, &pready[sb], (i / kPfSBufs) & 1,
+                        split_first && j >= 2 ? &folded[j & 1] : nullptr, ((j - 2) >> 1) & 1,
+                        p.err, &s_abort);
         if (!ok) break;
         if (key0 + kTile > kvl) {  // keys past the end: zero their V rows before PV
           const int first = kvl - key0;
@@ -1298,8 +1334,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
           tc_mma_ts(od, pa + 8 * kk, bd, kIdescPV, (split_first && kk == 0) ? 0u : 1u);
           tc_mma_ts(od, pa + 32 + 8 * kk, bd, kIdescPV, 1u);
         }
-        tc_commit(&pfree[sb]);
-        tc_commit(&vfree[stg]);
+        tc_commit(&pfree[sb]);  // buffer sb and V stage stg (the same index) are free
         if (split_last) tc_commit(&odone[j & 1]);
         last_bar = &pfree[sb];
         last_par = (i / kPfSBufs) & 1;
@@ -1338,24 +1373,23 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       // keys key0 .. key0 + nvis - 1 are visible to this row (the tile lies
       // inside one split, which starts at or before key0)
       const int nvis = pos >= key0 ? min(kTile, pos + 1 - key0) : 0;
-      if (key0 + kTile - 1 <= start + tok0) {  // every row of the block sees the whole tile
 #pragma unroll
-        for (int e = 0; e < 64; ++e) x[e] = __fmul_rn(x[e], p.scale_log2);
-      } else {
+      for (int e = 0; e < 64; e += 2) mul2_rn(x[e], x[e + 1], x[e], x[e + 1], p.scale_log2);
+      if (key0 + kTile - 1 > start + tok0) {  // some row of the block sees part of the tile
 #pragma unroll
-        for (int e = 0; e < 64; ++e)
-          x[e] = e < nvis ? __fmul_rn(x[e], p.scale_log2) : -CUDART_INF_F;
+        for (int e = 0; e < 64; ++e) x[e] = e < nvis ? x[e] : -CUDART_INF_F;
       }
       float mx;
       {
-        float t[32];  // the row maximum is exact in any order: a tree
+        float t[22];  // the row maximum is exact in any order: a tree of 3-way maxima
 #pragma unroll
-        for (int e = 0; e < 32; ++e) t[e] = fmaxf(x[2 * e], x[2 * e + 1]);
+        for (int e = 0; e < 21; ++e) t[e] = max3(x[3 * e], x[3 * e + 1], x[3 * e + 2]);
+        t[21] = x[63];
+        float u[8];
 #pragma unroll
-        for (int w = 16; w >= 1; w >>= 1)
-#pragma unroll
-          for (int e = 0; e < w; ++e) t[e] = fmaxf(t[2 * e], t[2 * e + 1]);
-        mx = t[0];
+        for (int e = 0; e < 7; ++e) u[e] = max3(t[3 * e], t[3 * e + 1], t[3 * e + 2]);
+        u[7] = t[21];
+        mx = max3(max3(u[0], u[1], u[2]), max3(u[3], u[4], u[5]), fmaxf(u[6], u[7]));
       }
       const float m_in = split_first ? -CUDART_INF_F : m;
       float mnew = m_in, alpha = 1.0f;  // the decode's reference rule (kRescaleLog2)
@@ -1383,14 +1417,22 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
         for (int c = 0; c < 4; ++c) {  // keys 32hf+8c .. 32hf+8c+7
           const int k0 = 32 * hf + 8 * c;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float pv = exp2_sfu(__fsub_rn(x[k0 + e], mb));
-            x[k0 + e] = pv;
-            cs[e] = __fadd_rn(cs[e], pv);
+          for (int e = 0; e < 8; e += 2) {  // x - mb as x + (-mb): the same rounding
+            add2_rn(x[k0 + e], x[k0 + e + 1], x[k0 + e], x[k0 + e + 1], -mb, -mb);
+            x[k0 + e] = exp2_sfu(x[k0 + e]);
+            x[k0 + e + 1] = exp2_sfu(x[k0 + e + 1]);
+            add2_rn(cs[e], cs[e + 1], cs[e], cs[e + 1], x[k0 + e], x[k0 + e + 1]);
           }
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            split_p_bf16(x[k0 + 2 * e], x[k0 + 2 * e + 1], ph[4 * c + e], pl[4 * c + e]);
+          for (int e = 0; e < 4; ++e) {  // split_p_bf16, both remainders in one instruction
+            const float p0 = x[k0 + 2 * e], p1 = x[k0 + 2 * e + 1];
+            const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+            ph[4 * c + e] = __byte_perm(b0, b1, 0x7632);
+            float r0, r1;
+            add2_rn(r0, r1, p0, p1, -__uint_as_float(b0 & 0xffff0000u),
+                    -__uint_as_float(b1 & 0xffff0000u));
+            pl[4 * c + e] = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+          }
         }
         tmem_st16(sa + 16 * hf, ph);
         tmem_st16(sa + 32 + 16 * hf, pl);
