@@ -117,7 +117,9 @@ size_t bi_rmsnorm_workspace_size(int64_t M, int64_t H, bi_mode mode);
  *   instruction and the split are the two freedoms to give up).  Needs no
  *   workspace.
  * VARIANT: same tile and instruction, but K is split into s slices chosen
- *   from M, N and the SM count (split-K, P1 §5.4); fp32 slice results are
+ *   from M, N and the SM count (split-K, P1 §5.4: only when the output tiles
+ *   cover at most a quarter of the SMs, then doubling until the slices cover
+ *   them, at least 4 k-blocks per slice); fp32 slice results are
  *   summed in slice order by a second kernel.  s = variant_splits if > 0.
  * Requirements: M >= 0, N >= 1, K >= 1, N % 8 == 0, K % 8 == 0 (16-byte rows
  *   for the tensor-memory-access engine), all dims < 2^31.

@@ -67,12 +67,15 @@ def test_workspace_sizes_are_host_arithmetic(lib):
 
 
 def test_gemm_variant_split_count(lib):
-    # split-K only when the tiles do not cover the SMs, at least 4 k-blocks per slice
+    # split-K only when the tiles cover at most a quarter of the SMs, then
+    # until the slices cover them, at least 4 k-blocks per slice
     assert bi.bi_gemm_variant_splits(8192, 6144, 4096, 152) == 1
     assert bi.bi_gemm_variant_splits(1, 6144, 4096, 152) == 8     # 24 tiles -> 8 slices
-    assert bi.bi_gemm_variant_splits(1, 14336, 4096, 152) == 4    # 56 tiles
+    assert bi.bi_gemm_variant_splits(1, 14336, 4096, 152) == 1    # 56 tiles: no split
     assert bi.bi_gemm_variant_splits(1, 512, 256, 152) == 1       # K = 4 k-blocks
-    assert bi.bi_gemm_variant_splits(256, 6144, 4096, 152) == 4   # 48 tiles
+    assert bi.bi_gemm_variant_splits(256, 6144, 4096, 152) == 1   # 48 tiles: no split
+    assert bi.bi_gemm_variant_splits(128, 6144, 4096, 152) == 8   # 24 tiles
+    assert bi.bi_gemm_variant_splits(1, 2048, 4096, 152) == 16    # 8 tiles, 4 k-blocks a slice
 
 
 def _call_rms(lib, x, w, y, M, H, eps=1e-6, mode=0, ws=None, wsb=0):
