@@ -333,15 +333,14 @@ __device__ __forceinline__ void issue_pages(uint8_t* buf, uint64_t* bar, const C
                                             int Hkv, int h) {
   // each cached K/V byte is read once per call: evict it first, so that the
   // split partials written meanwhile are still in L2 for the merge
+  // One copy per page and tensor: the page's 16 rows of this head, both
+  // 128-byte column groups (the maps' boxes are whole rows).
   const uint64_t pol = l2_policy_evict_first();
   for (int p = 0; p < np; ++p) {
     const int y = (pid[p] * Hkv + h) * kPage;
-#pragma unroll
-    for (int hf = 0; hf < TileGeom<D>::kHalves; ++hf) {
-      const int off = (p * TileGeom<D>::kHalves + hf) * 2048;
-      tma_load_2d_hint(buf + off, km, hf * 64, y, bar, pol);
-      tma_load_2d_hint(buf + TileGeom<D>::kKBytes + off, vm, hf * 64, y, bar, pol);
-    }
+    const int off = p * TileGeom<D>::kPageBytes;
+    tma_load_3d_hint(buf + off, km, 0, y, 0, bar, pol);
+    tma_load_3d_hint(buf + TileGeom<D>::kKBytes + off, vm, 0, y, 0, bar, pol);
   }
 }
 
@@ -396,8 +395,7 @@ struct KernelParams {
   int B, Hq, Hkv, G, max_blocks, max_kv_len, split_size, split_count, max_splits;
   int ml_stride;     // decode partials: {m, l} pairs per (b, q-head) row, even
   int local_plan;    // decode: the split kernel works out its units itself
-  int merge_slots;   // decode merge: staged chunks in flight
-  int* order;        // decode, in-kernel plan: sequences by decreasing split count
+  int2* order;       // decode, in-kernel plan: {sequence, split count}, most splits first
   int target_units;  // decode variant: work units the batch is cut into (about)
   int64_t num_pages;
   float scale_log2;
@@ -635,12 +633,23 @@ __global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
         }
       }
       ahead = __reduce_add_sync(kFull, ahead);
-      if (lane == 0) p.order[ahead] = x;
+      if (lane == 0) p.order[ahead] = make_int2(x, nx);
     }
   } else {
     total = *p.unit_count;
+    if (p.variant) csize = p.unit_count[1];
   }
   const int U = total * Hkv;
+  // A sequence with a single split has no merge: its unit writes the output
+  // itself (o / l, the merge's arithmetic for one split).  Split 0 is the
+  // only one iff it ends below the chunk size or the sequence is exactly
+  // one chunk long.
+  auto single_split = [&](int b, int j, int hi) -> bool {
+    if (j != 0) return false;
+    const int c = p.variant ? csize : p.split_size;
+    if (hi < c) return true;
+    return (p.local_plan ? s_len[b] : p.kv_lens[b]) == c;
+  };
   auto unit_at = [&](int s) -> int4 {  // {b, j, lo, hi} of split s; warp-uniform s
     if (!p.local_plan) return p.units[s];
     int b = 0;
@@ -772,7 +781,12 @@ __global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
     const int64_t row0 = (int64_t)b * p.Hq + (int64_t)h * G;  // first q-head row
     if (!pages_good || lo >= hi) {
       // bad pages (l = -1 makes the merge emit zeros) or an empty split
-      if (lane < G) {
+      if (!pages_good && single_split(b, j, hi)) {
+        for (int i = lane; i < G * D; i += 32) {
+          static_cast<__nv_bfloat16*>(p.out)[row0 * D + i] = __float2bfloat16_rn(0.0f);
+          if (p.out_f32) p.out_f32[row0 * D + i] = 0.0f;
+        }
+      } else if (lane < G) {
         const int64_t s = (row0 + lane) * p.ml_stride + j;
         p.ml[2 * s] = -CUDART_INF_F;
         p.ml[2 * s + 1] = pages_good ? 0.0f : -1.0f;
@@ -815,6 +829,31 @@ __global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
       issue();
     }
     if (!alive) break;
+    if (single_split(b, j, hi)) {
+      // ---- the output of the valid columns
+#pragma unroll
+      for (int nq = 0; nq < NQ; ++nq)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int col = 8 * nq + 2 * t + cc;
+          if (col >= G) continue;
+          const float lv = st.l[nq][cc];
+          const int64_t orow = (row0 + col) * D;
+#pragma unroll
+          for (int md = 0; md < D / 16; ++md)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const float v = lv > 0.0f ? __fdiv_rn(st.o[md][nq][2 * hh + cc], lv) : 0.0f;
+              const int64_t idx = orow + 16 * md + g + 8 * hh;
+              static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
+              if (p.out_f32) p.out_f32[idx] = v;
+            }
+        }
+      ++n_popped;
+      top_up();
+      issue();
+      continue;
+    }
     // ---- partial state of the valid columns
 #pragma unroll
     for (int nq = 0; nq < NQ; ++nq)
@@ -845,161 +884,102 @@ __global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
 }
 
 // ------------------------------------------------------------ decode merge
-// Block (qh, b): D/2 fold threads (two output columns each) and one
-// coefficient warp.  The left fold over the splits in index order, then
-// o / l.  Empty splits are skipped; a split marked l = -1 (bad pages) makes
-// the whole row zero.  The partial rows and their {m, l} pairs are staged by
-// bulk copies in chunks of kMergeChunk splits, merge_slots chunks in flight.
-// The fold's data dependences are split apart: the running maximum before
-// each split is a prefix maximum (exact in any order), so the coefficient
-// warp derives the coefficients of a whole chunk at once, a chunk or more
-// ahead of the fold threads; the fold proper is then a chain of products and
-// sums with one select per split and no branch, bit-identical to folding one
-// split at a time.  Per chunk and slot: `landed` (the copies), `ready` (its
-// coefficients), `consumed` (every fold thread is done with the slot).
-constexpr int kMergeChunk = 16;
-constexpr int kMergeSlots = 4;
+// Block (qh, rank): one q-head row of the rank-th longest sequence (longest
+// first), D threads, one output column each.  Each warp folds its 32
+// columns over the splits in index order, 32 splits per chunk.  Lane j of a
+// warp loads split j's {m, l} and derives that split's coefficients: the
+// running maximum before a split is a prefix maximum, exact in any order,
+// so the whole chunk's coefficients come from one scan; the fold proper is
+// then a chain of products and sums with one select per split and no
+// branch, bit-identical to folding one split at a time.  Empty splits are
+// skipped; a split marked l = -1 (bad pages) makes the whole row zero.  The
+// o values of a chunk are loaded at once (one coalesced 128-byte row per
+// split and warp), and the next chunk's loads are issued before the current
+// chunk is folded.  No shared memory and no waits: the row's latency is a
+// load round trip per chunk plus the fold chain.  A row of a sequence with a
+// single split was written by the split kernel and is skipped here.
+constexpr int kMergeChunk = 32;
 
 template <int D>
-__global__ void __launch_bounds__(D / 2 + 32) attn_decode_merge_kernel(const KernelParams p) {
-  constexpr int kFold = D / 2;  // fold threads; the coefficient warp follows them
-  extern __shared__ __align__(16) float mo[];  // [slot][kMergeChunk][D]
-  __shared__ __align__(16) float2 sml[kMergeSlots][kMergeChunk];
-  __shared__ float2 scoef[kMergeSlots][kMergeChunk];  // ca, cb of each split of the chunk
-  __shared__ int skind[kMergeSlots][kMergeChunk];     // 0 empty, 1 first non-empty, 2 fold in
-  __shared__ uint64_t landed[kMergeSlots], ready[kMergeSlots], consumed[kMergeSlots];
-  __shared__ int s_abort, s_bad;
-  const int qh = blockIdx.x, tid = threadIdx.x;
+__global__ void __launch_bounds__(D) attn_decode_merge_kernel(const KernelParams p) {
+  const int qh = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
   grid_dependency_wait();  // every split kernel block has finished
-  const int b = p.order ? p.order[blockIdx.y] : blockIdx.y;
+  int b, ns;
+  if (p.order) {
+    const int2 e = p.order[blockIdx.y];
+    b = e.x;
+    ns = e.y;
+  } else {
+    b = blockIdx.y;
+    const int L = p.kv_lens[b];
+    ns = (len_ok(L, p) && L > 0) ? plan_splits(L, p.variant ? p.unit_count[1] : 0, p) : 0;
+  }
+  if (ns == 1) return;  // the split kernel wrote this row
   const int64_t row = (int64_t)b * p.Hq + qh;
-  const int L = p.kv_lens[b];
-  const int ns = (len_ok(L, p) && L > 0) ? plan_splits(L, p.variant ? p.unit_count[1] : 0, p)
-                                          : 0;
-  const int nch = (ns + kMergeChunk - 1) / kMergeChunk;
-  const int slots = p.merge_slots;
   const float2* mlrow = reinterpret_cast<const float2*>(p.ml) + row * p.ml_stride;
-  const float* orow = p.o + row * p.max_splits * D;
-  auto issue = [&](int c) {  // one thread: chunk c into slot c % slots
-    const int j0 = c * kMergeChunk, cnt = min(kMergeChunk, ns - j0), slot = c % slots;
-    const uint32_t ob = cnt * D * 4, mb = ((cnt + 1) & ~1) * 8;  // the row stride is even
-    mbar_arrive_expect_tx(&landed[slot], ob + mb);
-    bulk_load(mo + slot * kMergeChunk * D, orow + (int64_t)j0 * D, ob, &landed[slot]);
-    bulk_load(&sml[slot][0], mlrow + j0, mb, &landed[slot]);
-  };
-  if (tid == 0) {
-    s_abort = 0;
-    s_bad = 0;
-    for (int i = 0; i < slots; ++i) {
-      mbar_init(&landed[i], 1);
-      mbar_init(&ready[i], 1);
-      mbar_init(&consumed[i], kFold);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (tid >= kFold) {
-    // ================================================= coefficient warp
-    // A slot is refilled once every fold thread has consumed it, so no
-    // barrier here is ever more than one phase ahead of its waiter.
-    const int lane = tid - kFold;
-    float run_m = -CUDART_INF_F;  // max over the splits folded so far
-    bool have = false;            // a non-empty split was folded
-    const int first = min(nch, slots);
-    if (lane == 0)
-      for (int c = 0; c < first; ++c) issue(c);
-    int issued = first, waited = 0;
-    bool ok = true;
-    for (int c = 0; c < nch; ++c) {
-      const int slot = c % slots;
-      if (c >= slots) {
-        ok = __all_sync(kFull, mbar_wait(&consumed[slot], ((c - slots) / slots) & 1, p.err,
-                                         &s_abort));
-        if (!ok) break;
-        if (lane == 0) issue(c);
-        ++issued;
-      }
-      ok = __all_sync(kFull, mbar_wait(&landed[slot], (c / slots) & 1, p.err, &s_abort));
-      if (!ok) break;
-      ++waited;
-      const int cnt = min(kMergeChunk, ns - c * kMergeChunk);
-      float m = -CUDART_INF_F, lj = 0.0f;
-      if (lane < cnt) {
-        const float2 v = sml[slot][lane];
-        m = v.x;
-        lj = v.y;
-      }
-      const bool nonempty = m != -CUDART_INF_F;
-      float pm = m;  // inclusive prefix max over the chunk
+  const float* ocol = p.o + row * p.max_splits * D + tid;
+  // chunk starting at split c0: {m, l} of split c0 + lane, o of every split
+  auto load = [&](int c0, float2& ml, float (&ov)[kMergeChunk]) {
+    const int cnt = min(kMergeChunk, ns - c0);
+    ml = lane < cnt ? mlrow[c0 + lane] : make_float2(-CUDART_INF_F, 0.0f);
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float t = __shfl_up_sync(kFull, pm, o);
-        if (lane >= o) pm = fmaxf(pm, t);
-      }
-      float before = __shfl_up_sync(kFull, pm, 1);
-      before = fmaxf(run_m, lane == 0 ? -CUDART_INF_F : before);
-      const unsigned ne = __ballot_sync(kFull, nonempty);
-      const bool had = have || (ne & ((1u << lane) - 1u)) != 0;
-      if (__any_sync(kFull, lj < 0.0f) && lane == 0) s_bad = 1;
-      if (lane < cnt) {
-        float ca = 0.0f, cb = 0.0f;
-        if (nonempty && had) {
-          float mn;
-          lse_coeffs(before, m, mn, ca, cb);
-        }
-        scoef[slot][lane] = make_float2(ca, cb);
-        skind[slot][lane] = nonempty ? (had ? 2 : 1) : 0;
-      }
-      run_m = fmaxf(run_m, __shfl_sync(kFull, pm, 31));
-      have = have || ne != 0;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ready[slot]);
+    for (int j = 0; j < kMergeChunk; ++j)
+      ov[j] = j < cnt ? ocol[static_cast<int64_t>(c0 + j) * D] : 0.0f;
+  };
+  float run_m = -CUDART_INF_F;  // max over the splits folded so far
+  bool have = false;            // a non-empty split was folded
+  bool bad = false;             // a split with bad pages
+  float o = 0.0f, l = 0.0f;
+  float2 ml;
+  float ov[kMergeChunk];
+  if (ns > 0) load(0, ml, ov);
+  for (int c0 = 0; c0 < ns; c0 += kMergeChunk) {
+    float2 ml_next = make_float2(-CUDART_INF_F, 0.0f);
+    float ov_next[kMergeChunk];
+    if (c0 + kMergeChunk < ns) load(c0 + kMergeChunk, ml_next, ov_next);
+    // coefficients of split c0 + lane
+    const float m = ml.x, lj = ml.y;
+    const bool nonempty = m != -CUDART_INF_F;
+    float pm = m;  // inclusive prefix max over the chunk
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+      const float t = __shfl_up_sync(kFull, pm, s);
+      if (lane >= s) pm = fmaxf(pm, t);
     }
-    if (!ok && lane == 0)
-      // a wait gave up: the copies still in flight land before the block exits
-      for (int i = waited; i < issued; ++i) mbar_wait(&landed[i % slots], (i / slots) & 1, nullptr);
-    return;
-  }
-  // ===================================================== fold threads
-  const int d = tid * 2;
-  float o0 = 0.0f, o1 = 0.0f, l = 0.0f;
-  bool ok = true;
-  for (int c = 0; c < nch; ++c) {
-    const int slot = c % slots;
-    // `ready` follows `landed`; waiting on both makes the copied bytes this
-    // thread's own observation (neither barrier can be a phase ahead here)
-    if (!mbar_wait(&ready[slot], (c / slots) & 1, p.err, &s_abort) ||
-        !mbar_wait(&landed[slot], (c / slots) & 1, p.err, &s_abort)) {
-      ok = false;
-      break;
+    float before = __shfl_up_sync(kFull, pm, 1);
+    before = fmaxf(run_m, lane == 0 ? -CUDART_INF_F : before);
+    const unsigned ne = __ballot_sync(kFull, nonempty);
+    const bool had = have || (ne & ((1u << lane) - 1u)) != 0;
+    bad = bad || __any_sync(kFull, lj < 0.0f);
+    float ca = 0.0f, cb = 0.0f;
+    if (nonempty && had) {
+      float mn;
+      lse_coeffs(before, m, mn, ca, cb);
     }
-    const int cnt = min(kMergeChunk, ns - c * kMergeChunk);
-    const float* ms = mo + slot * kMergeChunk * D + d;
-    // every entry of the slot is read (stale ones past cnt are discarded by
-    // the select), so the loads of later splits need not wait for earlier ones
+    const int kind = nonempty ? (had ? 2 : 1) : 0;  // 0 empty, 1 first non-empty, 2 fold in
+    run_m = fmaxf(run_m, __shfl_sync(kFull, pm, 31));
+    have = have || ne != 0;
 #pragma unroll
     for (int j = 0; j < kMergeChunk; ++j) {
-      const int kind = j < cnt ? skind[slot][j] : 0;
-      const float2 oj = *reinterpret_cast<const float2*>(ms + j * D);
-      const float lj = sml[slot][j].y;
-      const float2 cf = scoef[slot][j];
-      const float nl = lse_mix(l, cf.x, lj, cf.y);
-      const float n0 = lse_mix(o0, cf.x, oj.x, cf.y);
-      const float n1 = lse_mix(o1, cf.x, oj.y, cf.y);
-      l = kind == 2 ? nl : (kind == 1 ? lj : l);
-      o0 = kind == 2 ? n0 : (kind == 1 ? oj.x : o0);
-      o1 = kind == 2 ? n1 : (kind == 1 ? oj.y : o1);
+      const int kj = __shfl_sync(kFull, kind, j);
+      const float caj = __shfl_sync(kFull, ca, j), cbj = __shfl_sync(kFull, cb, j);
+      const float lsj = __shfl_sync(kFull, lj, j);
+      const float nl = lse_mix(l, caj, lsj, cbj);
+      const float no = lse_mix(o, caj, ov[j], cbj);
+      l = kj == 2 ? nl : (kj == 1 ? lsj : l);
+      o = kj == 2 ? no : (kj == 1 ? ov[j] : o);
     }
-    mbar_arrive(&consumed[slot]);
+    ml = ml_next;
+#pragma unroll
+    for (int j = 0; j < kMergeChunk; ++j) ov[j] = ov_next[j];
   }
-  float r0 = 0.0f, r1 = 0.0f;
-  if (ok && ns > 0 && !s_bad && l > 0.0f) {
-    r0 = __fdiv_rn(o0, l);
-    r1 = __fdiv_rn(o1, l);
-  }
-  const int64_t oidx = row * D + d;
-  *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.out) + oidx) = pack_bf16x2(r0, r1);
-  if (p.out_f32) *reinterpret_cast<float2*>(p.out_f32 + oidx) = make_float2(r0, r1);
+  const float r = (ns > 0 && !bad && l > 0.0f) ? __fdiv_rn(o, l) : 0.0f;
+  const int64_t oidx = row * D + tid;
+  const float r_next = __shfl_down_sync(kFull, r, 1);
+  if ((tid & 1) == 0)
+    *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.out) + oidx) =
+        pack_bf16x2(r, r_next);
+  if (p.out_f32) p.out_f32[oidx] = r;
 }
 
 // ---------------------------------------------------- prefill (tcgen05)
@@ -1624,6 +1604,12 @@ bool make_kv_maps(const AttnArgs& a, CUtensorMap* km, CUtensorMap* vm) {
   return make_tmap_2d_bf16(km, a.k_cache, rows, a.D, kPage, 64) &&
          make_tmap_2d_bf16(vm, a.v_cache, rows, a.D, kPage, 64);
 }
+// Decode: one box per (page, kv head), both column groups of its 16 rows.
+bool make_kv_page_maps(const AttnArgs& a, CUtensorMap* km, CUtensorMap* vm) {
+  const uint64_t rows = static_cast<uint64_t>(a.num_pages) * a.Hkv * kPage;
+  return make_tmap_pages_bf16(km, a.k_cache, rows, a.D, kPage) &&
+         make_tmap_pages_bf16(vm, a.v_cache, rows, a.D, kPage);
+}
 
 // Launch with programmatic stream serialisation: the kernel may begin while
 // the previous one in the stream drains, and waits for it in-kernel.
@@ -1651,7 +1637,7 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 
 // Workspace carve-up for decode: [unit count | units | {m,l} | o].  The
 // {m, l} rows hold an even number of pairs so that every row starts on a
-// 16-byte boundary for the merge's bulk copies.
+// 16-byte boundary.
 struct DecodeWs {
   size_t units_off, ml_off, o_off, total;
   int ml_stride;
@@ -1671,10 +1657,9 @@ DecodeWs decode_ws_layout(int B, int Hq, int D, int max_splits) {
 template <int D, int NQ>
 bi_status decode_impl(const AttnArgs& a, cudaStream_t s) {
   KernelParams p = make_params(a);
-  p.merge_slots = 1;
   if (a.max_splits > 0) {
     CUtensorMap km, vm;
-    if (!make_kv_maps(a, &km, &vm)) return BI_ERR_CUDA;
+    if (!make_kv_page_maps(a, &km, &vm)) return BI_ERR_CUDA;
     const DecodeWs w = decode_ws_layout(a.B, a.Hq, a.D, a.max_splits);
     char* base = reinterpret_cast<char*>(a.ws);
     p.unit_count = reinterpret_cast<int*>(base);
@@ -1683,9 +1668,7 @@ bi_status decode_impl(const AttnArgs& a, cudaStream_t s) {
     p.o = reinterpret_cast<float*>(base + w.o_off);
     p.ml_stride = w.ml_stride;
     p.local_plan = a.B <= kLocalPlanMax;
-    if (p.local_plan) p.order = reinterpret_cast<int*>(base + w.units_off);  // units unused
-    const int chunks = (a.max_splits + kMergeChunk - 1) / kMergeChunk;
-    p.merge_slots = chunks < kMergeSlots ? chunks : kMergeSlots;
+    if (p.local_plan) p.order = reinterpret_cast<int2*>(base + w.units_off);  // units unused
     const size_t sm = decode_smem<D, NQ>();
     if (set_smem(attn_decode_split_kernel<D, NQ>, sm) != cudaSuccess) return BI_ERR_CUDA;
     static int per_sm[2][3] = {};
@@ -1706,9 +1689,7 @@ bi_status decode_impl(const AttnArgs& a, cudaStream_t s) {
         cudaSuccess)
       return BI_ERR_CUDA;
   }
-  // at most 32 KB: under the default dynamic shared memory limit
-  const size_t msm = static_cast<size_t>(p.merge_slots) * kMergeChunk * D * sizeof(float);
-  if (launch_pdl(attn_decode_merge_kernel<D>, dim3(a.Hq, a.B), dim3(D / 2 + 32), msm, s, p) !=
+  if (launch_pdl(attn_decode_merge_kernel<D>, dim3(a.Hq, a.B), dim3(D), 0, s, p) !=
       cudaSuccess)
     return BI_ERR_CUDA;
   return BI_OK;

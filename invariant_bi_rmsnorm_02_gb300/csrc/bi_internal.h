@@ -21,6 +21,12 @@ int device_sm_count();
 // driver entry point is unavailable or the encoding is rejected.
 bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                        uint32_t box_rows, uint32_t box_cols);
+// Encode a bf16 tensor map over the same matrix whose box is box_rows whole
+// rows: the rows' 128-byte column groups land one after another in shared
+// memory (group g of every row, then group g + 1), each group with the
+// 128-byte swizzle of a box_rows x 64 box.  cols must be a multiple of 64.
+bool make_tmap_pages_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                          uint32_t box_rows);
 
 inline bi_status cuda_status(cudaError_t e) { return e == cudaSuccess ? BI_OK : BI_ERR_CUDA; }
 
