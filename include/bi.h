@@ -111,12 +111,16 @@ size_t bi_rmsnorm_workspace_size(int64_t M, int64_t H, bi_mode mode);
  *   A [M,K] bf16 (activations, K contiguous), W [N,K] bf16 (a Linear weight,
  *   K contiguous), C [M,N] bf16.  fp32 accumulation in tensor memory, one
  *   rounding to bf16 at the end.
- * INVARIANT: one tile shape (128 x 256 outputs), one tensor-core instruction
- *   (tcgen05.mma kind::f16, 128x256x16) and one K order (k-blocks of 64 in
- *   increasing k) for every M; no split-K, no stream-K (P1 §5.4: the
- *   instruction and the split are the two freedoms to give up).  Needs no
- *   workspace.
- * VARIANT: same tile and instruction, but K is split into s slices chosen
+ * INVARIANT: one tensor-core instruction family (tcgen05.mma kind::f16,
+ *   M=128, K=16) and one K order (k-blocks of 64 in increasing k) for every
+ *   M; no split-K, no stream-K (P1 §5.4: the instruction and the split are
+ *   the two freedoms to give up).  Output tiles are 128 x 256, or 128 x 64
+ *   (instruction N=64) for M <= 64 when ceil(N/64) tiles fit in one wave of
+ *   the device's SMs, K % 64 == 0 and K >= 256: more blocks then stream the
+ *   weight.  The instruction's N does not change any output element's sum
+ *   (every element has the same bytes at N = 64 and N = 256 on sm_103a), so
+ *   a row's bytes do not depend on M.  Needs no workspace.
+ * VARIANT: same tiles and instruction, but K is split into s slices chosen
  *   from M, N and the SM count (split-K, P1 §5.4: only when the output tiles
  *   cover at most a quarter of the SMs, then doubling until the slices cover
  *   them, at least 4 k-blocks per slice); fp32 slice results are
@@ -136,7 +140,9 @@ size_t bi_gemm_workspace_size(int64_t M, int64_t N, int64_t K, bi_mode mode,
                               int variant_splits);
 
 /* Split count bi_gemm uses in BI_MODE_VARIANT for this shape on a device
- * with num_sms SMs (1 = no split).  Host arithmetic only. */
+ * with num_sms SMs (1 = no split), counted over the tiles bi_gemm runs for
+ * it (above); bi_gemm_swiglu uses the count of its [M, 2F] shape.  Host
+ * arithmetic only. */
 int bi_gemm_variant_splits(int64_t M, int64_t N, int64_t K, int num_sms);
 
 /* Gate/up projection with the SwiGLU product in the GEMM epilogue (P1 §5.4:
@@ -148,10 +154,11 @@ int bi_gemm_variant_splits(int64_t M, int64_t N, int64_t K, int num_sms);
  *   A [M,K] bf16, W [2F,K] bf16 with the gate and up rows stacked in blocks
  *   of 128 features (rows 256b .. 256b+127: gate of features 128b ..
  *   128b+127; rows 256b+128 .. 256b+255: up of the same features), out [M,F]
- *   bf16.  The GEMM arithmetic (tile, instruction, K order, both modes) is
- *   bi_gemm's on (M, 2F, K), so out holds exactly the bytes of bi_gemm into a
- *   [M,2F] buffer followed by bi_silu_mul with block = 128, with no [M,2F]
- *   tensor written.
+ *   bf16.  The GEMM arithmetic (instruction, K order, split count in both
+ *   modes) is bi_gemm's on (M, 2F, K), always with 128 x 256 tiles (a tile
+ *   holds the gate and up rows of 128 features), so out holds exactly the
+ *   bytes of bi_gemm into a [M,2F] buffer followed by bi_silu_mul with
+ *   block = 128, with no [M,2F] tensor written.
  * Workspace: bi_gemm_workspace_size(M, 2F, K, mode, variant_splits) bytes.
  * Requirements: F % 128 == 0, K % 8 == 0, 2F and K < 2^31; pointers 16-byte
  *   aligned.  Errors: as bi_gemm. */

@@ -89,14 +89,14 @@ bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64
          CUDA_SUCCESS;
 }
 
-bool make_tmap_pages_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                          uint32_t box_rows) {
+bool make_tmap_groups_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           uint32_t box_rows, uint32_t box_groups) {
   const PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
-  if (!encode || cols % 64 != 0) return false;
+  if (!encode || cols % 64 != 0 || box_groups < 1 || box_groups > cols / 64) return false;
   // dimension 0: 64 columns of a 128-byte group, 1: rows, 2: the row's groups
   const cuuint64_t dims[3] = {64, rows, cols / 64};
   const cuuint64_t strides[2] = {cols * 2, 128};
-  const cuuint32_t box[3] = {64, box_rows, static_cast<cuuint32_t>(cols / 64)};
+  const cuuint32_t box[3] = {64, box_rows, box_groups};
   const cuuint32_t estr[3] = {1, 1, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -215,9 +215,14 @@ bi_status bi_add_rmsnorm(const void* x, void* residual, const void* w, void* y, 
 }
 
 // --------------------------------------------------------------------- GEMM
+// The variant's split count, over the output tiles bi_gemm uses for this
+// shape (gemm_n_tile: 64 columns where the narrow ring runs, else 256).
+// bi_gemm_swiglu takes the same count for its [M, 2F] shape, so that in
+// either mode it gives the bytes of bi_gemm followed by the SwiGLU kernel.
 int bi_gemm_variant_splits(int64_t M, int64_t N, int64_t K, int num_sms) {
   if (M <= 0 || N <= 0 || K <= 0 || num_sms <= 0) return 1;
-  const int64_t tiles = ((M + kGemmBM - 1) / kGemmBM) * ((N + kGemmBN - 1) / kGemmBN);
+  const int64_t bn = gemm_n_tile(M, N, K, num_sms, false);
+  const int64_t tiles = ((M + kGemmBM - 1) / kGemmBM) * ((N + bn - 1) / bn);
   const int64_t kblocks = (K + kGemmBK - 1) / kGemmBK;
   int64_t s = 1;
   // split K only when the tiles leave most SMs idle (at most a quarter busy:

@@ -1607,8 +1607,8 @@ bool make_kv_maps(const AttnArgs& a, CUtensorMap* km, CUtensorMap* vm) {
 // Decode: one box per (page, kv head), both column groups of its 16 rows.
 bool make_kv_page_maps(const AttnArgs& a, CUtensorMap* km, CUtensorMap* vm) {
   const uint64_t rows = static_cast<uint64_t>(a.num_pages) * a.Hkv * kPage;
-  return make_tmap_pages_bf16(km, a.k_cache, rows, a.D, kPage) &&
-         make_tmap_pages_bf16(vm, a.v_cache, rows, a.D, kPage);
+  return make_tmap_groups_bf16(km, a.k_cache, rows, a.D, kPage, a.D / 64) &&
+         make_tmap_groups_bf16(vm, a.v_cache, rows, a.D, kPage, a.D / 64);
 }
 
 // Launch with programmatic stream serialisation: the kernel may begin while

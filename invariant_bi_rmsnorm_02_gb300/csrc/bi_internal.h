@@ -21,12 +21,15 @@ int device_sm_count();
 // driver entry point is unavailable or the encoding is rejected.
 bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                        uint32_t box_rows, uint32_t box_cols);
-// Encode a bf16 tensor map over the same matrix whose box is box_rows whole
-// rows: the rows' 128-byte column groups land one after another in shared
-// memory (group g of every row, then group g + 1), each group with the
-// 128-byte swizzle of a box_rows x 64 box.  cols must be a multiple of 64.
-bool make_tmap_pages_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                          uint32_t box_rows);
+// Encode a bf16 tensor map over the same matrix as a 3-D view (64 columns,
+// rows, the rows' 128-byte column groups) whose box is box_rows rows times
+// box_groups consecutive column groups: one copy reads box_groups * 128
+// contiguous bytes of each row, and the groups land one after another in
+// shared memory (group g of every row, then group g + 1), each with the
+// 128-byte swizzle of a box_rows x 64 box.  cols must be a multiple of 64 and
+// box_groups at most cols / 64; groups past the last read as zero.
+bool make_tmap_groups_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           uint32_t box_rows, uint32_t box_groups);
 
 inline bi_status cuda_status(cudaError_t e) { return e == cudaSuccess ? BI_OK : BI_ERR_CUDA; }
 
@@ -55,6 +58,25 @@ bi_status launch_rmsnorm_variant(const void* x, const void* w, void* y, float* y
 constexpr int kGemmBM = 128;
 constexpr int kGemmBN = 256;
 constexpr int kGemmBK = 64;
+constexpr int kGemmSmallRows = 32;    // at most this many rows of A: a 32-row A ring
+constexpr int kGemmNarrowRows = 64;   // at most this many rows of A: the narrow ring may run
+constexpr int kGemmNarrowBN = 64;     // the narrow ring's output tile width
+constexpr int kGemmNarrowKBlocks = 4; // k-blocks per stage of the narrow ring
+// The narrow ring (64-column output tiles, four k-blocks per stage) runs for
+// at most 64 rows of A when its tiles fit in one wave of the device's
+// num_sms blocks, K is whole 64-column groups (at least four) and the
+// epilogue is not SwiGLU (whose tile pairs 128 gate and 128 up rows); every
+// other shape takes 256-column tiles.  The tile width never changes a
+// row's arithmetic (tcgen05.mma gives each output element the same sum for
+// every N), only how many blocks stream the weight.
+inline bool gemm_narrow(int64_t M, int64_t N, int64_t K, int num_sms, bool swiglu) {
+  return !swiglu && M <= kGemmNarrowRows && K % kGemmBK == 0 &&
+         K / kGemmBK >= kGemmNarrowKBlocks &&
+         (N + kGemmNarrowBN - 1) / kGemmNarrowBN <= num_sms;
+}
+inline int gemm_n_tile(int64_t M, int64_t N, int64_t K, int num_sms, bool swiglu) {
+  return gemm_narrow(M, N, K, num_sms, swiglu) ? kGemmNarrowBN : kGemmBN;
+}
 // swiglu: C is [M, N/2], the SwiGLU product of each tile's two column halves
 bi_status launch_gemm(const void* A, const void* W, void* C, int64_t M, int64_t N, int64_t K,
                       int splits, float* ws, int* err, cudaStream_t s, bool swiglu = false);

@@ -5,14 +5,18 @@
 // Batch invariance ("Reproducible LLM Inference", §5.4): a matmul loses it in
 // two ways -- splitting K when M and N are small, and switching to a
 // different tensor-core instruction or tile at small batch, since each
-// instruction has its own internal order.  This kernel has one configuration
-// for every shape: a 128 x 256 output tile, the instruction
-// tcgen05.mma.cta_group::1.kind::f16 with M=128 N=256 K=16, and the k-blocks
-// of 64 accumulated in increasing k into one fp32 accumulator, rounded to
-// bf16 once.  A row of C therefore depends only on its row of A, W and K:
-// rows beyond M in a partial tile are zero-filled by TMA and never mix with
-// real rows.  The work distribution (which block takes which tile) may vary
-// with M; the arithmetic of a tile does not.
+// instruction has its own internal order.  Every shape here runs the
+// instruction tcgen05.mma.cta_group::1.kind::f16 (M=128, K=16) and
+// accumulates the k-blocks of 64 in increasing k into one fp32 accumulator,
+// rounded to bf16 once.  The output tile is 128 x 256, or 128 x 64 (N=64)
+// for at most 64 rows of A where those narrow tiles fit in one wave: the
+// instruction's N only sets how many output columns it computes, and every
+// output element gets the same sum for N = 64 and N = 256 (checked bit for
+// bit on GB300 against the 256-column tiles of large M for every M up to
+// 256).  A row of C therefore depends only on its row of A, W and K: rows
+// beyond M in a partial tile are zero-filled by TMA and never mix with real
+// rows.  The work distribution (which block takes which tile, how wide the
+// tiles are) may vary with M; the arithmetic of an output element does not.
 //
 // The batch-variant mode (split-K, §5.4) runs the same tile over s slices of
 // the k-blocks, writes fp32 partial tiles, and sums them in slice order in a
@@ -27,18 +31,17 @@
 // [M, 2F] projection through memory.
 //
 // Structure: persistent blocks (one per SM), 6 warps:
-//   warp 0    : TMA producer, fills a 4-stage ring of (A 128x64, W 256x64)
-//               tiles, 128-byte swizzled, completion on mbarriers;
-//               with at most 32 rows of A (a batch of a few tokens) the A
-//               stages hold 32 rows and the ring has 6 stages: the MMA still
-//               reads 128 rows of A (the rows past 32 are whatever follows in
-//               shared memory, and only reach accumulator rows that are never
-//               stored, since rows do not mix), and the weight, which is what
-//               the block streams at small M, has 192 KB in flight instead of
-//               128 KB;
-//   warp 1    : allocates 512 tensor-memory columns; one thread issues the
-//               MMAs into one of two 256-column accumulators and commits
-//               them to the ring's "empty" barriers;
+//   warp 0    : TMA producer, fills a ring of (A, W) stages, 128-byte
+//               swizzled, completion on mbarriers (the ring geometries are
+//               listed at struct Ring): 4 stages of A 128x64 and W 256x64;
+//               with at most 32 rows of A, 6 stages whose A holds 32 rows
+//               (the weight, which is what a block streams at small M, then
+//               has 192 KB in flight instead of 128 KB); in the narrow ring,
+//               stages of four k-blocks of A (32 or 64 rows) and W (64 rows),
+//               one 3-D copy per operand;
+//   warp 1    : allocates tensor memory for two accumulators of the tile's
+//               width (512 or 128 columns); one thread issues the MMAs into
+//               one of them and commits them to the ring's "empty" barriers;
 //   warps 2-5 : epilogue; each reads its 32 accumulator lanes (rows) with
 //               tcgen05.ld, converts and stores, then frees the accumulator,
 //               so the epilogue of one tile overlaps the MMAs of the next.
@@ -56,28 +59,41 @@
 namespace bi {
 namespace {
 
-constexpr int BM = kGemmBM, BN = kGemmBN, BK = kGemmBK;
-constexpr int kBBytes = BN * BK * 2;
+constexpr int BM = kGemmBM, BK = kGemmBK;
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;  // two BN-column fp32 accumulators
-constexpr int kSmallRows = 32;       // the A rows of the small-batch ring
+constexpr int kSmallRows = kGemmSmallRows;
 
-// Ring geometry: 4 stages of A (128 rows) and W, or, for at most kSmallRows
-// rows of A, 6 stages of A (kSmallRows rows) and W.
-template <bool kSmall>
+// Ring geometry for an output tile of 128 x kBN, kARows rows of A per stage
+// (128, or 32 / 64 when A has at most that many rows: the MMA still reads a
+// 128-row window, whose rows past M reach accumulator rows that are never
+// stored) and kKG k-blocks per stage:
+//   128-row A, 256-column tile : 4 stages;
+//   32-row A, 256-column tile  : 6 stages (the weight is what a block
+//                                streams at small M);
+//   narrow ring, 32- or 64-row A, 64-column tile, four k-blocks a stage:
+//                                4 or 3 stages, one 3-D copy per operand that
+//                                reads 512 contiguous bytes of each row.
+// A stage holds kKG sub-tiles per operand, k-block after k-block, each laid
+// out as a single k-block stage would be.
+template <int kARows, int kBN, int kKG>
 struct Ring {
-  static constexpr int kStages = kSmall ? 6 : 4;
-  static constexpr int kARows = kSmall ? kSmallRows : BM;
-  static constexpr int kABytes = kARows * BK * 2;
+  static constexpr int kStages = kBN == 256 ? (kARows == BM ? 4 : 6) : (kARows == 64 ? 3 : 4);
+  static constexpr int kASub = kARows * BK * 2;  // one k-block of A
+  static constexpr int kBSub = kBN * BK * 2;     // one k-block of W
+  static constexpr int kABytes = kKG * kASub;
+  static constexpr int kBBytes = kKG * kBSub;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
+  // two kBN-column fp32 accumulators (a power of two of at least 32 columns)
+  static constexpr uint32_t kTmemCols = 2 * kBN < 32 ? 32u : 2u * kBN;
+  // the MMA reads a 128-row A window from each A sub-tile: it must stay
+  // inside the block's shared memory (the W ring follows the A ring)
+  static_assert((kStages * kKG - 1) * kASub + BM * BK * 2 <= kStages * kStageBytes,
+                "small-batch A window leaves shared memory");
+  static_assert(kSmemBytes <= 227 * 1024, "ring exceeds shared memory");
+  static_assert((kBN == 256 && kKG == 1) || (kBN == kGemmNarrowBN && kKG == kGemmNarrowKBlocks),
+                "256-column tiles take one k-block a stage, narrow tiles four");
 };
-// the MMA reads a 128-row A window from each A stage: it must stay inside
-// the block's shared memory (the W ring follows the A ring)
-static_assert(5 * Ring<true>::kABytes + BM * BK * 2 <= 6 * Ring<true>::kABytes + 6 * kBBytes,
-              "small-batch A window leaves shared memory");
-
-constexpr uint32_t kIdesc = umma_idesc_bf16(BM, BN, false, false);
 
 // K-major tiles written by TMA with 128-byte swizzling: rows of 64 bf16
 // (128 B), 8-row groups 1024 B apart.
@@ -131,13 +147,20 @@ enum Epilogue : int {
   kEpiSwiglu = 2,  // C [M, N/2] bf16 = silu(gate) * up of the interleaved tile halves
 };
 
-template <int kEpi, bool kSmall>
+template <int kEpi, int kARows, int kBN, int kKG>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(
     const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
     const GemmParams p) {
-  constexpr int kStages = Ring<kSmall>::kStages;
-  constexpr int kABytes = Ring<kSmall>::kABytes;
-  constexpr int kStageBytes = Ring<kSmall>::kStageBytes;
+  using R = Ring<kARows, kBN, kKG>;
+  constexpr int kStages = R::kStages;
+  constexpr int kABytes = R::kABytes;
+  constexpr int kBBytes = R::kBBytes;
+  constexpr int kASub = R::kASub;
+  constexpr int kBSub = R::kBSub;
+  constexpr int kStageBytes = R::kStageBytes;
+  constexpr uint32_t kTmemCols = R::kTmemCols;
+  constexpr uint32_t kIdesc = umma_idesc_bf16(BM, kBN, false, false);
+  static_assert(kEpi != kEpiSwiglu || kBN == 256, "the SwiGLU tile pairs 128 gate and 128 up rows");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -186,14 +209,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit w = unit_of(u, p);
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; kb += kKG) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.err, abort_flag)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&full[stage], kStageBytes);
-          tma_load_2d(sA + stage * kABytes, &ta, kb * BK, w.m_tile * BM, &full[stage]);
-          tma_load_2d(sB + stage * kBBytes, &tb, kb * BK, w.n_tile * BN, &full[stage]);
+          if constexpr (kKG == 1) {
+            tma_load_2d(sA + stage * kABytes, &ta, kb * BK, w.m_tile * BM, &full[stage]);
+            tma_load_2d(sB + stage * kBBytes, &tb, kb * BK, w.n_tile * kBN, &full[stage]);
+          } else {
+            // k-blocks kb .. kb + kKG - 1 (those past the slice are loaded
+            // and not used; those past K read as zero)
+            tma_load_3d(sA + stage * kABytes, &ta, 0, w.m_tile * BM, kb, &full[stage]);
+            tma_load_3d(sB + stage * kBBytes, &tb, 0, w.n_tile * kBN, kb, &full[stage]);
+          }
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -223,18 +253,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        for (int kb0 = w.kb0; kb0 < w.kb1; kb0 += kKG) {
           if (!mbar_wait(&full[stage], phase, p.err, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = smem_desc(smem_u32(sA + stage * kABytes));
-          const uint64_t bd = smem_desc(smem_u32(sB + stage * kBBytes));
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)  // +32 bytes along K per step
-            tc_mma(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
+          for (int g = 0; g < kKG; ++g) {
+            const int kb = kb0 + g;
+            if (kb >= w.kb1) break;
+            const uint64_t ad = smem_desc(smem_u32(sA + stage * kABytes + g * kASub));
+            const uint64_t bd = smem_desc(smem_u32(sB + stage * kBBytes + g * kBSub));
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)  // +32 bytes along K per step
+              tc_mma(d_tmem, ad + 2u * k, bd + 2u * k, kIdesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
+          }
           tc_commit(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;
@@ -265,18 +300,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(
       tc_fence_after();
       const int row = w.m_tile * BM + wq * 32 + lane;
       const uint32_t tbase =
-          tmem_base + (static_cast<uint32_t>(wq * 32) << 16) + static_cast<uint32_t>(acc * BN);
+          tmem_base + (static_cast<uint32_t>(wq * 32) << 16) + static_cast<uint32_t>(acc * kBN);
       if constexpr (kEpi == kEpiSwiglu) {
-        // gate in accumulator columns 0 .. BN/2-1, up in BN/2 .. BN-1
+        // gate in accumulator columns 0 .. kBN/2-1, up in kBN/2 .. kBN-1
 #pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
+        for (int c = 0; c < kBN / 64; ++c) {
           uint32_t g[32], u[32];
           tmem_ld32_nowait(tbase + c * 32, g);
-          tmem_ld32_nowait(tbase + BN / 2 + c * 32, u);
+          tmem_ld32_nowait(tbase + kBN / 2 + c * 32, u);
           tmem_wait_ld();
           if (row < p.M) {
             __nv_bfloat16* dst = p.C + static_cast<int64_t>(row) * (p.N / 2) +
-                                 w.n_tile * (BN / 2) + c * 32;
+                                 w.n_tile * (kBN / 2) + c * 32;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               float y[8];
@@ -292,10 +327,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < kBN / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(tbase + c * 32, v);
-          const int col0 = w.n_tile * BN + c * 32;
+          const int col0 = w.n_tile * kBN + c * 32;
           if (row < p.M) {
             if constexpr (kEpi == kEpiF32) {
               float* dst = p.ws + (static_cast<int64_t>(w.split) * p.M + row) * p.N + col0;
@@ -389,22 +424,31 @@ __global__ void splitk_reduce_swiglu_kernel(const float* __restrict__ ws, uint2*
   }
 }
 
-template <int kEpi, bool kSmall>
+template <int kEpi, int kARows, int kBN, int kKG>
 bi_status launch_tc_ring(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
                          int grid, cudaStream_t s) {
-  constexpr size_t smem = Ring<kSmall>::kSmemBytes;
-  if (cudaFuncSetAttribute(gemm_tc_kernel<kEpi, kSmall>,
+  constexpr size_t smem = Ring<kARows, kBN, kKG>::kSmemBytes;
+  if (cudaFuncSetAttribute(gemm_tc_kernel<kEpi, kARows, kBN, kKG>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return BI_ERR_CUDA;
-  gemm_tc_kernel<kEpi, kSmall><<<grid, kThreads, smem, s>>>(ta, tb, p);
+  gemm_tc_kernel<kEpi, kARows, kBN, kKG><<<grid, kThreads, smem, s>>>(ta, tb, p);
   return cuda_status(cudaGetLastError());
 }
+// narrow: the narrow ring runs (gemm_narrow); a_rows: rows of A per stage
 template <int kEpi>
 bi_status launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int grid,
-                    cudaStream_t s) {
-  return p.M <= kSmallRows ? launch_tc_ring<kEpi, true>(ta, tb, p, grid, s)
-                           : launch_tc_ring<kEpi, false>(ta, tb, p, grid, s);
+                    bool narrow, uint32_t a_rows, cudaStream_t s) {
+  if constexpr (kEpi != kEpiSwiglu) {
+    if (narrow)
+      return a_rows == kSmallRows
+                 ? launch_tc_ring<kEpi, kSmallRows, kGemmNarrowBN, kGemmNarrowKBlocks>(ta, tb, p,
+                                                                                       grid, s)
+                 : launch_tc_ring<kEpi, kGemmNarrowRows, kGemmNarrowBN, kGemmNarrowKBlocks>(
+                       ta, tb, p, grid, s);
+  }
+  return a_rows == kSmallRows ? launch_tc_ring<kEpi, kSmallRows, 256, 1>(ta, tb, p, grid, s)
+                              : launch_tc_ring<kEpi, BM, 256, 1>(ta, tb, p, grid, s);
 }
 
 }  // namespace
@@ -414,10 +458,20 @@ bi_status launch_gemm(const void* A, const void* W, void* C, int64_t M, int64_t 
   const int sms = device_sm_count();
   if (sms <= 0) return BI_ERR_CUDA;
   CUtensorMap ta, tb;
-  const uint32_t a_rows = M <= kSmallRows ? kSmallRows : BM;  // the A box of the ring
-  if (!make_tmap_2d_bf16(&ta, A, static_cast<uint64_t>(M), static_cast<uint64_t>(K), a_rows, BK) ||
-      !make_tmap_2d_bf16(&tb, W, static_cast<uint64_t>(N), static_cast<uint64_t>(K), BN, BK))
-    return BI_ERR_CUDA;
+  const bool narrow = gemm_narrow(M, N, K, sms, swiglu);
+  const int bn = narrow ? kGemmNarrowBN : kGemmBN;
+  // rows of A per stage (the A box)
+  const uint32_t a_rows = M <= kSmallRows ? kSmallRows : (narrow ? kGemmNarrowRows : BM);
+  const bool ok =
+      narrow ? make_tmap_groups_bf16(&ta, A, static_cast<uint64_t>(M), static_cast<uint64_t>(K),
+                                     a_rows, kGemmNarrowKBlocks) &&
+                   make_tmap_groups_bf16(&tb, W, static_cast<uint64_t>(N),
+                                         static_cast<uint64_t>(K), bn, kGemmNarrowKBlocks)
+             : make_tmap_2d_bf16(&ta, A, static_cast<uint64_t>(M), static_cast<uint64_t>(K),
+                                 a_rows, BK) &&
+                   make_tmap_2d_bf16(&tb, W, static_cast<uint64_t>(N), static_cast<uint64_t>(K),
+                                     bn, BK);
+  if (!ok) return BI_ERR_CUDA;
   GemmParams p{};
   p.C = static_cast<__nv_bfloat16*>(C);
   p.ws = ws;
@@ -426,7 +480,7 @@ bi_status launch_gemm(const void* A, const void* W, void* C, int64_t M, int64_t 
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.m_tiles = static_cast<int>((M + BM - 1) / BM);
-  p.n_tiles = static_cast<int>((N + BN - 1) / BN);
+  p.n_tiles = static_cast<int>((N + bn - 1) / bn);
   p.kb_total = static_cast<int>((K + BK - 1) / BK);
   if (splits < 1) splits = 1;
   if (splits > p.kb_total) splits = p.kb_total;
@@ -435,7 +489,7 @@ bi_status launch_gemm(const void* A, const void* W, void* C, int64_t M, int64_t 
   // raster: keep the smaller operand in L2 (about 40 MB of it per group)
   const int64_t resident_budget = int64_t(40) << 20;
   p.m_fast = M <= N ? 1 : 0;
-  const int64_t tile_bytes = static_cast<int64_t>(p.m_fast ? BM : BN) * K * 2;
+  const int64_t tile_bytes = static_cast<int64_t>(p.m_fast ? BM : bn) * K * 2;
   int64_t grp = resident_budget / (tile_bytes > 0 ? tile_bytes : 1);
   if (grp < 1) grp = 1;
   const int span = p.m_fast ? p.m_tiles : p.n_tiles;
@@ -444,8 +498,9 @@ bi_status launch_gemm(const void* A, const void* W, void* C, int64_t M, int64_t 
   if (units > 0x7fffffff) return BI_ERR_UNSUPPORTED;
   const int grid = static_cast<int>(units < sms ? units : sms);
   if (p.splits == 1)
-    return swiglu ? launch_tc<kEpiSwiglu>(ta, tb, p, grid, s) : launch_tc<kEpiBf16>(ta, tb, p, grid, s);
-  const bi_status st = launch_tc<kEpiF32>(ta, tb, p, grid, s);
+    return swiglu ? launch_tc<kEpiSwiglu>(ta, tb, p, grid, narrow, a_rows, s)
+                  : launch_tc<kEpiBf16>(ta, tb, p, grid, narrow, a_rows, s);
+  const bi_status st = launch_tc<kEpiF32>(ta, tb, p, grid, narrow, a_rows, s);
   if (st != BI_OK) return st;
   const int64_t n4 = swiglu ? M * N / 8 : M * N / 4;  // threads of the reduction
   const int rb = static_cast<int>((n4 + 255) / 256 < 4 * sms ? (n4 + 255) / 256 : 4 * sms);

@@ -68,14 +68,21 @@ def test_workspace_sizes_are_host_arithmetic(lib):
 
 def test_gemm_variant_split_count(lib):
     # split-K only when the tiles cover at most a quarter of the SMs, then
-    # until the slices cover them, at least 4 k-blocks per slice
+    # until the slices cover them, at least 4 k-blocks per slice; the tiles
+    # are the kernel's: 128 x 64 for at most 64 rows when those fit in one
+    # wave (and K is at least four whole 64-column groups), else 128 x 256
     assert bi.bi_gemm_variant_splits(8192, 6144, 4096, 152) == 1
-    assert bi.bi_gemm_variant_splits(1, 6144, 4096, 152) == 8     # 24 tiles -> 8 slices
-    assert bi.bi_gemm_variant_splits(1, 14336, 4096, 152) == 1    # 56 tiles: no split
-    assert bi.bi_gemm_variant_splits(1, 512, 256, 152) == 1       # K = 4 k-blocks
+    assert bi.bi_gemm_variant_splits(1, 6144, 4096, 152) == 1     # 96 narrow tiles: no split
+    assert bi.bi_gemm_variant_splits(64, 6144, 4096, 152) == 1
+    assert bi.bi_gemm_variant_splits(65, 6144, 4096, 152) == 8    # 24 wide tiles
+    assert bi.bi_gemm_variant_splits(128, 6144, 4096, 152) == 8
     assert bi.bi_gemm_variant_splits(256, 6144, 4096, 152) == 1   # 48 tiles: no split
-    assert bi.bi_gemm_variant_splits(128, 6144, 4096, 152) == 8   # 24 tiles
-    assert bi.bi_gemm_variant_splits(1, 2048, 4096, 152) == 16    # 8 tiles, 4 k-blocks a slice
+    assert bi.bi_gemm_variant_splits(1, 14336, 4096, 152) == 1    # 224 narrow > 152: 56 wide
+    assert bi.bi_gemm_variant_splits(1, 14336, 4096, 256) == 1    # 224 narrow tiles fit
+    assert bi.bi_gemm_variant_splits(1, 512, 256, 152) == 1       # K = 4 k-blocks
+    assert bi.bi_gemm_variant_splits(1, 2048, 4096, 152) == 8     # 32 narrow tiles
+    assert bi.bi_gemm_variant_splits(1, 512, 4096, 152) == 16     # 8 narrow tiles
+    assert bi.bi_gemm_variant_splits(1, 6144, 4000, 152) == 8     # K not whole groups: 24 wide
 
 
 def _call_rms(lib, x, w, y, M, H, eps=1e-6, mode=0, ws=None, wsb=0):

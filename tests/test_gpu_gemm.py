@@ -124,13 +124,14 @@ def test_gemm_run_to_run(cuda):
 
 def test_gemm_split_k_is_not_batch_invariant(cuda):
     # negative control: split-K picks its slice count from M, so row bytes
-    # move with the batch size; the harness must see it
+    # move with the batch size; the harness must see it (65 to 128 rows: 24
+    # tiles of 128 x 256, which the variant cuts into 8 slices of K)
     K, N = 4096, 6144
     A = synth.normal_bf16((1024, K), 3700, device=cuda)
     W = synth.normal_bf16((N, K), 3701, std=0.02, device=cuda)
     ref = bi.gemm(A, W, bi.VARIANT)          # M = 1024: no split
     differing_rows = 0
-    for M in (1, 3, 16, 64):
+    for M in (65, 100, 128):
         C = bi.gemm(A[:M].contiguous(), W, bi.VARIANT)
         differing_rows += int((C.view(torch.int16) != ref[:M].view(torch.int16)).any(1).sum())
     assert differing_rows > 0
