@@ -510,29 +510,39 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const KernelPar
 
 // ------------------------------------------------------------ decode split
 // Persistent: block x takes units u = x, x + gridDim.x, ... (unit u = split
-// u / Hkv of the plan, kv head u % Hkv).  One warp per block; the G query
-// heads of the kv head are the columns of NQ 8-wide n-tiles.  The TMA ring
-// of two tiles runs across unit boundaries.
-// Units are opened (descriptor, page ids checked and staged in shared
-// memory) only at unit boundaries, kQueue ahead of the compute; the page ids
-// of the next unit are fetched into registers one unit before they are
-// checked, so their latency hides behind a unit's worth of tiles, and the
-// tile loop itself reads nothing but shared memory.  A unit whose pages are
-// not all in the pool is recorded as BI_ERR_DEVICE_BOUNDS and marked with
-// l = -1.
+// u / Hkv of the plan, kv head u % Hkv).  Two warps per block:
+//   warp 1 (producer) works out the plan, opens the units in order (page ids
+//     fetched one unit ahead, checked and staged in shared memory, the unit's
+//     descriptor put in a queue of kQueue slots) and issues the TMA copies of
+//     every tile into a ring of two tile buffers, each as soon as the compute
+//     warp has freed its buffer; the q rows of a unit ride with its first
+//     tile;
+//   warp 0 (compute) takes the descriptors in order, runs the tile steps (the
+//     G query heads of the kv head are the columns of NQ 8-wide n-tiles) and
+//     writes the unit's partial state, or the output when the sequence has a
+//     single split.
+// Measured on one block: issuing a tile's copies (one lane, 9 copies) took as
+// long as a third of the tile's arithmetic, and opening a unit a quarter;
+// both are off the compute warp's path here.  Barriers: full / empty per ring
+// buffer, ready / free per descriptor slot; every wait is bounded, a wait
+// that runs out raises a flag that makes the other warp's waits return, and
+// the producer lets its copies in flight land before it exits.  A unit whose
+// pages are not all in the pool is recorded as BI_ERR_DEVICE_BOUNDS and
+// marked with l = -1.
 constexpr int kQueue = 4;
 constexpr int kUnitPages = 64;                     // page ids staged per unit
 constexpr int kLocalSlabs = 4;                     // 32 sequences per slab
 constexpr int kLocalPlanMax = 32 * kLocalSlabs;    // largest batch planned in-kernel
+constexpr int kSplitThreads = 64;                  // compute warp, producer warp
 
 __device__ __forceinline__ int unit_tiles(int4 d) {  // {b, j, lo, hi}
   return d.z < d.w ? (d.w - (d.z & ~(kTile - 1)) + kTile - 1) / kTile : 0;
 }
 
-// One warp per block and at most three blocks per SM (shared memory), so
-// registers are not what limits residency: the bound lets ptxas keep the
-// whole tile step in registers instead of its default of 128 for this
-// block size, which measurably starved the G <= 8 instantiation.
+// At most three blocks per SM (shared memory), so registers are not what
+// limits residency: the bound lets ptxas keep the whole tile step in
+// registers instead of its default for this block size, which measurably
+// starved the G <= 8 instantiation.
 template <int D, int NQ>
 __global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -542,246 +552,277 @@ __global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
                                              ~uintptr_t(1023));
   uint8_t* bufs = smem;  // 2 tile buffers
   __nv_bfloat16* qbuf = reinterpret_cast<__nv_bfloat16*>(smem + 2 * TileGeom<D>::kBufBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(qbuf + 2 * 8 * NQ * D);
-  __shared__ int4 q_unit[kQueue];              // b, j, lo, hi of opened units
-  __shared__ int q_head[kQueue];               // kv head h, or -(h+1) if its pages are bad
-  __shared__ int q_pid[kQueue][kUnitPages];    // page ids of the unit's first pages
+  uint64_t* full = reinterpret_cast<uint64_t*>(qbuf + 2 * 8 * NQ * D);  // [2]
+  uint64_t* empty = full + 2;                                            // [2]
+  uint64_t* ready = empty + 2;                                           // [kQueue]
+  uint64_t* freed = ready + kQueue;                                      // [kQueue]
+  __shared__ int4 q_unit[kQueue];            // b, j, lo, hi of opened units (b < 0: no more)
+  __shared__ int q_head[kQueue];             // kv head h, or -(h+1) if its pages are bad
+  __shared__ int q_single[kQueue];           // the sequence has this one split
+  __shared__ int q_pid[kQueue][kUnitPages];  // page ids of the unit's first pages
+  __shared__ int s_incl[kLocalPlanMax], s_len[kLocalPlanMax];
+  __shared__ int s_abort;
 
-  const int lane = threadIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G, Hkv = p.Hkv;
-  if (lane == 0) {
+  if (threadIdx.x == 0) {
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < kQueue; ++i) {
+      mbar_init(&ready[i], 1);
+      mbar_init(&freed[i], 1);
+    }
+    s_abort = 0;
     fence_mbar_init();
   }
   // padding query rows G .. 8*NQ-1 stay zero in both buffers
   {
     const int pad = (8 * NQ - G) * (D / 8);  // 16-byte chunks per buffer
-    for (int i = lane; i < 2 * pad; i += 32) {
+    for (int i = threadIdx.x; i < 2 * pad; i += kSplitThreads) {
       const int bsel = i / pad, rem = i % pad;
       const int r = G + rem / (D / 8), c = (rem % (D / 8)) * 8;
       *reinterpret_cast<uint4*>(qbuf + (bsel * 8 * NQ + r) * D + c) = make_uint4(0, 0, 0, 0);
     }
   }
+  fence_proxy_async_smem();  // the zeroed rows before any copy into the buffers
+  __syncthreads();
   launch_dependents();     // the merge kernel may queue up behind this grid
   grid_dependency_wait();  // inputs and the plan kernel's unit list are complete from here
-  // Units in sequence order.  For small batches the running split count
-  // (inclusive) and the length of every sequence are kept in shared memory;
-  // the sequence of split s is the number of sequences whose running count
-  // is <= s, found with one ballot per 32 sequences.
-  __shared__ int s_incl[kLocalPlanMax], s_len[kLocalPlanMax];
-  int total = 0;
-  int csize = 0;  // variant: the call's chunk size in keys
-  if (p.local_plan) {
-    if (p.variant) {
-      long long tiles = 0;
-      int tmax = 0;
+
+  if (warp == 1) {
+    // ============================================================ producer
+    // Units in sequence order.  For small batches the running split count
+    // (inclusive) and the length of every sequence are kept in shared
+    // memory; the sequence of split s is the number of sequences whose
+    // running count is <= s, found with one ballot per 32 sequences.
+    int total = 0;
+    int csize = 0;  // variant: the call's chunk size in keys
+    if (p.local_plan) {
+      if (p.variant) {
+        long long tiles = 0;
+        int tmax = 0;
+#pragma unroll
+        for (int k = 0; k < kLocalSlabs; ++k) {
+          const int b = lane + 32 * k;
+          const int L = b < p.B ? p.kv_lens[b] : 0;
+          if (b < p.B && len_ok(L, p)) {
+            tiles += (L + kTile - 1) / kTile;
+            tmax = max(tmax, (L + kTile - 1) / kTile);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+          tiles += __shfl_xor_sync(kFull, tiles, o);
+          tmax = max(tmax, __shfl_xor_sync(kFull, tmax, o));
+        }
+        csize = kTile * variant_chunk_tiles(tiles, tmax, p);
+        if (blockIdx.x == 0 && lane == 0) p.unit_count[1] = csize;  // for the merge
+      }
 #pragma unroll
       for (int k = 0; k < kLocalSlabs; ++k) {
         const int b = lane + 32 * k;
-        const int L = b < p.B ? p.kv_lens[b] : 0;
-        if (b < p.B && len_ok(L, p)) {
-          tiles += (L + kTile - 1) / kTile;
-          tmax = max(tmax, (L + kTile - 1) / kTile);
-        }
-      }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        tiles += __shfl_xor_sync(kFull, tiles, o);
-        tmax = max(tmax, __shfl_xor_sync(kFull, tmax, o));
-      }
-      csize = kTile * variant_chunk_tiles(tiles, tmax, p);
-      if (blockIdx.x == 0 && lane == 0) p.unit_count[1] = csize;  // for the merge
-    }
-#pragma unroll
-    for (int k = 0; k < kLocalSlabs; ++k) {
-      const int b = lane + 32 * k;
-      int L = 0, n = 0;
-      if (b < p.B) {
-        L = p.kv_lens[b];
-        if (!len_ok(L, p)) {
-          record_error(p.err, BI_ERR_DEVICE_BOUNDS);
-          L = 0;
-        }
-        if (L > 0) n = plan_splits(L, csize, p);
-      }
-      int v = n;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(kFull, v, o);
-        if (lane >= o) v += t;
-      }
-      s_incl[b] = total + v;
-      s_len[b] = L;
-      total += __shfl_sync(kFull, v, 31);
-    }
-    __syncwarp();
-    // the merge takes sequences longest first: rank of sequence x among all
-    // (more splits first, then lower index)
-    for (int x = blockIdx.x; x < p.B; x += gridDim.x) {
-      auto splits = [&](int b) { return s_incl[b] - (b > 0 ? s_incl[b - 1] : 0); };
-      const int nx = splits(x);
-      int ahead = 0;
-#pragma unroll
-      for (int k = 0; k < kLocalSlabs; ++k) {
-        const int b = lane + 32 * k;
+        int L = 0, n = 0;
         if (b < p.B) {
-          const int nb = splits(b);
-          ahead += (nb > nx || (nb == nx && b < x)) ? 1 : 0;
+          L = p.kv_lens[b];
+          if (!len_ok(L, p)) {
+            record_error(p.err, BI_ERR_DEVICE_BOUNDS);
+            L = 0;
+          }
+          if (L > 0) n = plan_splits(L, csize, p);
+        }
+        int v = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(kFull, v, o);
+          if (lane >= o) v += t;
+        }
+        s_incl[b] = total + v;
+        s_len[b] = L;
+        total += __shfl_sync(kFull, v, 31);
+      }
+      __syncwarp();
+      // the merge takes sequences longest first: rank of sequence x among all
+      // (more splits first, then lower index)
+      for (int x = blockIdx.x; x < p.B; x += gridDim.x) {
+        auto splits = [&](int b) { return s_incl[b] - (b > 0 ? s_incl[b - 1] : 0); };
+        const int nx = splits(x);
+        int ahead = 0;
+#pragma unroll
+        for (int k = 0; k < kLocalSlabs; ++k) {
+          const int b = lane + 32 * k;
+          if (b < p.B) {
+            const int nb = splits(b);
+            ahead += (nb > nx || (nb == nx && b < x)) ? 1 : 0;
+          }
+        }
+        ahead = __reduce_add_sync(kFull, ahead);
+        if (lane == 0) p.order[ahead] = make_int2(x, nx);
+      }
+    } else {
+      total = *p.unit_count;
+      if (p.variant) csize = p.unit_count[1];
+    }
+    const int U = total * Hkv;
+    // A sequence with a single split has no merge: its unit writes the
+    // output itself (o / l, the merge's arithmetic for one split).  Split 0
+    // is the only one iff it ends below the chunk size or the sequence is
+    // exactly one chunk long.
+    auto single_split = [&](int b, int j, int hi) -> bool {
+      if (j != 0) return false;
+      const int c = p.variant ? csize : p.split_size;
+      if (hi < c) return true;
+      return (p.local_plan ? s_len[b] : p.kv_lens[b]) == c;
+    };
+    auto unit_at = [&](int s) -> int4 {  // {b, j, lo, hi} of split s; warp-uniform s
+      if (!p.local_plan) return p.units[s];
+      int b = 0;
+#pragma unroll
+      for (int k = 0; k < kLocalSlabs; ++k)
+        b += __popc(__ballot_sync(kFull, s_incl[lane + 32 * k] <= s));
+      const int L = s_len[b];
+      const int j = s - (b > 0 ? s_incl[b - 1] : 0);
+      const int c = p.variant ? csize : p.split_size;
+      return make_int4(b, j, j * c, min((j + 1) * c, L));
+    };
+
+    // the pending unit: its descriptor and page ids (in flight in registers)
+    int lu = blockIdx.x;  // next unit to fetch
+    bool pend = false;
+    int4 pd = make_int4(0, 0, 0, 0);
+    int ph = 0;
+    int ppg[kUnitPages / 32];
+    auto fetch = [&]() {
+      pend = lu < U;
+      if (!pend) return;
+      ph = lu % Hkv;
+      pd = unit_at(lu / Hkv);
+      lu += gridDim.x;
+      const int first = pd.z & ~(kTile - 1);
+      const int npg = pd.z < pd.w ? (pd.w - first + kPage - 1) / kPage : 0;
+      const int32_t* bt = p.block_table + (int64_t)pd.x * p.max_blocks + (first >> 4);
+#pragma unroll
+      for (int k = 0; k < kUnitPages / 32; ++k) {
+        const int idx = lane + 32 * k;
+        ppg[k] = idx < npg ? bt[idx] : 0;
+      }
+    };
+
+    int n_units = 0, n_issued = 0, q_issued = 0;
+    bool ok = true;
+    fetch();
+    while (ok) {
+      const int slot = n_units % kQueue;
+      if (n_units >= kQueue)
+        ok = __all_sync(kFull, mbar_wait(&freed[slot], ((n_units / kQueue) - 1) & 1, p.err,
+                                         &s_abort));
+      if (!ok) break;
+      if (!pend) {  // no more units: the end marker
+        if (lane == 0) {
+          q_unit[slot] = make_int4(-1, 0, 0, 0);
+          mbar_arrive(&ready[slot]);
+        }
+        break;
+      }
+      // check the pending unit's pages, stage them, queue its descriptor
+      const int4 d = pd;
+      const int h = ph;
+      const int first = d.z & ~(kTile - 1);
+      const int npg = d.z < d.w ? (d.w - first + kPage - 1) / kPage : 0;
+      bool good = true;
+#pragma unroll
+      for (int k = 0; k < kUnitPages / 32; ++k) {
+        const int idx = lane + 32 * k;
+        if (idx < npg) {
+          if (ppg[k] < 0 || ppg[k] >= p.num_pages) good = false;
+          q_pid[slot][idx] = ppg[k];
         }
       }
-      ahead = __reduce_add_sync(kFull, ahead);
-      if (lane == 0) p.order[ahead] = make_int2(x, nx);
-    }
-  } else {
-    total = *p.unit_count;
-    if (p.variant) csize = p.unit_count[1];
-  }
-  const int U = total * Hkv;
-  // A sequence with a single split has no merge: its unit writes the output
-  // itself (o / l, the merge's arithmetic for one split).  Split 0 is the
-  // only one iff it ends below the chunk size or the sequence is exactly
-  // one chunk long.
-  auto single_split = [&](int b, int j, int hi) -> bool {
-    if (j != 0) return false;
-    const int c = p.variant ? csize : p.split_size;
-    if (hi < c) return true;
-    return (p.local_plan ? s_len[b] : p.kv_lens[b]) == c;
-  };
-  auto unit_at = [&](int s) -> int4 {  // {b, j, lo, hi} of split s; warp-uniform s
-    if (!p.local_plan) return p.units[s];
-    int b = 0;
-#pragma unroll
-    for (int k = 0; k < kLocalSlabs; ++k)
-      b += __popc(__ballot_sync(kFull, s_incl[lane + 32 * k] <= s));
-    const int L = s_len[b];
-    const int j = s - (b > 0 ? s_incl[b - 1] : 0);
-    const int c = p.variant ? csize : p.split_size;
-    return make_int4(b, j, j * c, min((j + 1) * c, L));
-  };
-
-  // ---- opening units: one pending (page ids in flight), kQueue opened
-  int lu = blockIdx.x;  // next unit to fetch
-  bool pend = false;
-  int4 pd = make_int4(0, 0, 0, 0);
-  int ph = 0;
-  int ppg[kUnitPages / 32];
-  int n_pushed = 0, n_popped = 0;
-  int l_q = 0, l_tile = 0;
-  int n_issued = 0, n_done = 0, q_issued = 0, q_used = 0;
-  auto fetch = [&]() {
-    pend = lu < U;
-    if (!pend) return;
-    ph = lu % Hkv;
-    pd = unit_at(lu / Hkv);
-    lu += gridDim.x;
-    const int first = pd.z & ~(kTile - 1);
-    const int npg = pd.z < pd.w ? (pd.w - first + kPage - 1) / kPage : 0;
-    const int32_t* bt = p.block_table + (int64_t)pd.x * p.max_blocks + (first >> 4);
-#pragma unroll
-    for (int k = 0; k < kUnitPages / 32; ++k) {
-      const int idx = lane + 32 * k;
-      ppg[k] = idx < npg ? bt[idx] : 0;
-    }
-  };
-  auto push = [&]() {  // check the pending unit's pages and queue it
-    const int slot = n_pushed % kQueue;
-    const int first = pd.z & ~(kTile - 1);
-    const int npg = pd.z < pd.w ? (pd.w - first + kPage - 1) / kPage : 0;
-    bool ok = true;
-#pragma unroll
-    for (int k = 0; k < kUnitPages / 32; ++k) {
-      const int idx = lane + 32 * k;
-      if (idx < npg) {
-        if (ppg[k] < 0 || ppg[k] >= p.num_pages) ok = false;
-        q_pid[slot][idx] = ppg[k];
+      if (npg > kUnitPages) {
+        const int32_t* bt_row = p.block_table + (int64_t)d.x * p.max_blocks;
+        if (!pages_ok(bt_row, first + kUnitPages * kPage, d.w, p.num_pages, lane, 32))
+          good = false;
       }
-    }
-    if (npg > kUnitPages) {
-      const int32_t* bt_row = p.block_table + (int64_t)pd.x * p.max_blocks;
-      if (!pages_ok(bt_row, first + kUnitPages * kPage, pd.w, p.num_pages, lane, 32)) ok = false;
-    }
-    ok = __all_sync(kFull, ok);
-    if (lane == 0) {
-      q_unit[slot] = pd;
-      q_head[slot] = ok ? ph : -(ph + 1);
-      if (!ok) record_error(p.err, BI_ERR_DEVICE_BOUNDS);
-    }
-    __syncwarp();
-    ++n_pushed;
-  };
-  auto top_up = [&]() {
-    // a slot is reused only once both the compute and the load cursor are past it
-    while (pend && n_pushed - n_popped < kQueue && n_pushed - l_q < kQueue) {
-      push();
-      fetch();
-    }
-  };
-
-  // ---- load cursor: queue position l_q, tile l_tile of that unit
-  auto issue = [&]() {  // the next tile into the free ring slot, if any
-    if (n_issued - n_done >= 2) return;
-    int4 d;
-    int h;
-    for (;;) {  // skip opened units with nothing to load
-      if (l_q >= n_pushed) return;
-      d = q_unit[l_q % kQueue];
-      h = q_head[l_q % kQueue];
-      if (h >= 0 && l_tile < unit_tiles(d)) break;
-      ++l_q;
-      l_tile = 0;
-    }
-    const int qs = l_q % kQueue;
-    const int first = d.z & ~(kTile - 1);
-    const int key0 = first + l_tile * kTile;
-    const int np = pages_below(key0, d.w);
-    int pid[4];
+      good = __all_sync(kFull, good);
+      const bool single = single_split(d.x, d.y, d.w);
+      if (lane == 0) {
+        q_unit[slot] = d;
+        q_head[slot] = good ? h : -(h + 1);
+        q_single[slot] = single ? 1 : 0;
+        if (!good) record_error(p.err, BI_ERR_DEVICE_BOUNDS);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ready[slot]);
+      ++n_units;
+      fetch();  // the next unit's page ids load while this unit's tiles are issued
+      if (!good || d.z >= d.w) continue;
+      const int ntiles = unit_tiles(d);
+      for (int lt = 0; lt < ntiles; ++lt) {
+        const int rs = n_issued & 1;
+        if (n_issued >= 2)
+          ok = __all_sync(kFull, mbar_wait(&empty[rs], ((n_issued >> 1) - 1) & 1, p.err,
+                                           &s_abort));
+        if (!ok) break;
+        const int key0 = first + lt * kTile;
+        const int np = pages_below(key0, d.w);
+        int pid[4];
 #pragma unroll
-    for (int pp = 0; pp < 4; ++pp) {
-      const int idx = 4 * l_tile + pp;  // page index within the unit
-      pid[pp] = pp >= np                ? 0
-                : idx < kUnitPages      ? q_pid[qs][idx]
+        for (int pp = 0; pp < 4; ++pp) {
+          const int idx = 4 * lt + pp;  // page index within the unit
+          pid[pp] = pp >= np            ? 0
+                    : idx < kUnitPages  ? q_pid[slot][idx]
                                         : p.block_table[(int64_t)d.x * p.max_blocks +
                                                         (first >> 4) + idx];
+        }
+        if (lane == 0) {
+          uint8_t* buf = bufs + rs * TileGeom<D>::kBufBytes;
+          const uint32_t qbytes = lt == 0 ? (uint32_t)(G * D * 2) : 0u;
+          mbar_arrive_expect_tx(&full[rs], np * 2 * TileGeom<D>::kPageBytes + qbytes);
+          if (lt == 0)
+            bulk_load(qbuf + (q_issued & 1) * 8 * NQ * D,
+                      p.q + ((int64_t)d.x * p.Hq + (int64_t)h * G) * D, qbytes, &full[rs]);
+          issue_pages<D>(buf, &full[rs], &kmap, &vmap, pid, np, Hkv, h);
+        }
+        if (lt == 0) ++q_issued;
+        ++n_issued;
+      }
     }
-    const int slot = n_issued & 1;
-    if (lane == 0) {
-      uint8_t* buf = bufs + slot * TileGeom<D>::kBufBytes;
-      const uint32_t qbytes = l_tile == 0 ? (uint32_t)(G * D * 2) : 0u;
-      mbar_arrive_expect_tx(&bars[slot], np * 2 * TileGeom<D>::kPageBytes + qbytes);
-      if (l_tile == 0)
-        bulk_load(qbuf + (q_issued & 1) * 8 * NQ * D,
-                  p.q + ((int64_t)d.x * p.Hq + (int64_t)h * G) * D, qbytes, &bars[slot]);
-      issue_pages<D>(buf, &bars[slot], &kmap, &vmap, pid, np, Hkv, h);
-    }
-    if (l_tile == 0) ++q_issued;
-    ++n_issued;
-    if (++l_tile == unit_tiles(d)) {
-      ++l_q;
-      l_tile = 0;
-    }
-  };
-
-  fetch();
-  top_up();
-  issue();
-  issue();
+    if (!ok) s_abort = 1;
+    // the copies in flight land before the block exits
+    if (lane == 0)
+      for (int i = n_issued > 2 ? n_issued - 2 : 0; i < n_issued; ++i)
+        mbar_wait(&full[i & 1], (i >> 1) & 1, nullptr);
+    return;
+  }
+  // ============================================================== compute
   SplitState<D, NQ> st;
   uint32_t qf[NQ][D / 16][2];
   const int g = lane >> 2, t = lane & 3;
+  int n = 0, n_done = 0, q_used = 0;
   bool alive = true;
-  while (alive && n_popped < n_pushed) {
-    const int4 d = q_unit[n_popped % kQueue];
-    const int hv = q_head[n_popped % kQueue];
+  for (;;) {
+    const int slot = n % kQueue;
+    if (!__all_sync(kFull, mbar_wait(&ready[slot], (n / kQueue) & 1, p.err, &s_abort))) {
+      alive = false;
+      break;
+    }
+    const int4 d = q_unit[slot];
+    const int hv = q_head[slot];
+    const bool single = q_single[slot] != 0;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&freed[slot]);
+    ++n;
+    if (d.x < 0) break;  // no more units
     const bool pages_good = hv >= 0;
     const int h = pages_good ? hv : -hv - 1;
     const int b = d.x, j = d.y, lo = d.z, hi = d.w;
     const int64_t row0 = (int64_t)b * p.Hq + (int64_t)h * G;  // first q-head row
     if (!pages_good || lo >= hi) {
       // bad pages (l = -1 makes the merge emit zeros) or an empty split
-      if (!pages_good && single_split(b, j, hi)) {
+      if (!pages_good && single) {
         for (int i = lane; i < G * D; i += 32) {
           static_cast<__nv_bfloat16*>(p.out)[row0 * D + i] = __float2bfloat16_rn(0.0f);
           if (p.out_f32) p.out_f32[row0 * D + i] = 0.0f;
@@ -791,9 +832,6 @@ __global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
         p.ml[2 * s] = -CUDART_INF_F;
         p.ml[2 * s + 1] = pages_good ? 0.0f : -1.0f;
       }
-      ++n_popped;
-      top_up();
-      issue();
       continue;
     }
     const int first = lo & ~(kTile - 1);
@@ -804,32 +842,34 @@ __global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) hcol[nq][cc] = (8 * nq + 2 * t + cc) < G ? hi : lo;
     for (int ti = 0; ti < ntiles; ++ti) {
-      const int slot = n_done & 1;
-      const bool landed = mbar_wait(&bars[slot], (n_done >> 1) & 1, p.err);
-      if (!__all_sync(kFull, landed)) {
+      const int rs = n_done & 1;
+      if (!__all_sync(kFull, mbar_wait(&full[rs], (n_done >> 1) & 1, p.err, &s_abort))) {
         alive = false;
         break;
       }
-      uint8_t* buf = bufs + slot * TileGeom<D>::kBufBytes;
+      uint8_t* buf = bufs + rs * TileGeom<D>::kBufBytes;
       if (ti == 0) {
         load_q_frags<D, NQ>(qf, qbuf + (q_used & 1) * 8 * NQ * D, D);
         ++q_used;
         st.reset();
       }
       const int key0 = first + ti * kTile;
-      if (key0 + kTile > hi) {
+      const bool tail = key0 + kTile > hi;
+      if (tail) {
         clear_v_tail<D>(buf, key0, hi, lane, 32);
         __syncwarp();
       }
       tile_step<D, NQ>(st, qf, smem_u32(buf), smem_u32(buf + TileGeom<D>::kKBytes), key0, lo,
                        hcol, p.scale_log2);
       ++n_done;
-      fence_proxy_async_smem();
+      // the buffer goes back to the producer; the rows this warp zeroed are
+      // ordered before the copy that will overwrite them
+      if (tail) fence_proxy_async_smem();
       __syncwarp();
-      issue();
+      if (lane == 0) mbar_arrive(&empty[rs]);
     }
     if (!alive) break;
-    if (single_split(b, j, hi)) {
+    if (single) {
       // ---- the output of the valid columns
 #pragma unroll
       for (int nq = 0; nq < NQ; ++nq)
@@ -849,9 +889,6 @@ __global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
               if (p.out_f32) p.out_f32[idx] = v;
             }
         }
-      ++n_popped;
-      top_up();
-      issue();
       continue;
     }
     // ---- partial state of the valid columns
@@ -873,14 +910,8 @@ __global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
           orow[16 * md + g + 8] = st.o[md][nq][2 + cc];
         }
       }
-    ++n_popped;
-    top_up();
-    issue();
   }
-  if (!alive && lane == 0) {
-    // a copy never landed: give the copies still in flight a bounded wait
-    for (int i = n_done; i < n_issued; ++i) mbar_wait(&bars[i & 1], (i >> 1) & 1, nullptr);
-  }
+  if (!alive) s_abort = 1;
 }
 
 // ------------------------------------------------------------ decode merge
@@ -1571,8 +1602,8 @@ __global__ void kv_write_kernel(const uint4* __restrict__ k_new, const uint4* __
 }
 
 template <int D, int NQ>
-size_t decode_smem() {
-  return 1024 + 2 * TileGeom<D>::kBufBytes + 2 * 8 * NQ * D * 2 + 64;
+size_t decode_smem() {  // ring, q buffers, barriers (full, empty: 2 each; ready, free)
+  return 1024 + 2 * TileGeom<D>::kBufBytes + 2 * 8 * NQ * D * 2 + (4 + 2 * kQueue) * 8;
 }
 KernelParams make_params(const AttnArgs& a) {
   KernelParams p{};
@@ -1674,7 +1705,8 @@ bi_status decode_impl(const AttnArgs& a, cudaStream_t s) {
     static int per_sm[2][3] = {};
     int& occ = per_sm[D == 128][NQ];
     if (occ == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                        &occ, attn_decode_split_kernel<D, NQ>, 32, sm) != cudaSuccess)
+                        &occ, attn_decode_split_kernel<D, NQ>, kSplitThreads, sm) !=
+                        cudaSuccess)
       return BI_ERR_CUDA;
     const int sms = device_sm_count();
     if (sms <= 0 || occ <= 0) return BI_ERR_CUDA;
@@ -1685,7 +1717,8 @@ bi_status decode_impl(const AttnArgs& a, cudaStream_t s) {
     p.target_units = static_cast<int>(16 * cap);
     if (!p.local_plan) attn_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
     const int grid = static_cast<int>(max_units < cap ? max_units : cap);
-    if (launch_pdl(attn_decode_split_kernel<D, NQ>, dim3(grid), dim3(32), sm, s, km, vm, p) !=
+    if (launch_pdl(attn_decode_split_kernel<D, NQ>, dim3(grid), dim3(kSplitThreads), sm, s, km,
+                   vm, p) !=
         cudaSuccess)
       return BI_ERR_CUDA;
   }
