@@ -933,7 +933,9 @@ constexpr int kMergeChunk = 32;
 
 template <int D>
 __global__ void __launch_bounds__(D) attn_decode_merge_kernel(const KernelParams p) {
-  const int qh = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+  // each warp's coefficients of the chunk being folded: {ca, cb, l, kind}
+  __shared__ float4 coef[D / 32][kMergeChunk];
+  const int qh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   grid_dependency_wait();  // every split kernel block has finished
   int b, ns;
   if (p.order) {
@@ -961,14 +963,11 @@ __global__ void __launch_bounds__(D) attn_decode_merge_kernel(const KernelParams
   bool have = false;            // a non-empty split was folded
   bool bad = false;             // a split with bad pages
   float o = 0.0f, l = 0.0f;
-  float2 ml;
-  float ov[kMergeChunk];
-  if (ns > 0) load(0, ml, ov);
-  for (int c0 = 0; c0 < ns; c0 += kMergeChunk) {
-    float2 ml_next = make_float2(-CUDART_INF_F, 0.0f);
-    float ov_next[kMergeChunk];
-    if (c0 + kMergeChunk < ns) load(c0 + kMergeChunk, ml_next, ov_next);
-    // coefficients of split c0 + lane
+  // two chunk buffers: the chunk being folded and the next one in flight
+  float2 ml0, ml1;
+  float ov0[kMergeChunk], ov1[kMergeChunk];
+  auto fold = [&](const float2 ml, const float (&ov)[kMergeChunk]) {
+    // coefficients of the chunk's split lane
     const float m = ml.x, lj = ml.y;
     const bool nonempty = m != -CUDART_INF_F;
     float pm = m;  // inclusive prefix max over the chunk
@@ -990,19 +989,29 @@ __global__ void __launch_bounds__(D) attn_decode_merge_kernel(const KernelParams
     const int kind = nonempty ? (had ? 2 : 1) : 0;  // 0 empty, 1 first non-empty, 2 fold in
     run_m = fmaxf(run_m, __shfl_sync(kFull, pm, 31));
     have = have || ne != 0;
+    // the fold reads split j's coefficients as one broadcast load, which
+    // can be issued ahead of the chain (shuffles issued in place stalled
+    // every step of it)
+    coef[warp][lane] = make_float4(ca, cb, lj, __int_as_float(kind));
+    __syncwarp();
 #pragma unroll
     for (int j = 0; j < kMergeChunk; ++j) {
-      const int kj = __shfl_sync(kFull, kind, j);
-      const float caj = __shfl_sync(kFull, ca, j), cbj = __shfl_sync(kFull, cb, j);
-      const float lsj = __shfl_sync(kFull, lj, j);
-      const float nl = lse_mix(l, caj, lsj, cbj);
-      const float no = lse_mix(o, caj, ov[j], cbj);
-      l = kj == 2 ? nl : (kj == 1 ? lsj : l);
+      const float4 cf = coef[warp][j];
+      const int kj = __float_as_int(cf.w);
+      const float nl = lse_mix(l, cf.x, cf.z, cf.y);
+      const float no = lse_mix(o, cf.x, ov[j], cf.y);
+      l = kj == 2 ? nl : (kj == 1 ? cf.z : l);
       o = kj == 2 ? no : (kj == 1 ? ov[j] : o);
     }
-    ml = ml_next;
-#pragma unroll
-    for (int j = 0; j < kMergeChunk; ++j) ov[j] = ov_next[j];
+    __syncwarp();  // every lane is done with the chunk's coefficients
+  };
+  if (ns > 0) load(0, ml0, ov0);
+  for (int c0 = 0; c0 < ns; c0 += 2 * kMergeChunk) {
+    if (c0 + kMergeChunk < ns) load(c0 + kMergeChunk, ml1, ov1);
+    fold(ml0, ov0);
+    if (c0 + kMergeChunk >= ns) break;
+    if (c0 + 2 * kMergeChunk < ns) load(c0 + 2 * kMergeChunk, ml0, ov0);
+    fold(ml1, ov1);
   }
   const float r = (ns > 0 && !bad && l > 0.0f) ? __fdiv_rn(o, l) : 0.0f;
   const int64_t oidx = row * D + tid;
