@@ -871,6 +871,29 @@ __global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
     if (!alive) break;
     if (single) {
       // ---- the output of the valid columns
+      if (NQ == 1 && G <= 4) {
+        // lanes with t >= 2 hold padding columns: each takes the odd column
+        // of lane t - 2 (one exchange), so every lane divides 16 values
+        const bool helper = t >= 2;
+        const int col = 2 * (t & 1) + (helper ? 1 : 0);
+        const float l_odd = __shfl_xor_sync(kFull, st.l[0][1], 2);
+        const float lv = helper ? l_odd : st.l[0][0];
+        const int64_t orow = (row0 + col) * D;
+#pragma unroll
+        for (int md = 0; md < D / 16; ++md)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const float o_odd = __shfl_xor_sync(kFull, st.o[md][0][2 * hh + 1], 2);
+            const float ov = helper ? o_odd : st.o[md][0][2 * hh];
+            if (col < G) {
+              const float v = lv > 0.0f ? __fdiv_rn(ov, lv) : 0.0f;
+              const int64_t idx = orow + 16 * md + g + 8 * hh;
+              static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
+              if (p.out_f32) p.out_f32[idx] = v;
+            }
+          }
+        continue;
+      }
 #pragma unroll
       for (int nq = 0; nq < NQ; ++nq)
 #pragma unroll
