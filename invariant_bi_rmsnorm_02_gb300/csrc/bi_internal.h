@@ -74,8 +74,25 @@ inline bool gemm_narrow(int64_t M, int64_t N, int64_t K, int num_sms, bool swigl
          K / kGemmBK >= kGemmNarrowKBlocks &&
          (N + kGemmNarrowBN - 1) / kGemmNarrowBN <= num_sms;
 }
+// Above the small batches, a 128 x 192 tile where its tiles fill the SMs
+// better than 128 x 256 ones: rounds of num_sms tiles times the tile width,
+// the 192-column cost weighted by 10/9 (its tiles ran ~10% slower per flop
+// on GB300: 8192 x 6144 x 4096 took 266 us against 252 with 256-column
+// tiles, while at 256 and 1024 rows, one or two rounds, it took 28 and 47 us
+// against 35 and 57); 256 always with SwiGLU.
+constexpr int kGemmMidBN = 192;
+inline int gemm_wide_tile(int64_t M, int64_t N, int num_sms, bool swiglu) {
+  if (swiglu || M <= kGemmSmallRows || num_sms <= 0) return kGemmBN;
+  const int64_t mt = (M + kGemmBM - 1) / kGemmBM;
+  auto cost = [&](int64_t bn) {
+    const int64_t tiles = mt * ((N + bn - 1) / bn);
+    return ((tiles + num_sms - 1) / num_sms) * bn;
+  };
+  return cost(kGemmMidBN) * 10 < cost(kGemmBN) * 9 ? kGemmMidBN : kGemmBN;
+}
 inline int gemm_n_tile(int64_t M, int64_t N, int64_t K, int num_sms, bool swiglu) {
-  return gemm_narrow(M, N, K, num_sms, swiglu) ? kGemmNarrowBN : kGemmBN;
+  return gemm_narrow(M, N, K, num_sms, swiglu) ? kGemmNarrowBN
+                                                : gemm_wide_tile(M, N, num_sms, swiglu);
 }
 // swiglu: C is [M, N/2], the SwiGLU product of each tile's two column halves
 bi_status launch_gemm(const void* A, const void* W, void* C, int64_t M, int64_t N, int64_t K,

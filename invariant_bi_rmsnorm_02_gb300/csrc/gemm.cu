@@ -77,22 +77,26 @@ constexpr int kSmallRows = kGemmSmallRows;
 // out as a single k-block stage would be.
 template <int kARows, int kBN, int kKG>
 struct Ring {
-  static constexpr int kStages = kBN == 256 ? (kARows == BM ? 4 : 6) : (kARows == 64 ? 3 : 4);
+  static constexpr int kStages =
+      kBN == 256 ? (kARows == BM ? 4 : 6) : kBN == 192 ? 5 : (kARows == 64 ? 3 : 4);
   static constexpr int kASub = kARows * BK * 2;  // one k-block of A
   static constexpr int kBSub = kBN * BK * 2;     // one k-block of W
   static constexpr int kABytes = kKG * kASub;
   static constexpr int kBBytes = kKG * kBSub;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
-  // two kBN-column fp32 accumulators (a power of two of at least 32 columns)
-  static constexpr uint32_t kTmemCols = 2 * kBN < 32 ? 32u : 2u * kBN;
+  // two kBN-column fp32 accumulators, allocated as a power of two of at
+  // least 32 columns
+  static constexpr uint32_t kTmemCols = 2 * kBN <= 32 ? 32u : 2 * kBN <= 128 ? 128u
+                                        : 2 * kBN <= 256 ? 256u : 512u;
   // the MMA reads a 128-row A window from each A sub-tile: it must stay
   // inside the block's shared memory (the W ring follows the A ring)
   static_assert((kStages * kKG - 1) * kASub + BM * BK * 2 <= kStages * kStageBytes,
                 "small-batch A window leaves shared memory");
   static_assert(kSmemBytes <= 227 * 1024, "ring exceeds shared memory");
-  static_assert((kBN == 256 && kKG == 1) || (kBN == kGemmNarrowBN && kKG == kGemmNarrowKBlocks),
-                "256-column tiles take one k-block a stage, narrow tiles four");
+  static_assert(((kBN == 256 || kBN == kGemmMidBN) && kKG == 1) ||
+                    (kBN == kGemmNarrowBN && kKG == kGemmNarrowKBlocks),
+                "wide tiles take one k-block a stage, narrow tiles four");
 };
 
 // K-major tiles written by TMA with 128-byte swizzling: rows of 64 bf16
@@ -435,10 +439,11 @@ bi_status launch_tc_ring(const CUtensorMap& ta, const CUtensorMap& tb, const Gem
   gemm_tc_kernel<kEpi, kARows, kBN, kKG><<<grid, kThreads, smem, s>>>(ta, tb, p);
   return cuda_status(cudaGetLastError());
 }
-// narrow: the narrow ring runs (gemm_narrow); a_rows: rows of A per stage
+// narrow: the narrow ring runs (gemm_narrow); a_rows: rows of A per stage;
+// bn: the tile width (gemm_n_tile)
 template <int kEpi>
 bi_status launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int grid,
-                    bool narrow, uint32_t a_rows, cudaStream_t s) {
+                    bool narrow, uint32_t a_rows, int bn, cudaStream_t s) {
   if constexpr (kEpi != kEpiSwiglu) {
     if (narrow)
       return a_rows == kSmallRows
@@ -447,8 +452,11 @@ bi_status launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const GemmPara
                  : launch_tc_ring<kEpi, kGemmNarrowRows, kGemmNarrowBN, kGemmNarrowKBlocks>(
                        ta, tb, p, grid, s);
   }
-  return a_rows == kSmallRows ? launch_tc_ring<kEpi, kSmallRows, 256, 1>(ta, tb, p, grid, s)
-                              : launch_tc_ring<kEpi, BM, 256, 1>(ta, tb, p, grid, s);
+  if (a_rows == kSmallRows) return launch_tc_ring<kEpi, kSmallRows, 256, 1>(ta, tb, p, grid, s);
+  if constexpr (kEpi != kEpiSwiglu) {
+    if (bn == kGemmMidBN) return launch_tc_ring<kEpi, BM, kGemmMidBN, 1>(ta, tb, p, grid, s);
+  }
+  return launch_tc_ring<kEpi, BM, 256, 1>(ta, tb, p, grid, s);
 }
 
 }  // namespace
@@ -459,7 +467,7 @@ bi_status launch_gemm(const void* A, const void* W, void* C, int64_t M, int64_t 
   if (sms <= 0) return BI_ERR_CUDA;
   CUtensorMap ta, tb;
   const bool narrow = gemm_narrow(M, N, K, sms, swiglu);
-  const int bn = narrow ? kGemmNarrowBN : kGemmBN;
+  const int bn = gemm_n_tile(M, N, K, sms, swiglu);
   // rows of A per stage (the A box)
   const uint32_t a_rows = M <= kSmallRows ? kSmallRows : (narrow ? kGemmNarrowRows : BM);
   const bool ok =
@@ -498,9 +506,9 @@ bi_status launch_gemm(const void* A, const void* W, void* C, int64_t M, int64_t 
   if (units > 0x7fffffff) return BI_ERR_UNSUPPORTED;
   const int grid = static_cast<int>(units < sms ? units : sms);
   if (p.splits == 1)
-    return swiglu ? launch_tc<kEpiSwiglu>(ta, tb, p, grid, narrow, a_rows, s)
-                  : launch_tc<kEpiBf16>(ta, tb, p, grid, narrow, a_rows, s);
-  const bi_status st = launch_tc<kEpiF32>(ta, tb, p, grid, narrow, a_rows, s);
+    return swiglu ? launch_tc<kEpiSwiglu>(ta, tb, p, grid, narrow, a_rows, bn, s)
+                  : launch_tc<kEpiBf16>(ta, tb, p, grid, narrow, a_rows, bn, s);
+  const bi_status st = launch_tc<kEpiF32>(ta, tb, p, grid, narrow, a_rows, bn, s);
   if (st != BI_OK) return st;
   const int64_t n4 = swiglu ? M * N / 8 : M * N / 4;  // threads of the reduction
   const int rb = static_cast<int>((n4 + 255) / 256 < 4 * sms ? (n4 + 255) / 256 : 4 * sms);
