@@ -121,7 +121,7 @@ def fingerprint(dev, rank):
         "driver": driver, "cuda_runtime": torch.version.cuda, "torch": torch.__version__,
         "libbi": bi.bi_version(), "libbi_sources_sha": source_hash(
             *sorted(f for f in os.listdir(csrc) if os.path.isfile(os.path.join(csrc, f)))),
-        "gemm_tile": "128x256 (128x64 for M<=64 where those tiles fit one wave), k-block 64, tcgen05 kind::f16 M=128 K=16",
+        "gemm_tile": "128x256 (128x64 for M<=64 where those tiles fit one wave, 128x192 where it fills the SMs better), k-block 64, tcgen05 kind::f16 M=128 K=16",
         "attention_key_tile": 64, "split_size": DEC["S"], "page_size": DEC["page"],
         "seeds": "workload seeds 100000*rank + 1..11 (rank %d)" % rank,
         "host_cores": os.cpu_count(),

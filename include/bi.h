@@ -114,12 +114,15 @@ size_t bi_rmsnorm_workspace_size(int64_t M, int64_t H, bi_mode mode);
  * INVARIANT: one tensor-core instruction family (tcgen05.mma kind::f16,
  *   M=128, K=16) and one K order (k-blocks of 64 in increasing k) for every
  *   M; no split-K, no stream-K (P1 §5.4: the instruction and the split are
- *   the two freedoms to give up).  Output tiles are 128 x 256, or 128 x 64
- *   (instruction N=64) for M <= 64 when ceil(N/64) tiles fit in one wave of
- *   the device's SMs, K % 64 == 0 and K >= 256: more blocks then stream the
- *   weight.  The instruction's N does not change any output element's sum
- *   (every element has the same bytes at N = 64 and N = 256 on sm_103a), so
- *   a row's bytes do not depend on M.  Needs no workspace.
+ *   the two freedoms to give up).  Output tiles are 128 x 64 (instruction
+ *   N=64) for M <= 64 when ceil(N/64) tiles fit in one wave of the device's
+ *   SMs, K % 64 == 0 and K >= 256 (more blocks then stream the weight);
+ *   otherwise 128 x 192 above 32 rows when its tiles fill the SMs' rounds
+ *   better (rounds of #SM tiles times the width, 192's weighted by 10/9),
+ *   else 128 x 256.  The instruction's N does not change any output
+ *   element's sum (every element has the same bytes at N = 64, 192 and 256
+ *   on sm_103a), so a row's bytes do not depend on M.  Needs no
+ *   workspace.
  * VARIANT: same tiles and instruction, but K is split into s slices chosen
  *   from M, N and the SM count (split-K, P1 §5.4: only when the output tiles
  *   cover at most a quarter of the SMs, then doubling until the slices cover
