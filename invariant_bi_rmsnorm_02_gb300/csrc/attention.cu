@@ -521,9 +521,10 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const KernelPar
 //     G query heads of the kv head are the columns of NQ 8-wide n-tiles) and
 //     writes the unit's partial state, or the output when the sequence has a
 //     single split.
-// Measured on one block: issuing a tile's copies (one lane, 9 copies) took as
-// long as a third of the tile's arithmetic, and opening a unit a quarter;
-// both are off the compute warp's path here.  Barriers: full / empty per ring
+// Measured on one block with a single warp doing everything: issuing a
+// tile's copies (one lane, 9 copies) took ~1,400 cycles against ~1,800 for
+// the tile's arithmetic, and opening a unit ~870; both are off the compute
+// warp's path here.  Barriers: full / empty per ring
 // buffer, ready / free per descriptor slot; every wait is bounded, a wait
 // that runs out raises a flag that makes the other warp's waits return, and
 // the producer lets its copies in flight land before it exits.  A unit whose
