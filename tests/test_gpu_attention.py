@@ -336,11 +336,23 @@ def test_bad_page_id_is_reported_not_faulted(cuda):
     bt = kvd.block_table.clone()
     bt[1, 2] = kv.num_pages + 5      # outside the pool
     q = synth.normal_bf16((2, 4, 64), 5401, device=cuda)
-    decode(q, kvd, 128, 64, bt=bt)
+    bad, _ = decode(q, kvd, 128, 64, bt=bt)
     assert bi.bi_check_device_errors() == bi.ERR_DEVICE_BOUNDS
     assert bi.bi_check_device_errors() == bi.OK          # cleared by the read
     out, _ = decode(q, kvd, 128, 64)                      # the context still works
     assert bi.bi_check_device_errors() == bi.OK
+    # the offending sequence (one split of 64: written by the split kernel)
+    # comes out as zeros, the other one is untouched
+    assert not bool(bad[1].float().abs().sum())
+    assert same_bytes(bad[0], out[0])
+    # a bad page in the second split of a two-split sequence: zeros through
+    # the merge's l = -1 mark
+    bt2 = kvd.block_table.clone()
+    bt2[0, 5] = -3                   # keys 80..95 of the 100
+    bad2, _ = decode(q, kvd, 128, 64, bt=bt2)
+    assert bi.bi_check_device_errors() == bi.ERR_DEVICE_BOUNDS
+    assert not bool(bad2[0].float().abs().sum())
+    assert same_bytes(bad2[1], out[1])
     lens = kvd.kv_lens.clone()
     lens[0] = 10 ** 6                                      # beyond the page table
     decode(q, kvd, 128, 64, kv_lens=lens)
