@@ -197,7 +197,7 @@ bi_status bi_gemm_swiglu(const void* A, const void* W, void* out, int64_t M, int
  *   pages name as not batch-invariant): one chunk size C for the call,
  *   C = 64 * max(ceil(Hkv * T / U), ceil(T_max / c)), where T is the sum and
  *   T_max the largest of the sequences' 64-key tile counts ceil(L/64),
- *   U = 16 * (resident split-kernel blocks on the device) the target number
+ *   U = 4 * (resident split-kernel blocks on the device) the target number
  *   of work units, and c = variant_splits if > 0, else
  *   c = min(128, ceil(max_kv_len / 256)) the largest number of chunks a
  *   sequence may get (it sizes the workspace);
