@@ -105,6 +105,22 @@ def test_gemm_batch_invariance_over_m(cuda):
     assert same_bytes(bi.gemm(other, W)[50], full[3])
 
 
+def test_gemm_last_round_rows_match_small_batches(cuda):
+    # at 8192 rows the QKV projection's last round of 128 x 256 tiles (the
+    # last rows in raster order) runs on a few SMs while the others are done:
+    # every row there, and elsewhere, has the bytes of a small batch
+    K, N = 4096, 6144
+    A = synth.normal_bf16((8192, K), 3450, device=cuda)
+    W = synth.normal_bf16((N, K), 3451, std=0.02, device=cuda)
+    full = bi.gemm(A, W)
+    assert bi.bi_check_device_errors() == bi.OK
+    for r0 in (0, 4096, 7680, 7936):
+        part = bi.gemm(A[r0:r0 + 256].contiguous(), W)
+        assert same_bytes(part, full[r0:r0 + 256]), (r0, first_divergence(part, full[r0:r0 + 256]))
+    # the same rows again at 8192, run to run
+    assert same_bytes(bi.gemm(A, W), full)
+
+
 def test_gemm_batch_invariance_mlp_up(cuda):
     K, N = 4096, 14336
     A = synth.normal_bf16((1024, K), 3500, device=cuda)
