@@ -528,21 +528,24 @@ def run_reference(args):
 GEMM_M_SWEEP = (1, 3, 16, 64, 256, 1024, 8192)
 
 
-def gemm_m_sweep(wl, flush, stream, reps=3):
+def gemm_m_sweep(wl, flush, stream, reps=9):
     """The cost of invariance across batch sizes: the QKV and MLP-up GEMMs at
     every M of the projection workload, invariant and batch-variant (split-K),
     L2 clean before each call; returns {M: {...}} of median times and the
-    invariant slowdown t_inv / t_var - 1."""
+    invariant slowdown t_inv / t_var - 1. The two modes alternate call by call
+    so that a drift of the clock or of a neighbour's load falls on both; at the
+    M where the variant plan takes one split both run the same kernel and the
+    slowdown is the timing noise of a 20-50 us call."""
     bi = wl.bi
     out = {}
+    modes = (bi.INVARIANT, bi.VARIANT)
     with torch.cuda.stream(stream):
         for m in GEMM_M_SWEEP:
             row = {}
             for name, W, C in (("qkv", wl.Wqkv, wl.qkv), ("up", wl.Wup, wl.up)):
-                ms = {}
-                for mode in (bi.INVARIANT, bi.VARIANT):
-                    ts = []
-                    for r in range(reps + 1):
+                ts = {mode: [] for mode in modes}
+                for r in range(reps + 1):
+                    for mode in modes:
                         flush.zero_()
                         torch.cuda._sleep(HOST_LEAD_CYCLES)
                         e0 = torch.cuda.Event(enable_timing=True)
@@ -552,8 +555,8 @@ def gemm_m_sweep(wl, flush, stream, reps=3):
                         e1.record(stream)
                         stream.synchronize()
                         if r:
-                            ts.append(e0.elapsed_time(e1))
-                    ms[mode] = statistics.median(ts)
+                            ts[mode].append(e0.elapsed_time(e1))
+                ms = {mode: statistics.median(ts[mode]) for mode in modes}
                 row[name] = {"ms": ms[bi.INVARIANT], "ms_variant": ms[bi.VARIANT],
                              "slowdown": ms[bi.INVARIANT] / ms[bi.VARIANT] - 1.0}
             out[m] = row

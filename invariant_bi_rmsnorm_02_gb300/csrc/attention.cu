@@ -1071,15 +1071,18 @@ __global__ void __launch_bounds__(D) attn_decode_merge_kernel(const KernelParams
 // lanes of quadrant w), keeping each row's split state (reference maximum m,
 // sum l) in registers; warps 4-7 fold every finished split into the merged
 // state (in shared memory) while the next split runs, and write out = o / l
-// at the end; warp 8 issues the MMAs; warp 9 the TMA copies (K
-// and V rings, page ids cached in shared memory).  A split's accumulator is
-// reused two splits later, once its fold is done.  The fold and TMA warps
-// sleep in their barrier waits instead of polling, so that they leave the
-// issue slots of their scheduler to the softmax warp beside them.  Blocks
-// are started longest first.
+// at the end; warp 8 issues the MMAs; warps 9-12 the TMA copies, one column
+// half of K or of V each (page ids cached in shared memory).  A single lane
+// issuing all of a tile's copies was the kernel's bottleneck: it shares its
+// scheduler with a softmax warp and took ~130 cycles per 2 KB page box, as
+// long as the softmax and MMA work of the tile together.  A split's
+// accumulator is reused two splits later, once its fold is done.  The fold
+// and copy warps sleep in their barrier waits instead of polling, so that
+// they leave the issue slots of their scheduler to the softmax warp beside
+// them.  Blocks are started longest first.
 constexpr int kPfRows = 128;
-constexpr int kPfThreads = 10 * 32;
-constexpr int kPfSoftWarp0 = 0, kPfFoldWarp0 = 4, kPfMmaWarp = 8, kPfTmaWarp = 9;
+constexpr int kPfThreads = 13 * 32;
+constexpr int kPfSoftWarp0 = 0, kPfFoldWarp0 = 4, kPfMmaWarp = 8, kPfTmaWarp0 = 9;
 constexpr int kPfPageCache = 1024;  // page ids held in shared memory (16384 keys)
 constexpr int kPfKStages = 3;
 constexpr int kPfSBufs = 4;         // S / P buffers in tensor memory
@@ -1230,11 +1233,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
     for (int i = 0; i < kPfKStages; ++i) {
-      mbar_init(&kfull[i], 1);
+      mbar_init(&kfull[i], Gm::kHalves);
       mbar_init(&kfree[i], 1);
     }
     for (int i = 0; i < kPfVStages; ++i) {
-      mbar_init(&vfull[i], 1);
+      mbar_init(&vfull[i], Gm::kHalves);
     }
     for (int i = 0; i < kPfSBufs; ++i) {
       mbar_init(&sfull[i], 1);
@@ -1265,48 +1268,48 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == kPfTmaWarp) {
+  if (warp >= kPfTmaWarp0) {
     // ================================================================ copies
-    // One thread.  Tile i: K into stage i % KS once the S of tile i - KS is
-    // done, V into stage i % VS once the PV of tile i - VS is (pfree).
-    if (lane == 0) {
-      auto issue_tile = [&](int i, bool is_v) {
-        uint8_t* dst = is_v ? vst + (i % kPfVStages) * Gm::kTBytes
-                            : kst + (i % kPfKStages) * Gm::kTBytes;
+    // Warps 9, 10: column halves 0, 1 of K; warps 11, 12: those of V (one
+    // lane each; with D = 64 only warps 9 and 11 copy).  Tile i: K into stage
+    // i % KS once the S of tile i - KS is done (kfree), V into stage i % VS
+    // once the PV of tile i - VS is (pfree).  Each copying warp arrives on
+    // the stage's full barrier with the bytes of its half.
+    const int role = warp - kPfTmaWarp0;
+    const bool is_v = role >= 2;
+    const int hf = role & 1;
+    if (lane == 0 && hf < Gm::kHalves) {
+      const CUtensorMap* map = is_v ? &vmap : &kmap;
+      auto issue_tile = [&](int i) {
+        uint8_t* dst = (is_v ? vst + (i % kPfVStages) * Gm::kTBytes
+                             : kst + (i % kPfKStages) * Gm::kTBytes) + hf * (kTile * 128);
         uint64_t* bar = is_v ? &vfull[i % kPfVStages] : &kfull[i % kPfKStages];
         const int key0 = i * kTile;
         const int np = pages_below(key0, kvl);
-        mbar_arrive_expect_tx(bar, np * Gm::kHalves * 2048);
+        mbar_arrive_expect_tx(bar, np * 2048);
         for (int pp = 0; pp < np; ++pp) {
           const int pg = (key0 >> 4) + pp;
           const int y = ((pg < kPfPageCache ? pid_s[pg] : bt_row[pg]) * p.Hkv + h) * kPage;
-#pragma unroll
-          for (int hf = 0; hf < Gm::kHalves; ++hf)
-            tma_load_2d(dst + hf * (kTile * 128) + pp * 2048, is_v ? &vmap : &kmap, hf * 64, y,
-                        bar);
+          tma_load_2d(dst + pp * 2048, map, hf * 64, y, bar);
         }
       };
       bool ok = true;
-      int nk = 0, nv = 0;
+      int n = 0;
       for (int i = 0; i < ntiles && ok; ++i) {
-        if (i >= kPfKStages)
+        if (!is_v && i >= kPfKStages)
           ok = pf_wait_lazy(&kfree[i % kPfKStages], ((i / kPfKStages) - 1) & 1, p.err, &s_abort);
-        if (!ok) break;
-        issue_tile(i, false);
-        ++nk;
-        if (i >= kPfVStages)
+        if (is_v && i >= kPfVStages)
           ok = pf_wait_lazy(&pfree[i % kPfVStages], ((i / kPfVStages) - 1) & 1, p.err, &s_abort);
         if (!ok) break;
-        issue_tile(i, true);
-        ++nv;
+        issue_tile(i);
+        ++n;
       }
       // every copy lands before the block exits (bounded waits)
-      for (int k = max(0, nk - kPfKStages); k < nk; ++k)
-        pf_wait_lazy(&kfull[k % kPfKStages], (k / kPfKStages) & 1, ok ? p.err : nullptr,
-                     ok ? &s_abort : nullptr);
-      for (int j = max(0, nv - kPfVStages); j < nv; ++j)
-        pf_wait_lazy(&vfull[j % kPfVStages], (j / kPfVStages) & 1, ok ? p.err : nullptr,
-                     ok ? &s_abort : nullptr);
+      const int stages = is_v ? kPfVStages : kPfKStages;
+      for (int k = max(0, n - stages); k < n; ++k) {
+        uint64_t* fb = is_v ? &vfull[k % kPfVStages] : &kfull[k % kPfKStages];
+        pf_wait_lazy(fb, (k / stages) & 1, ok ? p.err : nullptr, ok ? &s_abort : nullptr);
+      }
     }
     __syncwarp();
   } else if (warp == kPfMmaWarp) {
@@ -1342,14 +1345,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
         return true;
       };
       bool ok = issue_s(0);
-      for (int i = 0; i < ntiles && ok; ++i) {
+      // split of tile i and the tile's place in it, kept by counters: a
+      // division by the runtime tiles-per-split costs the single issuing
+      // thread a few hundred cycles per tile
+      int j = 0, t_in = 0;
+      for (int i = 0; i < ntiles && ok; ++i, (++t_in == tps ? (t_in = 0, ++j) : 0)) {
         const int sb = i % kPfSBufs;
         const int stg = i % kPfVStages;
         uint8_t* vt = vst + stg * Gm::kTBytes;
         const int key0 = i * kTile;
-        const int j = i / tps;
-        const bool split_first = i % tps == 0;
-        const bool split_last = (i + 1) % tps == 0 || i + 1 == ntiles;
+        const bool split_first = t_in == 0;
+        const bool split_last = t_in == tps - 1 || i + 1 == ntiles;
         // the next tile's S goes to the tensor core ahead of this tile's PV,
         // so that its softmax can start as soon as this one's ends
         if (i + 1 < ntiles && !issue_s(i + 1)) {
@@ -1399,12 +1405,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     float m = -CUDART_INF_F, l = 0.0f;  // the split's reference maximum and sum
     bool live = true;                   // no wait has run out
-    for (int i = 0; i < ntiles && live; ++i) {
+    int j = 0, t_in = 0;  // split of tile i and the tile's place in it (counters)
+    for (int i = 0; i < ntiles && live; ++i, (++t_in == tps ? (t_in = 0, ++j) : 0)) {
       const int sb = i % kPfSBufs;
       const int key0 = i * kTile;
-      const int j = i / tps;
-      const bool split_first = i % tps == 0;
-      const bool split_last = (i + 1) % tps == 0 || i + 1 == ntiles;
+      const bool split_first = t_in == 0;
+      const bool split_last = t_in == tps - 1 || i + 1 == ntiles;
       const uint32_t sa = tl + Gm::kColS + kTile * sb;
       // ---- scores of the tile: all 64 in registers
       live = __all_sync(kFull, mbar_wait(&sfull[sb], (i / kPfSBufs) & 1, p.err, &s_abort));
