@@ -123,7 +123,7 @@ def fingerprint(dev, rank):
             *sorted(f for f in os.listdir(csrc) if os.path.isfile(os.path.join(csrc, f)))),
         "gemm_tile": "128x256 (128x64 for M<=64 where those tiles fit one wave, 128x192 where it fills the SMs better), k-block 64, tcgen05 kind::f16 M=128 K=16",
         "attention_key_tile": 64, "split_size": DEC["S"], "page_size": DEC["page"],
-        "seeds": "workload seeds 100000*rank + 1..11 (rank %d)" % rank,
+        "seeds": "workload seeds 100000*rank + 1..15 (rank %d)" % rank,
         "host_cores": os.cpu_count(),
     }
 
@@ -205,8 +205,11 @@ class Workload:
         self.lens0 = self.kv.kv_lens.clone()
         self.lens = self.kv.kv_lens.clone()
         self.seq = torch.arange(d["B"], dtype=torch.int32, device=dev)
-        self.q = synth.normal_bf16((d["B"], d["Hq"], d["D"]), s + 7, device=dev)
-        self.k_new = synth.normal_bf16((d["B"], d["Hkv"], d["D"]), s + 8, device=dev)
+        # seeds apart from the cache's: paged_kv(seed) draws K from seed + 1
+        # and V from seed + 2, and queries equal to cached keys would be a
+        # degenerate input (their own key scores ~11 sigma above the rest)
+        self.q = synth.normal_bf16((d["B"], d["Hq"], d["D"]), s + 13, device=dev)
+        self.k_new = synth.normal_bf16((d["B"], d["Hkv"], d["D"]), s + 14, device=dev)
         self.v_new = synth.normal_bf16((d["B"], d["Hkv"], d["D"]), s + 9, device=dev)
         self.dec_out = torch.empty_like(self.q)
         self.dec_ws = {}
@@ -215,7 +218,7 @@ class Workload:
                                                   d["max_len"], d["S"], mode)
             self.dec_ws[mode] = torch.empty(nb // 4 + 4, dtype=torch.float32, device=dev)
         self.pkv = synth.paged_kv([PRE["T"]], d["Hkv"], d["D"], d["page"], s + 10, device=dev)
-        self.pq = synth.normal_bf16((PRE["chunk"], d["Hq"], d["D"]), s + 11, device=dev)
+        self.pq = synth.normal_bf16((PRE["chunk"], d["Hq"], d["D"]), s + 15, device=dev)
         self.pout = torch.empty_like(self.pq)
         self.cu = torch.tensor([0, PRE["chunk"]], dtype=torch.int32, device=dev)
         self.pstart = torch.tensor([PRE["start"]], dtype=torch.int32, device=dev)
@@ -531,11 +534,12 @@ GEMM_M_SWEEP = (1, 3, 16, 64, 256, 1024, 8192)
 def gemm_m_sweep(wl, flush, stream, reps=9):
     """The cost of invariance across batch sizes: the QKV and MLP-up GEMMs at
     every M of the projection workload, invariant and batch-variant (split-K),
-    L2 clean before each call; returns {M: {...}} of median times and the
+    L2 clean before each call; returns {M: {...}} of mean times and the
     invariant slowdown t_inv / t_var - 1. The two modes alternate call by call
-    so that a drift of the clock or of a neighbour's load falls on both; at the
-    M where the variant plan takes one split both run the same kernel and the
-    slowdown is the timing noise of a 20-50 us call."""
+    so that a drift of the clock or of a neighbour's load falls on both, and
+    the mean (not the median) is taken because the event times of a 20 us call
+    come in steps of ~0.7 us; at the M where the variant plan takes one split
+    both run the same kernel and the slowdown is timing noise."""
     bi = wl.bi
     out = {}
     modes = (bi.INVARIANT, bi.VARIANT)
@@ -556,7 +560,7 @@ def gemm_m_sweep(wl, flush, stream, reps=9):
                         stream.synchronize()
                         if r:
                             ts[mode].append(e0.elapsed_time(e1))
-                ms = {mode: statistics.median(ts[mode]) for mode in modes}
+                ms = {mode: statistics.fmean(ts[mode]) for mode in modes}
                 row[name] = {"ms": ms[bi.INVARIANT], "ms_variant": ms[bi.VARIANT],
                              "slowdown": ms[bi.INVARIANT] / ms[bi.VARIANT] - 1.0}
             out[m] = row
@@ -596,7 +600,7 @@ def tiny_layer(dev, stream, reps=20):
     W = synth.normal_bf16((c["N"], c["H"]), 1003, std=0.02, device=dev)
     lens = synth.uniform_int(c["B"], 1, c["max_len"], 1004).tolist()
     kv = synth.paged_kv(lens, c["Hkv"], c["D"], c["page"], 1005, device=dev)
-    q = synth.normal_bf16((c["B"], c["Hq"], c["D"]), 1006, device=dev)
+    q = synth.normal_bf16((c["B"], c["Hq"], c["D"]), 1016, device=dev)  # apart from K, V
     y, C, out = torch.empty_like(x), torch.empty(c["B"], c["N"], dtype=torch.bfloat16,
                                                  device=dev), torch.empty_like(q)
     ws = torch.empty(bi.bi_attn_decode_workspace_size(c["B"], c["Hq"], c["Hkv"], c["D"],
@@ -627,7 +631,7 @@ def prefill_schedules(dev, stream, flush):
     c = synth.CHUNKED_PREFILL
     T, d = c["T"], DEC
     kv = synth.paged_kv([T], c["Hkv"], c["D"], c["page"], 4001, device=dev)
-    q = synth.normal_bf16((T, c["Hq"], c["D"]), 4002, device=dev)
+    q = synth.normal_bf16((T, c["Hq"], c["D"]), 4012, device=dev)  # apart from K, V
     out = torch.empty_like(q)
     scale = c["D"] ** -0.5
     flops = 4.0 * c["Hq"] * c["D"] * T * (T + 1) / 2.0

@@ -78,7 +78,7 @@ def main(argv=None):
     elif a.op == "decode":
         lens = synth.loguniform_int(a.B, 1, a.max_len, 3).tolist()
         kv = synth.paged_kv(lens, 8, 128, 16, 4, device=dev)
-        q = synth.normal_bf16((a.B, 32, 128), 5, device=dev)
+        q = synth.normal_bf16((a.B, 32, 128), 15, device=dev)  # apart from K (5), V (6)
         fn = lambda: bi.attn_decode(q, kv.k_cache, kv.v_cache, kv.block_table, kv.kv_lens,
                                     max_kv_len=a.max_len, split_size=a.split, mode=a.mode)
     elif a.op == "add_rmsnorm":
@@ -110,7 +110,7 @@ def main(argv=None):
         nbytes = 2 * a.M * a.H * 2 + a.M * 4
     else:
         kv = synth.paged_kv([a.T], 8, 128, 16, 6, device=dev)
-        q = synth.normal_bf16((a.chunk, 32, 128), 7, device=dev)
+        q = synth.normal_bf16((a.chunk, 32, 128), 17, device=dev)  # apart from K (7), V (8)
         cu = torch.tensor([0, a.chunk], dtype=torch.int32, device=dev)
         st = torch.tensor([a.T - a.chunk], dtype=torch.int32, device=dev)
         fn = lambda: bi.attn_prefill_chunk(q, cu, st, kv.k_cache, kv.v_cache, kv.block_table,

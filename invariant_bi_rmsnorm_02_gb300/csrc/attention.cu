@@ -1052,63 +1052,72 @@ __global__ void __launch_bounds__(D) attn_decode_merge_kernel(const KernelParams
 }
 
 // ---------------------------------------------------- prefill (tcgen05)
-// Block (qb, h, b): 128 query rows -- up to 128 / G tokens times the G heads
-// of kv head h (row r is token r / G, head r % G).  Per tile i of 64 keys:
-//   S = Q K^T   tcgen05.mma M=128 N=64, k = d in steps of 16, into TMEM
-//               buffer i % 4 (the next tiles' S are computed while this
-//               tile's softmax runs);
-//   softmax     the decode tile step's per-element arithmetic, key summation
-//               tree and P = hi + lo split, one row per thread; P (bf16
-//               pairs) is stored back over the tile's own score columns;
+// Block: 128 query rows -- up to 128 / G tokens times the G heads of one kv
+// head (row r is token r / G, head r % G).  Keys come in tiles of 64; the
+// scores are computed for pairs of tiles:
+//   S = Q K^T   tcgen05.mma M=128 N=128 over a pair of key tiles, k = d in
+//               steps of 16, A = Q from tensor memory, into pair buffer
+//               q % 2 (the next pair's S is computed while this pair's
+//               softmax runs);
+//   softmax     per 64-key tile, the decode tile step's per-element
+//               arithmetic, key summation tree and P = hi + lo split, one
+//               row per thread; P (bf16 pairs) is stored back over the
+//               tile's own score columns;
 //   O += P V    tcgen05.mma M=128 N=D with A = P read from tensor memory,
 //               per 16-key chunk the hi part then the lo part, V read as an
-//               MN-major operand, into the accumulator of the tile's split
-//               (two accumulators, alternating by split).
+//               MN-major operand, into the accumulator (started afresh at
+//               each split's first tile, once the fold has read the
+//               previous split's).
+// An MMA instruction costs the tensor core about the same time at N = 64
+// as at N = 128, so pairs of tiles take 12 MMAs per 64 keys instead of 16.
 // tcgen05.mma and mma.sync give bit-identical fp32 results for the same
 // operands and k order, so every output row equals the decode of its
 // position bit for bit.
 // Roles: warps 0-3 run the softmax (warp w owns rows 32w..32w+31, the TMEM
 // lanes of quadrant w), keeping each row's split state (reference maximum m,
 // sum l) in registers; warps 4-7 fold every finished split into the merged
-// state (in shared memory) while the next split runs, and write out = o / l
-// at the end; warp 8 issues the MMAs; warps 9-12 the TMA copies, one column
-// half of K or of V each (page ids cached in shared memory).  A single lane
-// issuing all of a tile's copies was the kernel's bottleneck: it shares its
-// scheduler with a softmax warp and took ~130 cycles per 2 KB page box, as
-// long as the softmax and MMA work of the tile together.  A split's
-// accumulator is reused two splits later, once its fold is done.  The fold
-// and copy warps sleep in their barrier waits instead of polling, so that
-// they leave the issue slots of their scheduler to the softmax warp beside
-// them.  Blocks are started longest first.
+// state (in shared memory) and write out = o / l at the end; one lane of
+// warp 13 issues the S MMAs and one of warp 8 the PV MMAs (two schedulers:
+// a single issuing lane shares its scheduler with a softmax warp and falls
+// behind); warps 9-12 the TMA copies, one column half of K or of V each
+// (page ids cached in shared memory).  A single lane issuing all of a tile's
+// copies was the bottleneck: it shares its scheduler with a softmax warp and
+// took ~130 cycles per 2 KB page box.  The fold and copy warps sleep in
+// their barrier waits instead of polling, so that they leave the issue slots
+// of their scheduler to the softmax warp beside them.  Blocks start longest
+// first.
 constexpr int kPfRows = 128;
-constexpr int kPfThreads = 13 * 32;
-constexpr int kPfSoftWarp0 = 0, kPfFoldWarp0 = 4, kPfMmaWarp = 8, kPfTmaWarp0 = 9;
+constexpr int kPfThreads = 14 * 32;
+constexpr int kPfSoftWarp0 = 0, kPfFoldWarp0 = 4, kPfMmaWarp = 8, kPfTmaWarp0 = 9, kPfSWarp = 13;
 constexpr int kPfPageCache = 1024;  // page ids held in shared memory (16384 keys)
-constexpr int kPfKStages = 3;
-constexpr int kPfSBufs = 4;         // S / P buffers in tensor memory
-constexpr int kPfVStages = kPfSBufs;  // V stage i % 4 is freed by the same commit as buffer i % 4
+constexpr int kPfPair = 2 * kTile;  // keys per S computation
+constexpr int kPfKStages = 2;       // K stages, a pair of tiles each
+constexpr int kPfVStages = 4;       // V stages, one tile each
+constexpr int kPfPready = 4;        // P-ready barriers (tiles in flight)
 
 template <int D>
 struct PfGeom {
   static constexpr int kHalves = D / 64;
-  static constexpr int kQBytes = kHalves * kPfRows * 128;    // [half][row][128 B]
-  static constexpr int kTBytes = kHalves * kTile * 128;       // one K or V tile: [half][key][128 B]
-  static constexpr int kKOff = kQBytes;
-  static constexpr int kVOff = kKOff + kPfKStages * kTBytes;
+  static constexpr int kKBytes = kHalves * kPfPair * 128;  // K pair: [half][128 keys][128 B]
+  static constexpr int kVBytes = kHalves * kTile * 128;    // V tile: [half][64 keys][128 B]
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + kPfKStages * kKBytes;
   // merged o, fp32 [D / 4][128 rows][4]: a row's four consecutive columns
   // are one 16-byte vector, and a warp's 32 rows a contiguous 512 bytes
-  static constexpr int kMOff = kVOff + kPfVStages * kTBytes;
-  static constexpr int kXOff = kMOff + D * kPfRows * 4;       // split m, l: [parity][2][128]
+  static constexpr int kMOff = kVOff + kPfVStages * kVBytes;
+  static constexpr int kXOff = kMOff + D * kPfRows * 4;  // split m, l: [parity][2][128]
   static constexpr int kPidOff = kXOff + 4 * kPfRows * 4;
   static constexpr int kBarOff = kPidOff + kPfPageCache * 4;
-  // kfull, kfree [KS]; vfull [VS]; sfull, pready, pfree [SB]; odone, sdone,
-  // folded [2]
-  static constexpr int kNumBars = 2 * kPfKStages + kPfVStages + 3 * kPfSBufs + 6;
+  // kfull, kfree [KS]; vfull, vfree [VS]; sfull, pfree [2]; pready [4];
+  // odone, ofree; sdone, folded [2]
+  static constexpr int kNumBars = 2 * kPfKStages + 2 * kPfVStages + 4 + kPfPready + 2 + 4;
   static constexpr int kSmem = 1024 + kBarOff + kNumBars * 8;
   static constexpr uint32_t kTmemCols = 512;
-  // four S / P buffers of 64 columns, two split accumulators of D columns
-  static constexpr uint32_t kColS = 0, kColO = kPfSBufs * kTile;
+  // two S / P pair buffers of 128 columns, the accumulator (D columns), Q
+  // (bf16 pairs, D / 2 columns)
+  static constexpr uint32_t kColS = 0, kColO = 2 * kPfPair, kColQ = kColO + 128;
 };
+static_assert(PfGeom<128>::kSmem <= 232448, "prefill shared memory");
 
 // mbarrier wait for the roles with slack (the fold and TMA warps): the thread
 // suspends in the wait (a hint of 20 us, then it tries again), leaving the
@@ -1169,31 +1178,34 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const KernelParams p) {
   using Gm = PfGeom<D>;
-  constexpr uint32_t kIdescS = umma_idesc_bf16(kPfRows, kTile, false, false);
+  constexpr uint32_t kIdescS = umma_idesc_bf16(kPfRows, kPfPair, false, false);
   constexpr uint32_t kIdescPV = umma_idesc_bf16(kPfRows, D, false, true);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* qs = smem;
   uint8_t* kst = smem + Gm::kKOff;
   uint8_t* vst = smem + Gm::kVOff;
   float* xsplit = reinterpret_cast<float*>(smem + Gm::kXOff);  // [parity][m, l][128]
   float4* omg = reinterpret_cast<float4*>(smem + Gm::kMOff);   // merged o [D/4][128]
   int* pid_s = reinterpret_cast<int*>(smem + Gm::kPidOff);      // page ids of this sequence
-  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + Gm::kBarOff);  // K tile landed
-  uint64_t* kfree = kfull + kPfKStages;    // the S that read the K stage is done
-  uint64_t* vfull = kfree + kPfKStages;    // V tile landed
-  uint64_t* sfull = vfull + kPfVStages;    // S of the tile computed
-  uint64_t* pready = sfull + kPfSBufs;     // P of the tile written over it
-  uint64_t* pfree = pready + kPfSBufs;     // PV of the tile done (buffer and V stage free)
-  uint64_t* odone = pfree + kPfSBufs;      // the last PV of a split done
-  uint64_t* sdone = odone + 2;             // a split's m, l written
-  uint64_t* folded = sdone + 2;            // a split folded (its accumulator free)
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + Gm::kBarOff);  // K pair landed
+  uint64_t* kfree = kfull + kPfKStages;  // the S that read the K stage is done
+  uint64_t* vfull = kfree + kPfKStages;  // V tile landed
+  uint64_t* vfree = vfull + kPfVStages;  // the PV that read the V stage is done
+  uint64_t* sfull = vfree + kPfVStages;  // S of the pair computed [2]
+  uint64_t* pfree = sfull + 2;           // both PVs of the pair done: its buffer is free [2]
+  uint64_t* pready = pfree + 2;          // P of the tile written over its scores [4]
+  uint64_t* odone = pready + kPfPready;  // the last PV of a split done
+  uint64_t* ofree = odone + 1;           // the fold has read the accumulator
+  uint64_t* sdone = ofree + 1;           // a split's m, l written [2]
+  uint64_t* folded = sdone + 2;          // a split folded, its m, l slot free [2]
   __shared__ uint32_t tmem_slot;
   __shared__ int s_abort;
 
-  const int qb = gridDim.x - 1 - blockIdx.x;  // the longest query blocks start first
-  const int h = blockIdx.y, b = blockIdx.z;
+  // blocks in launch order: the longest query blocks of every kv head first
+  const int nqb = static_cast<int>(gridDim.x) / p.Hkv;
+  const int qb = nqb - 1 - static_cast<int>(blockIdx.x) / p.Hkv;
+  const int h = static_cast<int>(blockIdx.x) % p.Hkv, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.G, TPB = kPfRows / G;
   const int q_begin = p.cu_q[b];
@@ -1210,14 +1222,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   const int p_last = start + tok0 + ntok - 1;  // last position in this block
   const int32_t* bt_row = p.block_table + (int64_t)b * p.max_blocks;
   const int ntiles = (p_last + kTile) / kTile;  // tiles 0 .. covering key p_last
+  const int npairs = (ntiles + 1) / 2;
+  const int key_hi = min(kvl, ntiles * kTile);  // keys the copies read: 0 .. key_hi - 1
   const int S = p.split_size;
   const int tps = S / kTile;                    // tiles per split
   const int nsplits = (ntiles + tps - 1) / tps;
   {
-    // check every page a tile copy may read, and keep the first ids at hand
-    const int loaded_hi = min(kvl, ntiles * kTile);
+    // check every page a copy may read, and keep the first ids at hand
     bool ok = true;
-    for (int pg = tid; pg * kPage < loaded_hi; pg += kPfThreads) {
+    for (int pg = tid; pg * kPage < key_hi; pg += kPfThreads) {
       const int v = bt_row[pg];
       if (v < 0 || v >= p.num_pages) ok = false;
       if (pg < kPfPageCache) pid_s[pg] = v;
@@ -1233,140 +1246,168 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
     for (int i = 0; i < kPfKStages; ++i) {
-      mbar_init(&kfull[i], Gm::kHalves);
+      mbar_init(&kfull[i], Gm::kHalves);  // one arrival per copying warp
       mbar_init(&kfree[i], 1);
     }
     for (int i = 0; i < kPfVStages; ++i) {
       mbar_init(&vfull[i], Gm::kHalves);
-    }
-    for (int i = 0; i < kPfSBufs; ++i) {
-      mbar_init(&sfull[i], 1);
-      mbar_init(&pready[i], 4);  // the four softmax warps
-      mbar_init(&pfree[i], 1);
+      mbar_init(&vfree[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&odone[i], 1);
-      mbar_init(&sdone[i], 4);
+      mbar_init(&sfull[i], 1);
+      mbar_init(&pfree[i], 1);
+      mbar_init(&sdone[i], 4);   // the four softmax warps
       mbar_init(&folded[i], 4);  // the four fold warps
     }
+    for (int i = 0; i < kPfPready; ++i) mbar_init(&pready[i], 4);
+    mbar_init(odone, 1);
+    mbar_init(ofree, 4);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&tmem_slot, Gm::kTmemCols);
-  // Q rows, swizzled K-major [half][row][128 B]; padding rows are zero
-  for (int i = tid; i < kPfRows * (D / 8); i += kPfThreads) {
-    const int r = i / (D / 8), c = i % (D / 8);
-    const int tk = r / G;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < TPB * G && tk < ntok)
-      v = *reinterpret_cast<const uint4*>(
-          p.q + ((int64_t)(q_begin + tok0 + tk) * p.Hq + h * G + r % G) * D + c * 8);
-    *reinterpret_cast<uint4*>(qs + (c >> 3) * (kPfRows * 128) + sw128_off(r, c & 7)) = v;
-  }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  if (warp < 4) {
+    // Q row r into tensor memory lane r, the A operand of the S MMA: column
+    // c holds elements 2c, 2c + 1; padding rows are zero
+    const int r = warp * 32 + lane;
+    const int tk = r / G;
+    const bool valid = r < TPB * G && tk < ntok;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        p.q + ((int64_t)(q_begin + tok0 + (valid ? tk : 0)) * p.Hq + h * G + r % G) * D);
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+      uint32_t v[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint4 w = valid ? src[8 * c + u] : make_uint4(0, 0, 0, 0);
+        v[4 * u] = w.x;
+        v[4 * u + 1] = w.y;
+        v[4 * u + 2] = w.z;
+        v[4 * u + 3] = w.w;
+      }
+      tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + Gm::kColQ + 32 * c, v);
+    }
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
-  if (warp >= kPfTmaWarp0) {
+  if (warp >= kPfTmaWarp0 && warp < kPfSWarp) {
     // ================================================================ copies
     // Warps 9, 10: column halves 0, 1 of K; warps 11, 12: those of V (one
-    // lane each; with D = 64 only warps 9 and 11 copy).  Tile i: K into stage
-    // i % KS once the S of tile i - KS is done (kfree), V into stage i % VS
-    // once the PV of tile i - VS is (pfree).  Each copying warp arrives on
-    // the stage's full barrier with the bytes of its half.
+    // lane each; with D = 64 only warps 9 and 11 copy).  K goes by pairs of
+    // tiles: pair q into stage q % KS once the S of pair q - KS is done
+    // (kfree); V by tiles: tile i into stage i % VS once the PV of tile
+    // i - VS is (vfree).  Each copying warp arrives on the stage's full
+    // barrier with the bytes of its half.
     const int role = warp - kPfTmaWarp0;
     const bool is_v = role >= 2;
     const int hf = role & 1;
     if (lane == 0 && hf < Gm::kHalves) {
       const CUtensorMap* map = is_v ? &vmap : &kmap;
-      auto issue_tile = [&](int i) {
-        uint8_t* dst = (is_v ? vst + (i % kPfVStages) * Gm::kTBytes
-                             : kst + (i % kPfKStages) * Gm::kTBytes) + hf * (kTile * 128);
-        uint64_t* bar = is_v ? &vfull[i % kPfVStages] : &kfull[i % kPfKStages];
-        const int key0 = i * kTile;
-        const int np = pages_below(key0, kvl);
+      // the pages of keys k0 .. k0 + nkeys - 1 below key_hi, 2 KB apart
+      auto issue = [&](uint8_t* dst, uint64_t* bar, int k0, int nkeys) {
+        const int np = max(0, min(nkeys / kPage, (key_hi - k0 + kPage - 1) / kPage));
         mbar_arrive_expect_tx(bar, np * 2048);
         for (int pp = 0; pp < np; ++pp) {
-          const int pg = (key0 >> 4) + pp;
+          const int pg = (k0 >> 4) + pp;
           const int y = ((pg < kPfPageCache ? pid_s[pg] : bt_row[pg]) * p.Hkv + h) * kPage;
           tma_load_2d(dst + pp * 2048, map, hf * 64, y, bar);
         }
       };
       bool ok = true;
       int n = 0;
-      for (int i = 0; i < ntiles && ok; ++i) {
-        if (!is_v && i >= kPfKStages)
-          ok = pf_wait_lazy(&kfree[i % kPfKStages], ((i / kPfKStages) - 1) & 1, p.err, &s_abort);
-        if (is_v && i >= kPfVStages)
-          ok = pf_wait_lazy(&pfree[i % kPfVStages], ((i / kPfVStages) - 1) & 1, p.err, &s_abort);
-        if (!ok) break;
-        issue_tile(i);
-        ++n;
-      }
-      // every copy lands before the block exits (bounded waits)
-      const int stages = is_v ? kPfVStages : kPfKStages;
-      for (int k = max(0, n - stages); k < n; ++k) {
-        uint64_t* fb = is_v ? &vfull[k % kPfVStages] : &kfull[k % kPfKStages];
-        pf_wait_lazy(fb, (k / stages) & 1, ok ? p.err : nullptr, ok ? &s_abort : nullptr);
+      if (!is_v) {
+        for (int q = 0; q < npairs && ok; ++q) {
+          if (q >= kPfKStages)
+            ok = pf_wait_lazy(&kfree[q % kPfKStages], ((q / kPfKStages) - 1) & 1, p.err,
+                              &s_abort);
+          if (!ok) break;
+          issue(kst + (q % kPfKStages) * Gm::kKBytes + hf * (kPfPair * 128),
+                &kfull[q % kPfKStages], q * kPfPair, kPfPair);
+          ++n;
+        }
+        // every copy lands before the block exits (bounded waits)
+        for (int k = max(0, n - kPfKStages); k < n; ++k)
+          pf_wait_lazy(&kfull[k % kPfKStages], (k / kPfKStages) & 1, ok ? p.err : nullptr,
+                       ok ? &s_abort : nullptr);
+      } else {
+        for (int i = 0; i < ntiles && ok; ++i) {
+          if (i >= kPfVStages)
+            ok = pf_wait_lazy(&vfree[i % kPfVStages], ((i / kPfVStages) - 1) & 1, p.err,
+                              &s_abort);
+          if (!ok) break;
+          issue(vst + (i % kPfVStages) * Gm::kVBytes + hf * (kTile * 128),
+                &vfull[i % kPfVStages], i * kTile, kTile);
+          ++n;
+        }
+        for (int k = max(0, n - kPfVStages); k < n; ++k)
+          pf_wait_lazy(&vfull[k % kPfVStages], (k / kPfVStages) & 1, ok ? p.err : nullptr,
+                       ok ? &s_abort : nullptr);
       }
     }
     __syncwarp();
-  } else if (warp == kPfMmaWarp) {
+  } else if (warp == kPfMmaWarp || warp == kPfSWarp) {
     // ================================================================ MMA
-    // One thread issues everything: no warp collective sits between two MMA
-    // batches, so the tensor core's short issue queue is refilled as soon as
-    // a batch's inputs are ready.
+    // Warp 13 issues the S of every pair as soon as its K has landed and its
+    // buffer is free; warp 8 the PVs.  One lane each, no warp collective
+    // between two MMA batches.  The two lanes' MMAs meet only through the
+    // barriers: sfull (S done) before the softmax, pready (P written) before
+    // the PV, pfree (both PVs of a pair done) before the next S into that
+    // buffer.
     if (lane == 0) {
-      const uint64_t qd = umma_desc_sw128(smem_u32(qs), 16, 1024);
       const uint64_t kd = umma_desc_sw128(smem_u32(kst), 16, 1024);
       const uint64_t vd = umma_desc_sw128(smem_u32(vst), kTile * 128, 1024);
       uint64_t* last_bar = nullptr;  // the latest MMA commit
       uint32_t last_par = 0;
-      // S of tile i once its K landed and the PV of tile i - 4 (the last
-      // reader of its buffer) is done
-      auto issue_s = [&](int i) -> bool {
-        const int ks_ = i % kPfKStages, sb = i % kPfSBufs;
-        if (!mbar_wait3(&kfull[ks_], (i / kPfKStages) & 1, i >= kPfSBufs ? &pfree[sb] : nullptr,
-                        ((i / kPfSBufs) - 1) & 1, nullptr, 0, p.err, &s_abort))
+      // S of pair q once its K landed and both PVs of pair q - 2 (the last
+      // readers of its buffer) are done
+      auto issue_s = [&](int q) -> bool {
+        const int ks_ = q % kPfKStages, sb = q & 1;
+        if (!mbar_wait3(&kfull[ks_], (q / kPfKStages) & 1, q >= 2 ? &pfree[sb] : nullptr,
+                        ((q >> 1) - 1) & 1, nullptr, 0, p.err, &s_abort))
           return false;
         tc_fence_after();
-        const uint64_t kb = kd + static_cast<uint64_t>(ks_ * (Gm::kTBytes >> 4));
+        const uint64_t kb = kd + static_cast<uint64_t>(ks_ * (Gm::kKBytes >> 4));
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          tc_mma(tmem + Gm::kColS + kTile * sb,
-                 qd + static_cast<uint64_t>((ks >> 2) * (kPfRows * 8) + (ks & 3) * 2),
-                 kb + static_cast<uint64_t>((ks >> 2) * (kTile * 8) + (ks & 3) * 2), kIdescS,
-                 ks > 0 ? 1u : 0u);
+          tc_mma_ts(tmem + Gm::kColS + kPfPair * sb, tmem + Gm::kColQ + 8 * ks,
+                    kb + static_cast<uint64_t>((ks >> 2) * (kPfPair * 8) + (ks & 3) * 2),
+                    kIdescS, ks > 0 ? 1u : 0u);
         tc_commit(&sfull[sb]);
         tc_commit(&kfree[ks_]);
         last_bar = &sfull[sb];
-        last_par = (i / kPfSBufs) & 1;
+        last_par = (q >> 1) & 1;
         return true;
       };
-      bool ok = issue_s(0);
+      if (warp == kPfSWarp) {  // every pair's S, in order
+        bool sok = true;
+        for (int q = 0; q < npairs && sok; ++q) sok = issue_s(q);
+        if (!sok && last_bar) mbar_wait(last_bar, last_par, nullptr);  // MMAs in flight
+      }
+      bool ok = warp == kPfMmaWarp;  // warp 8: every tile's PV, in order
       // split of tile i and the tile's place in it, kept by counters: a
       // division by the runtime tiles-per-split costs the single issuing
       // thread a few hundred cycles per tile
       int j = 0, t_in = 0;
       for (int i = 0; i < ntiles && ok; ++i, (++t_in == tps ? (t_in = 0, ++j) : 0)) {
-        const int sb = i % kPfSBufs;
+        const int q = i >> 1, u = i & 1;
         const int stg = i % kPfVStages;
-        uint8_t* vt = vst + stg * Gm::kTBytes;
+        uint8_t* vt = vst + stg * Gm::kVBytes;
         const int key0 = i * kTile;
         const bool split_first = t_in == 0;
         const bool split_last = t_in == tps - 1 || i + 1 == ntiles;
-        // the next tile's S goes to the tensor core ahead of this tile's PV,
-        // so that its softmax can start as soon as this one's ends
-        if (i + 1 < ntiles && !issue_s(i + 1)) {
-          ok = false;
-          break;
-        }
-        // V landed, P written, and (at a split's first tile) the fold of the
-        // split that last used this accumulator, two splits ago, done
-        ok = mbar_wait3(&vfull[stg], (i / kPfVStages) & 1, &pready[sb], (i / kPfSBufs) & 1,
-                        split_first && j >= 2 ? &folded[j & 1] : nullptr, ((j - 2) >> 1) & 1,
-                        p.err, &s_abort);
+        // the next pair's S goes to the tensor core as this pair's first
+        // tile comes up, so that it is ready when this pair's softmax ends
+        // V landed, P written, and (at a split's first tile) the fold has
+        // read the previous split's accumulator
+        ok = mbar_wait3(&vfull[stg], (i / kPfVStages) & 1, &pready[i % kPfPready],
+                        (i / kPfPready) & 1, split_first && j >= 1 ? ofree : nullptr,
+                        (j - 1) & 1, p.err, &s_abort);
         if (!ok) break;
         if (key0 + kTile > kvl) {  // keys past the end: zero their V rows before PV
           const int first = kvl - key0;
@@ -1380,21 +1421,23 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
         }
         tc_fence_after();
         // ---- O += P V, per 16-key chunk the hi part then the lo part
-        const uint64_t vb = vd + static_cast<uint64_t>(stg * (Gm::kTBytes >> 4));
-        const uint32_t pa = tmem + Gm::kColS + kTile * sb;  // P hi: columns 0-31, lo: 32-63
-        const uint32_t od = tmem + Gm::kColO + D * (j & 1);
+        const uint64_t vb = vd + static_cast<uint64_t>(stg * (Gm::kVBytes >> 4));
+        // P of tile i: hi in columns 0-31 of its 64, lo in 32-63
+        const uint32_t pa = tmem + Gm::kColS + kPfPair * (q & 1) + kTile * u;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint64_t bd = vb + static_cast<uint64_t>(kk * 128);
-          tc_mma_ts(od, pa + 8 * kk, bd, kIdescPV, (split_first && kk == 0) ? 0u : 1u);
-          tc_mma_ts(od, pa + 32 + 8 * kk, bd, kIdescPV, 1u);
+          tc_mma_ts(tmem + Gm::kColO, pa + 8 * kk, bd, kIdescPV,
+                    (split_first && kk == 0) ? 0u : 1u);
+          tc_mma_ts(tmem + Gm::kColO, pa + 32 + 8 * kk, bd, kIdescPV, 1u);
         }
-        tc_commit(&pfree[sb]);  // buffer sb and V stage stg (the same index) are free
-        if (split_last) tc_commit(&odone[j & 1]);
-        last_bar = &pfree[sb];
-        last_par = (i / kPfSBufs) & 1;
+        tc_commit(&vfree[stg]);
+        if (u == 1 || i + 1 == ntiles) tc_commit(&pfree[q & 1]);
+        if (split_last) tc_commit(odone);
+        last_bar = &vfree[stg];
+        last_par = (i / kPfVStages) & 1;
       }
-      if (!ok && last_bar) mbar_wait(last_bar, last_par, nullptr);  // MMAs in flight
+      if (warp == kPfMmaWarp && !ok && last_bar) mbar_wait(last_bar, last_par, nullptr);
     }
     __syncwarp();
   } else if (warp < kPfFoldWarp0) {
@@ -1405,15 +1448,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     float m = -CUDART_INF_F, l = 0.0f;  // the split's reference maximum and sum
     bool live = true;                   // no wait has run out
-    int j = 0, t_in = 0;  // split of tile i and the tile's place in it (counters)
+    int j = 0, t_in = 0;                // split of tile i and the tile's place in it
     for (int i = 0; i < ntiles && live; ++i, (++t_in == tps ? (t_in = 0, ++j) : 0)) {
-      const int sb = i % kPfSBufs;
+      const int q = i >> 1, u = i & 1;
       const int key0 = i * kTile;
       const bool split_first = t_in == 0;
       const bool split_last = t_in == tps - 1 || i + 1 == ntiles;
-      const uint32_t sa = tl + Gm::kColS + kTile * sb;
+      const uint32_t sa = tl + Gm::kColS + kPfPair * (q & 1) + kTile * u;
       // ---- scores of the tile: all 64 in registers
-      live = __all_sync(kFull, mbar_wait(&sfull[sb], (i / kPfSBufs) & 1, p.err, &s_abort));
+      live = __all_sync(kFull, mbar_wait(&sfull[q & 1], (q >> 1) & 1, p.err, &s_abort));
       if (!live) break;
       tc_fence_after();
       float x[64];
@@ -1500,11 +1543,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       // before this one's (the tensor core accumulates in issue order)
       if (!split_first && __any_sync(kFull, alpha != 1.0f)) {
         const int ip = i - 1;
-        live = __all_sync(kFull, mbar_wait(&pfree[ip % kPfSBufs], (ip / kPfSBufs) & 1, p.err,
-                                         &s_abort));
+        live = __all_sync(kFull, mbar_wait(&vfree[ip % kPfVStages], (ip / kPfVStages) & 1,
+                                         p.err, &s_abort));
         if (!live) break;
         tc_fence_after();
-        const uint32_t oc = tl + Gm::kColO + D * (j & 1);
+        const uint32_t oc = tl + Gm::kColO;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t v0[32];
@@ -1518,7 +1561,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&pready[sb]);
+      if (lane == 0) mbar_arrive(&pready[i % kPfPready]);
       if (split_last) {
         // hand the split's m, l to the fold warps (their slot was read when
         // the fold of split j - 2 finished)
@@ -1535,7 +1578,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   } else {
     // ================================================================ fold
     // Split j's accumulator (m_s, l_s, o_s) into the merged state, in split
-    // order: the decode merge's left fold, one row per thread.
+    // order: the decode merge's left fold, one row per thread.  The
+    // accumulator is released (ofree) as soon as its last columns are read.
     const int r = (warp - kPfFoldWarp0) * 32 + lane;
     const int tk = r / G;
     const int pos = (r < TPB * G && tk < ntok) ? start + tok0 + tk : -1;
@@ -1545,7 +1589,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     bool live = true;
     for (int j = 0; j < nsplits && live; ++j) {
       live = __all_sync(kFull, pf_wait_lazy(&sdone[j & 1], (j >> 1) & 1, p.err, &s_abort) &&
-                                   pf_wait_lazy(&odone[j & 1], (j >> 1) & 1, p.err, &s_abort));
+                                   pf_wait_lazy(odone, j & 1, p.err, &s_abort));
       if (!live) break;
       tc_fence_after();
       const float m_s = xsplit[(j & 1) * 2 * kPfRows + r];
@@ -1553,27 +1597,30 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       const bool part = pos >= j * S;  // the split holds keys this row sees
       float mn = 0.0f, ca = 0.0f, cb = 0.0f;
       if (part && have) lse_coeffs(mg_m, m_s, mn, ca, cb);
-      if (__any_sync(kFull, part)) {
-        const uint32_t os = tl + Gm::kColO + D * (j & 1);
+      const bool any = __any_sync(kFull, part);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t vo[32];
-          tmem_ld32(os + 32 * c, vo);
-          if (part) {
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t vo[32];
+        if (any) tmem_ld32(Gm::kColO + tl + 32 * c, vo);
+        if (c == D / 32 - 1) {  // the accumulator is read: the next split may start
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ofree);
+        }
+        if (part) {
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              float4* slot = omg + (8 * c + v) * kPfRows + r;
-              const float4 add = make_float4(__uint_as_float(vo[4 * v]),
-                                             __uint_as_float(vo[4 * v + 1]),
-                                             __uint_as_float(vo[4 * v + 2]),
-                                             __uint_as_float(vo[4 * v + 3]));
-              if (have) {
-                const float4 m4 = *slot;
-                *slot = make_float4(lse_mix(m4.x, ca, add.x, cb), lse_mix(m4.y, ca, add.y, cb),
-                                    lse_mix(m4.z, ca, add.z, cb), lse_mix(m4.w, ca, add.w, cb));
-              } else {
-                *slot = add;
-              }
+          for (int v = 0; v < 8; ++v) {
+            float4* slot = omg + (8 * c + v) * kPfRows + r;
+            const float4 add = make_float4(__uint_as_float(vo[4 * v]),
+                                           __uint_as_float(vo[4 * v + 1]),
+                                           __uint_as_float(vo[4 * v + 2]),
+                                           __uint_as_float(vo[4 * v + 3]));
+            if (have) {
+              const float4 m4 = *slot;
+              *slot = make_float4(lse_mix(m4.x, ca, add.x, cb), lse_mix(m4.y, ca, add.y, cb),
+                                  lse_mix(m4.z, ca, add.z, cb), lse_mix(m4.w, ca, add.w, cb));
+            } else {
+              *slot = add;
             }
           }
         }
@@ -1588,7 +1635,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
           have = true;
         }
       }
-      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&folded[j & 1]);
     }
@@ -1783,7 +1829,7 @@ bi_status prefill_impl(const AttnArgs& a, cudaStream_t s) {
   const int nqb = (a.max_q_len + TPB - 1) / TPB;
   const size_t sm = PfGeom<D>::kSmem;
   if (set_smem(attn_prefill_kernel<D>, sm) != cudaSuccess) return BI_ERR_CUDA;
-  attn_prefill_kernel<D><<<dim3(nqb, a.Hkv, a.B), kPfThreads, sm, s>>>(km, vm, p);
+  attn_prefill_kernel<D><<<dim3(nqb * a.Hkv, 1, a.B), kPfThreads, sm, s>>>(km, vm, p);
   return cuda_status(cudaGetLastError());
 }
 
