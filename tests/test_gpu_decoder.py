@@ -299,3 +299,30 @@ def test_llama3_8b_shaped_64_requests_identical_under_every_batch_mix(cuda):
     assert any(0 < r.prefill_tokens < 1024 and r.decode_tokens > 0 for r in rec_arr)
     toks = np.concatenate([np.asarray(t) for t in runs["burst, 64 slots"].values()])
     assert len(np.unique(toks)) > 64                 # not a degenerate constant output
+
+
+def test_llama3_8b_shaped_256_requests_at_full_scale(cuda, capsys):
+    """The serving workload at its stated scale: a random-init 32-layer
+    Llama-3-8B-shaped decoder serves 256 requests (prompts uniform in
+    16..4096 tokens, 256 greedy tokens each) in one burst with all 256 slots,
+    as a Poisson stream into 128 slots with prefill chunks of 512, and two of
+    them alone (eager, then decode steps from CUDA graphs); every request's
+    tokens must be identical across the mixes.  The serving replay module is
+    called as a user runs it; it exits non-zero when an invariant run
+    differs."""
+    import json
+    from invariant_bi_rmsnorm_02_gb300 import replay
+    rc = replay.main(["--requests", "256", "--prompt-lo", "16", "--prompt-hi", "4096",
+                      "--new-tokens", "256", "--alone", "2"])
+    lines = [json.loads(t) for t in capsys.readouterr().out.splitlines() if t.startswith("{")]
+    assert rc == 0
+    assert lines[-1]["summary"] == "identical under every batch mix"
+    mixes = [t for t in lines if "mix" in t]
+    assert len(mixes) == 4
+    burst = mixes[0]
+    assert burst["generated_tokens"] == 256 * 256
+    assert burst["max_sequences_in_a_step"] >= 200      # large batches, not one at a time
+    assert burst["distinct_step_shapes"] > 16          # batches of many shapes
+    for t in mixes[1:]:
+        assert t["requests_differing"] == 0
+    assert mixes[3]["graph_replays"] > 2 * (256 - 2) // 2
