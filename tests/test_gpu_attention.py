@@ -359,6 +359,35 @@ def test_bad_page_id_is_reported_not_faulted(cuda):
     assert bi.bi_check_device_errors() == bi.ERR_DEVICE_BOUNDS
 
 
+def test_prefill_bad_page_id_is_reported_not_faulted(cuda):
+    # two prompts in one call; a page of the second lies outside the pool:
+    # the blocks that would read it refuse before any copy and report it,
+    # the first prompt's rows are the bytes of a clean call
+    qlens = [100, 70]
+    kv = to_dev(synth.paged_kv(qlens, 2, 64, 16, 5600), cuda)
+    q = synth.normal_bf16((sum(qlens), 8, 64), 5601, device=cuda)
+    cu = torch.tensor([0, qlens[0], sum(qlens)], dtype=torch.int32, device=cuda)
+    st = torch.zeros(2, dtype=torch.int32, device=cuda)
+    good, _ = prefill(q, cu, st, kv, kv.kv_lens, 100, 100, 64)
+    assert bi.bi_check_device_errors() == bi.OK
+    bt = kv.block_table.clone()
+    bt[1, 2] = kv.k_cache.shape[0] + 7          # keys 32..47 of the second prompt
+    bad = bi.attn_prefill_chunk(q, cu, st, kv.k_cache, kv.v_cache, bt, kv.kv_lens,
+                                max_q_len=100, max_kv_len=100, split_size=64)
+    assert bi.bi_check_device_errors() == bi.ERR_DEVICE_BOUNDS
+    assert bi.bi_check_device_errors() == bi.OK            # cleared by the read
+    assert same_bytes(bad[:qlens[0]], good[:qlens[0]])
+    # a chunk that ends past its sequence's KV length
+    lens = kv.kv_lens.clone()
+    lens[0] = 60
+    bi.attn_prefill_chunk(q, cu, st, kv.k_cache, kv.v_cache, kv.block_table, lens,
+                          max_q_len=100, max_kv_len=100, split_size=64)
+    assert bi.bi_check_device_errors() == bi.ERR_DEVICE_BOUNDS
+    again, _ = prefill(q, cu, st, kv, kv.kv_lens, 100, 100, 64)   # the context still works
+    assert bi.bi_check_device_errors() == bi.OK
+    assert same_bytes(again, good)
+
+
 def test_kv_write_places_rows_in_pages(cuda):
     kv = to_dev(synth.paged_kv([40, 3], 2, 64, 16, 5500, reserve_tokens=20), cuda)
     kc, vc = kv.k_cache.clone(), kv.v_cache.clone()
