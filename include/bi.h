@@ -278,7 +278,10 @@ bi_status bi_attn_decode_noalloc(const void* q, const void* k_cache, const void*
  * bi_attn_decode in BI_MODE_INVARIANT with L = position + 1 and the same
  * split_size.  BI_MODE_VARIANT sizes the chunks from max_kv_len and c
  * (split size = 64 * ceil(max_kv_len / (64 c))), so results move with the
- * chunking.  Needs no workspace (pass NULL, 0). */
+ * chunking.  Needs no workspace (pass NULL, 0).
+ * Errors: as bi_attn_decode; a block whose sequence has a page id outside
+ *   the pool (among the pages its keys use) or a chunk past kv_lens records
+ *   BI_ERR_DEVICE_BOUNDS before any copy and leaves its rows unwritten. */
 bi_status bi_attn_prefill_chunk(const void* q, const int32_t* cu_q,
                                 const int32_t* q_start_pos, const void* k_cache,
                                 const void* v_cache, const int32_t* block_table,
