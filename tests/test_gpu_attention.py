@@ -230,6 +230,30 @@ def test_prefill_equals_decode_small(cuda):
     assert same_bytes(pre, dec)
 
 
+def test_prefill_equals_decode_pairs_across_splits(cuda):
+    # S over pairs of key tiles with three tiles per split (split size 192:
+    # every other pair straddles a split boundary), an odd tile count (300
+    # keys: the last pair holds one tile) and a second chunk that starts
+    # inside a tile: every position still equals a decode with L = p + 1
+    L, Hq, Hkv, D, S = 300, 8, 2, 128, 192
+    kv = to_dev(synth.paged_kv([L], Hkv, D, 16, 4850), cuda)
+    q = synth.normal_bf16((L, Hq, D), 4851, device=cuda)
+    pre = torch.empty_like(q)
+    pre32 = torch.empty(q.shape, dtype=torch.float32, device=cuda)
+    for s0, n in ((0, 137), (137, L - 137)):
+        cu = torch.tensor([0, n], dtype=torch.int32, device=cuda)
+        st = torch.tensor([s0], dtype=torch.int32, device=cuda)
+        kl = torch.tensor([s0 + n], dtype=torch.int32, device=cuda)
+        o, o32 = prefill(q[s0:s0 + n].contiguous(), cu, st, kv, kl, n, s0 + n, S)
+        pre[s0:s0 + n], pre32[s0:s0 + n] = o, o32
+    assert bi.bi_check_device_errors() == bi.OK
+    bt = kv.block_table.expand(L, -1).contiguous()
+    lens = torch.arange(1, L + 1, dtype=torch.int32, device=cuda)
+    dec, dec32 = decode(q, kv, L, S, kv_lens=lens, bt=bt)
+    assert same_bytes(pre32, dec32), first_divergence(pre32, dec32)
+    assert same_bytes(pre, dec)
+
+
 def test_prefill_chunked_equivalence_full_prompt(cuda):
     # one 8192-token prompt, 32/8 heads, D=128, split 256: chunks of 512,
     # 2048 and 8192, and token-by-token decode, give the same bytes at every
