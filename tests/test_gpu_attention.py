@@ -196,8 +196,10 @@ def prefill(q, cu, starts, kv, kv_lens, max_q, max_kv, S, mode=bi.INVARIANT, spl
 
 
 @pytest.mark.parametrize("D,Hq,Hkv,S", [(64, 8, 2, 64), (128, 8, 2, 256), (128, 32, 8, 128),
-                                        (64, 6, 6, 64)])
+                                        (64, 6, 6, 64), (128, 6, 2, 256)])
 def test_prefill_matches_oracle(cuda, D, Hq, Hkv, S):
+    # (the last case: 3 q heads per kv head, so a block holds 42 tokens and
+    # two padding rows)
     # two sequences: a first chunk from position 0 and a later chunk
     starts, qlens = [0, 700], [300, 77]
     kvl = [s + n for s, n in zip(starts, qlens)]
