@@ -183,6 +183,31 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- workload
+# Input seeds of every workload, as offsets (the step's are added to
+# 100000 * rank).  synth.paged_kv(seed) draws K from seed + 1 and V from
+# seed + 2, so no other input of a workload may use those: queries equal to
+# cached keys would be a degenerate input (their own key scores ~11 sigma
+# above the rest).  "kv" entries name paged caches, the others plain tensors.
+SEEDS = {
+    "step": dict(x=1, w=2, wqkv=3, wup=4, lens=5, kv=6, q=13, k_new=14, v_new=9, pkv=10,
+                 pq=15),
+    "tiny": dict(x=1001, w=1002, W=1003, lens=1004, kv=1005, q=1016),
+    "schedules": dict(kv=4001, q=4012),
+}
+KV_SEEDS = {"step": ("kv", "pkv"), "tiny": ("kv",), "schedules": ("kv",)}
+
+
+def seed_collisions():
+    """Pairs (workload, input) whose seed is the K or V stream of one of the
+    workload's paged caches; empty when the inputs are independent."""
+    bad = []
+    for wl, seeds in SEEDS.items():
+        streams = {seeds[k] + o for k in KV_SEEDS[wl] for o in (1, 2)}
+        bad += [(wl, name) for name, v in seeds.items()
+                if name not in KV_SEEDS[wl] and v in streams]
+    return bad
+
+
 class Workload:
     """Device-resident inputs of one step, seeded."""
 
@@ -191,34 +216,33 @@ class Workload:
         from invariant_bi_rmsnorm_02_gb300 import synth
         self.bi, self.dev = bi, dev
         s = 100000 * rank
-        self.x = synth.normal_bf16((M, H), s + 1, device=dev)
-        self.w = synth.normal_bf16((H,), s + 2, std=0.1, mean=1.0, device=dev)
-        self.Wqkv = synth.normal_bf16((N_QKV, H), s + 3, std=0.02, device=dev)
-        self.Wup = synth.normal_bf16((N_UP, H), s + 4, std=0.02, device=dev)
+        sd = SEEDS["step"]
+        self.x = synth.normal_bf16((M, H), s + sd["x"], device=dev)
+        self.w = synth.normal_bf16((H,), s + sd["w"], std=0.1, mean=1.0, device=dev)
+        self.Wqkv = synth.normal_bf16((N_QKV, H), s + sd["wqkv"], std=0.02, device=dev)
+        self.Wup = synth.normal_bf16((N_UP, H), s + sd["wup"], std=0.02, device=dev)
         self.y = torch.empty_like(self.x)
         self.qkv = torch.empty(M, N_QKV, dtype=torch.bfloat16, device=dev)
         self.up = torch.empty(M, N_UP, dtype=torch.bfloat16, device=dev)
         d = DEC
-        lens = synth.loguniform_int(d["B"], 1, d["max_len"] - reserve, s + 5).tolist()
-        self.kv = synth.paged_kv(lens, d["Hkv"], d["D"], d["page"], s + 6,
+        lens = synth.loguniform_int(d["B"], 1, d["max_len"] - reserve, s + sd["lens"]).tolist()
+        self.kv = synth.paged_kv(lens, d["Hkv"], d["D"], d["page"], s + sd["kv"],
                                  reserve_tokens=reserve, device=dev)
         self.lens0 = self.kv.kv_lens.clone()
         self.lens = self.kv.kv_lens.clone()
         self.seq = torch.arange(d["B"], dtype=torch.int32, device=dev)
-        # seeds apart from the cache's: paged_kv(seed) draws K from seed + 1
-        # and V from seed + 2, and queries equal to cached keys would be a
-        # degenerate input (their own key scores ~11 sigma above the rest)
-        self.q = synth.normal_bf16((d["B"], d["Hq"], d["D"]), s + 13, device=dev)
-        self.k_new = synth.normal_bf16((d["B"], d["Hkv"], d["D"]), s + 14, device=dev)
-        self.v_new = synth.normal_bf16((d["B"], d["Hkv"], d["D"]), s + 9, device=dev)
+        self.q = synth.normal_bf16((d["B"], d["Hq"], d["D"]), s + sd["q"], device=dev)
+        self.k_new = synth.normal_bf16((d["B"], d["Hkv"], d["D"]), s + sd["k_new"], device=dev)
+        self.v_new = synth.normal_bf16((d["B"], d["Hkv"], d["D"]), s + sd["v_new"], device=dev)
         self.dec_out = torch.empty_like(self.q)
         self.dec_ws = {}
         for mode in (bi.INVARIANT, bi.VARIANT):
             nb = bi.bi_attn_decode_workspace_size(d["B"], d["Hq"], d["Hkv"], d["D"],
                                                   d["max_len"], d["S"], mode)
             self.dec_ws[mode] = torch.empty(nb // 4 + 4, dtype=torch.float32, device=dev)
-        self.pkv = synth.paged_kv([PRE["T"]], d["Hkv"], d["D"], d["page"], s + 10, device=dev)
-        self.pq = synth.normal_bf16((PRE["chunk"], d["Hq"], d["D"]), s + 15, device=dev)
+        self.pkv = synth.paged_kv([PRE["T"]], d["Hkv"], d["D"], d["page"], s + sd["pkv"],
+                                  device=dev)
+        self.pq = synth.normal_bf16((PRE["chunk"], d["Hq"], d["D"]), s + sd["pq"], device=dev)
         self.pout = torch.empty_like(self.pq)
         self.cu = torch.tensor([0, PRE["chunk"]], dtype=torch.int32, device=dev)
         self.pstart = torch.tensor([PRE["start"]], dtype=torch.int32, device=dev)
@@ -595,12 +619,13 @@ def tiny_layer(dev, stream, reps=20):
     import invariant_bi_rmsnorm_02_gb300 as bi
     from invariant_bi_rmsnorm_02_gb300 import synth
     c = synth.TINY
-    x = synth.normal_bf16((c["B"], c["H"]), 1001, device=dev)
-    w = synth.normal_bf16((c["H"],), 1002, std=0.1, mean=1.0, device=dev)
-    W = synth.normal_bf16((c["N"], c["H"]), 1003, std=0.02, device=dev)
-    lens = synth.uniform_int(c["B"], 1, c["max_len"], 1004).tolist()
-    kv = synth.paged_kv(lens, c["Hkv"], c["D"], c["page"], 1005, device=dev)
-    q = synth.normal_bf16((c["B"], c["Hq"], c["D"]), 1016, device=dev)  # apart from K, V
+    sd = SEEDS["tiny"]
+    x = synth.normal_bf16((c["B"], c["H"]), sd["x"], device=dev)
+    w = synth.normal_bf16((c["H"],), sd["w"], std=0.1, mean=1.0, device=dev)
+    W = synth.normal_bf16((c["N"], c["H"]), sd["W"], std=0.02, device=dev)
+    lens = synth.uniform_int(c["B"], 1, c["max_len"], sd["lens"]).tolist()
+    kv = synth.paged_kv(lens, c["Hkv"], c["D"], c["page"], sd["kv"], device=dev)
+    q = synth.normal_bf16((c["B"], c["Hq"], c["D"]), sd["q"], device=dev)
     y, C, out = torch.empty_like(x), torch.empty(c["B"], c["N"], dtype=torch.bfloat16,
                                                  device=dev), torch.empty_like(q)
     ws = torch.empty(bi.bi_attn_decode_workspace_size(c["B"], c["Hq"], c["Hkv"], c["D"],
@@ -630,8 +655,8 @@ def prefill_schedules(dev, stream, flush):
     from invariant_bi_rmsnorm_02_gb300 import synth
     c = synth.CHUNKED_PREFILL
     T, d = c["T"], DEC
-    kv = synth.paged_kv([T], c["Hkv"], c["D"], c["page"], 4001, device=dev)
-    q = synth.normal_bf16((T, c["Hq"], c["D"]), 4012, device=dev)  # apart from K, V
+    kv = synth.paged_kv([T], c["Hkv"], c["D"], c["page"], SEEDS["schedules"]["kv"], device=dev)
+    q = synth.normal_bf16((T, c["Hq"], c["D"]), SEEDS["schedules"]["q"], device=dev)
     out = torch.empty_like(q)
     scale = c["D"] ** -0.5
     flops = 4.0 * c["Hq"] * c["D"] * T * (T + 1) / 2.0

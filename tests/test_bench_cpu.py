@@ -73,3 +73,16 @@ def test_reference_arm_rejects_short_warmup():
                         "--steps", "3", "--warmup", "1"], capture_output=True, text=True,
                        timeout=300, cwd=ROOT)
     assert r.returncode != 0 and "warmup" in r.stderr
+
+
+def test_bench_inputs_do_not_reuse_a_cache_stream():
+    # paged_kv(seed) draws K and V from seeds seed + 1 and seed + 2; a query
+    # drawn from one of them would equal cached keys row for row
+    assert bench.seed_collisions() == []
+    bad = dict(bench.SEEDS["step"], q=bench.SEEDS["step"]["kv"] + 1)
+    saved = bench.SEEDS["step"]
+    try:
+        bench.SEEDS["step"] = bad
+        assert ("step", "q") in bench.seed_collisions()
+    finally:
+        bench.SEEDS["step"] = saved
