@@ -614,8 +614,9 @@ def _median_ms(fn, stream, flush=None, reps=3):
 def tiny_layer(dev, stream, reps=20):
     """The tiny-layer workload (RMSNorm over 256, GEMM 256->512, decode with
     4/2 heads of 64 over 8 requests of KV 1..512, page 16, split 64) at batch
-    1 and 8: microseconds per op and for the three back to back (launch-latency
-    bound: no roofline fraction is meaningful at this size)."""
+    1 and 8: microseconds per op and for the three back to back, eager and
+    replayed from a CUDA graph (launch-latency bound: no roofline fraction is
+    meaningful at this size)."""
     import invariant_bi_rmsnorm_02_gb300 as bi
     from invariant_bi_rmsnorm_02_gb300 import synth
     c = synth.TINY
@@ -643,6 +644,17 @@ def tiny_layer(dev, stream, reps=20):
         layer = 1000.0 * _median_ms(lambda: [f() for f in ops], stream, reps=reps)
         res["b%d" % m] = {"rmsnorm_us": per[0], "gemm_us": per[1], "decode_us": per[2],
                           "layer_us": layer}
+        # the same three calls captured once in a CUDA graph and replayed: what
+        # is left of the launch latency
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for f in ops:
+                    f()
+            res["b%d" % m]["layer_us_graph"] = 1000.0 * _median_ms(g.replay, stream, reps=reps)
+        except RuntimeError as e:  # capture refused: report why, keep the eager figures
+            res["b%d" % m]["layer_us_graph"] = None
+            res["b%d" % m]["graph_error"] = str(e).splitlines()[0][:200]
     return res
 
 
