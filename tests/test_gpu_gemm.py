@@ -44,7 +44,12 @@ def run_parity(cuda, M, N, K, mode, seed, splits=0):
 
 @pytest.mark.parametrize("M,N,K", [(1, 512, 256), (8, 512, 256), (3, 6144, 512),
                                    (130, 768, 320), (257, 1024, 1024), (64, 264, 72),
-                                   (129, 256, 64), (200, 520, 136)])
+                                   (129, 256, 64), (200, 520, 136),
+                                   # small batches over wide weights: narrow tiles with a
+                                   # partial last tile or 64 rows of A, and the wide
+                                   # tiles a weight too wide for one wave of them takes
+                                   (5, 4104, 256), (7, 6152, 256), (40, 9216, 512),
+                                   (2, 14336, 256)])
 def test_gemm_matches_oracle(cuda, M, N, K):
     run_parity(cuda, M, N, K, bi.INVARIANT, 3000 + M + N + K)
 
@@ -128,6 +133,19 @@ def test_gemm_batch_invariance_mlp_up(cuda):
     full = bi.gemm(A, W)
     for M in (1, 3, 16, 64, 256):
         assert same_bytes(bi.gemm(A[:M].contiguous(), W), full[:M]), M
+
+
+@pytest.mark.parametrize("N", [4096, 9216])
+def test_gemm_batch_invariance_wide_weights(cuda, N):
+    # small batches run the narrow 64-column tiles, a 1024-row batch 128 x
+    # 256 ones: every row has the same bytes in both
+    K = 4096
+    A = synth.normal_bf16((1024, K), 3550 + N, device=cuda)
+    W = synth.normal_bf16((N, K), 3551 + N, std=0.02, device=cuda)
+    full = bi.gemm(A, W)
+    for M in (1, 3, 16, 33, 64):
+        assert same_bytes(bi.gemm(A[:M].contiguous(), W), full[:M]), M
+    assert bi.bi_check_device_errors() == bi.OK
 
 
 def test_gemm_run_to_run(cuda):
