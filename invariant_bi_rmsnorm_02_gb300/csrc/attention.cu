@@ -44,8 +44,11 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include <algorithm>
+#include <queue>
 #include <type_traits>
 #include <utility>
+#include <vector>
 
 #include "bi_internal.h"
 #include "device_common.cuh"
@@ -1085,7 +1088,8 @@ __global__ void __launch_bounds__(D) attn_decode_merge_kernel(const KernelParams
 // took ~130 cycles per 2 KB page box.  The fold and copy warps sleep in
 // their barrier waits instead of polling, so that they leave the issue slots
 // of their scheduler to the softmax warp beside them.  Blocks start longest
-// first.
+// first, or, for one sequence whose blocks leave the last wave part full, in
+// a host-planned order (plan_prefill_order).
 constexpr int kPfRows = 128;
 constexpr int kPfThreads = 14 * 32;
 constexpr int kPfSoftWarp0 = 0, kPfFoldWarp0 = 4, kPfMmaWarp = 8, kPfTmaWarp0 = 9, kPfSWarp = 13;
@@ -1173,10 +1177,31 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
-template <int D>
+// Which query block and kv head a block of the launch computes.  LpOrder:
+// the longest query blocks (of every kv head) first.  TableOrder: a
+// host-planned order of one sequence's blocks (see plan_prefill_order), one
+// index qb * Hkv + h per block, carried in the kernel's parameters.
+struct LpOrder {
+  __device__ __forceinline__ void map(int x, int nqb, int Hkv, int& qb, int& h) const {
+    qb = nqb - 1 - x / Hkv;
+    h = x % Hkv;
+  }
+};
+constexpr int kPfOrderMax = 4096;
+struct TableOrder {
+  uint16_t blk[kPfOrderMax];
+  __device__ __forceinline__ void map(int x, int nqb, int Hkv, int& qb, int& h) const {
+    (void)nqb;
+    const int v = blk[x];
+    qb = v / Hkv;
+    h = v % Hkv;
+  }
+};
+
+template <int D, class Order>
 __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-    const KernelParams p) {
+    const KernelParams p, const __grid_constant__ Order order) {
   using Gm = PfGeom<D>;
   constexpr uint32_t kIdescS = umma_idesc_bf16(kPfRows, kPfPair, false, false);
   constexpr uint32_t kIdescPV = umma_idesc_bf16(kPfRows, D, false, true);
@@ -1202,10 +1227,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   __shared__ uint32_t tmem_slot;
   __shared__ int s_abort;
 
-  // blocks in launch order: the longest query blocks of every kv head first
   const int nqb = static_cast<int>(gridDim.x) / p.Hkv;
-  const int qb = nqb - 1 - static_cast<int>(blockIdx.x) / p.Hkv;
-  const int h = static_cast<int>(blockIdx.x) % p.Hkv, b = blockIdx.z;
+  int qb, h;
+  order.map(static_cast<int>(blockIdx.x), nqb, p.Hkv, qb, h);
+  const int b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.G, TPB = kPfRows / G;
   const int q_begin = p.cu_q[b];
@@ -1819,6 +1844,76 @@ bi_status decode_impl(const AttnArgs& a, cudaStream_t s) {
   return BI_OK;
 }
 
+// Launch order of one sequence's prefill blocks.  The hardware gives each
+// block, in launch order, to the SM that frees first; with n similar blocks
+// on m SMs (n = a m + r) longest-first leaves the last r blocks running
+// alone after every SM has run a.  A block's time is modelled as a fixed
+// start-up (as long as ~640 keys) plus its key count (the chunk assumed to
+// end at max_kv_len).  The plan gives the r SMs that must run a + 1 blocks
+// the shortest blocks and the others the longest a each (longest first
+// within each group), then orders all blocks by their planned start times,
+// so that the hardware's own dispatch reproduces it.  Both orders are
+// simulated with the model; the plan is used only where it predicts a
+// shorter run (1% or more).  The order changes no block's work or result.
+bool plan_prefill_order(int nqb, int Hkv, int TPB, int max_q_len, int max_kv_len, int sms,
+                        TableOrder* out) {
+  const int n = nqb * Hkv;
+  if (sms <= 0 || n <= sms || n > kPfOrderMax) return false;
+  const int a = n / sms, r = n % sms;
+  if (r == 0) return false;
+  const int64_t start = std::max<int64_t>(0, int64_t(max_kv_len) - max_q_len);
+  std::vector<double> d(n);  // modelled time of block b = qb * Hkv + h
+  for (int qb = 0; qb < nqb; ++qb) {
+    const int64_t keys = std::min<int64_t>(max_kv_len, start + int64_t(TPB) * (qb + 1));
+    for (int h = 0; h < Hkv; ++h) d[qb * Hkv + h] = 640.0 + static_cast<double>(keys);
+  }
+  using Ev = std::pair<double, int>;  // (time the SM frees, SM)
+  auto simulate = [&](const std::vector<int>& ord) {
+    std::priority_queue<Ev, std::vector<Ev>, std::greater<Ev>> q;
+    for (int i = 0; i < sms; ++i) q.push({0.0, i});
+    double end = 0.0;
+    for (int b : ord) {
+      Ev e = q.top();
+      q.pop();
+      e.first += d[b];
+      end = std::max(end, e.first);
+      q.push(e);
+    }
+    return end;
+  };
+  std::vector<int> lp(n);
+  for (int x = 0; x < n; ++x) lp[x] = (nqb - 1 - x / Hkv) * Hkv + x % Hkv;
+  std::vector<int> by_len(lp);  // longest first (ties: as the default order)
+  std::stable_sort(by_len.begin(), by_len.end(), [&](int u, int v) { return d[u] > d[v]; });
+  // the two groups, each by longest-first onto its SMs with a fixed count each
+  std::vector<std::pair<double, int>> starts;  // (planned start, block)
+  starts.reserve(n);
+  auto place = [&](int first, int count, int nsm, int per) {
+    std::vector<double> t(nsm, 0.0);
+    std::vector<int> cnt(nsm, 0);
+    for (int k = first; k < first + count; ++k) {
+      int best = -1;
+      for (int i = 0; i < nsm; ++i)
+        if (cnt[i] < per && (best < 0 || t[i] < t[best])) best = i;
+      const int b = by_len[k];
+      starts.push_back({t[best], b});
+      t[best] += d[b];
+      ++cnt[best];
+    }
+  };
+  place(0, (sms - r) * a, sms - r, a);
+  place((sms - r) * a, r * (a + 1), r, a + 1);
+  std::stable_sort(starts.begin(), starts.end(),
+                   [](const std::pair<double, int>& u, const std::pair<double, int>& v) {
+                     return u.first < v.first;
+                   });
+  std::vector<int> planned(n);
+  for (int k = 0; k < n; ++k) planned[k] = starts[k].second;
+  if (simulate(planned) > 0.99 * simulate(lp)) return false;
+  for (int k = 0; k < n; ++k) out->blk[k] = static_cast<uint16_t>(planned[k]);
+  return true;
+}
+
 template <int D>
 bi_status prefill_impl(const AttnArgs& a, cudaStream_t s) {
   CUtensorMap km, vm;
@@ -1828,8 +1923,25 @@ bi_status prefill_impl(const AttnArgs& a, cudaStream_t s) {
   const int TPB = kPfRows / G;  // tokens per block
   const int nqb = (a.max_q_len + TPB - 1) / TPB;
   const size_t sm = PfGeom<D>::kSmem;
-  if (set_smem(attn_prefill_kernel<D>, sm) != cudaSuccess) return BI_ERR_CUDA;
-  attn_prefill_kernel<D><<<dim3(nqb * a.Hkv, 1, a.B), kPfThreads, sm, s>>>(km, vm, p);
+  const dim3 grid(nqb * a.Hkv, 1, a.B);
+  // one sequence: a planned order, kept for the next call of the same shape
+  thread_local TableOrder plan;
+  thread_local int plan_key[6] = {-1, -1, -1, -1, -1, -1};
+  thread_local bool plan_ok = false;
+  if (a.B == 1) {
+    const int key[6] = {nqb, a.Hkv, TPB, a.max_q_len, a.max_kv_len, device_sm_count()};
+    if (!std::equal(key, key + 6, plan_key)) {
+      plan_ok = plan_prefill_order(nqb, a.Hkv, TPB, a.max_q_len, a.max_kv_len, key[5], &plan);
+      std::copy(key, key + 6, plan_key);
+    }
+    if (plan_ok) {
+      if (set_smem(attn_prefill_kernel<D, TableOrder>, sm) != cudaSuccess) return BI_ERR_CUDA;
+      attn_prefill_kernel<D, TableOrder><<<grid, kPfThreads, sm, s>>>(km, vm, p, plan);
+      return cuda_status(cudaGetLastError());
+    }
+  }
+  if (set_smem(attn_prefill_kernel<D, LpOrder>, sm) != cudaSuccess) return BI_ERR_CUDA;
+  attn_prefill_kernel<D, LpOrder><<<grid, kPfThreads, sm, s>>>(km, vm, p, LpOrder{});
   return cuda_status(cudaGetLastError());
 }
 

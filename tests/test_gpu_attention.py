@@ -300,6 +300,38 @@ def test_prefill_chunked_equivalence_full_prompt(cuda):
     check_attn(base[idx], base32[idx], ref, "8192-token prompt sample")
 
 
+@pytest.mark.parametrize("T,chunk", [(8192, 2048), (32768, 4096)])
+def test_prefill_planned_order_matches_batch_and_decode(cuda, T, chunk):
+    # a single sequence's blocks launch in a host-planned order (the shapes
+    # here are ones it is planned for); two copies of the sequence in one
+    # call launch longest first: every row's bytes agree, and sampled
+    # positions equal a decode with L = p + 1
+    Hq, Hkv, D, S = 32, 8, 128, 256
+    kv1 = synth.paged_kv([T], Hkv, D, 16, 5300 + chunk, device=cuda)
+    q = synth.normal_bf16((chunk, Hq, D), 5301 + chunk, device=cuda)
+    start = T - chunk
+    one, one32 = prefill(q, torch.tensor([0, chunk], dtype=torch.int32, device=cuda),
+                         torch.tensor([start], dtype=torch.int32, device=cuda), kv1,
+                         kv1.kv_lens, chunk, T, S)
+    bt2 = kv1.block_table.expand(2, -1).contiguous()
+    kv2 = synth.PagedKV(kv1.k_cache, kv1.v_cache, bt2, kv1.kv_lens.expand(2).contiguous(),
+                        kv1.page_size)
+    two, two32 = prefill(torch.cat([q, q]), torch.tensor([0, chunk, 2 * chunk],
+                                                         dtype=torch.int32, device=cuda),
+                         torch.tensor([start, start], dtype=torch.int32, device=cuda), kv2,
+                         kv2.kv_lens, chunk, T, S)
+    assert bi.bi_check_device_errors() == bi.OK
+    for half in (two32[:chunk], two32[chunk:]):
+        assert same_bytes(half, one32), first_divergence(half, one32)
+    assert same_bytes(two[:chunk], one) and same_bytes(two[chunk:], one)
+    rows = torch.tensor([0, 1, 31, 32, chunk // 2, chunk - 33, chunk - 1], device=cuda)
+    lens = (rows + start + 1).to(torch.int32)
+    dec, dec32 = decode(q[rows].contiguous(), kv1, T, S, kv_lens=lens,
+                        bt=kv1.block_table.expand(len(rows), -1).contiguous())
+    assert same_bytes(dec32, one32[rows]), first_divergence(dec32, one32[rows])
+    assert same_bytes(dec, one[rows])
+
+
 def test_prefill_independent_of_neighbour_sequences(cuda):
     Hq, Hkv, D, S = 32, 8, 128, 256
     lens = [900, 1500, 64]
