@@ -190,7 +190,8 @@ bi_status bi_gemm_swiglu(const void* A, const void* W, void* out, int64_t M, int
  *   0..L-1 of a query are cut at multiples of split_size; each chunk is
  *   reduced with an online softmax over key tiles of 64 in increasing order
  *   (partial max m, sum l, unnormalised o), and the chunks are merged by a
- *   left fold in chunk order with the log-sum-exp rule, then o/l is rounded.
+ *   left fold in chunk order with the log-sum-exp rule, then o times the
+ *   correctly rounded 1/l is rounded.
  *   Boundaries depend on absolute key indices only, never on L, B, the grid
  *   or the chunking of a prompt.
  * BI_MODE_VARIANT (a split plan sized from the batch, the kind of plan the

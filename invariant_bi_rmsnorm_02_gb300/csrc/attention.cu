@@ -10,8 +10,8 @@
 //     reduced in increasing order with an online softmax (FlashAttention,
 //     cited by the pages): running max m, running sum l, unnormalised o.
 //   * Splits are merged by a left fold in split order with the log-sum-exp
-//     rule, then o/l is rounded once ("Reproducible LLM Inference", §4.3: a
-//     fixed, non-parallel clean-up step).
+//     rule, then o times the rounded 1/l is rounded once ("Reproducible LLM
+//     Inference", §4.3: a fixed, non-parallel clean-up step).
 //   * New tokens are written into the paged cache before attention runs, so
 //     cached and fresh keys are read from one layout (§5.5).
 // Decode runs a small plan kernel (the list of (sequence, split) units), a
@@ -327,6 +327,12 @@ __device__ __forceinline__ void lse_coeffs(float m, float mb, float& mn, float& 
 __device__ __forceinline__ float lse_mix(float a, float ca, float b, float cb) {
   return __fadd_rn(__fmul_rn(a, ca), __fmul_rn(b, cb));
 }
+// The output's normalisation: o times the correctly rounded reciprocal of l
+// (one reciprocal per row, then one product per element; an IEEE division
+// per element cost the prefill's output phase 2.7 us a block).  Decode, its
+// merge and prefill all normalise with this, so they stay bit-identical.
+__device__ __forceinline__ float inv_l(float l) { return __frcp_rn(l); }
+__device__ __forceinline__ float normalize(float o, float rl) { return __fmul_rn(o, rl); }
 
 // ---------------------------------------------------------------- staging
 // Issue the TMA copies of the first np pages of a tile; page ids in pid.
@@ -677,7 +683,7 @@ __global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
     }
     const int U = total * Hkv;
     // A sequence with a single split has no merge: its unit writes the
-    // output itself (o / l, the merge's arithmetic for one split).  Split 0
+    // output itself (o * (1/l), the merge's arithmetic for one split).  Split 0
     // is the only one iff it ends below the chunk size or the sequence is
     // exactly one chunk long.
     auto single_split = [&](int b, int j, int hi) -> bool {
@@ -895,7 +901,7 @@ __global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
             const float o_odd = __shfl_xor_sync(kFull, st.o[md][0][2 * hh + 1], 2);
             const float ov = helper ? o_odd : st.o[md][0][2 * hh];
             if (col < G) {
-              const float v = lv > 0.0f ? __fdiv_rn(ov, lv) : 0.0f;
+              const float v = lv > 0.0f ? normalize(ov, inv_l(lv)) : 0.0f;
               const int64_t idx = orow + 16 * md + g + 8 * hh;
               static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
               if (p.out_f32) p.out_f32[idx] = v;
@@ -915,7 +921,7 @@ __global__ void __maxnreg__(NQ == 1 ? 192 : 255) attn_decode_split_kernel(
           for (int md = 0; md < D / 16; ++md)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-              const float v = lv > 0.0f ? __fdiv_rn(st.o[md][nq][2 * hh + cc], lv) : 0.0f;
+              const float v = lv > 0.0f ? normalize(st.o[md][nq][2 * hh + cc], inv_l(lv)) : 0.0f;
               const int64_t idx = orow + 16 * md + g + 8 * hh;
               static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
               if (p.out_f32) p.out_f32[idx] = v;
@@ -1045,7 +1051,7 @@ __global__ void __launch_bounds__(D) attn_decode_merge_kernel(const KernelParams
     if (c0 + 2 * kMergeChunk < ns) load(c0 + 2 * kMergeChunk, ml0, ov0);
     fold(ml1, ov1);
   }
-  const float r = (ns > 0 && !bad && l > 0.0f) ? __fdiv_rn(o, l) : 0.0f;
+  const float r = (ns > 0 && !bad && l > 0.0f) ? normalize(o, inv_l(l)) : 0.0f;
   const int64_t oidx = row * D + tid;
   const float r_next = __shfl_down_sync(kFull, r, 1);
   if ((tid & 1) == 0)
@@ -1079,7 +1085,7 @@ __global__ void __launch_bounds__(D) attn_decode_merge_kernel(const KernelParams
 // Roles: warps 0-3 run the softmax (warp w owns rows 32w..32w+31, the TMEM
 // lanes of quadrant w), keeping each row's split state (reference maximum m,
 // sum l) in registers; warps 4-7 fold every finished split into the merged
-// state (in shared memory) and write out = o / l at the end; one lane of
+// state (in shared memory) and write out = o * (1/l) at the end; one lane of
 // warp 13 issues the S MMAs and one of warp 8 the PV MMAs (two schedulers:
 // a single issuing lane shares its scheduler with a softmax warp and falls
 // behind); warps 9-12 the TMA copies, one column half of K or of V each
@@ -1663,15 +1669,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       __syncwarp();
       if (lane == 0) mbar_arrive(&folded[j & 1]);
     }
-    // ---- out = o / l, rounded once
+    // ---- out = o * (1/l), rounded once
     if (live && !s_abort && pos >= 0) {
       const int64_t orow = ((int64_t)(q_begin + tok0 + tk) * p.Hq + h * G + r % G) * D;
+      const float rl = inv_l(mg_l);
 #pragma unroll 4
       for (int e = 0; e < D; e += 8) {
         const float4 a4 = omg[(e / 4) * kPfRows + r], b4 = omg[(e / 4 + 1) * kPfRows + r];
         float o[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-        for (int u = 0; u < 8; ++u) o[u] = __fdiv_rn(o[u], mg_l);
+        for (int u = 0; u < 8; ++u) o[u] = normalize(o[u], rl);
         *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + e) =
             make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
                        pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
