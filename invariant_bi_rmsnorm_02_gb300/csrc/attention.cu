@@ -1232,6 +1232,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   uint64_t* folded = sdone + 2;          // a split folded, its m, l slot free [2]
   __shared__ uint32_t tmem_slot;
   __shared__ int s_abort;
+  __shared__ int s_out[2];  // for the output: first row's (token * Hq + head), tokens
 
   const int nqb = static_cast<int>(gridDim.x) / p.Hkv;
   int qb, h;
@@ -1261,10 +1262,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   {
     // check every page a copy may read, and keep the first ids at hand
     bool ok = true;
-    for (int pg = tid; pg * kPage < key_hi; pg += kPfThreads) {
+    for (int pg = tid; pg * kPage < key_hi; pg += 2 * kPfThreads) {  // two loads in flight
+      const int pg1 = pg + kPfThreads;
+      const bool has1 = pg1 * kPage < key_hi;
       const int v = bt_row[pg];
-      if (v < 0 || v >= p.num_pages) ok = false;
+      const int v1 = has1 ? bt_row[pg1] : 0;
+      if (v < 0 || v >= p.num_pages || v1 < 0 || v1 >= p.num_pages) ok = false;
       if (pg < kPfPageCache) pid_s[pg] = v;
+      if (has1 && pg1 < kPfPageCache) pid_s[pg1] = v1;
     }
     ok = __syncthreads_and(ok);
     if (!ok) {
@@ -1274,6 +1279,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
   }
   if (tid == 0) {
     s_abort = 0;
+    // kept here rather than in registers through the main loops
+    s_out[0] = (q_begin + tok0) * p.Hq + h * G;
+    s_out[1] = ntok;
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
     for (int i = 0; i < kPfKStages; ++i) {
@@ -1308,19 +1316,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
     const bool valid = r < TPB * G && tk < ntok;
     const uint4* src = reinterpret_cast<const uint4*>(
         p.q + ((int64_t)(q_begin + tok0 + (valid ? tk : 0)) * p.Hq + h * G + r % G) * D);
+    uint32_t v[D / 2];  // the row's D bf16 values: every load goes out before the stores
 #pragma unroll
-    for (int c = 0; c < D / 64; ++c) {
-      uint32_t v[32];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const uint4 w = valid ? src[8 * c + u] : make_uint4(0, 0, 0, 0);
-        v[4 * u] = w.x;
-        v[4 * u + 1] = w.y;
-        v[4 * u + 2] = w.z;
-        v[4 * u + 3] = w.w;
-      }
-      tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + Gm::kColQ + 32 * c, v);
+    for (int u = 0; u < D / 8; ++u) {
+      const uint4 w = valid ? src[u] : make_uint4(0, 0, 0, 0);
+      v[4 * u] = w.x;
+      v[4 * u + 1] = w.y;
+      v[4 * u + 2] = w.z;
+      v[4 * u + 3] = w.w;
     }
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c)
+      tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + Gm::kColQ + 32 * c,
+                *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
     tmem_wait_st();
   }
   tc_fence_before();
@@ -1669,31 +1677,34 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       __syncwarp();
       if (lane == 0) mbar_arrive(&folded[j & 1]);
     }
-    // ---- out = o * (1/l), rounded once
-    if (live && !s_abort && pos >= 0) {
-      const int64_t orow = ((int64_t)(q_begin + tok0 + tk) * p.Hq + h * G + r % G) * D;
-      const float rl = inv_l(mg_l);
-#pragma unroll 4
-      for (int e = 0; e < D; e += 8) {
-        const float4 a4 = omg[(e / 4) * kPfRows + r], b4 = omg[(e / 4 + 1) * kPfRows + r];
-        float o[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-        for (int u = 0; u < 8; ++u) o[u] = normalize(o[u], rl);
-        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + orow + e) =
-            make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
-                       pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
-        if (p.out_f32) {
-          *reinterpret_cast<float4*>(p.out_f32 + orow + e) = make_float4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<float4*>(p.out_f32 + orow + e + 4) =
-              make_float4(o[4], o[5], o[6], o[7]);
-        }
-      }
-    }
+    // the row's 1/l for the output below (the split m, l slots are free now)
+    if (live && pos >= 0) xsplit[r] = inv_l(mg_l);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, Gm::kTmemCols);
+  // ---- out = o * (1/l), rounded once, by every warp: a warp takes 8 rows x
+  // 16 columns at a time (lane: row 8 rg + lane / 4, columns 4 c4 .. 4 c4 + 3
+  // with c4 = 4 cg + lane % 4), so its reads of the merged state are 128-byte
+  // runs and its writes 32-byte runs of each row
+  if (s_abort) return;
+  const int64_t row0 = s_out[0];
+  const int otok = s_out[1], oG = p.G;
+  for (int u = warp; u < (kPfRows / 8) * (D / 16); u += kPfThreads / 32) {
+    const int r = 8 * (u % (kPfRows / 8)) + (lane >> 2);
+    const int c4 = 4 * (u / (kPfRows / 8)) + (lane & 3);
+    const int tk = r / oG;
+    if (r >= (kPfRows / oG) * oG || tk >= otok) continue;
+    const float rl = xsplit[r];
+    const float4 a = omg[c4 * kPfRows + r];
+    const float o0 = normalize(a.x, rl), o1 = normalize(a.y, rl);
+    const float o2 = normalize(a.z, rl), o3 = normalize(a.w, rl);
+    const int64_t idx = (row0 + (int64_t)tk * p.Hq + r % oG) * D + 4 * c4;
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + idx) =
+        make_uint2(pack_bf16x2(o0, o1), pack_bf16x2(o2, o3));
+    if (p.out_f32) *reinterpret_cast<float4*>(p.out_f32 + idx) = make_float4(o0, o1, o2, o3);
+  }
 }
 
 // --------------------------------------------------------------- KV write
