@@ -182,8 +182,9 @@ bi_status bi_gemm_swiglu(const void* A, const void* W, void* out, int64_t M, int
  *     (P1 §5.5).
  *   block_table [B][max_blocks_per_seq] int32, kv_lens [B] int32: device.
  *   Grouped-query attention: q-head h reads kv-head h / (Hq/Hkv).
- *   scores = sm_scale * q.k (pass 1/sqrt(D) for the usual scale); softmax
- *   over the visible keys; out = sum softmax * v.
+ *   scores = sm_scale * q.k (pass 1/sqrt(D) for the usual scale; sm_scale
+ *   must be positive and finite, else BI_ERR_INVALID_ARG); softmax over the
+ *   visible keys; out = sum softmax * v.
  *   out is bf16; out_f32 (may be NULL) receives the same values before the
  *   final rounding, in fp32, same layout.
  * Split plan (BI_MODE_INVARIANT, P1 §5.5 fixed split SIZE): the keys

@@ -311,6 +311,11 @@ bi_status bi_gemm_swiglu(const void* A, const void* W, void* out, int64_t M, int
 }
 
 // ---------------------------------------------------------------- attention
+// The softmax scale must be positive and finite: the kernels take the
+// reference maximum of the raw scores and scale it once, which equals the
+// maximum of the scaled scores only for a positive scale.
+static bool scale_ok(float s) { return s > 0.0f && s <= 3.4e38f; }
+
 static bi_status attn_common_checks(const void* q, const void* k, const void* v,
                                     const int32_t* bt, const int32_t* kl, const void* out,
                                     const float* out_f32, int B, int Hq, int Hkv, int D,
@@ -356,6 +361,7 @@ bi_status bi_attn_decode(const void* q, const void* k_cache, const void* v_cache
                                     Hq, Hkv, D, page_size, num_pages, max_blocks_per_seq,
                                     max_kv_len, split_size, mode);
   if (st != BI_OK || B == 0) return st;
+  if (!scale_ok(sm_scale)) return BI_ERR_INVALID_ARG;
   AttnArgs a{};
   a.q = q; a.k_cache = k_cache; a.v_cache = v_cache; a.block_table = block_table;
   a.kv_lens = kv_lens; a.out = out; a.out_f32 = out_f32;
@@ -395,7 +401,7 @@ bi_status bi_attn_prefill_chunk(const void* q, const int32_t* cu_q, const int32_
                                     Hq, Hkv, D, page_size, num_pages, max_blocks_per_seq,
                                     max_kv_len, split_size, mode);
   if (st != BI_OK || B == 0) return st;
-  if (total_q < 0 || max_q_len < 0) return BI_ERR_INVALID_ARG;
+  if (total_q < 0 || max_q_len < 0 || !scale_ok(sm_scale)) return BI_ERR_INVALID_ARG;
   if (total_q == 0 || max_q_len == 0) return BI_OK;
   if (!cu_q || !q_start_pos) return BI_ERR_INVALID_ARG;
   if (total_q * Hq >= (int64_t(1) << 31)) return BI_ERR_UNSUPPORTED;

@@ -28,11 +28,13 @@
 // with mma.sync m16n8k16 bf16 -> fp32, every sum over k in increasing order.
 // P^T comes from the S^T accumulators by an in-register 8x8 transpose
 // (movmatrix).  A decode row group (the G query heads of one kv head) fills
-// one 8-wide n-tile, so padding costs at most half of an n-tile.  Scores are
-// scaled by sm_scale*log2(e) and exponentiated with ex2.approx; P is split into a
+// one 8-wide n-tile, so padding costs at most half of an n-tile.  With
+// c = sm_scale*log2(e) a probability is 2^(s c - m), one fused multiply-add
+// before ex2.approx, and the reference maximum is the raw scores' maximum
+// scaled once (rounding is monotone, c > 0); P is split into a
 // bf16 high part and a bf16 low part (P - hi), both taken by truncation and
 // both multiplied with V, so the probabilities keep 16 significant bits.
-// Column max / sum use a fixed shuffle tree.  Explicit __fmul_rn/__fadd_rn keep the compiler from
+// Column max / sum use a fixed shuffle tree.  Explicit __fmul_rn/__fadd_rn/__fmaf_rn keep the compiler from
 // contracting differently in the two kernels.
 //
 // K/V staging: each 16-token page of one kv head is a contiguous [16][D]
@@ -168,7 +170,7 @@ __device__ __forceinline__ void split_p_bf16(float p0, float p1, uint32_t& hp, u
 // Two fp32 operations in one instruction (the packed f32x2 forms of sm_100
 // and later): each lane is the IEEE operation, rounded to nearest, that the
 // scalar form computes, so the results are bit-identical to __fadd_rn /
-// __fmul_rn; the prefill softmax uses them to issue fewer instructions.
+// __fmaf_rn; the prefill softmax uses them to issue fewer instructions.
 __device__ __forceinline__ void add2_rn(float& r0, float& r1, float a0, float a1, float b0,
                                         float b1) {
   asm("{\n\t.reg .b64 a, b, r;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
@@ -176,11 +178,12 @@ __device__ __forceinline__ void add2_rn(float& r0, float& r1, float a0, float a1
       : "=f"(r0), "=f"(r1)
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
-__device__ __forceinline__ void mul2_rn(float& r0, float& r1, float a0, float a1, float b) {
-  asm("{\n\t.reg .b64 a, b, r;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %4};\n\t"
-      "mul.rn.f32x2 r, a, b;\n\tmov.b64 {%0, %1}, r;\n\t}"
+__device__ __forceinline__ void fma2_rn(float& r0, float& r1, float a0, float a1, float b,
+                                        float c) {
+  asm("{\n\t.reg .b64 a, b, c, r;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %4};\n\t"
+      "mov.b64 c, {%5, %5};\n\tfma.rn.f32x2 r, a, b, c;\n\tmov.b64 {%0, %1}, r;\n\t}"
       : "=f"(r0), "=f"(r1)
-      : "f"(a0), "f"(a1), "f"(b));
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
 }
 // The largest of three values (exact, as any fmaxf order).
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -223,7 +226,8 @@ __device__ __forceinline__ void tile_step(SplitState<D, NQ>& st,
 #pragma unroll
       for (int nq = 0; nq < NQ; ++nq) mma_bf16(s[mt][nq], a, qf[nq][ks][0], qf[nq][ks][1]);
     }
-  // ---- scale, mask, column max
+  // ---- mask, column max of the raw scores, scaled once: rounding is
+  // monotone, so RN(max s * c) = max RN(s * c) for the positive scale c
   float mx[NQ][2];
 #pragma unroll
   for (int nq = 0; nq < NQ; ++nq) {
@@ -235,7 +239,7 @@ __device__ __forceinline__ void tile_step(SplitState<D, NQ>& st,
         const int cc = c & 1;
         const int k = key0 + 16 * mt + g + 8 * (c >> 1);
         const bool ok = k >= lo && k < hi[nq][cc];
-        const float x = ok ? __fmul_rn(s[mt][nq][c], scale_log2) : -CUDART_INF_F;
+        const float x = ok ? s[mt][nq][c] : -CUDART_INF_F;
         s[mt][nq][c] = x;
         mx[nq][cc] = fmaxf(mx[nq][cc], x);
       }
@@ -244,6 +248,7 @@ __device__ __forceinline__ void tile_step(SplitState<D, NQ>& st,
       mx[nq][cc] = fmaxf(mx[nq][cc], __shfl_xor_sync(kFull, mx[nq][cc], 4));
       mx[nq][cc] = fmaxf(mx[nq][cc], __shfl_xor_sync(kFull, mx[nq][cc], 8));
       mx[nq][cc] = fmaxf(mx[nq][cc], __shfl_xor_sync(kFull, mx[nq][cc], 16));
+      mx[nq][cc] = __fmul_rn(mx[nq][cc], scale_log2);
     }
   }
   // ---- probabilities, rescale factors, column sums
@@ -275,7 +280,7 @@ __device__ __forceinline__ void tile_step(SplitState<D, NQ>& st,
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int cc = c & 1;
-        const float pv = exp2_sfu(__fsub_rn(s[mt][nq][c], mb[cc]));
+        const float pv = exp2_sfu(__fmaf_rn(s[mt][nq][c], scale_log2, -mb[cc]));
         s[mt][nq][c] = pv;
         cs[cc] = __fadd_rn(cs[cc], pv);
       }
@@ -1510,15 +1515,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       // keys key0 .. key0 + nvis - 1 are visible to this row (the tile lies
       // inside one split, which starts at or before key0)
       const int nvis = pos >= key0 ? min(kTile, pos + 1 - key0) : 0;
-#pragma unroll
-      for (int e = 0; e < 64; e += 2) mul2_rn(x[e], x[e + 1], x[e], x[e + 1], p.scale_log2);
       if (key0 + kTile - 1 > start + tok0) {  // some row of the block sees part of the tile
 #pragma unroll
         for (int e = 0; e < 64; ++e) x[e] = e < nvis ? x[e] : -CUDART_INF_F;
       }
       float mx;
       {
-        float t[22];  // the row maximum is exact in any order: a tree of 3-way maxima
+        // the row maximum of the raw scores is exact in any order (a tree of
+        // 3-way maxima), and scaled once it is the maximum of the scaled
+        // scores (rounding is monotone, the scale positive): the decode's
+        float t[22];
 #pragma unroll
         for (int e = 0; e < 21; ++e) t[e] = max3(x[3 * e], x[3 * e + 1], x[3 * e + 2]);
         t[21] = x[63];
@@ -1526,7 +1532,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
 #pragma unroll
         for (int e = 0; e < 7; ++e) u[e] = max3(t[3 * e], t[3 * e + 1], t[3 * e + 2]);
         u[7] = t[21];
-        mx = max3(max3(u[0], u[1], u[2]), max3(u[3], u[4], u[5]), fmaxf(u[6], u[7]));
+        mx = __fmul_rn(max3(max3(u[0], u[1], u[2]), max3(u[3], u[4], u[5]), fmaxf(u[6], u[7])),
+                       p.scale_log2);
       }
       const float m_in = split_first ? -CUDART_INF_F : m;
       float mnew = m_in, alpha = 1.0f;  // the decode's reference rule (kRescaleLog2)
@@ -1542,7 +1549,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       // ---- probabilities: P = hi + lo as bf16 pairs (column c holds keys
       // 2c, 2c+1), written over the scores; key e adds to partial sum e % 8
       // in increasing key order, then the tree ((0+1)+(2+3))+((4+5)+(6+7))
-      // masked keys hold -inf, and 2^(-inf - base) = +0 for any finite base
+      // p = 2^(s * scale - base), one rounding (the decode's fma); masked keys
+      // hold -inf, and 2^(-inf) = +0 for any finite base
       const float mb = mnew == -CUDART_INF_F ? 0.0f : mnew;
       float cs[8];
 #pragma unroll
@@ -1554,8 +1562,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
         for (int c = 0; c < 4; ++c) {  // keys 32hf+8c .. 32hf+8c+7
           const int k0 = 32 * hf + 8 * c;
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {  // x - mb as x + (-mb): the same rounding
-            add2_rn(x[k0 + e], x[k0 + e + 1], x[k0 + e], x[k0 + e + 1], -mb, -mb);
+          for (int e = 0; e < 8; e += 2) {
+            fma2_rn(x[k0 + e], x[k0 + e + 1], x[k0 + e], x[k0 + e + 1], p.scale_log2, -mb);
             x[k0 + e] = exp2_sfu(x[k0 + e]);
             x[k0 + e + 1] = exp2_sfu(x[k0 + e + 1]);
             add2_rn(cs[e], cs[e + 1], cs[e], cs[e + 1], x[k0 + e], x[k0 + e + 1]);

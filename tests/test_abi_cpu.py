@@ -156,6 +156,10 @@ def test_attention_argument_checks(lib):
     assert _decode(lib, q=None) == bi.ERR_INVALID_ARG
     assert _decode(lib, out=(1 << 20) + 4) == bi.ERR_INVALID_ARG
     assert _decode(lib, npages=0) == bi.ERR_INVALID_ARG
+    assert _decode(lib, scale=0.0) == bi.ERR_INVALID_ARG          # the scale must be > 0
+    assert _decode(lib, scale=-0.125) == bi.ERR_INVALID_ARG
+    assert _decode(lib, scale=float("inf")) == bi.ERR_INVALID_ARG
+    assert _decode(lib, scale=float("nan")) == bi.ERR_INVALID_ARG
     assert _decode(lib, B=0) == bi.OK
 
 
