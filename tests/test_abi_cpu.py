@@ -163,6 +163,34 @@ def test_attention_argument_checks(lib):
     assert _decode(lib, B=0) == bi.OK
 
 
+def _prefill(lib, **kw):
+    p = 1 << 20
+    a = dict(q=p, cu=p, st=p, k=p, v=p, bt=p, kl=p, out=p, o32=None, B=1, Hq=4, Hkv=2, D=64,
+             page=16, npages=8, maxblk=4, tq=16, mq=16, maxkv=64, S=64, scale=0.125, mode=0,
+             vs=0)
+    a.update(kw)
+    return lib.bi_attn_prefill_chunk(a["q"], a["cu"], a["st"], a["k"], a["v"], a["bt"], a["kl"],
+                                     a["out"], a["o32"], a["B"], a["Hq"], a["Hkv"], a["D"],
+                                     a["page"], a["npages"], a["maxblk"], a["tq"], a["mq"],
+                                     a["maxkv"], a["S"], a["scale"], a["mode"], a["vs"], None, 0,
+                                     None)
+
+
+def test_prefill_argument_checks(lib):
+    # every rejection happens on the host, before any device call
+    assert _prefill(lib, D=96) == bi.ERR_UNSUPPORTED
+    assert _prefill(lib, S=100) == bi.ERR_UNSUPPORTED
+    assert _prefill(lib, q=None) == bi.ERR_INVALID_ARG
+    assert _prefill(lib, tq=-1) == bi.ERR_INVALID_ARG
+    assert _prefill(lib, mq=-1) == bi.ERR_INVALID_ARG
+    assert _prefill(lib, scale=0.0) == bi.ERR_INVALID_ARG         # the scale must be > 0
+    assert _prefill(lib, scale=float("nan")) == bi.ERR_INVALID_ARG
+    assert _prefill(lib, cu=None) == bi.ERR_INVALID_ARG
+    assert _prefill(lib, st=None) == bi.ERR_INVALID_ARG
+    assert _prefill(lib, B=0) == bi.OK
+    assert _prefill(lib, tq=0) == bi.OK                           # nothing to do
+
+
 def test_binding_rejects_host_tensors():
     import torch
     x = torch.zeros(2, 64, dtype=torch.bfloat16)
