@@ -300,13 +300,18 @@ def test_prefill_chunked_equivalence_full_prompt(cuda):
     check_attn(base[idx], base32[idx], ref, "8192-token prompt sample")
 
 
-@pytest.mark.parametrize("T,chunk", [(8192, 2048), (32768, 4096)])
-def test_prefill_planned_order_matches_batch_and_decode(cuda, T, chunk):
+@pytest.mark.parametrize("Hq,Hkv,D,T,chunk", [
+    (32, 8, 128, 8192, 2048), (32, 8, 128, 32768, 4096),
+    (24, 8, 64, 8192, 1664),    # 3 q heads per kv head: two padding rows per block
+    (16, 2, 128, 8192, 2560),   # 8 q heads per kv head: 16 tokens per block
+    (8, 8, 64, 8192, 4992),     # 1 q head per kv head: 128 tokens per block
+])
+def test_prefill_planned_order_matches_batch_and_decode(cuda, Hq, Hkv, D, T, chunk):
     # a single sequence's blocks launch in a host-planned order (the shapes
     # here are ones it is planned for); two copies of the sequence in one
     # call launch longest first: every row's bytes agree, and sampled
     # positions equal a decode with L = p + 1
-    Hq, Hkv, D, S = 32, 8, 128, 256
+    S = 256
     kv1 = synth.paged_kv([T], Hkv, D, 16, 5300 + chunk, device=cuda)
     q = synth.normal_bf16((chunk, Hq, D), 5301 + chunk, device=cuda)
     start = T - chunk
