@@ -1915,16 +1915,18 @@ bool plan_prefill_order(int nqb, int Hkv, int TPB, int max_q_len, int max_kv_len
   std::vector<std::pair<double, int>> starts;  // (planned start, block)
   starts.reserve(n);
   auto place = [&](int first, int count, int nsm, int per) {
-    std::vector<double> t(nsm, 0.0);
+    // longest first onto the SM that frees first (the lowest index among
+    // equals), exactly `per` blocks each
+    std::priority_queue<Ev, std::vector<Ev>, std::greater<Ev>> q;
+    for (int i = 0; i < nsm; ++i) q.push({0.0, i});
     std::vector<int> cnt(nsm, 0);
     for (int k = first; k < first + count; ++k) {
-      int best = -1;
-      for (int i = 0; i < nsm; ++i)
-        if (cnt[i] < per && (best < 0 || t[i] < t[best])) best = i;
+      Ev e = q.top();
+      q.pop();
       const int b = by_len[k];
-      starts.push_back({t[best], b});
-      t[best] += d[b];
-      ++cnt[best];
+      starts.push_back({e.first, b});
+      e.first += d[b];
+      if (++cnt[e.second] < per) q.push(e);
     }
   };
   place(0, (sms - r) * a, sms - r, a);
