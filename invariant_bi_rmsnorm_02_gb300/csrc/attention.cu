@@ -1595,7 +1595,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
         if (!live) break;
         tc_fence_after();
         const uint32_t oc = tl + Gm::kColO;
-#pragma unroll
+#pragma unroll 1  // a rare path: kept compact, out of the way of the hot loop's code
         for (int c = 0; c < D / 32; ++c) {
           uint32_t v0[32];
           tmem_ld32(oc + 32 * c, v0);
@@ -1645,7 +1645,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) attn_prefill_kernel(
       float mn = 0.0f, ca = 0.0f, cb = 0.0f;
       if (part && have) lse_coeffs(mg_m, m_s, mn, ca, cb);
       const bool any = __any_sync(kFull, part);
-#pragma unroll
+#pragma unroll 1  // once per split: compact code
       for (int c = 0; c < D / 32; ++c) {
         uint32_t vo[32];
         if (any) tmem_ld32(Gm::kColO + tl + 32 * c, vo);
